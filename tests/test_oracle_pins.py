@@ -1,0 +1,370 @@
+"""Pins for the float64 oracle against facts fixed by the pages and by mathematics.
+
+Each check is independent of the oracle's own code path:
+  * the YaRN temperature table printed on "YaRN › Attention Temperature Scaling";
+  * closed forms derived by hand (uniform bids -> harmonic numbers, the
+    two-query case through the logistic function, T = 1);
+  * invariants stated on "DilutionAttention v0.1.0 · results", section
+    "The operator" (one unit of demand per query, shares at most one, rows of
+    A summing to one, the diagonal entry defined through the current bid);
+  * a scalar brute-force that walks queries in order and keeps one running
+    demand total per key (the cached-decoding formulation) instead of the
+    oracle's matrix cumulative sum;
+  * the large-eps limit, which reduces to ordinary causal softmax attention
+    computed by a library routine (torch SDPA in float64);
+  * finite differences and float64 autograd for the backward.
+``test_planted_mistakes_are_caught`` plants plausible mistakes in the oracle
+(on the CPU) and checks that at least one pin fails for each.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle.dilution as od
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(T, d, seed, dv=None, q_std=1.0):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((T, d)) * q_std
+    k = rng.standard_normal((T, d))
+    v = rng.standard_normal((T, dv or d))
+    return q, k, v
+
+
+def _harmonic(n):
+    return sum(1.0 / m for m in range(1, n + 1))
+
+
+# ---------------------------------------------------------------------------
+# Pin functions: each returns the max abs deviation from what it pins.
+# ---------------------------------------------------------------------------
+def pin_yarn_table():
+    worst = 0.0
+    with open(os.path.join(GOLDEN, "yarn_temperature_table.txt")) as fh:
+        for line in fh:
+            if line.startswith("#") or not line.strip():
+                continue
+            s, t, st = line.split()
+            worst = max(worst, abs(round(od.yarn_temperature(float(s)), 4) - float(t)))
+            worst = max(worst, abs(round(od.yarn_tau(float(s)), 4) - float(st)))
+    return worst
+
+
+def pin_uniform_bids_harmonic(T=23, d=8, eps=1e-6, seed=3):
+    """q = 0 makes every visible bid equal: p_ik = 1/(i+1).  Then
+    committed_ik = H_i - H_k and share_ik = 1/((i+1) (H_{i+1} - H_k + eps))."""
+    _, k, v = _rand(T, d, seed)
+    q = np.zeros((T, d))
+    r = od.dilution_forward_head(q, k, v, 1.0, eps, full=True)
+    H = [_harmonic(n) for n in range(T + 2)]
+    p_cf = np.zeros((T, T))
+    c_cf = np.zeros((T, T))
+    s_cf = np.zeros((T, T))
+    for i in range(T):
+        for kk in range(i + 1):
+            p_cf[i, kk] = 1.0 / (i + 1)
+            c_cf[i, kk] = H[i] - H[kk]
+            s_cf[i, kk] = 1.0 / ((i + 1) * (H[i + 1] - H[kk] + eps))
+    a_cf = s_cf / s_cf.sum(axis=1, keepdims=True)
+    out_cf = a_cf @ v
+    return max(np.abs(r["p"] - p_cf).max(), np.abs(r["committed"] - c_cf).max(),
+               np.abs(r["share"] - s_cf).max(), np.abs(r["out"] - out_cf).max())
+
+
+def pin_equal_keys_harmonic(T=19, d=8, seed=4):
+    """All keys equal -> all visible logits equal, whatever q: same harmonic form."""
+    q, k, v = _rand(T, d, seed)
+    k = np.tile(k[:1], (T, 1))
+    r = od.dilution_forward_head(q, k, v, 0.9, 1e-6, full=True)
+    H = [_harmonic(n) for n in range(T + 2)]
+    c_cf = np.array([[H[i] - H[kk] if kk <= i else 0.0 for kk in range(T)] for i in range(T)])
+    return np.abs(r["committed"] - c_cf).max()
+
+
+def pin_first_rows(T=9, d=8, seed=5, eps=1e-6):
+    """Row 0 attends only to key 0: out_0 = v_0.  Row 1, with sigma = p_10 given
+    by the logistic function of the logit gap: committed_10 = p_00 = 1 and
+    committed_11 = 0, so share_10 = sigma/(1+sigma+eps), share_11 = (1-sigma)/(1-sigma+eps)."""
+    q, k, v = _rand(T, d, seed)
+    tau = 1.3
+    r = od.dilution_forward_head(q, k, v, tau, eps, full=True)
+    c = tau / math.sqrt(d)
+    gap = c * (q[1] @ k[1] - q[1] @ k[0])
+    sigma = 1.0 / (1.0 + math.exp(gap))
+    s10 = sigma / (1.0 + sigma + eps)
+    s11 = (1.0 - sigma) / (1.0 - sigma + eps)
+    out1 = (s10 * v[0] + s11 * v[1]) / (s10 + s11)
+    return max(np.abs(r["out"][0] - v[0]).max(), abs(r["share"][1, 0] - s10),
+               abs(r["share"][1, 1] - s11), np.abs(r["out"][1] - out1).max())
+
+
+def pin_single_token(d=8, seed=6):
+    q, k, v = _rand(1, d, seed)
+    r = od.dilution_forward_head(q, k, v, 1.0, 1e-6)
+    return np.abs(r["out"] - v).max()
+
+
+def pin_invariants(T=41, d=16, seed=7, eps=1e-6, tau=1.0, q_std=1.5):
+    """Rows of A sum to 1; every query adds exactly one unit of demand, so the
+    column totals of p sum to T; 0 <= share <= 1; the diagonal committed is 0,
+    so share_ii = p_ii / (p_ii + eps); masked entries are 0."""
+    q, k, v = _rand(T, d, seed, q_std=q_std)
+    r = od.dilution_forward_head(q, k, v, tau, eps, full=True)
+    dev = abs(r["A"].sum(axis=1) - 1.0).max()
+    dev = max(dev, abs(r["demand"].sum() - T))
+    dev = max(dev, max(0.0, -r["share"].min()), max(0.0, r["share"].max() - 1.0))
+    diag = np.diag(r["p"])
+    dev = max(dev, np.abs(np.diag(r["share"]) - diag / (diag + eps)).max())
+    upper = np.triu(np.ones((T, T), dtype=bool), 1)
+    dev = max(dev, np.abs(r["share"][upper]).max(), np.abs(r["p"][upper]).max())
+    return dev
+
+
+def brute_force_running_demand(q, k, v, tau, eps):
+    """Scalar loops: walk queries in order; each key keeps a running demand
+    total (sum of the bids it received from earlier queries)."""
+    T, d = len(q), len(q[0])
+    c = tau / math.sqrt(d)
+    demand = [0.0] * T
+    outs, shares = [], []
+    for i in range(T):
+        logits = [c * sum(q[i][t] * k[j][t] for t in range(d)) for j in range(i + 1)]
+        mx = max(logits)
+        ex = [math.exp(x - mx) for x in logits]
+        z = sum(ex)
+        bids = [x / z for x in ex]
+        sh = [bids[j] / (demand[j] + bids[j] + eps) for j in range(i + 1)]
+        tot = sum(sh)
+        outs.append([sum(sh[j] * v[j][t] for j in range(i + 1)) / tot for t in range(len(v[0]))])
+        shares.append(sh + [0.0] * (T - i - 1))
+        for j in range(i + 1):
+            demand[j] += bids[j]
+    return np.array(outs), np.array(shares), np.array(demand)
+
+
+def pin_brute_force(T=8, d=4, seed=8, tau=0.8, eps=1e-3):
+    q, k, v = _rand(T, d, seed, dv=3, q_std=2.0)
+    bo, bs, bd = brute_force_running_demand(q.tolist(), k.tolist(), v.tolist(), tau, eps)
+    r = od.dilution_forward_head(q, k, v, tau, eps, full=True)
+    return max(np.abs(r["out"] - bo).max(), np.abs(r["share"] - bs).max(), np.abs(r["demand"] - bd).max())
+
+
+def pin_large_eps_softmax_limit(T=33, d=16, seed=9, tau=1.2):
+    """As eps -> inf, share -> p/eps and A -> p: the output becomes ordinary
+    causal softmax attention (torch's SDPA in float64)."""
+    torch = pytest.importorskip("torch")
+    q, k, v = _rand(T, d, seed)
+    r = od.dilution_forward_head(q, k, v, tau, 1e12)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q)[None, None], torch.tensor(k)[None, None], torch.tensor(v)[None, None],
+        is_causal=True, scale=tau / math.sqrt(d))[0, 0].numpy()
+    return np.abs(r["out"] - ref).max()
+
+
+def pin_decode_equals_prefill(T=12, d=8, seed=10, tau=1.1, eps=1e-6):
+    """Prefill of the first n tokens, then one cached decode step with token n,
+    reproduces row n of a prefill of n+1 tokens, and the demand cache after the
+    step equals the column totals of that longer prefill."""
+    q, k, v = _rand(T, d, seed, q_std=1.5)
+    worst = 0.0
+    for n in range(1, T):
+        pre = od.dilution_forward_head(q[:n], k[:n], v[:n], tau, eps)
+        out, dn, _, _ = od.dilution_decode_step_head(q[n], k[n], v[n], k[:n], v[:n], pre["demand"], n, tau, eps)
+        full = od.dilution_forward_head(q[:n + 1], k[:n + 1], v[:n + 1], tau, eps)
+        worst = max(worst, np.abs(out - full["out"][n]).max(), np.abs(dn - full["demand"]).max())
+    return worst
+
+
+def pin_rowblocked(T=77, d=8, seed=11):
+    q, k, v = _rand(T, d, seed, q_std=1.5)
+    full = od.dilution_forward_head(q, k, v, 0.9, 1e-6)
+    worst = 0.0
+    for blk in (1, 7, 32, 100):
+        rb = od.dilution_forward_rowblocked_head(q, k, v, 0.9, 1e-6, block=blk)
+        worst = max(worst, np.abs(rb["out"] - full["out"]).max(), np.abs(rb["demand"] - full["demand"]).max(),
+                    np.abs(rb["rowsum"] - full["rowsum"]).max(), np.abs(rb["lse"] - full["lse"]).max())
+    part = od.dilution_forward_rowblocked_head(q, k, v, 0.9, 1e-6, rows=30, block=8)
+    worst = max(worst, np.abs(part["out"] - full["out"][:30]).max())
+    return worst
+
+
+def pin_lse(T=17, d=8, seed=12, tau=0.7):
+    """lse_i is log(sum_k<=i exp(s_ik)) computed by scipy's logsumexp."""
+    from scipy.special import logsumexp
+    q, k, v = _rand(T, d, seed)
+    r = od.dilution_forward_head(q, k, v, tau, 1e-6)
+    s = tau / math.sqrt(d) * (q @ k.T)
+    ref = np.array([logsumexp(s[i, :i + 1]) for i in range(T)])
+    return np.abs(r["lse"] - ref).max()
+
+
+def pin_backward_fd(T=16, d=6, seed=13, tau=0.9, eps=1e-3, h=1e-6):
+    """Central finite differences of L = sum(dout * out) in float64."""
+    q, k, v = _rand(T, d, seed, dv=5)
+    g = np.random.default_rng(seed + 1).standard_normal((T, 5))
+    dq, dk, dv = od.dilution_backward_head(q, k, v, g, tau, eps)
+
+    def L(qq, kk, vv):
+        return float(np.sum(g * od.dilution_forward_head(qq, kk, vv, tau, eps)["out"]))
+
+    worst = 0.0
+    for X, dX, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(*X.shape):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += h
+            Xm[idx] -= h
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which], args_m[which] = Xp, Xm
+            num[idx] = (L(*args_p) - L(*args_m)) / (2 * h)
+        worst = max(worst, np.abs(num - dX).max() / max(1.0, np.abs(num).max()))
+    return worst
+
+
+def pin_backward_autograd(T=24, d=8, seed=14, tau=1.1, eps=1e-6):
+    """float64 torch autograd through a torch statement of the forward."""
+    torch = pytest.importorskip("torch")
+    q, k, v = _rand(T, d, seed, q_std=1.5)
+    g = np.random.default_rng(seed + 1).standard_normal((T, d))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    s = (tau / math.sqrt(d)) * tq @ tk.T
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    p = torch.softmax(s.masked_fill(~mask, float("-inf")), dim=1)
+    committed = torch.cumsum(p, dim=0) - p
+    share = p / (committed + p + eps)
+    out = share / share.sum(dim=1, keepdim=True) @ tv
+    (out * torch.tensor(g)).sum().backward()
+    dq, dk, dv = od.dilution_backward_head(q, k, v, g, tau, eps)
+    return max(np.abs(tq.grad.numpy() - dq).max(), np.abs(tk.grad.numpy() - dk).max(),
+               np.abs(tv.grad.numpy() - dv).max())
+
+
+FORWARD_PINS = [
+    (pin_uniform_bids_harmonic, 1e-12),
+    (pin_equal_keys_harmonic, 1e-12),
+    (pin_first_rows, 1e-12),
+    (pin_single_token, 1e-15),
+    (pin_invariants, 1e-11),
+    (pin_brute_force, 1e-12),
+    (pin_large_eps_softmax_limit, 1e-9),
+    (pin_decode_equals_prefill, 1e-12),
+    (pin_rowblocked, 1e-12),
+    (pin_lse, 1e-12),
+]
+
+
+# ---------------------------------------------------------------------------
+# Tests
+# ---------------------------------------------------------------------------
+def test_yarn_table_reproduced():
+    assert pin_yarn_table() < 1e-9
+
+
+def test_yarn_value_for_eightfold_extension():
+    # sqrt(0.1 ln 8 + 1), the logit multiplier for the 128K prefill workload.
+    assert abs(od.yarn_tau(8) - 1.0990651) < 1e-7
+
+
+@pytest.mark.parametrize("pin,tol", FORWARD_PINS, ids=[f.__name__ for f, _ in FORWARD_PINS])
+def test_forward_pin(pin, tol):
+    assert pin() < tol
+
+
+def test_tau_zero_matches_q_zero():
+    q, k, v = _rand(15, 8, 20)
+    a = od.dilution_forward_head(q, k, v, 0.0, 1e-6)["out"]
+    b = od.dilution_forward_head(np.zeros_like(q), k, v, 1.0, 1e-6)["out"]
+    assert np.abs(a - b).max() < 1e-14
+
+
+def test_invariants_many_shapes():
+    for T, tau, q_std in ((2, 1.0, 1.0), (3, 2.5, 1.5), (64, 1.0, 1.5), (129, 0.5, 3.0)):
+        assert pin_invariants(T=T, tau=tau, q_std=q_std, seed=T) < 1e-10
+
+
+def test_eps_must_be_positive():
+    q, k, v = _rand(4, 4, 0)
+    with pytest.raises(ValueError):
+        od.dilution_forward_head(q, k, v, 1.0, 0.0)
+
+
+def test_batched_matches_per_head():
+    rng = np.random.default_rng(21)
+    q, k, v = (rng.standard_normal((2, 3, 10, 4)) for _ in range(3))
+    r = od.dilution_forward(q, k, v, 1.0, 1e-6)
+    for b in range(2):
+        for h in range(3):
+            rh = od.dilution_forward_head(q[b, h], k[b, h], v[b, h], 1.0, 1e-6)
+            assert np.array_equal(r["out"][b, h], rh["out"])
+    out, dn = od.dilution_decode_step(q[:, :, 0], k[:, :, 0], v[:, :, 0], k, v, np.zeros((2, 3, 10)), 0)
+    assert np.allclose(out, v[:, :, 0])
+
+
+def test_backward_finite_differences():
+    assert pin_backward_fd() < 1e-7
+
+
+def test_backward_autograd():
+    assert pin_backward_autograd() < 1e-10
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each must make at least one pin fail.
+# ---------------------------------------------------------------------------
+def _inclusive_cumsum(p):
+    return np.cumsum(p, axis=0)
+
+
+def _cumsum_along_keys(p):
+    c = np.zeros_like(p)
+    c[:, 1:] = np.cumsum(p, axis=1)[:, :-1]
+    return c
+
+
+def _softmax_without_diagonal(s):
+    T = s.shape[0]
+    mask = np.tril(np.ones((T, T), dtype=bool), -1)
+    mask[0, 0] = True
+    z = np.where(mask, s, -np.inf)
+    e = np.where(mask, np.exp(z - z.max(axis=1, keepdims=True)), 0.0)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def _softmax_unmasked(s):
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
+MUTANTS = {
+    "inclusive_cumsum": ("_exclusive_cumsum_cols", _inclusive_cumsum),
+    "cumsum_along_keys": ("_exclusive_cumsum_cols", _cumsum_along_keys),
+    "no_diagonal_in_mask": ("_causal_softmax", _softmax_without_diagonal),
+    "no_causal_mask": ("_causal_softmax", _softmax_unmasked),
+    "scale_not_sqrt_d": ("logit_scale", lambda d, tau: tau / d),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name, monkeypatch):
+    attr, bad = MUTANTS[name]
+    monkeypatch.setattr(od, attr, bad)
+    failed = []
+    for pin, tol in FORWARD_PINS:
+        try:
+            ok = pin() < tol
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_planted_backward_mistake_is_caught(monkeypatch):
+    # Dropping the demand that later queries place on a key from the backward.
+    monkeypatch.setattr(od, "_reverse_exclusive_cumsum_cols", lambda x: np.zeros_like(x))
+    assert pin_backward_fd() > 1e-4
