@@ -1,0 +1,149 @@
+/*
+ * dilution_attn.h -- C ABI of the GB300 (sm_103a) dilution-attention library.
+ *
+ * The operator ("DilutionAttention v0.1.0 · results", section "The operator"):
+ * for every (batch b, head h) independently, with queries i and keys k,
+ *
+ *     s_ik      = tau * (q_i . k_k) / sqrt(d)                    (k <= i only)
+ *     p_ik      = exp(s_ik) / sum_{k' <= i} exp(s_ik')           causal softmax: the bids
+ *     committed = sum_{j < i} p_jk                               demand from earlier queries
+ *     share_ik  = p_ik / (committed_ik + p_ik + eps)
+ *     out_i     = sum_k share_ik v_k / sum_k share_ik             A = share / rowsum(share)
+ *
+ * tau is a logit multiplier (1 by default).  A focal temperature t
+ * ("Focal Attention", arXiv 2511.06818, section "Transformer with Constant
+ * Temperature", eq. focal-const) is tau = 1/t; YaRN's sharpening
+ * ("YaRN › Attention Temperature Scaling", temperature formula) is
+ * tau = sqrt(0.1 ln s + 1).
+ *
+ * Conventions shared by every entry point
+ *   - Layout: q, k, v, out are contiguous [B, H, T, d] (d fastest); per-row
+ *     vectors (lse2, rowsum, demand) are contiguous [B, H, T].
+ *   - Pointers are DEVICE pointers unless stated otherwise, 16-byte aligned.
+ *     The caller owns every buffer; the library allocates nothing and keeps
+ *     no state between calls.  Scratch memory is the caller's workspace.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Compute
+ *     calls are asynchronous: argument errors are returned synchronously
+ *     before anything is enqueued; kernel-side errors (a bounded wait that
+ *     timed out) are written to a status word at the start of the workspace
+ *     and read back with dilution_attn_get_error().
+ *   - Supported: d == 64; dtype DA_F32 (fp32 in/out, fp32 SIMT arithmetic)
+ *     or DA_BF16 (bf16 in/out, bf16 tensor-core products, fp32 accumulation
+ *     and fp32 softmax/demand arithmetic).  tau >= 0 and finite; eps > 0 and
+ *     finite (eps = 0 would make masked and underflowed entries 0/0).
+ *     B, H, T >= 0; a call with B*H*T == 0 does nothing and returns DA_OK.
+ *     T <= DA_MAX_T.
+ */
+#ifndef DILUTION_ATTN_H
+#define DILUTION_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every call. */
+#define DA_OK              0
+#define DA_ERR_INVALID     1   /* bad argument: null/misaligned pointer, negative size, eps <= 0, ... */
+#define DA_ERR_UNSUPPORTED 2   /* valid but not implemented: d != 64, T > DA_MAX_T, ...          */
+#define DA_ERR_CUDA        3   /* a CUDA runtime call failed (launch, tensor-map encode, copy)   */
+#define DA_ERR_TIMEOUT     4   /* a kernel's bounded wait expired; results are not valid         */
+#define DA_ERR_WORKSPACE   5   /* workspace pointer null or smaller than the *_workspace_size    */
+
+/* Element types. */
+#define DA_F32  0
+#define DA_BF16 1
+
+#define DA_MAX_T (1 << 24)
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *dilution_attn_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int dilution_attn_version(void);
+
+/* ------------------------------------------------------------------------
+ * Prefill forward.
+ *
+ * Computes out for all T queries of each (b, h) (the operator above), plus
+ * optional per-row side outputs:
+ *   lse2_out   [B,H,T] fp32, nullable: log2 of the softmax normaliser of the
+ *              scaled logits, log2(sum_{k<=i} 2^(s_ik * log2 e)); the bid is
+ *              p_ik = 2^(s_ik*log2 e - lse2_i).
+ *   rowsum_out [B,H,T] fp32, nullable: sum_k share_ik (before renormalising).
+ *   demand_out [B,H,T] fp32, nullable: column totals sum_i p_ik over all T
+ *              queries -- the decode demand cache after prefill
+ *              ("DilutionAttention v0.1.0 · results", section "The operator",
+ *              cached decoding).
+ * workspace: device scratch of at least dilution_attn_fwd_workspace_size()
+ * bytes; its first 256 bytes hold the status word.  Every call overwrites the
+ * workspace, so concurrent calls on different streams need distinct
+ * workspaces.  Errors: DA_ERR_INVALID, DA_ERR_UNSUPPORTED, DA_ERR_WORKSPACE,
+ * DA_ERR_CUDA (launch failure).
+ * ---------------------------------------------------------------------- */
+size_t dilution_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype);
+
+int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                      float *lse2_out, float *rowsum_out, float *demand_out,
+                      int B, int H, int T, int d, float tau, float eps, int dtype,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Cached decode step ("DilutionAttention v0.1.0 · results", section "The
+ * operator": the ordinary key/value cache plus one running demand total per
+ * key and head).
+ *
+ * For each (b, h): the cache holds keys/values 0 .. n_ctx-1 in
+ * k_cache/v_cache [B,H,T_cap,d] and their demand totals in demand
+ * [B,H,T_cap] (fp32; sum of every bid each key has received so far).  The
+ * step
+ *   1. writes k_new/v_new [B,H,d] to position n_ctx of the caches,
+ *   2. forms the bids p_k of q_new [B,H,d] over keys 0 .. n_ctx (causal
+ *      softmax of the scaled logits),
+ *   3. share_k = p_k / (demand_k + p_k + eps), with demand_{n_ctx} = 0,
+ *   4. out [B,H,d] = sum_k share_k v_k / sum_k share_k,
+ *   5. demand_k += p_k for k <= n_ctx (in place; demand_{n_ctx} = p_{n_ctx}).
+ * Requires 0 <= n_ctx < T_cap.  After the call the cache holds n_ctx + 1
+ * tokens.  dtype applies to q/k/v/out and the caches (DA_BF16 only).
+ * workspace: at least dilution_attn_decode_workspace_size(B,H,T_cap,d).
+ * ---------------------------------------------------------------------- */
+size_t dilution_attn_decode_workspace_size(int B, int H, int T_cap, int d);
+
+int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, float *demand,
+                              int n_ctx, int T_cap, void *out,
+                              int B, int H, int d, float tau, float eps, int dtype,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Synchronises `stream`, reads the status word that kernels of the last call
+ * on `workspace` may have set, clears it and returns it (DA_OK if none).
+ * Returns DA_ERR_CUDA if the synchronisation or the copy fails.
+ * ---------------------------------------------------------------------- */
+int dilution_attn_get_error(void *workspace, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host-only introspection of integer artefacts (no GPU needed).
+ *
+ * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's
+ * kernels for a problem of BH = B*H heads and T tokens.  kernel = 0 (row
+ * statistics) or 1 (demand sweep).  For each CTA index c (in launch order),
+ * writes 4 int32 to out[4c..4c+3]: head index, first query tile, number of
+ * query tiles (row stats: the query tiles it owns; sweep: the query tiles it
+ * walks), first key (sweep) or 0.  Returns the number of CTAs; if cap (in
+ * int32 elements) is too small, writes nothing and returns -(needed).
+ *
+ * dilution_attn_debug_tile_mask: the causal mask the kernels apply to the
+ * 128 x 128 tile (query tile qt, key tile kt) of a T-token head: out[r*128+c]
+ * = 1 if query qt*128+r may see key kt*128+c (key <= query < T), else 0.
+ * ---------------------------------------------------------------------- */
+int dilution_attn_debug_tile_schedule(int BH, int T, int kernel, int32_t *out, size_t cap);
+int dilution_attn_debug_tile_mask(int T, int qt, int kt, uint8_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DILUTION_ATTN_H */

@@ -1,0 +1,167 @@
+// C ABI of the dilution-attention library: argument validation, workspace
+// layout, dispatch to the kernels, status reporting and host-only debug
+// exports of the integer artefacts (tile schedules, causal mask).
+#include <cmath>
+#include <cstring>
+
+#include <cuda_bf16.h>
+
+#include "da_internal.h"
+
+namespace da {
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
+                           float *rowsum_out, float *demand_out, int BH, int T, float c2, float eps,
+                           float *lse2_ws, float *acc, cudaStream_t stream);
+int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
+                    float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
+                    cudaStream_t stream);
+cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                          float *demand, int n_ctx, int T_cap, void *out, int BH, float c2, float eps, int dtype,
+                          float *logits, float2 *part_ml, float *part_acc, int nchunk, cudaStream_t stream);
+}  // namespace da
+
+using namespace da;
+
+namespace {
+
+constexpr double kLog2e = 1.4426950408889634;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned16_or_null(const void *p) { return p == nullptr || aligned16(p); }
+
+// Scale applied to q.k in the log2 domain: tau / sqrt(d) * log2(e).
+float logit_scale_log2(float tau, int d) { return (float)((double)tau / std::sqrt((double)d) * kLog2e); }
+
+int check_common(int B, int H, int T, int d, float tau, float eps, int dtype) {
+  if (B < 0 || H < 0 || T < 0) return DA_ERR_INVALID;
+  if (!std::isfinite(tau) || tau < 0.f) return DA_ERR_INVALID;
+  if (!std::isfinite(eps) || eps <= 0.f) return DA_ERR_INVALID;
+  if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_INVALID;
+  if (d != kD) return DA_ERR_UNSUPPORTED;
+  if (T > DA_MAX_T) return DA_ERR_UNSUPPORTED;
+  if ((int64_t)B * H > (1 << 24)) return DA_ERR_UNSUPPORTED;
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dilution_attn_status_string(int status) {
+  switch (status) {
+    case DA_OK: return "DA_OK";
+    case DA_ERR_INVALID: return "DA_ERR_INVALID: invalid argument";
+    case DA_ERR_UNSUPPORTED: return "DA_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case DA_ERR_CUDA: return "DA_ERR_CUDA: CUDA runtime call failed";
+    case DA_ERR_TIMEOUT: return "DA_ERR_TIMEOUT: a kernel wait timed out";
+    case DA_ERR_WORKSPACE: return "DA_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int dilution_attn_version(void) { return 100; }
+
+size_t dilution_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype) {
+  (void)d;
+  (void)dtype;
+  if (B < 0 || H < 0 || T < 0) return 0;
+  return fwd_workspace_layout((int64_t)B * H, T).total;
+}
+
+int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
+                      float *demand_out, int B, int H, int T, int d, float tau, float eps, int dtype,
+                      void *workspace, size_t workspace_bytes, void *stream_) {
+  int st = check_common(B, H, T, d, tau, eps, dtype);
+  if (st != DA_OK) return st;
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0 || T == 0) return DA_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return DA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DA_ERR_INVALID;
+  if (!aligned16_or_null(lse2_out) || !aligned16_or_null(rowsum_out) || !aligned16_or_null(demand_out))
+    return DA_ERR_INVALID;
+  const FwdWorkspace L = fwd_workspace_layout(BH, T);
+  if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  float *lse2_ws = reinterpret_cast<float *>(ws + L.lse2_off);
+  float *acc = reinterpret_cast<float *>(ws + L.acc_off);
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
+  const float c2 = logit_scale_log2(tau, d);
+  if (dtype == DA_F32) {
+    if (launch_fwd_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse2_out, rowsum_out,
+                       demand_out, (int)BH, T, c2, eps, lse2_ws, acc, stream) != cudaSuccess)
+      return DA_ERR_CUDA;
+    return DA_OK;
+  }
+  return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, c2, eps, lse2_ws, acc, status,
+                         stream);
+}
+
+size_t dilution_attn_decode_workspace_size(int B, int H, int T_cap, int d) {
+  (void)d;
+  if (B < 0 || H < 0 || T_cap < 0) return 0;
+  return dec_workspace_layout((int64_t)B * H, T_cap).total;
+}
+
+int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
+                              void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
+                              float tau, float eps, int dtype, void *workspace, size_t workspace_bytes,
+                              void *stream_) {
+  int st = check_common(B, H, T_cap, d, tau, eps, dtype);
+  if (st != DA_OK) return st;
+  if (n_ctx < 0 || n_ctx >= T_cap) return DA_ERR_INVALID;
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0) return DA_OK;
+  const void *ptrs[] = {q_new, k_new, v_new, k_cache, v_cache, demand, out};
+  for (const void *p : ptrs)
+    if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
+  const DecWorkspace L = dec_workspace_layout(BH, T_cap);
+  if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
+  if (launch_decode(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, (int)BH,
+                    logit_scale_log2(tau, d), eps, dtype, reinterpret_cast<float *>(ws + L.logit_off),
+                    reinterpret_cast<float2 *>(ws + L.ml_off), reinterpret_cast<float *>(ws + L.acc_off), L.nchunk,
+                    stream) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+int dilution_attn_get_error(void *workspace, void *stream_) {
+  if (workspace == nullptr) return DA_ERR_INVALID;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int host = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaMemcpy(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+  if (host != DA_OK && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return DA_ERR_CUDA;
+  return host;
+}
+
+int dilution_attn_debug_tile_schedule(int BH, int T, int kernel, int32_t *out, size_t cap) {
+  if (BH < 0 || T < 0 || (kernel != 0 && kernel != 1)) return -1;
+  if (BH == 0 || T == 0) return 0;
+  const int n = (kernel == 0) ? rowstats_num_ctas(BH, T) : sweep_num_ctas(BH, T);
+  if (out == nullptr || cap < (size_t)n * 4) return -n;
+  for (int c = 0; c < n; ++c) {
+    const TileWork w = (kernel == 0) ? rowstats_work(c, BH, T) : sweep_work(c, BH, T);
+    out[4 * c + 0] = w.bh;
+    out[4 * c + 1] = w.q_tile0;
+    out[4 * c + 2] = w.n_q_tiles;
+    out[4 * c + 3] = w.key0;
+  }
+  return n;
+}
+
+int dilution_attn_debug_tile_mask(int T, int qt, int kt, uint8_t *out) {
+  if (T < 0 || qt < 0 || kt < 0 || out == nullptr) return DA_ERR_INVALID;
+  for (int r = 0; r < kTile; ++r)
+    for (int c = 0; c < kTile; ++c)
+      out[r * kTile + c] = visible((int64_t)qt * kTile + r, (int64_t)kt * kTile + c, T) ? 1 : 0;
+  return DA_OK;
+}
+
+}  // extern "C"

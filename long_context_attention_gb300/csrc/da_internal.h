@@ -1,0 +1,109 @@
+// Internal constants, workspace layout and tile schedules shared by the
+// host-side C ABI and the kernels.  Host and device evaluate the same
+// schedule functions, so the debug export reproduces the kernels' order.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dilution_attn.h"
+
+#if defined(__CUDACC__)
+#define DA_HD __host__ __device__ __forceinline__
+#else
+#define DA_HD inline
+#endif
+
+namespace da {
+
+constexpr int kD = 64;             // head dimension handled by every kernel
+constexpr int kTile = 128;         // query / key tile edge (one TMEM lane per row)
+constexpr int kSpan = 256;         // keys owned by one demand-sweep CTA (two key tiles)
+constexpr int kAccStride = 68;     // fp32 per accumulator row: 64 numerator + rowsum + 3 pad
+constexpr size_t kStatusBytes = 256;
+
+DA_HD int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+DA_HD int64_t t_pad(int64_t T) { return round_up(T, kSpan); }
+
+// ---------------------------------------------------------------------------
+// Workspace of the forward: [status | lse2 [BH][Tp] | acc [BH][Tp][68]].
+// Padded rows (T <= row < Tp) carry lse2 = +inf so their bids are exactly 0.
+// ---------------------------------------------------------------------------
+struct FwdWorkspace {
+  size_t lse2_off, acc_off, total;
+};
+
+DA_HD FwdWorkspace fwd_workspace_layout(int64_t BH, int64_t T) {
+  FwdWorkspace w;
+  const int64_t Tp = t_pad(T);
+  w.lse2_off = kStatusBytes;
+  w.acc_off = (size_t)round_up((int64_t)w.lse2_off + BH * Tp * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.acc_off + BH * Tp * kAccStride * 4, 256);
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// Decode workspace: [status | logits [BH][T_cap] | part_ml [BH][nchunk][2] |
+//                    part_acc [BH][nchunk][68]]
+// ---------------------------------------------------------------------------
+constexpr int kDecChunk = 4096;    // keys per decode CTA
+
+struct DecWorkspace {
+  size_t logit_off, ml_off, acc_off, total;
+  int nchunk;
+};
+
+DA_HD DecWorkspace dec_workspace_layout(int64_t BH, int64_t T_cap) {
+  DecWorkspace w;
+  w.nchunk = (int)((T_cap + kDecChunk - 1) / kDecChunk);
+  w.logit_off = kStatusBytes;
+  w.ml_off = (size_t)round_up((int64_t)w.logit_off + BH * T_cap * 4, 256);
+  w.acc_off = (size_t)round_up((int64_t)w.ml_off + BH * w.nchunk * 2 * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.acc_off + BH * w.nchunk * kAccStride * 4, 256);
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// Tile schedules (bf16 forward).  Launch order puts the CTAs with the most
+// causal work first so the hardware block scheduler approximates
+// longest-processing-time-first across the 152 SMs.
+// ---------------------------------------------------------------------------
+struct TileWork {
+  int bh, q_tile0, n_q_tiles, key0;
+};
+
+// Row statistics: one CTA per pair of query tiles (2 x 128 rows).
+DA_HD int rowstats_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / (2 * kTile)); }
+DA_HD TileWork rowstats_work(int cta, int BH, int64_t T) {
+  const int npairs = (int)(t_pad(T) / (2 * kTile));
+  TileWork w;
+  w.bh = cta % BH;
+  const int pair = npairs - 1 - cta / BH;   // the last pair sees the most keys
+  w.q_tile0 = 2 * pair;
+  w.n_q_tiles = 2;
+  w.key0 = 0;
+  return w;
+}
+
+// Demand sweep: one CTA per span of 256 keys, walking query tiles from the
+// span's diagonal tile to the last tile.
+DA_HD int sweep_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / kSpan); }
+DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
+  const int nqt = (int)(t_pad(T) / kTile);
+  TileWork w;
+  w.bh = cta % BH;
+  const int span = cta / BH;                 // span 0 walks every query tile
+  w.key0 = span * kSpan;
+  w.q_tile0 = span * (kSpan / kTile);
+  w.n_q_tiles = nqt - w.q_tile0;
+  return w;
+}
+
+// Causal mask predicate used by every kernel: query i sees key k iff k <= i
+// and i < T ("DilutionAttention v0.1.0 · results", section "The operator":
+// causal softmax, diagonal included).
+DA_HD bool visible(int64_t i, int64_t k, int64_t T) { return k <= i && i < T; }
+
+}  // namespace da

@@ -1,0 +1,279 @@
+// Cached decode step of dilution attention ("DilutionAttention v0.1.0 ·
+// results", section "The operator": the key/value cache plus one running
+// demand total per key and head).
+//
+// A share needs the new query's softmax normaliser before it can be formed,
+// so the step has two streaming phases separated by kernel boundaries (no
+// cross-CTA spinning):
+//   dec_logits  : x_k = (q . k_k) * tau/sqrt(d) * log2(e) for k <= n_ctx, written
+//                 to a logit scratch, plus one (max, sum 2^(x - max)) per chunk.
+//                 The chunk holding position n_ctx also appends k_new / v_new.
+//   dec_update  : lse2 from the chunk partials; p_k = 2^(x_k - lse2);
+//                 share_k = p_k / (D_k + p_k + eps) with D_{n_ctx} = 0;
+//                 D_k += p_k in place; per-chunk sum_k share_k v_k and sum_k share_k.
+//   dec_combine : out = sum of chunk numerators / sum of chunk row sums
+//                 (fixed order: deterministic).
+// Memory: K, V bf16 rows are read once each with 16-byte vector loads (8 lanes
+// per 128-byte row), the demand is read and written once; the fp32 logit
+// scratch (4 B per key) stays mostly in L2.
+#include "da_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace da {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecUnroll = 4;                       // keys per 8-lane group per round
+
+template <typename E>
+struct Vec16;   // 16 bytes of one row: 8 bf16 or 4 fp32 elements
+
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void to_float(const uint4 &u, float *f) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void to_float(const uint4 &u, float *f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Lanes per row: a row of d = 64 elements is 128 B (bf16) or 256 B (fp32).
+template <typename E>
+constexpr int lanes_per_row() {
+  return kD / Vec16<E>::N;
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kDecThreads)
+    dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
+               E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
+               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, float c2) {
+  constexpr int LPR = lanes_per_row<E>();          // lanes cooperating on one key
+  constexpr int NV = Vec16<E>::N;
+  constexpr int KPR = kDecThreads / LPR;           // keys per round
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int sub = tid % LPR;                       // which 16-byte piece of the row
+  const int grp = tid / LPR;
+  const int n_keys = n_ctx + 1;
+  const int k_begin = chunk * kDecChunk;
+  const int k_end = min(k_begin + kDecChunk, n_keys);
+
+  float qf[NV];
+  Vec16<E>::to_float(*reinterpret_cast<const uint4 *>(q_new + (size_t)bh * kD + sub * NV), qf);
+  const E *kb = k_cache + (size_t)bh * T_cap * kD;
+  float m = -INFINITY, l = 0.f;
+  // Warp-uniform trip count: every lane runs every round (the shuffles below
+  // need the full warp); keys past the chunk are predicated off.
+  for (int r0 = k_begin; r0 < k_end; r0 += KPR * kDecUnroll) {
+    const int k0 = r0 + grp;
+    uint4 raw[kDecUnroll];
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int key = k0 + u * KPR;
+      if (key < k_end) {
+        const E *src = (key == n_ctx) ? k_new + (size_t)bh * kD : kb + (size_t)key * kD;
+        raw[u] = ld_stream(src + sub * NV);
+      } else {
+        raw[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int key = k0 + u * KPR;
+      float kf[NV];
+      Vec16<E>::to_float(raw[u], kf);
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) s = fmaf(qf[i], kf[i], s);
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (key < k_end) {
+        const float x = s * c2;
+        if (sub == 0) logits[(size_t)bh * T_cap + key] = x;
+        if (x > m) {
+          l = l * exp2f(m - x) + 1.f;
+          m = x;
+        } else {
+          l += exp2f(x - m);
+        }
+      }
+    }
+  }
+  // Append the new key/value at position n_ctx (done by the chunk holding it).
+  if (n_ctx >= k_begin && n_ctx < k_begin + kDecChunk && tid < 2 * LPR) {
+    const E *src = (tid < LPR) ? k_new : v_new;
+    E *dst = (tid < LPR) ? k_cache : v_cache;
+    const int piece = tid % LPR;
+    *reinterpret_cast<uint4 *>(dst + ((size_t)bh * T_cap + n_ctx) * kD + piece * NV) =
+        *reinterpret_cast<const uint4 *>(src + (size_t)bh * kD + piece * NV);
+  }
+  // Block reduction of (m, l): only lane sub == 0 of each group holds data.
+  __shared__ float sm[kDecThreads], sl[kDecThreads];
+  sm[tid] = (sub == 0) ? m : -INFINITY;
+  sl[tid] = (sub == 0) ? l : 0.f;
+  __syncthreads();
+  for (int stride = kDecThreads / 2; stride > 0; stride >>= 1) {
+    if (tid < stride) {
+      const float m1 = sm[tid], m2 = sm[tid + stride];
+      const float mx = fmaxf(m1, m2);
+      float ls = 0.f;
+      if (mx != -INFINITY) ls = sl[tid] * exp2f(m1 - mx) + sl[tid + stride] * exp2f(m2 - mx);
+      sm[tid] = mx;
+      sl[tid] = ls;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) part_ml[(size_t)bh * nchunk + chunk] = make_float2(sm[0], sl[0]);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kDecThreads)
+    dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
+               float *__restrict__ demand, float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
+               int nchunk_used, float eps) {
+  constexpr int LPR = lanes_per_row<E>();
+  constexpr int NV = Vec16<E>::N;
+  constexpr int KPR = kDecThreads / LPR;
+  const int bh = blockIdx.y, chunk = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int sub = tid % LPR, grp = tid / LPR;
+  __shared__ float s_lse2;
+  if (tid < 32) {
+    // Combine the per-chunk (max, sum) pairs of this head into lse2.
+    float m = -INFINITY, l = 0.f;
+    for (int c = tid; c < nchunk_used; c += 32) {
+      const float2 ml = part_ml[(size_t)bh * nchunk + c];
+      if (ml.x == -INFINITY) continue;
+      const float mx = fmaxf(m, ml.x);
+      l = l * exp2f(m - mx) + ml.y * exp2f(ml.x - mx);
+      m = mx;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+      const float mx = fmaxf(m, m2);
+      if (mx != -INFINITY) {
+        l = l * exp2f(m - mx) + l2 * exp2f(m2 - mx);
+        m = mx;
+      }
+    }
+    if (tid == 0) s_lse2 = m + log2f(l);
+  }
+  __syncthreads();
+  const float lse2 = s_lse2;
+  const int k_begin = chunk * kDecChunk;
+  const int k_end = min(k_begin + kDecChunk, n_ctx + 1);
+  const E *vb = v_cache + (size_t)bh * T_cap * kD;
+  float num[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) num[i] = 0.f;
+  float rs = 0.f;
+  for (int r0 = k_begin; r0 < k_end; r0 += KPR * kDecUnroll) {
+    const int k0 = r0 + grp;
+    uint4 raw[kDecUnroll];
+    float x[kDecUnroll], dm[kDecUnroll];
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int key = k0 + u * KPR;
+      const bool ok = key < k_end;
+      raw[u] = ok ? ld_stream(vb + (size_t)key * kD + sub * NV) : make_uint4(0, 0, 0, 0);
+      x[u] = ok ? logits[(size_t)bh * T_cap + key] : -INFINITY;
+      dm[u] = (ok && key < n_ctx) ? demand[(size_t)bh * T_cap + key] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int key = k0 + u * KPR;
+      if (key >= k_end) continue;
+      const float p = exp2f(x[u] - lse2);
+      const float den = dm[u] + p + eps;
+      const float share = p / den;
+      if (sub == 0) demand[(size_t)bh * T_cap + key] = dm[u] + p;
+      float vf[NV];
+      Vec16<E>::to_float(raw[u], vf);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) num[i] = fmaf(share, vf[i], num[i]);
+      rs += share;
+    }
+  }
+  // Reduce the KPR key groups: partial rows [KPR][64 + 1] in shared memory.
+  __shared__ float sacc[KPR][kD + 1];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) sacc[grp][sub * NV + i] = num[i];
+  if (sub == 0) sacc[grp][kD] = rs;
+  __syncthreads();
+  if (tid <= kD) {
+    float a = 0.f;
+    for (int gi = 0; gi < KPR; ++gi) a += sacc[gi][tid];
+    part_acc[((size_t)bh * nchunk + chunk) * kAccStride + tid] = a;
+  }
+}
+
+template <typename E>
+__global__ void dec_combine(const float *__restrict__ part_acc, E *__restrict__ out, int nchunk, int nchunk_used) {
+  const int bh = blockIdx.x;
+  const int t = threadIdx.x;   // 0..63
+  float a = 0.f, rs = 0.f;
+  for (int c = 0; c < nchunk_used; ++c) {
+    const float *pa = part_acc + ((size_t)bh * nchunk + c) * kAccStride;
+    a += pa[t];
+    rs += pa[kD];
+  }
+  const float o = a / rs;
+  if constexpr (sizeof(E) == 4) {
+    out[(size_t)bh * kD + t] = o;
+  } else {
+    out[(size_t)bh * kD + t] = __float2bfloat16_rn(o);
+  }
+}
+
+template <typename E>
+static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
+                                   void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int BH, float c2,
+                                   float eps, float *logits, float2 *part_ml, float *part_acc, int nchunk,
+                                   cudaStream_t stream) {
+  const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
+  dec_logits<E><<<dim3(used, BH), kDecThreads, 0, stream>>>(
+      (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
+      T_cap, nchunk, c2);
+  dec_update<E><<<dim3(used, BH), kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc,
+                                                           n_ctx, T_cap, nchunk, used, eps);
+  dec_combine<E><<<BH, kD, 0, stream>>>(part_acc, (E *)out, nchunk, used);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                          float *demand, int n_ctx, int T_cap, void *out, int BH, float c2, float eps, int dtype,
+                          float *logits, float2 *part_ml, float *part_acc, int nchunk, cudaStream_t stream) {
+  if (dtype == DA_BF16)
+    return launch_decode_t<__nv_bfloat16>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, c2,
+                                          eps, logits, part_ml, part_acc, nchunk, stream);
+  return launch_decode_t<float>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, c2, eps,
+                                logits, part_ml, part_acc, nchunk, stream);
+}
+
+}  // namespace da

@@ -1,0 +1,592 @@
+// bf16 forward of dilution attention on sm_103a tensor cores.
+//
+// The operator ("DilutionAttention v0.1.0 · results", section "The
+// operator") needs every query row's softmax normaliser before any share can
+// be formed: share_ik = e_ik / (Z_i (committed_ik + eps) + e_ik) is not
+// linear in the normaliser Z_i, so a single online-softmax pass cannot
+// produce it.  The forward therefore runs two tensor-core passes over the
+// causal triangle plus a memory pass:
+//
+//  rowstats_kernel  (one CTA per pair of 128-row query tiles)
+//     S = Q K^T on tcgen05 (bf16 x bf16 -> fp32 in TMEM), K tiles streamed by
+//     TMA through a 4-stage ring; one thread per query row keeps an online
+//     max / sum and writes lse2_i = log2 sum_k 2^(x_ik), x = s * c2,
+//     c2 = tau / sqrt(d) * log2(e).  Also zeroes the rows of the fp32
+//     accumulator that the sweep adds into.
+//
+//  sweep_kernel  (one CTA per span of 256 keys, both tiles resident in smem)
+//     Walks the query tiles from the span's diagonal to the end, in causal
+//     order.  S^T = K Q^T puts keys on TMEM lanes, so each thread owns one key
+//     and carries that key's demand (committed + eps) in a register across
+//     query tiles: for each query column in order
+//         p = 2^(x - lse2),  den = committed + eps + p,
+//         share = p / den,   committed + eps <- den
+//     which is exactly the exclusive cumulative sum down the key column.  The
+//     shares (bf16) are written to shared memory as the MN-major A operand of
+//     a second tcgen05 product, share^T [V | 1]: TMEM columns 0..63 collect
+//     sum_k share_ik v_k and columns 64..79 sum_k share_ik (a constant all-ones
+//     B operand).  An epilogue warpgroup adds each query tile's partials into
+//     acc[row][0..64] with vector fp32 reductions in L2.
+//
+//  finalize (fwd_f32.cu) divides the numerator by the row sum.
+//
+// Warp specialisation, all waits bounded (timeout -> DA_ERR_TIMEOUT):
+//   rowstats: warps 0-3 / 4-7 = softmax-statistics warpgroups for the two
+//             query tiles, warp 8 = TMA producer, warp 9 = MMA issuer.
+//   sweep:    warps 0-3 / 4-7 = demand warpgroups (key tiles 0 / 1 of the
+//             span), warps 8-11 = epilogue, warp 12 = TMA, warp 13 = MMA.
+#include "da_internal.h"
+#include "da_ptx.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace da {
+
+constexpr uint32_t kTileBytes = kTile * kD * 2;   // one 128 x 64 bf16 tile, 128-byte swizzled rows
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  const uint32_t a = smem_u32(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Bounded wait that ignores the abort flag: used only to let copies and MMAs
+// that are already in flight land before a CTA that gave up exits.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 100ull * 1000ull * 1000ull) break;
+  }
+}
+
+// K-major operand tile: 128 rows x 64 bf16 (128-byte rows, 128B swizzle, as
+// TMA writes it).  8-row groups are 1024 bytes apart; a K step of 16
+// elements advances the start address by 32 bytes inside the swizzle atom.
+__device__ __forceinline__ uint64_t kmajor_desc(const uint8_t *tile, int kstep) {
+  return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
+}
+
+// ============================================================================
+// Row statistics
+// ============================================================================
+constexpr int kRsThreads = 320;
+constexpr int kRsKStages = 4;
+constexpr int kRsSmemBytes = (2 + kRsKStages) * kTileBytes + 256 + 1024;
+
+__global__ void __launch_bounds__(kRsThreads, 2)
+    rowstats_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    float *__restrict__ lse2, float *__restrict__ acc, int BH, int T, int Tp, float c2,
+                    int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sQ = smem;                    // 2 query tiles
+  uint8_t *sK = smem + 2 * kTileBytes;   // K ring
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + kRsKStages) * kTileBytes);
+  uint64_t *q_full = bars;
+  uint64_t *k_full = bars + 1;
+  uint64_t *k_empty = k_full + kRsKStages;
+  uint64_t *s_full = k_empty + kRsKStages;
+  uint64_t *s_free = s_full + 2;
+  uint64_t *drain = s_free + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const TileWork w = rowstats_work(blockIdx.x, BH, T);
+  const int n_kt = w.q_tile0 + 2;   // key tiles 0 .. last query tile
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kRsKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&s_free[g], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, status};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+      tma_load_3d(sQ, &tmQ, q_full, 0, w.q_tile0 * kTile, w.bh);
+      tma_load_3d(sQ + kTileBytes, &tmQ, q_full, 0, (w.q_tile0 + 1) * kTile, w.bh);
+      int issued = 0;
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int s = kt % kRsKStages;
+        if (!mbar_wait(&k_empty[s], ((kt / kRsKStages) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&k_full[s], kTileBytes);
+        tma_load_3d(sK + s * kTileBytes, &tmK, &k_full[s], 0, kt * kTile, w.bh);
+        ++issued;
+      }
+      if (*abort_flag) {
+        drain_wait(q_full, 0);
+        for (int kt = (issued > kRsKStages ? issued - kRsKStages : 0); kt < issued; ++kt)
+          drain_wait(&k_full[kt % kRsKStages], (kt / kRsKStages) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kTile, kTile, false, false);
+      uint32_t n_free[2] = {0, 0};
+      if (mbar_wait(q_full, 0, wc)) {
+        tc_fence_after();
+        for (int kt = 0; kt < n_kt; ++kt) {
+          const int s = kt % kRsKStages;
+          if (!mbar_wait(&k_full[s], (kt / kRsKStages) & 1, wc)) break;
+          tc_fence_after();
+          bool ok = true;
+          for (int g = 0; g < 2; ++g) {
+            if (kt > w.q_tile0 + g) continue;   // key tile entirely after this query tile
+            if (!mbar_wait(&s_free[g], (n_free[g] & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            ++n_free[g];
+            tc_fence_after();
+            const uint32_t d = tmem + g * kTile;
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_bf16(d, kmajor_desc(sQ + g * kTileBytes, kk), kmajor_desc(sK + s * kTileBytes, kk), idesc,
+                       kk > 0);
+            mma_commit(&s_full[g]);
+          }
+          if (!ok) break;
+          mma_commit(&k_empty[s]);
+        }
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else {
+    // ------------------------------------------- softmax statistics (2 WGs)
+    const int g = warp / 4;
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;
+    const int qt = w.q_tile0 + g;
+    const int64_t qi = (int64_t)qt * kTile + row;
+    float m = -INFINITY, l = 0.f;
+    const uint32_t tbase = tmem + g * kTile + ((uint32_t)(quarter * 32) << 16);
+    for (int kt = 0; kt <= qt; ++kt) {
+      if (!mbar_wait(&s_full[g], kt & 1, wc)) break;
+      tc_fence_after();
+      const bool diag = (kt == qt);
+#pragma unroll 1
+      for (int ch = 0; ch < kTile / 32; ++ch) {
+        float s[32];
+        tmem_ld32(tbase + ch * 32, s);
+        tmem_wait_ld();
+        if (ch == kTile / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[g]);
+        }
+        float mx = -INFINITY;
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (ch * 32 + c <= row) mx = fmaxf(mx, s[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, s[c]);
+        }
+        if (mx == -INFINITY) continue;   // every key of this chunk is masked
+        const float mn = fmaxf(m, mx * c2);
+        l *= ex2_approx(m - mn);
+        m = mn;
+        float acc0 = 0.f, acc1 = 0.f;
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            if (ch * 32 + c <= row) acc0 += ex2_approx(fmaf(s[c], c2, -m));
+            if (ch * 32 + c + 1 <= row) acc1 += ex2_approx(fmaf(s[c + 1], c2, -m));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            acc0 += ex2_approx(fmaf(s[c], c2, -m));
+            acc1 += ex2_approx(fmaf(s[c + 1], c2, -m));
+          }
+        }
+        l += acc0 + acc1;
+      }
+      if (*abort_flag) break;
+    }
+    if (qi < Tp) {
+      lse2[(size_t)w.bh * Tp + qi] = (qi < T) ? m + log2f(l) : INFINITY;
+      float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)w.bh * Tp + qi) * kAccStride);
+#pragma unroll
+      for (int t = 0; t < kAccStride / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ============================================================================
+// Demand sweep
+// ============================================================================
+constexpr int kSwThreads = 448;
+constexpr int kSwQStages = 3;
+constexpr uint32_t kShBytes = 2 * 16 * 1024;   // share^T tile: 2 M-blocks x 16 K-groups x 1024 B
+// Shared-memory map (offsets from the 1024-aligned base).
+constexpr uint32_t kSwOffK = 0;                                  // 2 key tiles (resident)
+constexpr uint32_t kSwOffV = kSwOffK + 2 * kTileBytes;           // 2 value tiles (resident)
+constexpr uint32_t kSwOffQ = kSwOffV + 2 * kTileBytes;           // query ring
+constexpr uint32_t kSwOffSh = kSwOffQ + kSwQStages * kTileBytes; // share^T, one per key tile
+constexpr uint32_t kSwOffOnes = kSwOffSh + 2 * kShBytes;         // 16 x 64 bf16 ones (2 KB)
+constexpr uint32_t kSwOffL = kSwOffOnes + 2048;                  // lse2 ring (512 B per stage)
+constexpr uint32_t kSwOffBar = kSwOffL + kSwQStages * 512;
+constexpr int kSwSmemBytes = kSwOffBar + 256 + 1024;
+
+constexpr uint32_t kTmemS = 0;      // S^T of key tile g at columns g*128 .. g*128+127
+constexpr uint32_t kTmemD = 256;    // partials of query tile t at 256 + (t&1)*128: 64 numerator + 16 rowsum
+
+__global__ void __launch_bounds__(kSwThreads, 1)
+    sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const float *__restrict__ lse2,
+                 float *__restrict__ acc, float *__restrict__ demand_out, int BH, int T, int Tp, float c2,
+                 float eps, int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sK = smem + kSwOffK;
+  uint8_t *sV = smem + kSwOffV;
+  uint8_t *sQ = smem + kSwOffQ;
+  uint8_t *sSh = smem + kSwOffSh;
+  uint8_t *sOnes = smem + kSwOffOnes;
+  const float *sL = reinterpret_cast<const float *>(smem + kSwOffL);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSwOffBar);
+  uint64_t *kv_full = bars;
+  uint64_t *q_full = bars + 1;
+  uint64_t *q_empty = q_full + kSwQStages;
+  uint64_t *s_full = q_empty + kSwQStages;
+  uint64_t *s_free = s_full + 2;
+  uint64_t *sh_full = s_free + 2;
+  uint64_t *sh_free = sh_full + 2;
+  uint64_t *d_full = sh_free + 2;
+  uint64_t *d_free = d_full + 2;
+  uint64_t *drain = d_free + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const TileWork w = sweep_work(blockIdx.x, BH, T);
+  const int nt = w.n_q_tiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < kSwQStages; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1 + 8);   // MMA commit + the 8 demand warps (done with lse2)
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&s_free[g], 4);
+      mbar_init(&sh_full[g], 4);
+      mbar_init(&sh_free[g], 1);
+      mbar_init(&d_full[g], 1);
+      mbar_init(&d_free[g], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Constant all-ones B operand for the share row sums.
+  for (int e = threadIdx.x; e < 2048 / 4; e += kSwThreads)
+    reinterpret_cast<uint32_t *>(sOnes)[e] = 0x3F803F80u;
+  fence_proxy_async_smem();
+  if (warp == 13) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, status};
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(kv_full, 4 * kTileBytes);
+      for (int g = 0; g < 2; ++g) {
+        tma_load_3d(sK + g * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
+        tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < nt; ++t) {
+        const int s = t % kSwQStages;
+        if (!mbar_wait(&q_empty[s], ((t / kSwQStages) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&q_full[s], kTileBytes + 512);
+        const int qrow = (w.q_tile0 + t) * kTile;
+        tma_load_3d(sQ + s * kTileBytes, &tmQ, &q_full[s], 0, qrow, w.bh);
+        bulk_load(smem + kSwOffL + s * 512, lse2 + (size_t)w.bh * Tp + qrow, 512, &q_full[s]);
+        ++issued;
+      }
+      if (*abort_flag) {
+        drain_wait(kv_full, 0);
+        for (int t = (issued > kSwQStages ? issued - kSwQStages : 0); t < issued; ++t)
+          drain_wait(&q_full[t % kSwQStages], (t / kSwQStages) & 1);
+      }
+    }
+  } else if (warp == 13) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(kTile, kTile, false, false);
+      const uint32_t idesc_pv = idesc_bf16(kTile, kD, true, true);
+      const uint32_t idesc_rs = idesc_bf16(kTile, 16, true, false);
+      const uint64_t ones_desc = smem_desc(smem_u32(sOnes), 16, 1024);
+      auto issue_s = [&](int t) -> bool {
+        const int s = t % kSwQStages;
+        if (!mbar_wait(&q_full[s], (t / kSwQStages) & 1, wc)) return false;
+        tc_fence_after();
+        for (int g = 0; g < 2; ++g) {
+          if (!mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_bf16(tmem + kTmemS + g * kTile, kmajor_desc(sK + g * kTileBytes, kk),
+                     kmajor_desc(sQ + s * kTileBytes, kk), idesc_s, kk > 0);
+          mma_commit(&s_full[g]);
+        }
+        mma_commit(&q_empty[s]);
+        return true;
+      };
+      auto issue_pv = [&](int t) -> bool {
+        const int b = t & 1;
+        if (!mbar_wait(&d_free[b], ((t >> 1) & 1) ^ 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t dcol = tmem + kTmemD + b * 128;
+        for (int g = 0; g < 2; ++g) {
+          if (!mbar_wait(&sh_full[g], t & 1, wc)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
+            const uint64_t a = smem_desc(smem_u32(sSh + g * kShBytes) + kk * 2048, 16384, 1024);
+            // V tile as an MN-major B operand: 8-key groups 1 KB apart; one 64-wide N block.
+            const uint64_t bv = smem_desc(smem_u32(sV + g * kTileBytes) + kk * 2048, 8192, 1024);
+            const uint32_t accum = (g > 0 || kk > 0) ? 1u : 0u;
+            mma_bf16(dcol, a, bv, idesc_pv, accum);
+            mma_bf16(dcol + kD, a, ones_desc, idesc_rs, accum);
+          }
+          mma_commit(&sh_free[g]);
+        }
+        mma_commit(&d_full[b]);
+        return true;
+      };
+      if (mbar_wait(kv_full, 0, wc)) {
+        tc_fence_after();
+        bool ok = issue_s(0);
+        for (int t = 0; ok && t < nt; ++t) {
+          if (t + 1 < nt) ok = issue_s(t + 1);
+          if (ok) ok = issue_pv(t);
+        }
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;
+    for (int t = 0; t < nt; ++t) {
+      const int b = t & 1;
+      if (!mbar_wait(&d_full[b], (t >> 1) & 1, wc)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + kTmemD + b * 128 + ((uint32_t)(quarter * 32) << 16);
+      float a0[32], a1[32], rs;
+      tmem_ld32(taddr, a0);
+      tmem_ld32(taddr + 32, a1);
+      tmem_ld1(taddr + kD, rs);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_free[b]);
+      const int64_t qi = (int64_t)(w.q_tile0 + t) * kTile + row;
+      if (qi < T) {
+        float *dst = acc + ((size_t)w.bh * Tp + qi) * kAccStride;
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) red_add_v4(dst + c, a0[c], a0[c + 1], a0[c + 2], a0[c + 3]);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) red_add_v4(dst + 32 + c, a1[c], a1[c + 1], a1[c + 2], a1[c + 3]);
+        atomicAdd(dst + kD, rs);
+      }
+    }
+  } else {
+    // -------------------------------------------- demand warpgroups (2 WGs)
+    const int g = warp / 4;
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;            // key row inside the key tile
+    const int kbase = w.key0 + g * kTile;           // first key of this warpgroup's tile
+    const uint32_t tbase = tmem + kTmemS + g * kTile + ((uint32_t)(quarter * 32) << 16);
+    uint8_t *sh_rows = sSh + g * kShBytes + (row / 8) * 1024 + (row % 8) * 128;
+    const int swz = row % 8;
+    float ceps = eps;   // committed + eps: demand this key received from earlier queries
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % kSwQStages;
+      const int j = w.q_tile0 + t;
+      const bool all_masked = kbase > j * kTile;    // every key after every query of the tile
+      const bool diag = kbase == j * kTile;
+      if (!mbar_wait(&q_full[s], (t / kSwQStages) & 1, wc)) break;
+      if (!mbar_wait(&s_full[g], t & 1, wc)) break;
+      tc_fence_after();
+      const float *lrow = sL + s * 128;
+      bool ok = true;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float sv[64];
+        tmem_ld32(tbase + h * 64, *reinterpret_cast<float(*)[32]>(&sv[0]));
+        tmem_ld32(tbase + h * 64 + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+        tmem_wait_ld();
+        if (h == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[g]);
+        }
+        uint32_t pk[32];
+        if (all_masked) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = 0u;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const int col = h * 64 + c;
+            float p0 = ex2_approx(fmaf(sv[c], c2, -lrow[col]));
+            float p1 = ex2_approx(fmaf(sv[c + 1], c2, -lrow[col + 1]));
+            if (diag) {
+              if (row > col) p0 = 0.f;
+              if (row > col + 1) p1 = 0.f;
+            }
+            const float d0 = ceps + p0;
+            const float sh0 = p0 * rcp_approx(d0);
+            const float d1 = d0 + p1;
+            const float sh1 = p1 * rcp_approx(d1);
+            ceps = d1;
+            pk[c / 2] = pack_bf16x2(sh0, sh1);
+          }
+        }
+        if (h == 0) {
+          // the product of the previous query tile must be done reading this buffer
+          if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+        }
+        uint8_t *dst = sh_rows + h * 16384;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4 *>(dst + ((c8 ^ swz) * 16)) =
+              make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+      }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh_full[g]);
+        mbar_arrive(&q_empty[s]);
+      }
+    }
+    const int64_t key = (int64_t)kbase + row;
+    if (demand_out != nullptr && key < T && !*abort_flag) demand_out[(size_t)w.bh * T + key] = ceps - eps;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================
+// Host side
+// ============================================================================
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// [BH, T, 64] bf16 viewed as a 3-D tensor; box = one 128-row tile of one head.
+// Rows past T read as zero.
+static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)T, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)T * kD * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)kTile, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bfloat16 *out, float *rowsum_out,
+                                 float *lse2_out, int BH, int T, cudaStream_t stream);
+
+int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
+                    float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
+                    cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  if (!make_tile_map(&tq, q, BH, T) || !make_tile_map(&tk, k, BH, T) || !make_tile_map(&tv, v, BH, T))
+    return DA_ERR_CUDA;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(rowstats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRsSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes) !=
+            cudaSuccess)
+      return DA_ERR_CUDA;
+    attr_done = true;
+  }
+  const int Tp = (int)t_pad(T);
+  rowstats_kernel<<<rowstats_num_ctas(BH, T), kRsThreads, kRsSmemBytes, stream>>>(tq, tk, lse2_ws, acc, BH, T,
+                                                                                  Tp, c2, status);
+  sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, lse2_ws, acc, demand_out,
+                                                                            BH, T, Tp, c2, eps, status);
+  if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
+  if (launch_finalize_bf16(acc, lse2_ws, reinterpret_cast<__nv_bfloat16 *>(out), rowsum_out, lse2_out, BH, T,
+                           stream) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+}  // namespace da

@@ -1,0 +1,197 @@
+// fp32 SIMT forward of dilution attention: the correctness anchor.
+//
+// Three steps per (batch, head), "DilutionAttention v0.1.0 · results",
+// section "The operator":
+//   1. f32_rowstats: the causal-softmax normaliser of every query row,
+//      lse2_i = log2 sum_{k<=i} 2^(x_ik), x = s * tau/sqrt(d) * log2(e).
+//   2. f32_sweep: one CTA per 128 keys, one thread per key.  Walking the
+//      queries in causal order, each thread keeps its key's demand from
+//      earlier queries (the exclusive column cumsum) in a register:
+//      p = 2^(x - lse2), share = p / (committed + p + eps), committed += p.
+//      The shares of 32 queries are staged in shared memory and multiplied
+//      by the CTA's 128 value rows; the partial numerators and share row
+//      sums are added (fp32 atomics) into the accumulator acc[row][0..64].
+//   3. finalize (shared with the bf16 path): out = acc[0:64] / acc[64].
+// No tensor cores: TF32 products would not hold the 1e-5 fp32 bound.
+#include "da_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace da {
+
+constexpr int kF32RowsPerCta = 64;
+constexpr int kF32KeysPerCta = 128;
+constexpr int kF32QChunk = 32;
+
+__global__ void __launch_bounds__(kF32RowsPerCta)
+    f32_rowstats(const float *__restrict__ q, const float *__restrict__ k, float *__restrict__ lse2,
+                 float *__restrict__ acc, int T, int Tp, float c2) {
+  __shared__ float sk[kF32RowsPerCta][kD];
+  const int bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int i = blockIdx.x * kF32RowsPerCta + tid;
+  const float *qb = q + (size_t)bh * T * kD;
+  const float *kb = k + (size_t)bh * T * kD;
+
+  float qr[kD];
+#pragma unroll
+  for (int t = 0; t < kD; ++t) qr[t] = (i < T) ? qb[(size_t)i * kD + t] : 0.f;
+
+  float m = -INFINITY, l = 0.f;
+  const int last_key = min(blockIdx.x * kF32RowsPerCta + kF32RowsPerCta - 1, T - 1);
+  for (int k0 = 0; k0 <= last_key; k0 += kF32RowsPerCta) {
+    __syncthreads();
+    const int kr = k0 + tid;
+#pragma unroll 4
+    for (int t = 0; t < kD; ++t) sk[tid][t] = (kr < T) ? kb[(size_t)kr * kD + t] : 0.f;
+    __syncthreads();
+    for (int kk = 0; kk < kF32RowsPerCta; ++kk) {
+      const int key = k0 + kk;
+      if (!visible(i, key, T)) continue;
+      float s = 0.f;
+#pragma unroll
+      for (int t = 0; t < kD; ++t) s = fmaf(qr[t], sk[kk][t], s);
+      const float x = s * c2;
+      if (x > m) {
+        l = l * exp2f(m - x) + 1.f;
+        m = x;
+      } else {
+        l += exp2f(x - m);
+      }
+    }
+  }
+  if (i < Tp) {
+    lse2[(size_t)bh * Tp + i] = (i < T) ? m + log2f(l) : INFINITY;
+    float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)bh * Tp + i) * kAccStride);
+#pragma unroll
+    for (int t = 0; t < kAccStride / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+struct F32SweepSmem {
+  float v[kF32KeysPerCta][kD];                 // value rows of this CTA's keys
+  float q[kF32QChunk][kD];                     // current query chunk
+  float l2[kF32QChunk];                        // its lse2
+  float sh[kF32QChunk][kF32KeysPerCta + 1];    // shares [query][key]
+};
+
+__global__ void __launch_bounds__(kF32KeysPerCta)
+    f32_sweep(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+              const float *__restrict__ lse2, float *__restrict__ acc, float *__restrict__ demand_out, int T,
+              int Tp, float c2, float eps) {
+  extern __shared__ float4 f32_smem_raw[];
+  F32SweepSmem &S = *reinterpret_cast<F32SweepSmem *>(f32_smem_raw);
+  const int bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int key0 = blockIdx.x * kF32KeysPerCta;
+  const int key = key0 + tid;
+  const float *qb = q + (size_t)bh * T * kD;
+  const float *kb = k + (size_t)bh * T * kD;
+  const float *vb = v + (size_t)bh * T * kD;
+
+  float kr[kD];
+#pragma unroll
+  for (int t = 0; t < kD; ++t) kr[t] = (key < T) ? kb[(size_t)key * kD + t] : 0.f;
+#pragma unroll 4
+  for (int t = 0; t < kD; ++t) S.v[tid][t] = (key < T) ? vb[(size_t)key * kD + t] : 0.f;
+
+  float committed = 0.f;   // sum of bids this key received from earlier queries
+  const int dv = tid % kD;
+  const int rhalf = tid / kD;
+  for (int q0 = key0; q0 < T; q0 += kF32QChunk) {
+    __syncthreads();
+    for (int e = tid; e < kF32QChunk * kD; e += kF32KeysPerCta) {
+      const int r = e / kD, t = e % kD;
+      S.q[r][t] = (q0 + r < T) ? qb[(size_t)(q0 + r) * kD + t] : 0.f;
+    }
+    if (tid < kF32QChunk) S.l2[tid] = lse2[(size_t)bh * Tp + q0 + tid];
+    __syncthreads();
+    for (int r = 0; r < kF32QChunk; ++r) {
+      const int i = q0 + r;
+      float share = 0.f;
+      if (visible(i, key, T)) {
+        float s = 0.f;
+#pragma unroll
+        for (int t = 0; t < kD; ++t) s = fmaf(S.q[r][t], kr[t], s);
+        const float p = exp2f(s * c2 - S.l2[r]);
+        share = p / ((committed + p) + eps);
+        committed += p;
+      }
+      S.sh[r][tid] = share;
+    }
+    __syncthreads();
+    // Partial numerators: thread (rhalf, dv) owns 16 query rows of column dv.
+    for (int rr = 0; rr < kF32QChunk / 2; ++rr) {
+      const int r = rhalf * (kF32QChunk / 2) + rr;
+      if (q0 + r >= T) break;
+      float a = 0.f;
+      for (int kk = 0; kk < kF32KeysPerCta; ++kk) a = fmaf(S.sh[r][kk], S.v[kk][dv], a);
+      atomicAdd(acc + ((size_t)bh * Tp + q0 + r) * kAccStride + dv, a);
+    }
+    if (tid < kF32QChunk && q0 + tid < T) {
+      float rs = 0.f;
+      for (int kk = 0; kk < kF32KeysPerCta; ++kk) rs += S.sh[tid][kk];
+      atomicAdd(acc + ((size_t)bh * Tp + q0 + tid) * kAccStride + kD, rs);
+    }
+  }
+  if (demand_out != nullptr && key < T) demand_out[(size_t)bh * T + key] = committed;
+}
+
+// out_i = acc_i[0:64] / acc_i[64]; optional rowsum and lse2 side outputs.
+// 16 threads per row, 4 columns each.
+template <typename OutT>
+__global__ void finalize_kernel(const float *__restrict__ acc, const float *__restrict__ lse2_ws,
+                                OutT *__restrict__ out, float *__restrict__ rowsum_out,
+                                float *__restrict__ lse2_out, int BH, int T, int Tp) {
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = g / 16;
+  const int part = (int)(g % 16);
+  if (row >= (int64_t)BH * T) return;
+  const int64_t bh = row / T, i = row % T;
+  const float *ar = acc + ((size_t)bh * Tp + i) * kAccStride;
+  const float rs = ar[kD];
+  const float inv = 1.f / rs;
+  const float4 a = reinterpret_cast<const float4 *>(ar)[part];
+  if constexpr (sizeof(OutT) == 4) {
+    reinterpret_cast<float4 *>(out + row * kD)[part] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(out + row * kD)[part] = pk;
+  }
+  if (part == 0) {
+    if (rowsum_out) rowsum_out[row] = rs;
+    if (lse2_out) lse2_out[row] = lse2_ws[(size_t)bh * Tp + i];
+  }
+}
+
+// ------------------------------------------------------------ host launchers
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
+                           float *rowsum_out, float *demand_out, int BH, int T, float c2, float eps,
+                           float *lse2_ws, float *acc, cudaStream_t stream) {
+  const int Tp = (int)t_pad(T);
+  f32_rowstats<<<dim3(Tp / kF32RowsPerCta, BH), kF32RowsPerCta, 0, stream>>>(q, k, lse2_ws, acc, T, Tp, c2);
+  const size_t smem = sizeof(F32SweepSmem);
+  cudaError_t e = cudaFuncSetAttribute(f32_sweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  f32_sweep<<<dim3(Tp / kF32KeysPerCta, BH), kF32KeysPerCta, smem, stream>>>(q, k, v, lse2_ws, acc, demand_out,
+                                                                            T, Tp, c2, eps);
+  const int64_t threads = (int64_t)BH * T * 16;
+  finalize_kernel<float><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(acc, lse2_ws, out, rowsum_out,
+                                                                                lse2_out, BH, T, Tp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bfloat16 *out, float *rowsum_out,
+                                 float *lse2_out, int BH, int T, cudaStream_t stream) {
+  const int Tp = (int)t_pad(T);
+  const int64_t threads = (int64_t)BH * T * 16;
+  finalize_kernel<__nv_bfloat16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
+      acc, lse2_ws, out, rowsum_out, lse2_out, BH, T, Tp);
+  return cudaGetLastError();
+}
+
+}  // namespace da

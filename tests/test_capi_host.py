@@ -1,0 +1,138 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every symbol the
+header declares, validates arguments before touching the GPU, and its integer
+artefacts (tile schedules, causal mask) match independent CPU generators bit
+for bit."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from long_context_attention_gb300 import binding as b
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return b.load()
+
+
+def test_exports_every_header_symbol(lib):
+    names = b.header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert b.status_string(b.DA_OK) == "DA_OK"
+    for s in range(1, 6):
+        assert b.status_string(s).startswith("DA_ERR_")
+    assert b.status_string(99) == "unknown status"
+    assert b.dilution_attn_version() >= 100
+
+
+def _sched_rowstats(BH, T):
+    Tp = -(-T // 256) * 256
+    npairs = Tp // 256
+    rows = []
+    for c in range(BH * npairs):
+        pair = npairs - 1 - c // BH
+        rows.append((c % BH, 2 * pair, 2, 0))
+    return np.array(rows, dtype=np.int32).reshape(-1, 4)
+
+
+def _sched_sweep(BH, T):
+    Tp = -(-T // 256) * 256
+    nqt = Tp // 128
+    rows = []
+    for c in range(BH * (Tp // 256)):
+        span = c // BH
+        rows.append((c % BH, 2 * span, nqt - 2 * span, 256 * span))
+    return np.array(rows, dtype=np.int32).reshape(-1, 4)
+
+
+@pytest.mark.parametrize("BH,T", [(1, 1), (2, 255), (3, 256), (5, 257), (48, 16384), (12, 131072)])
+def test_tile_schedules_bit_exact(lib, BH, T):
+    assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 0), _sched_rowstats(BH, T))
+    assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 1), _sched_sweep(BH, T))
+
+
+def test_tile_schedules_cover_triangle_once():
+    # every (head, key tile, query tile) pair with key tile <= query tile is
+    # visited by exactly one sweep CTA, and every query tile by one row-stats CTA
+    BH, T = 3, 1000
+    Tp = 1024
+    seen = {}
+    for bh, q0, n, key0 in b.dilution_attn_debug_tile_schedule(BH, T, 1):
+        for kt in (key0 // 128, key0 // 128 + 1):
+            for qt in range(q0, q0 + n):
+                if kt <= qt:
+                    seen[(bh, kt, qt)] = seen.get((bh, kt, qt), 0) + 1
+    want = {(bh, kt, qt) for bh in range(BH) for qt in range(Tp // 128) for kt in range(qt + 1)}
+    assert set(seen) == want and all(v == 1 for v in seen.values())
+    rs = b.dilution_attn_debug_tile_schedule(BH, T, 0)
+    tiles = sorted((int(r[0]), int(r[1]) + i) for r in rs for i in range(r[2]))
+    assert tiles == sorted((bh, qt) for bh in range(BH) for qt in range(Tp // 128))
+
+
+@pytest.mark.parametrize("T,qt,kt", [(256, 0, 0), (256, 1, 0), (200, 1, 1), (130, 1, 1), (1000, 3, 5), (5, 0, 0)])
+def test_tile_mask_bit_exact(lib, T, qt, kt):
+    r = np.arange(128)[:, None] + qt * 128
+    c = np.arange(128)[None, :] + kt * 128
+    want = ((c <= r) & (r < T)).astype(np.uint8)
+    assert np.array_equal(b.dilution_attn_debug_tile_mask(T, qt, kt), want)
+
+
+def test_workspace_sizes(lib):
+    Tp = 16384
+    want = 256 + 48 * Tp * 4
+    want = -(-want // 256) * 256 + 48 * Tp * 68 * 4
+    assert b.dilution_attn_fwd_workspace_size(4, 12, 16384, 64, b.DA_BF16) == want
+    assert b.dilution_attn_fwd_workspace_size(0, 12, 16384, 64, b.DA_BF16) == 256
+    assert b.dilution_attn_decode_workspace_size(8, 12, 131328, 64) > 8 * 12 * 131328 * 4
+
+
+# Argument validation happens before any CUDA call, so it runs without a GPU.
+FAKE = ctypes.c_void_p(0x10000)
+MIS = ctypes.c_void_p(0x10004)
+
+
+def _fwd(lib, q=FAKE, out=FAKE, B=1, H=1, T=8, d=64, tau=1.0, eps=1e-6, dtype=1, ws=FAKE, wsb=1 << 30):
+    return lib.dilution_attn_fwd(q, FAKE, FAKE, out, None, None, None, B, H, T, d, tau, eps, dtype, ws, wsb, None)
+
+
+def test_fwd_argument_validation(lib):
+    assert _fwd(lib, eps=0.0) == b.DA_ERR_INVALID
+    assert _fwd(lib, eps=-1.0) == b.DA_ERR_INVALID
+    assert _fwd(lib, eps=float("nan")) == b.DA_ERR_INVALID
+    assert _fwd(lib, tau=-0.5) == b.DA_ERR_INVALID
+    assert _fwd(lib, tau=float("inf")) == b.DA_ERR_INVALID
+    assert _fwd(lib, d=128) == b.DA_ERR_UNSUPPORTED
+    assert _fwd(lib, T=(1 << 24) + 1) == b.DA_ERR_UNSUPPORTED
+    assert _fwd(lib, B=-1) == b.DA_ERR_INVALID
+    assert _fwd(lib, dtype=7) == b.DA_ERR_INVALID
+    assert _fwd(lib, q=None) == b.DA_ERR_INVALID
+    assert _fwd(lib, out=MIS) == b.DA_ERR_INVALID
+    assert _fwd(lib, ws=None) == b.DA_ERR_WORKSPACE
+    assert _fwd(lib, wsb=1024) == b.DA_ERR_WORKSPACE
+    # empty problems are valid no-ops, whatever the pointers
+    assert _fwd(lib, q=None, T=0) == b.DA_OK
+    assert _fwd(lib, q=None, B=0) == b.DA_OK
+
+
+def _dec(lib, n_ctx=4, T_cap=16, d=64, eps=1e-6, dtype=1, ws=FAKE, wsb=1 << 30, k_cache=FAKE):
+    return lib.dilution_attn_decode_step(FAKE, FAKE, FAKE, k_cache, FAKE, FAKE, n_ctx, T_cap, FAKE, 1, 1, d, 1.0, eps,
+                                         dtype, ws, wsb, None)
+
+
+def test_decode_argument_validation(lib):
+    assert _dec(lib, n_ctx=16) == b.DA_ERR_INVALID          # no room for the new token
+    assert _dec(lib, n_ctx=-1) == b.DA_ERR_INVALID
+    assert _dec(lib, eps=0.0) == b.DA_ERR_INVALID
+    assert _dec(lib, d=32) == b.DA_ERR_UNSUPPORTED
+    assert _dec(lib, k_cache=None) == b.DA_ERR_INVALID
+    assert _dec(lib, k_cache=MIS) == b.DA_ERR_INVALID
+    assert _dec(lib, wsb=16) == b.DA_ERR_WORKSPACE
+
+
+def test_get_error_rejects_null(lib):
+    assert lib.dilution_attn_get_error(None, None) == b.DA_ERR_INVALID

@@ -1,0 +1,192 @@
+"""GPU parity of dilution_attn_fwd (through the C ABI) against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.dilution as od
+from long_context_attention_gb300 import binding as b
+from long_context_attention_gb300 import inputs
+from tests._parity import BF16_OUT_ABS, F32_OUT_REL, LOG2E, host64, oracle_forward, row_rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_fwd(q, k, v, tau=1.0, eps=1e-6):
+    B, H, T, _ = q.shape
+    out = torch.empty_like(q)
+    lse2 = torch.empty(B, H, T, device=DEV)
+    rs = torch.empty(B, H, T, device=DEV)
+    dem = torch.empty(B, H, T, device=DEV)
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, 64, b._dtype_code(q)), dtype=torch.uint8,
+                     device=DEV)
+    b.dilution_attn_fwd(q, k, v, out, lse2, rs, dem, tau=tau, eps=eps, workspace=ws)
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+    torch.cuda.synchronize()
+    return out, lse2, rs, dem
+
+
+def check_head(got, ref, dtype, rows=None):
+    out, lse2, rs, dem = got
+    n = rows if rows is not None else out.shape[0]
+    o_ref = ref["out"][:n]
+    if dtype == "f32":
+        assert row_rel_err(out[:n], o_ref) <= F32_OUT_REL
+        assert np.abs(lse2[:n] - ref["lse"][:n] * LOG2E).max() <= 1e-5 * max(1.0, np.abs(lse2[:n]).max())
+        assert np.abs(rs[:n] / ref["rowsum"][:n] - 1).max() <= 1e-5
+        if rows is None:
+            assert np.all(np.abs(dem - ref["demand"]) <= 1e-6 * np.maximum(ref["demand"], 1.0))
+    else:
+        assert np.abs(out[:n] - o_ref).max() <= BF16_OUT_ABS
+        assert np.abs(lse2[:n] - ref["lse"][:n] * LOG2E).max() <= 2e-3
+        assert np.abs(rs[:n] / ref["rowsum"][:n] - 1).max() <= 2e-2
+        if rows is None:
+            assert np.all(np.abs(dem - ref["demand"]) <= 1e-3 * np.maximum(ref["demand"], 1.0) + 1e-4)
+
+
+def compare(q, k, v, tau=1.0, eps=1e-6, heads=None, rows=None):
+    dtype = "f32" if q.dtype == torch.float32 else "bf16"
+    got = [host64(x) for x in run_fwd(q, k, v, tau, eps)]
+    ref = oracle_forward(q, k, v, tau, eps, rows=rows, heads=heads)
+    for (bb, hh), r in ref.items():
+        check_head([g[bb, hh] for g in got], r, dtype, rows)
+    return got, ref
+
+
+# ----------------------------------------------------------------------------- fp32
+def test_f32_config_t256():
+    w = inputs.WORKLOADS["fwd_f32_t256"]
+    q, k, v = (x.to(DEV) for x in inputs.make_workload(w))
+    got, ref = compare(q, k, v, 1.0, w.eps)
+    # the unit-demand invariant on the GPU's own demand output
+    assert abs(got[3][0, 0].sum() - 256) < 1e-3
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 7, 8, 127, 129, 255, 300])
+def test_f32_ragged(T):
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(2, 3, T, 64, q_std=1.5, pairs=min(4, T - 1) if T > 1 else 0,
+                                                   seed=T))
+    compare(q, k, v, tau=1.3, eps=1e-6)
+
+
+def test_f32_single_token_is_v():
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(3, 2, 1, 64, seed=11))
+    out = run_fwd(q, k, v)[0]
+    assert torch.allclose(out, v, rtol=1e-6, atol=1e-6)
+
+
+def test_f32_tau_zero_uniform_bids():
+    # tau = 0: every visible bid is 1/(i+1); committed = H_i - H_k (harmonic numbers)
+    T = 100
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 1, T, 64, seed=12))
+    out, lse2, rs, dem = (host64(x)[0, 0] for x in run_fwd(q, k, v, tau=0.0, eps=1e-6))
+    Hn = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, T + 2))])
+    share = np.array([[1.0 / ((i + 1) * (Hn[i + 1] - Hn[kk] + 1e-6)) if kk <= i else 0.0 for kk in range(T)]
+                      for i in range(T)])
+    ref = (share / share.sum(1, keepdims=True)) @ host64(v)[0, 0]
+    assert row_rel_err(out, ref) <= F32_OUT_REL
+    assert np.abs(lse2 - np.log2(np.arange(1, T + 1))).max() < 1e-5
+
+
+# ----------------------------------------------------------------------------- bf16
+@pytest.mark.parametrize("T", [1, 2, 5, 127, 128, 129, 255, 256, 257, 300, 640])
+def test_bf16_ragged(T):
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 2, T, 64, q_std=1.5, pairs=min(8, max(T - 1, 0)), seed=T,
+                                                   dtype="bf16"))
+    compare(q, k, v, tau=1.0, eps=1e-6)
+
+
+def test_bf16_tau_and_eps():
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(2, 2, 700, 64, q_std=1.5, pairs=8, seed=21, dtype="bf16"))
+    compare(q, k, v, tau=od.yarn_tau(8), eps=1e-6)
+    compare(q, k, v, tau=2.5, eps=1e-3)
+
+
+def test_bf16_rows_of_A_sum_to_one():
+    q, k, _ = inputs.make_qkv(2, 3, 1000, 64, q_std=1.5, pairs=16, seed=22, dtype="bf16")
+    q, k = q.to(DEV), k.to(DEV)
+    ones = torch.ones_like(q)
+    out = run_fwd(q, k, ones)[0].float()
+    assert (out - 1).abs().max().item() <= 1e-5
+
+
+def test_bf16_config_t4096():
+    w = inputs.WORKLOADS["fwd_bf16_t4096"]
+    q, k, v = (x.to(DEV) for x in inputs.make_workload(w))
+    got, _ = compare(q, k, v, 1.0, w.eps, heads=[(0, 0), (0, 7), (1, 3), (1, 11)])
+    dem = got[3]
+    assert np.abs(dem.sum(axis=-1) - w.T).max() < 0.05 * 1e-3 * w.T + 0.1
+
+
+def test_bf16_planted_pairs_retrieved():
+    # a planted key k_j = q_i carries a logit of about |q|^2/8 ~ 18: query i's
+    # output is close to v_j.
+    w = inputs.WORKLOADS["fwd_bf16_t4096"]
+    q, k, v = (x.to(DEV) for x in inputs.make_workload(w, B=1))
+    out = run_fwd(q, k, v)[0].float()
+    pp = inputs.planted_pairs(1, w.H, w.T, w.pairs, w.seed)
+    hits = 0
+    for (_, h, i, j) in pp:
+        hits += int(torch.nn.functional.cosine_similarity(out[0, h, i], v[0, h, j].float(), dim=0) > 0.5)
+    assert hits >= 0.9 * len(pp)
+
+
+def test_bf16_config_t16384_sampled():
+    """The benchmark's workload at full size: exact oracle values for the first
+    2048 rows of sampled heads, for sampled lse2 rows anywhere, and for the
+    demand of the last 256 keys; invariants on every head."""
+    w = inputs.WORKLOADS["fwd_bf16_t16384"]
+    q, k, v = (x.to(DEV) for x in inputs.make_workload(w, device=DEV))
+    T = w.T
+    got = run_fwd(q, k, v, 1.0, w.eps)
+    out, lse2, rs, dem = got
+    # invariant: every query adds exactly one unit of demand
+    assert (dem.double().sum(-1) - T).abs().max().item() < 2.0
+    assert torch.isfinite(out.float()).all()
+    heads = [(0, 0), (3, 11)]
+    ref = oracle_forward(q, k, v, 1.0, w.eps, rows=2048, heads=heads)
+    g = [host64(x) for x in got]
+    for (bb, hh), r in ref.items():
+        check_head([x[bb, hh] for x in g], r, "bf16", rows=2048)
+    # lse2 of sampled late rows and the demand of the last 256 keys (exact:
+    # only queries >= key contribute to it)
+    c = 1.0 / 8.0
+    for (bb, hh) in heads:
+        qh, kh = host64(q[bb, hh]), host64(k[bb, hh])
+        rows = np.arange(T - 256, T)
+        s = c * (qh[rows] @ kh.T)
+        mask = np.arange(T)[None, :] <= rows[:, None]
+        s = np.where(mask, s, -np.inf)
+        m = s.max(1, keepdims=True)
+        e = np.exp(s - m)
+        lse = (m[:, 0] + np.log(e.sum(1)))
+        assert np.abs(g[1][bb, hh, rows] - lse * LOG2E).max() <= 2e-3
+        p = e / e.sum(1, keepdims=True)
+        d_tail = p[:, T - 256:].sum(0)
+        assert np.all(np.abs(g[3][bb, hh, T - 256:] - d_tail) <= 1e-3 * np.maximum(d_tail, 1) + 1e-4)
+
+
+def test_error_status_clean_and_invalid_args():
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 1, 64, 64, dtype="bf16", seed=3))
+    with pytest.raises(b.DilutionAttnError) as ei:
+        b.dilution_attn_fwd(q, k, v, eps=0.0)
+    assert ei.value.status == b.DA_ERR_INVALID
+    with pytest.raises(b.DilutionAttnError) as ei:
+        b.dilution_attn_fwd(q, k, v, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert ei.value.status == b.DA_ERR_WORKSPACE
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(1, 1, 64, 64, 1), dtype=torch.uint8, device=DEV)
+    b.dilution_attn_fwd(q, k, v, workspace=ws)
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+
+
+def test_repeatable_and_stream_ordered():
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 4, 1500, 64, q_std=1.5, pairs=8, seed=31, dtype="bf16"))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1 = b.dilution_attn_fwd(q, k, v, stream=s)
+        o2 = b.dilution_attn_fwd(q, k, v, stream=s)
+    s.synchronize()
+    # fp32 reductions in L2 may add partials in any order: equal to rounding
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
