@@ -3,11 +3,13 @@
 // Three steps per (batch, head), "DilutionAttention v0.1.0 · results",
 // section "The operator":
 //   1. f32_rowstats: the causal-softmax normaliser of every query row,
-//      lse2_i = log2 sum_{k<=i} 2^(x_ik), x = s * tau/sqrt(d) * log2(e).
+//      lse2_i = log2 sum_{k<=i} 2^(x_ik), x = s * tau/sqrt(d) * log2(e), kept
+//      as the row max m_i and log2 of the max-shifted sum.
 //   2. f32_sweep: one CTA per 128 keys, one thread per key.  Walking the
 //      queries in causal order, each thread keeps its key's demand from
 //      earlier queries (the exclusive column cumsum) in a register:
-//      p = 2^(x - lse2), share = p / (committed + p + eps), committed += p.
+//      p = 2^(x - lse2), share = p / (committed + p + eps), committed += p
+//      (Kahan-compensated).
 //      The shares of 32 queries are staged in shared memory and multiplied
 //      by the CTA's 128 value rows; the partial numerators and share row
 //      sums are added (fp32 atomics) into the accumulator acc[row][0..64].
@@ -51,27 +53,34 @@ __global__ void __launch_bounds__(kF32RowsPerCta)
       float s = 0.f;
 #pragma unroll
       for (int t = 0; t < kD; ++t) s = fmaf(qr[t], sk[kk][t], s);
+      // max in fl(s*c2); every term of the sum as fma(s, c2, -m), so no
+      // term carries the rounding of a large logit.
       const float x = s * c2;
       if (x > m) {
-        l = l * exp2f(m - x) + 1.f;
+        l = l * exp2f(m - x) + exp2f(fmaf(s, c2, -x));
         m = x;
       } else {
-        l += exp2f(x - m);
+        l += exp2f(fmaf(s, c2, -m));
       }
     }
   }
   if (i < Tp) {
-    lse2[(size_t)bh * Tp + i] = (i < T) ? m + log2f(l) : INFINITY;
+    // The normaliser is kept as (m, log2 l): at logits of magnitude ~30 a
+    // single fp32 lse2 would carry ~2e-6 absolute rounding into every bid.
+    // m goes to the lse2 slot, log2 l to pad column 65 of the accumulator row.
+    lse2[(size_t)bh * Tp + i] = (i < T) ? m : INFINITY;
     float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)bh * Tp + i) * kAccStride);
 #pragma unroll
     for (int t = 0; t < kAccStride / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[((size_t)bh * Tp + i) * kAccStride + kD + 1] = (i < T) ? log2f(l) : 0.f;
   }
 }
 
 struct F32SweepSmem {
   float v[kF32KeysPerCta][kD];                 // value rows of this CTA's keys
   float q[kF32QChunk][kD];                     // current query chunk
-  float l2[kF32QChunk];                        // its lse2
+  float m2[kF32QChunk];                        // its row maxima (log2 domain)
+  float ll[kF32QChunk];                        // and log2 of the normalisers
   float sh[kF32QChunk][kF32KeysPerCta + 1];    // shares [query][key]
 };
 
@@ -96,6 +105,7 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
   for (int t = 0; t < kD; ++t) S.v[tid][t] = (key < T) ? vb[(size_t)key * kD + t] : 0.f;
 
   float committed = 0.f;   // sum of bids this key received from earlier queries
+  float comp = 0.f;        // Kahan compensation of that sum
   const int dv = tid % kD;
   const int rhalf = tid / kD;
   for (int q0 = key0; q0 < T; q0 += kF32QChunk) {
@@ -104,7 +114,10 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
       const int r = e / kD, t = e % kD;
       S.q[r][t] = (q0 + r < T) ? qb[(size_t)(q0 + r) * kD + t] : 0.f;
     }
-    if (tid < kF32QChunk) S.l2[tid] = lse2[(size_t)bh * Tp + q0 + tid];
+    if (tid < kF32QChunk) {
+      S.m2[tid] = lse2[(size_t)bh * Tp + q0 + tid];
+      S.ll[tid] = acc[((size_t)bh * Tp + q0 + tid) * kAccStride + kD + 1];
+    }
     __syncthreads();
     for (int r = 0; r < kF32QChunk; ++r) {
       const int i = q0 + r;
@@ -113,9 +126,12 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
         float s = 0.f;
 #pragma unroll
         for (int t = 0; t < kD; ++t) s = fmaf(S.q[r][t], kr[t], s);
-        const float p = exp2f(s * c2 - S.l2[r]);
+        const float p = exp2f(fmaf(s, c2, -S.m2[r]) - S.ll[r]);
         share = p / ((committed + p) + eps);
-        committed += p;
+        const float y = p - comp;
+        const float t2 = committed + y;
+        comp = (t2 - committed) - y;
+        committed = t2;
       }
       S.sh[r][tid] = share;
     }
@@ -139,10 +155,11 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
 
 // out_i = acc_i[0:64] / acc_i[64]; optional rowsum and lse2 side outputs.
 // 16 threads per row, 4 columns each.
+// split_lse: the workspace holds the row max and log2(l) separately (fp32 path).
 template <typename OutT>
 __global__ void finalize_kernel(const float *__restrict__ acc, const float *__restrict__ lse2_ws,
                                 OutT *__restrict__ out, float *__restrict__ rowsum_out,
-                                float *__restrict__ lse2_out, int BH, int T, int Tp) {
+                                float *__restrict__ lse2_out, int BH, int T, int Tp, bool split_lse) {
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = g / 16;
   const int part = (int)(g % 16);
@@ -164,7 +181,7 @@ __global__ void finalize_kernel(const float *__restrict__ acc, const float *__re
   }
   if (part == 0) {
     if (rowsum_out) rowsum_out[row] = rs;
-    if (lse2_out) lse2_out[row] = lse2_ws[(size_t)bh * Tp + i];
+    if (lse2_out) lse2_out[row] = lse2_ws[(size_t)bh * Tp + i] + (split_lse ? ar[kD + 1] : 0.f);
   }
 }
 
@@ -181,7 +198,7 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
                                                                             T, Tp, c2, eps);
   const int64_t threads = (int64_t)BH * T * 16;
   finalize_kernel<float><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(acc, lse2_ws, out, rowsum_out,
-                                                                                lse2_out, BH, T, Tp);
+                                                                                lse2_out, BH, T, Tp, true);
   return cudaGetLastError();
 }
 
@@ -190,7 +207,7 @@ cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bf
   const int Tp = (int)t_pad(T);
   const int64_t threads = (int64_t)BH * T * 16;
   finalize_kernel<__nv_bfloat16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
-      acc, lse2_ws, out, rowsum_out, lse2_out, BH, T, Tp);
+      acc, lse2_ws, out, rowsum_out, lse2_out, BH, T, Tp, false);
   return cudaGetLastError();
 }
 
