@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the dilution-attention forward (and cached decode) on GB300.
+
+Default workload: bf16 forward, B=4, H=12, T=16384, d=64 (the training
+context of the 24-layer decoders), tau = 1, eps = 1e-6, seeded synthetic
+inputs with 128 planted retrieval pairs per head.  One step = one call of
+dilution_attn_fwd (row statistics, demand sweep, finalize).  The JSON line
+reports forward TFLOP/s on the algorithmic count 3 * d * T(T+1) * B * H
+(q.k for the normaliser, q.k again in the sweep, share.v; causal pairs only),
+plus tokens/s, the dominant kernel's roofline, an end-to-end number through
+host buffers, clocks, the cached-decode step at 8 x 131072 tokens, and the
+float64 CPU oracle timed on a bounded sample as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(heads are independent; there is no data-path collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dilution-attn fwd TFLOP/s & tokens/s at T=16K, % of GB300 BF16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SWEEP_SOURCES = ["long_context_attention_gb300/csrc/fwd_bf16.cu", "long_context_attention_gb300/csrc/da_ptx.cuh",
+                 "long_context_attention_gb300/csrc/da_internal.h"]
+SWEEP_PROFILE = os.path.join(ROOT, "profiles", "sweep_kernel_fwd_bf16_t16384.md")
+
+
+# --------------------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="fwd_bf16_t16384")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=4096, help="query rows of the oracle's CPU sample")
+    return ap.parse_args(argv)
+
+
+def fwd_flops(B, H, T, d):
+    """Algorithmic forward FLOP: 3 contractions x 2d x causal pairs."""
+    return 3 * d * T * (T + 1) * B * H
+
+
+def sweep_flops(B, H, T, d):
+    """The demand sweep's share: q.k again and share.v over the causal pairs."""
+    return 2 * d * T * (T + 1) * B * H
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_hash():
+    h = hashlib.sha256()
+    for rel in SWEEP_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per sweep launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    try:
+        text = open(SWEEP_PROFILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().lstrip("-* ")
+        if ":" in line:
+            key, _, val = line.partition(":")
+            vals[key.strip().strip("`")] = val.strip().strip("`")
+    if vals.get("kernel_source_hash") != sources_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1):
+        """Median SM clock of the samples taken in [t0, t1] (wall clock)."""
+        samples = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                samples.append((ts, float(f[2]), float(f[3]), f[5:]))
+            except ValueError:
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [s for s in samples if t0 - 1.0 <= s[0] <= t1 + 1.0] or samples
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in inside:
+            for n, v in zip(names[1:], s[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(q, k, v, rows, tau=1.0, eps=1e-6):
+    """Time the float64 oracle on the first ``rows`` queries of one head."""
+    import oracle.dilution as od
+    t0 = time.perf_counter()
+    od.dilution_forward_rowblocked_head(q, k, v, tau, eps, rows=rows)
+    dt = time.perf_counter() - t0
+    d = q.shape[1]
+    flops = 3 * d * rows * (rows + 1)    # causal pairs of the first `rows` queries, 3 x 2d each
+    return flops, dt
+
+
+def cpu_baseline(rows, seed=2):
+    import numpy as np
+    from long_context_attention_gb300 import inputs
+    w = inputs.WORKLOADS["fwd_bf16_t16384"]
+    q, k, v = inputs.make_qkv(1, 1, rows, w.d, q_std=w.q_std, pairs=w.pairs * rows // w.T, seed=seed, dtype="bf16")
+    qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
+    flops, dt = oracle_sample(qh, kh, vh, rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"float64 NumPy oracle, 1 head x first {rows} query rows of the 4x12x16384x64 workload "
+                      f"({flops / 1e9:.1f} GFLOP algorithmic, {dt:.1f} s)",
+            "seconds": dt, "cpu_count": os.cpu_count(), "np": np.__version__}
+
+
+# ---------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    from long_context_attention_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    rows = 2048
+    q, k, v = inputs.make_qkv(1, 1, rows, w.d, q_std=w.q_std, pairs=max(1, w.pairs * rows // w.T), seed=w.seed,
+                              dtype=w.dtype)
+    qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
+    for _ in range(args.warmup):
+        oracle_sample(qh, kh, vh, rows)
+    tot_f, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        f, t = oracle_sample(qh, kh, vh, rows)
+        tot_f += f
+        tot_t += t
+    val = tot_f / tot_t / 1e12
+    sample = f"float64 NumPy oracle, 1 head x first {rows} query rows per step ({args.workload} shape)"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "tau": 1.0, "eps": w.eps},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------ our arm
+def run_decode(torch, b, inputs, dev, warmup, peaks):
+    """8 independent 131072-token caches (built by an untimed prefill), 256 steps."""
+    w = inputs.WORKLOADS["decode_bf16_ctx131072"]
+    B, H, N, d = w.B, w.H, w.T, w.d
+    steps = w.extra["steps"]
+    from long_context_attention_gb300 import yarn_tau
+    tau = yarn_tau(w.tau_scale)
+    T_cap = N + steps
+    q, k, v = inputs.make_workload(w, device=dev)
+    kc = torch.empty(B, H, T_cap, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    kc[:, :, :N] = k
+    vc[:, :, :N] = v
+    dem = torch.zeros(B, H, T_cap, device=dev)
+    dem_n = torch.empty(B, H, N, device=dev)
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, N, d, b.DA_BF16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    # prefill at 131072 tokens (also reported, as the long-context prefill)
+    b.dilution_attn_fwd(q, k, v, out, None, None, dem_n, tau=tau, eps=w.eps, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    b.dilution_attn_fwd(q, k, v, out, None, None, dem_n, tau=tau, eps=w.eps, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+    pre_ms = e0.elapsed_time(e1)
+    pre = {"workload": "prefill_bf16_t131072_b8", "B": B, "H": H, "T": N, "tau": tau,
+           "ms": pre_ms, "tflops": fwd_flops(B, H, N, d) / (pre_ms * 1e-3) / 1e12,
+           "tokens_per_s": B * N / (pre_ms * 1e-3)}
+    dem[:, :, :N] = dem_n
+    del q, out, ws, dem_n
+    qs = inputs.make_like((steps, B, H, d), std=w.q_std, seed=w.seed + 100, dtype="bf16", device=dev)
+    ks = inputs.make_like((steps, B, H, d), seed=w.seed + 101, dtype="bf16", device=dev)
+    vs = inputs.make_like((steps, B, H, d), seed=w.seed + 102, dtype="bf16", device=dev)
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    dws = torch.empty(b.dilution_attn_decode_workspace_size(B, H, T_cap, d), dtype=torch.uint8, device=dev)
+    dem0 = dem.clone()
+    for i in range(warmup):   # warm-up steps on the real state, then restore it
+        b.dilution_attn_decode_step(qs[i], ks[i], vs[i], kc, vc, dem, N, o, tau=tau, eps=w.eps, workspace=dws)
+    torch.cuda.synchronize()
+    dem.copy_(dem0)
+    del dem0
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(steps):
+        b.dilution_attn_decode_step(qs[i], ks[i], vs[i], kc, vc, dem, N + i, o, tau=tau, eps=w.eps, workspace=dws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert b.dilution_attn_get_error(dws) == b.DA_OK
+    ms = e0.elapsed_time(e1)
+    keys = sum((N + i + 1) for i in range(steps)) * B * H
+    algo_bytes = (4 * d + 8) * keys     # K and V rows (bf16) + demand read and write (fp32)
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    return pre, {"workload": "decode_bf16_ctx131072", "B": B, "H": H, "n_ctx": N, "steps": steps, "tau": tau,
+                 "ms_per_step": ms / steps, "tokens_per_s": B * steps / (ms * 1e-3),
+                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                              "bytes_per_step": algo_bytes / steps},
+                 "gpu_launches": 3 * steps}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from long_context_attention_gb300 import binding as b
+    from long_context_attention_gb300 import inputs
+    b.load(build_if_missing=True)
+    peaks, peaks_kind = load_peaks()
+
+    w = inputs.WORKLOADS[args.workload]
+    B, H, T, d = w.B, w.H, w.T, w.d
+    # each rank is an independent replica with its own seeded batch
+    q, k, v = inputs.make_qkv(B, H, T, d, q_std=w.q_std, pairs=w.pairs, seed=w.seed + 1000 * rank, dtype=w.dtype,
+                              device=dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b._dtype_code(q)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in evs:            # materialise the CUDA events before timing
+        for e in e4:
+            e.record()
+    for _ in range(W):
+        b.dilution_attn_fwd(q, k, v, out, workspace=ws)
+    torch.cuda.synchronize()
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        barrier()
+        torch.cuda.synchronize()
+        w0 = time.time()
+        t_start.record(stream)
+        for i in range(K):
+            b.dilution_attn_fwd_with_events(q, k, v, out, workspace=ws, events=evs[i], check=False)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        w1 = time.time()
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    per = {"rowstats": [], "sweep": [], "finalize": []}
+    for e4 in evs:
+        per["rowstats"].append(e4[0].elapsed_time(e4[1]))
+        per["sweep"].append(e4[1].elapsed_time(e4[2]))
+        per["finalize"].append(e4[2].elapsed_time(e4[3]))
+    kern_ms = {k_: statistics.mean(v_) for k_, v_ in per.items()}
+    flops_step = fwd_flops(B, H, T, d)
+    ms_step = ms / K
+    value = world * flops_step * K / (ms * 1e-3) / 1e12
+    timed_s = ms * 1e-3
+    peak_t = peaks["bf16_tflops_sustained"] if timed_s > 1.0 else peaks["bf16_tflops"]
+    sweep_tf = sweep_flops(B, H, T, d) / (kern_ms["sweep"] * 1e-3) / 1e12
+    rs_tf = (flops_step - sweep_flops(B, H, T, d)) / (kern_ms["rowstats"] * 1e-3) / 1e12
+    clocks = clk.summary(w0, w1)
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d, "tau": 1.0, "eps": w.eps,
+                       "planted_pairs_per_head": w.pairs, "parallelism": f"replicas{world}",
+                       "l2": f"no flush; inputs {3 * q.numel() * q.element_size() / 1e6:.0f} MB + accumulator "
+                             f"{ws.numel() / 1e6:.0f} MB per step, larger than the 129 MB L2"},
+            "tokens_per_s": world * B * T * K / (ms * 1e-3),
+            "pct_of_bf16_peak": 100.0 * value / world / peak_t,
+            "kernels_ms": kern_ms,
+            "roofline": {"bound": "tensor", "kernel": "sweep_kernel", "achieved": sweep_tf, "peak": peak_t,
+                         "unit": "TFLOP/s", "frac": sweep_tf / peak_t, "traffic": profiled_traffic(),
+                         "peak_source": f"{peaks_kind} {'sustained' if timed_s > 1.0 else 'burst'} bf16",
+                         "rowstats_achieved": rs_tf, "rowstats_frac": rs_tf / peak_t},
+            "gpu_launches": 3 * K, "clocks": clocks}
+
+    if not args.no_e2e:
+        Ke = max(1, min(K, 10))
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+        b.dilution_attn_fwd(dq.copy_(hq), dk.copy_(hk), dv.copy_(hv), out, workspace=ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record()
+        for _ in range(Ke):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            b.dilution_attn_fwd(dq, dk, dv, out, workspace=ws)
+            hout.copy_(out, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        line["e2e"] = {"value": world * flops_step * Ke / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+                       "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": Ke,
+                       "ms_per_step": ems / Ke}
+        del hq, hk, hv, hout, dq, dk, dv
+
+    del q, k, v, out, ws
+    torch.cuda.empty_cache()
+    if not args.no_decode:
+        pre, dec = run_decode(torch, b, inputs, dev, max(3, W), peaks)
+        line["prefill_131072"] = pre
+        line["decode"] = dec
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

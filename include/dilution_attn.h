@@ -90,6 +90,17 @@ int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out,
                       int B, int H, int T, int d, float tau, float eps, int dtype,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* Same computation as dilution_attn_fwd; additionally records events[0..3]
+ * (cudaEvent_t handles created by the caller, each may be NULL) on `stream`:
+ * [0] before the row-statistics kernel, [1] before the demand sweep, [2]
+ * before the finalize kernel, [3] after it.  Used to time each kernel on the
+ * stream it runs on.  events == NULL is the same as dilution_attn_fwd. */
+int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, void *out,
+                                  float *lse2_out, float *rowsum_out, float *demand_out,
+                                  int B, int H, int T, int d, float tau, float eps, int dtype,
+                                  void *workspace, size_t workspace_bytes, void *stream,
+                                  void *const *events);
+
 /* ------------------------------------------------------------------------
  * Cached decode step ("DilutionAttention v0.1.0 · results", section "The
  * operator": the ordinary key/value cache plus one running demand total per

@@ -35,6 +35,9 @@ _SIGNATURES = {
     "dilution_attn_fwd_workspace_size": (_c_size_t, [_c_int] * 5),
     "dilution_attn_fwd": (_c_int, [_c_void_p] * 7 + [_c_int] * 4 + [_c_float, _c_float, _c_int, _c_void_p,
                                                                         _c_size_t, _c_void_p]),
+    "dilution_attn_fwd_with_events": (_c_int, [_c_void_p] * 7 + [_c_int] * 4 + [_c_float, _c_float, _c_int,
+                                                                                    _c_void_p, _c_size_t, _c_void_p,
+                                                                                    _c_void_p]),
     "dilution_attn_decode_workspace_size": (_c_size_t, [_c_int] * 4),
     "dilution_attn_decode_step": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                   [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
@@ -134,6 +137,24 @@ def dilution_attn_fwd(q, k, v, out=None, lse2_out=None, rowsum_out=None, demand_
     outputs are filled when passed.  ``workspace`` (uint8 CUDA tensor) is
     allocated when omitted.
     """
+    return dilution_attn_fwd_with_events(q, k, v, out, lse2_out, rowsum_out, demand_out, tau=tau, eps=eps,
+                                         workspace=workspace, stream=stream, check=check, events=None)
+
+
+def _event_handle(e):
+    if e is None:
+        return None
+    if e.cuda_event == 0:   # torch creates the CUDA event lazily, on first record
+        e.record()
+    return e.cuda_event
+
+
+def dilution_attn_fwd_with_events(q, k, v, out=None, lse2_out=None, rowsum_out=None, demand_out=None, *,
+                                  tau: float = 1.0, eps: float = 1e-6, workspace=None, stream=None,
+                                  check: bool = True, events=None):
+    """dilution_attn_fwd that also records up to four torch.cuda.Event
+    (timing-enabled) on the stream: before row statistics, before the sweep,
+    before finalize, after finalize."""
     lib = load()
     _need(q, "q")
     B, H, T, d = q.shape
@@ -149,9 +170,12 @@ def dilution_attn_fwd(q, k, v, out=None, lse2_out=None, rowsum_out=None, demand_
     need = dilution_attn_fwd_workspace_size(B, H, T, d, dt)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = lib.dilution_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2_out), _ptr(rowsum_out),
-                               _ptr(demand_out), B, H, T, d, float(tau), float(eps), dt, _ptr(workspace),
-                               workspace.numel(), _stream_handle(stream))
+    ev = None
+    if events is not None:
+        ev = (ctypes.c_void_p * 4)(*[_event_handle(e) for e in events])
+    st = lib.dilution_attn_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2_out), _ptr(rowsum_out),
+                                           _ptr(demand_out), B, H, T, d, float(tau), float(eps), dt,
+                                           _ptr(workspace), workspace.numel(), _stream_handle(stream), ev)
     if check:
         _check(st, "dilution_attn_fwd")
     return out

@@ -11,10 +11,10 @@
 namespace da {
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
                            float *rowsum_out, float *demand_out, int BH, int T, float c2, float eps,
-                           float *lse2_ws, float *acc, cudaStream_t stream);
+                           float *lse2_ws, float *acc, cudaStream_t stream, cudaEvent_t const *ev);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                     float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
-                    cudaStream_t stream);
+                    cudaStream_t stream, cudaEvent_t const *ev);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, float c2, float eps, int dtype,
                           float *logits, float2 *part_ml, float *part_acc, int nchunk, cudaStream_t stream);
@@ -71,6 +71,17 @@ size_t dilution_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype) {
 int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                       float *demand_out, int B, int H, int T, int d, float tau, float eps, int dtype,
                       void *workspace, size_t workspace_bytes, void *stream_) {
+  return dilution_attn_fwd_with_events(q, k, v, out, lse2_out, rowsum_out, demand_out, B, H, T, d, tau, eps, dtype,
+                                       workspace, workspace_bytes, stream_, nullptr);
+}
+
+int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, void *out, float *lse2_out,
+                                  float *rowsum_out, float *demand_out, int B, int H, int T, int d, float tau,
+                                  float eps, int dtype, void *workspace, size_t workspace_bytes, void *stream_,
+                                  void *const *events) {
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  if (events != nullptr)
+    for (int i = 0; i < 4; ++i) ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   int st = check_common(B, H, T, d, tau, eps, dtype);
   if (st != DA_OK) return st;
   const int64_t BH = (int64_t)B * H;
@@ -91,12 +102,12 @@ int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out, fl
   const float c2 = logit_scale_log2(tau, d);
   if (dtype == DA_F32) {
     if (launch_fwd_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse2_out, rowsum_out,
-                       demand_out, (int)BH, T, c2, eps, lse2_ws, acc, stream) != cudaSuccess)
+                       demand_out, (int)BH, T, c2, eps, lse2_ws, acc, stream, ev) != cudaSuccess)
       return DA_ERR_CUDA;
     return DA_OK;
   }
   return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, c2, eps, lse2_ws, acc, status,
-                         stream);
+                         stream, ev);
 }
 
 size_t dilution_attn_decode_workspace_size(int B, int H, int T_cap, int d) {

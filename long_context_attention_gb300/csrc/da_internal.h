@@ -88,13 +88,30 @@ DA_HD TileWork rowstats_work(int cta, int BH, int64_t T) {
 }
 
 // Demand sweep: one CTA per span of 256 keys, walking query tiles from the
-// span's diagonal tile to the last tile.
+// span's diagonal tile to the last tile.  Heads are taken in groups whose fp32
+// accumulators (Tp x 272 B per head) together stay near 64 MB, so the
+// reductions of the CTAs in flight hit L2; inside a group the spans with the
+// most query tiles launch first.
+constexpr int64_t kAccGroupBytes = 64ll << 20;
+DA_HD int sweep_head_group(int BH, int64_t T) {
+  const int64_t per_head = t_pad(T) * kAccStride * 4;
+  int64_t hg = kAccGroupBytes / per_head;
+  if (hg < 1) hg = 1;
+  if (hg > BH) hg = BH;
+  return (int)hg;
+}
 DA_HD int sweep_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / kSpan); }
 DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
   const int nqt = (int)(t_pad(T) / kTile);
+  const int nspan = (int)(t_pad(T) / kSpan);
+  const int hg = sweep_head_group(BH, T);
+  const int group = cta / (hg * nspan);
+  const int h0 = group * hg;
+  const int ng = (BH - h0 < hg) ? BH - h0 : hg;    // heads in this (possibly last, smaller) group
+  const int r = cta - h0 * nspan;
   TileWork w;
-  w.bh = cta % BH;
-  const int span = cta / BH;                 // span 0 walks every query tile
+  w.bh = h0 + r % ng;
+  const int span = r / ng;                   // span 0 walks every query tile
   w.key0 = span * kSpan;
   w.q_tile0 = span * (kSpan / kTile);
   w.n_q_tiles = nqt - w.q_tile0;

@@ -10,7 +10,7 @@
 //  rowstats_kernel  (one CTA per pair of 128-row query tiles)
 //     S = Q K^T on tcgen05 (bf16 x bf16 -> fp32 in TMEM), K tiles streamed by
 //     TMA through a 4-stage ring; one thread per query row keeps an online
-//     max / sum and writes lse2_i = log2 sum_k 2^(x_ik), x = s * c2,
+//     max / sum and writes -lse2_i, lse2_i = log2 sum_k 2^(x_ik), x = s * c2,
 //     c2 = tau / sqrt(d) * log2(e).  Also zeroes the rows of the fp32
 //     accumulator that the sweep adds into.
 //
@@ -66,6 +66,90 @@ __device__ __forceinline__ uint64_t kmajor_desc(const uint8_t *tile, int kstep) 
   return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
 }
 
+// After the last tcgen05.ld of a TMEM buffer has completed: hand the buffer
+// back to the MMA issuer (one arrival per warp).
+__device__ __forceinline__ void release_tmem(uint64_t *bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Online softmax normaliser of one query row in the log2 domain:
+// m = running max of x = s * c2, l = sum 2^(x - m) in four partial sums.
+struct RowStat {
+  float m = -INFINITY;
+  float2 l0 = make_float2(0.f, 0.f), l1 = make_float2(0.f, 0.f);
+
+  // 32 consecutive keys (columns col0 ..) of the row; DIAG masks key > query.
+  template <bool DIAG>
+  __device__ __forceinline__ void chunk(float (&s)[32], int col0, int row, float c2) {
+    if (DIAG) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (col0 + c > row) s[c] = -INFINITY;
+    }
+    float t[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) t[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+    t[10] = fmaxf(s[30], s[31]);
+    const float mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], fmax3(t[8], t[9], t[10])));
+    if (DIAG && mx == -INFINITY) return;   // every key of the chunk is after the query
+    const float mn = fmaxf(m, mx * c2);
+    const float sc = ex2_approx(m - mn);    // 0 on the first chunk (m = -inf)
+    l0 = fmul2(l0, make_float2(sc, sc));
+    l1 = fmul2(l1, make_float2(sc, sc));
+    m = mn;
+    const float2 c2v = make_float2(c2, c2), nm = make_float2(-mn, -mn);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const float2 x0 = ffma2(make_float2(s[2 * j], s[2 * j + 1]), c2v, nm);
+      const float2 x1 = ffma2(make_float2(s[2 * j + 2], s[2 * j + 3]), c2v, nm);
+      l0 = fadd2(l0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
+      l1 = fadd2(l1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
+    }
+  }
+};
+
+// Demand step for 32 consecutive queries (columns col0 ..) of one key row:
+//   p = 2^(s*c2 - lse2),  den = (committed + eps) + p,  share = p / den,
+//   committed + eps <- den   (queries in causal order: the exclusive cumsum).
+// nl holds -lse2 of those queries (shared memory, read as float4).  DIAG
+// zeroes the bids of queries before the key (key row > query column).
+template <bool DIAG>
+__device__ __forceinline__ void demand_chunk(const float (&s)[32], const float *nl, int col0, int row, float c2,
+                                             float &ceps, uint32_t (&pk)[16]) {
+  const float4 *nl4 = reinterpret_cast<const float4 *>(nl);
+  const float2 c2v = make_float2(c2, c2);
+  float p[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 l = nl4[i];
+    const float2 x0 = ffma2(make_float2(s[4 * i], s[4 * i + 1]), c2v, make_float2(l.x, l.y));
+    const float2 x1 = ffma2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2v, make_float2(l.z, l.w));
+    p[4 * i] = ex2_approx(x0.x);
+    p[4 * i + 1] = ex2_approx(x0.y);
+    p[4 * i + 2] = ex2_approx(x1.x);
+    p[4 * i + 3] = ex2_approx(x1.y);
+  }
+  if (DIAG) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      if (row > col0 + c) p[c] = 0.f;
+  }
+  float r[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float den = ceps + p[c];
+    r[c] = rcp_approx(den);
+    ceps = den;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 sh = fmul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(r[2 * i], r[2 * i + 1]));
+    pk[i] = pack_bf16x2(sh.x, sh.y);
+  }
+}
+
 // ============================================================================
 // Row statistics
 // ============================================================================
@@ -75,7 +159,7 @@ constexpr int kRsSmemBytes = (2 + kRsKStages) * kTileBytes + 256 + 1024;
 
 __global__ void __launch_bounds__(kRsThreads, 2)
     rowstats_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    float *__restrict__ lse2, float *__restrict__ acc, int BH, int T, int Tp, float c2,
+                    float *__restrict__ nlse2, float *__restrict__ acc, int BH, int T, int Tp, float c2,
                     int *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -181,55 +265,47 @@ __global__ void __launch_bounds__(kRsThreads, 2)
     const int row = quarter * 32 + lane;
     const int qt = w.q_tile0 + g;
     const int64_t qi = (int64_t)qt * kTile + row;
-    float m = -INFINITY, l = 0.f;
+    RowStat st;
     const uint32_t tbase = tmem + g * kTile + ((uint32_t)(quarter * 32) << 16);
     for (int kt = 0; kt <= qt; ++kt) {
       if (!mbar_wait(&s_full[g], kt & 1, wc)) break;
       tc_fence_after();
-      const bool diag = (kt == qt);
-#pragma unroll 1
-      for (int ch = 0; ch < kTile / 32; ++ch) {
-        float s[32];
-        tmem_ld32(tbase + ch * 32, s);
-        tmem_wait_ld();
-        if (ch == kTile / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[g]);
-        }
-        float mx = -INFINITY;
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (ch * 32 + c <= row) mx = fmaxf(mx, s[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, s[c]);
-        }
-        if (mx == -INFINITY) continue;   // every key of this chunk is masked
-        const float mn = fmaxf(m, mx * c2);
-        l *= ex2_approx(m - mn);
-        m = mn;
-        float acc0 = 0.f, acc1 = 0.f;
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            if (ch * 32 + c <= row) acc0 += ex2_approx(fmaf(s[c], c2, -m));
-            if (ch * 32 + c + 1 <= row) acc1 += ex2_approx(fmaf(s[c + 1], c2, -m));
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            acc0 += ex2_approx(fmaf(s[c], c2, -m));
-            acc1 += ex2_approx(fmaf(s[c + 1], c2, -m));
-          }
-        }
-        l += acc0 + acc1;
+      // 32-column chunks; the load of chunk c+1 is in flight while chunk c is reduced.
+      float A[32], B[32];
+      if (kt < qt) {
+        tmem_ld32(tbase, A);
+        tmem_wait_ld_r(A);
+        tmem_ld32(tbase + 32, B);
+        st.chunk<false>(A, 0, row, c2);
+        tmem_wait_ld_r(B);
+        tmem_ld32(tbase + 64, A);
+        st.chunk<false>(B, 32, row, c2);
+        tmem_wait_ld_r(A);
+        tmem_ld32(tbase + 96, B);
+        st.chunk<false>(A, 64, row, c2);
+        tmem_wait_ld_r(B);
+        release_tmem(&s_free[g], lane);
+        st.chunk<false>(B, 96, row, c2);
+      } else {
+        tmem_ld32(tbase, A);
+        tmem_wait_ld_r(A);
+        tmem_ld32(tbase + 32, B);
+        st.chunk<true>(A, 0, row, c2);
+        tmem_wait_ld_r(B);
+        tmem_ld32(tbase + 64, A);
+        st.chunk<true>(B, 32, row, c2);
+        tmem_wait_ld_r(A);
+        tmem_ld32(tbase + 96, B);
+        st.chunk<true>(A, 64, row, c2);
+        tmem_wait_ld_r(B);
+        release_tmem(&s_free[g], lane);
+        st.chunk<true>(B, 96, row, c2);
       }
       if (*abort_flag) break;
     }
     if (qi < Tp) {
-      lse2[(size_t)w.bh * Tp + qi] = (qi < T) ? m + log2f(l) : INFINITY;
+      // negated, so the sweep forms x - lse2 with one packed fma
+      nlse2[(size_t)w.bh * Tp + qi] = (qi < T) ? -(st.m + log2f(st.l0.x + st.l0.y + st.l1.x + st.l1.y)) : -INFINITY;
       float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)w.bh * Tp + qi) * kAccStride);
 #pragma unroll
       for (int t = 0; t < kAccStride / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -257,7 +333,7 @@ constexpr uint32_t kSwOffV = kSwOffK + 2 * kTileBytes;           // 2 value tile
 constexpr uint32_t kSwOffQ = kSwOffV + 2 * kTileBytes;           // query ring
 constexpr uint32_t kSwOffSh = kSwOffQ + kSwQStages * kTileBytes; // share^T, one per key tile
 constexpr uint32_t kSwOffOnes = kSwOffSh + 2 * kShBytes;         // 16 x 64 bf16 ones (2 KB)
-constexpr uint32_t kSwOffL = kSwOffOnes + 2048;                  // lse2 ring (512 B per stage)
+constexpr uint32_t kSwOffL = kSwOffOnes + 2048;                  // -lse2 ring (512 B per stage)
 constexpr uint32_t kSwOffBar = kSwOffL + kSwQStages * 512;
 constexpr int kSwSmemBytes = kSwOffBar + 256 + 1024;
 
@@ -266,7 +342,7 @@ constexpr uint32_t kTmemD = 256;    // partials of query tile t at 256 + (t&1)*1
 
 __global__ void __launch_bounds__(kSwThreads, 1)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const float *__restrict__ lse2,
+                 const __grid_constant__ CUtensorMap tmV, const float *__restrict__ nlse2,
                  float *__restrict__ acc, float *__restrict__ demand_out, int BH, int T, int Tp, float c2,
                  float eps, int *status) {
   extern __shared__ uint8_t smem_raw[];
@@ -344,7 +420,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         mbar_arrive_expect_tx(&q_full[s], kTileBytes + 512);
         const int qrow = (w.q_tile0 + t) * kTile;
         tma_load_3d(sQ + s * kTileBytes, &tmQ, &q_full[s], 0, qrow, w.bh);
-        bulk_load(smem + kSwOffL + s * 512, lse2 + (size_t)w.bh * Tp + qrow, 512, &q_full[s]);
+        bulk_load(smem + kSwOffL + s * 512, nlse2 + (size_t)w.bh * Tp + qrow, 512, &q_full[s]);
         ++issued;
       }
       if (*abort_flag) {
@@ -447,6 +523,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     uint8_t *sh_rows = sSh + g * kShBytes + (row / 8) * 1024 + (row % 8) * 128;
     const int swz = row % 8;
     float ceps = eps;   // committed + eps: demand this key received from earlier queries
+    // 32 shares (bf16 pairs) of query chunk c -> the share^T operand:
+    // 64-query M-block c/2, 16-byte pieces (c%2)*4 .. +3, 128B-swizzled by key row.
+    auto store = [&](const uint32_t (&pk)[16], int c) {
+      uint8_t *dst = sh_rows + (c >> 1) * 16384;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(dst + ((((c & 1) * 4 + i) ^ swz) * 16)) =
+            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    };
     for (int t = 0; t < nt; ++t) {
       const int s = t % kSwQStages;
       const int j = w.q_tile0 + t;
@@ -455,55 +540,42 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       if (!mbar_wait(&q_full[s], (t / kSwQStages) & 1, wc)) break;
       if (!mbar_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
-      const float *lrow = sL + s * 128;
-      bool ok = true;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float sv[64];
-        tmem_ld32(tbase + h * 64, *reinterpret_cast<float(*)[32]>(&sv[0]));
-        tmem_ld32(tbase + h * 64 + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-        tmem_wait_ld();
-        if (h == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[g]);
-        }
-        uint32_t pk[32];
-        if (all_masked) {
+      const float *nl = sL + s * 128;   // -lse2 of the tile's 128 queries
+      uint32_t pk[16];
+      if (all_masked) {
+        release_tmem(&s_free[g], lane);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = 0u;
-        } else {
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const int col = h * 64 + c;
-            float p0 = ex2_approx(fmaf(sv[c], c2, -lrow[col]));
-            float p1 = ex2_approx(fmaf(sv[c + 1], c2, -lrow[col + 1]));
-            if (diag) {
-              if (row > col) p0 = 0.f;
-              if (row > col + 1) p1 = 0.f;
-            }
-            const float d0 = ceps + p0;
-            const float sh0 = p0 * rcp_approx(d0);
-            const float d1 = d0 + p1;
-            const float sh1 = p1 * rcp_approx(d1);
-            ceps = d1;
-            pk[c / 2] = pack_bf16x2(sh0, sh1);
-          }
-        }
-        if (h == 0) {
-          // the product of the previous query tile must be done reading this buffer
-          if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) {
-            ok = false;
-            break;
-          }
-        }
-        uint8_t *dst = sh_rows + h * 16384;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4 *>(dst + ((c8 ^ swz) * 16)) =
-              make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+        for (int c = 0; c < 4; ++c) store(pk, c);
+      } else {
+        // 32-column chunks; the load of chunk c+1 is in flight while chunk c is formed.
+        float A[32], B[32];
+        tmem_ld32(tbase, A);
+        tmem_wait_ld_r(A);
+        tmem_ld32(tbase + 32, B);
+        if (diag) demand_chunk<true>(A, nl, 0, row, c2, ceps, pk);
+        else demand_chunk<false>(A, nl, 0, row, c2, ceps, pk);
+        // the product of the previous query tile must be done reading this buffer
+        if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
+        store(pk, 0);
+        tmem_wait_ld_r(B);
+        tmem_ld32(tbase + 64, A);
+        if (diag) demand_chunk<true>(B, nl + 32, 32, row, c2, ceps, pk);
+        else demand_chunk<false>(B, nl + 32, 32, row, c2, ceps, pk);
+        store(pk, 1);
+        tmem_wait_ld_r(A);
+        tmem_ld32(tbase + 96, B);
+        if (diag) demand_chunk<true>(A, nl + 64, 64, row, c2, ceps, pk);
+        else demand_chunk<false>(A, nl + 64, 64, row, c2, ceps, pk);
+        store(pk, 2);
+        tmem_wait_ld_r(B);
+        release_tmem(&s_free[g], lane);
+        if (diag) demand_chunk<true>(B, nl + 96, 96, row, c2, ceps, pk);
+        else demand_chunk<false>(B, nl + 96, 96, row, c2, ceps, pk);
+        store(pk, 3);
       }
-      if (!ok) break;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -564,28 +636,38 @@ cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bf
 
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                     float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, cudaEvent_t const *ev) {
   CUtensorMap tq, tk, tv;
   if (!make_tile_map(&tq, q, BH, T) || !make_tile_map(&tk, k, BH, T) || !make_tile_map(&tv, v, BH, T))
     return DA_ERR_CUDA;
-  static bool attr_done = false;
-  if (!attr_done) {
+  // The shared-memory opt-in is a per-device function attribute.
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+  if (dev >= 64 || !attr_done[dev]) {
     if (cudaFuncSetAttribute(rowstats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRsSmemBytes) !=
             cudaSuccess ||
         cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes) !=
             cudaSuccess)
       return DA_ERR_CUDA;
-    attr_done = true;
+    if (dev < 64) attr_done[dev] = true;
   }
   const int Tp = (int)t_pad(T);
+  // Masked logits enter as -inf; with tau = 0 a zero scale would turn them
+  // into NaN.  1e-30 keeps every finite logit at 0 (uniform bids) and -inf at -inf.
+  if (c2 < 1e-30f) c2 = 1e-30f;
+  if (ev[0]) cudaEventRecord(ev[0], stream);
   rowstats_kernel<<<rowstats_num_ctas(BH, T), kRsThreads, kRsSmemBytes, stream>>>(tq, tk, lse2_ws, acc, BH, T,
                                                                                   Tp, c2, status);
+  if (ev[1]) cudaEventRecord(ev[1], stream);
   sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, lse2_ws, acc, demand_out,
                                                                             BH, T, Tp, c2, eps, status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
+  if (ev[2]) cudaEventRecord(ev[2], stream);
   if (launch_finalize_bf16(acc, lse2_ws, reinterpret_cast<__nv_bfloat16 *>(out), rowsum_out, lse2_out, BH, T,
                            stream) != cudaSuccess)
     return DA_ERR_CUDA;
+  if (ev[3]) cudaEventRecord(ev[3], stream);
   return DA_OK;
 }
 

@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
 
 // out_i = acc_i[0:64] / acc_i[64]; optional rowsum and lse2 side outputs.
 // 16 threads per row, 4 columns each.
-// split_lse: the workspace holds the row max and log2(l) separately (fp32 path).
+// split_lse: the workspace holds the row max and log2(l) separately (fp32
+// path); otherwise it holds -lse2 (bf16 path).
 template <typename OutT>
 __global__ void finalize_kernel(const float *__restrict__ acc, const float *__restrict__ lse2_ws,
                                 OutT *__restrict__ out, float *__restrict__ rowsum_out,
@@ -181,24 +182,28 @@ __global__ void finalize_kernel(const float *__restrict__ acc, const float *__re
   }
   if (part == 0) {
     if (rowsum_out) rowsum_out[row] = rs;
-    if (lse2_out) lse2_out[row] = lse2_ws[(size_t)bh * Tp + i] + (split_lse ? ar[kD + 1] : 0.f);
+    if (lse2_out) lse2_out[row] = split_lse ? lse2_ws[(size_t)bh * Tp + i] + ar[kD + 1] : -lse2_ws[(size_t)bh * Tp + i];
   }
 }
 
 // ------------------------------------------------------------ host launchers
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
                            float *rowsum_out, float *demand_out, int BH, int T, float c2, float eps,
-                           float *lse2_ws, float *acc, cudaStream_t stream) {
+                           float *lse2_ws, float *acc, cudaStream_t stream, cudaEvent_t const *ev) {
   const int Tp = (int)t_pad(T);
+  if (ev[0]) cudaEventRecord(ev[0], stream);
   f32_rowstats<<<dim3(Tp / kF32RowsPerCta, BH), kF32RowsPerCta, 0, stream>>>(q, k, lse2_ws, acc, T, Tp, c2);
   const size_t smem = sizeof(F32SweepSmem);
   cudaError_t e = cudaFuncSetAttribute(f32_sweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (ev[1]) cudaEventRecord(ev[1], stream);
   f32_sweep<<<dim3(Tp / kF32KeysPerCta, BH), kF32KeysPerCta, smem, stream>>>(q, k, v, lse2_ws, acc, demand_out,
                                                                             T, Tp, c2, eps);
   const int64_t threads = (int64_t)BH * T * 16;
+  if (ev[2]) cudaEventRecord(ev[2], stream);
   finalize_kernel<float><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(acc, lse2_ws, out, rowsum_out,
                                                                                 lse2_out, BH, T, Tp, true);
+  if (ev[3]) cudaEventRecord(ev[3], stream);
   return cudaGetLastError();
 }
 

@@ -42,11 +42,14 @@ def _sched_rowstats(BH, T):
 
 def _sched_sweep(BH, T):
     Tp = -(-T // 256) * 256
-    nqt = Tp // 128
+    nqt, nspan = Tp // 128, Tp // 256
+    hg = min(BH, max(1, (64 << 20) // (Tp * 68 * 4)))
     rows = []
-    for c in range(BH * (Tp // 256)):
-        span = c // BH
-        rows.append((c % BH, 2 * span, nqt - 2 * span, 256 * span))
+    for h0 in range(0, BH, hg):
+        heads = list(range(h0, min(BH, h0 + hg)))
+        for span in range(nspan):
+            for bh in heads:
+                rows.append((bh, 2 * span, nqt - 2 * span, 256 * span))
     return np.array(rows, dtype=np.int32).reshape(-1, 4)
 
 

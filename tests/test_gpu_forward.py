@@ -190,3 +190,14 @@ def test_repeatable_and_stream_ordered():
     s.synchronize()
     # fp32 reductions in L2 may add partials in any order: equal to rounding
     assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+
+
+def test_bf16_tau_zero_uniform_bids():
+    # tau = 0: every visible bid is 1/(i+1), whatever q and k
+    T = 300
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 2, T, 64, q_std=1.5, seed=13, dtype="bf16"))
+    got = [host64(x) for x in run_fwd(q, k, v, tau=0.0, eps=1e-6)]
+    ref = oracle_forward(q, k, v, 0.0, 1e-6)
+    for (bb, hh), r in ref.items():
+        check_head([x[bb, hh] for x in got], r, "bf16")
+    assert np.abs(got[1][0, 0] - np.log2(np.arange(1, T + 1))).max() < 2e-3
