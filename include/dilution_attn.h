@@ -32,7 +32,9 @@
  *     and fp32 softmax/demand arithmetic).  tau >= 0 and finite; eps > 0 and
  *     finite (eps = 0 would make masked and underflowed entries 0/0).
  *     B, H, T >= 0; a call with B*H*T == 0 does nothing and returns DA_OK.
- *     T <= DA_MAX_T.
+ *     T <= DA_MAX_T.  The DA_BF16 forward needs eps >= 1e-18 (it forms one
+ *     reciprocal for each pair of denominators, each >= eps); smaller eps
+ *     returns DA_ERR_UNSUPPORTED.
  */
 #ifndef DILUTION_ATTN_H
 #define DILUTION_ATTN_H
@@ -135,15 +137,22 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
  * ---------------------------------------------------------------------- */
 int dilution_attn_get_error(void *workspace, void *stream);
 
+/* Copies the workspace's 4-word status block to host `out` after a device
+ * synchronisation: [0] status, and when a bounded wait timed out, [1] the
+ * shared-memory offset of the mbarrier it waited on, [2] the block index,
+ * [3] the thread index of the first wait that gave up.  Diagnostic only. */
+int dilution_attn_debug_last_timeout(void *workspace, int32_t *out);
+
 /* ------------------------------------------------------------------------
  * Host-only introspection of integer artefacts (no GPU needed).
  *
  * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's
  * kernels for a problem of BH = B*H heads and T tokens.  kernel = 0 (row
- * statistics) or 1 (demand sweep).  For each CTA index c (in launch order),
- * writes 4 int32 to out[4c..4c+3]: head index, first query tile, number of
- * query tiles (row stats: the query tiles it owns; sweep: the query tiles it
- * walks), first key (sweep) or 0.  Returns the number of CTAs; if cap (in
+ * statistics, 128-row query tiles) or 1 (demand sweep, 128-row query tiles,
+ * 384-key spans).  For each CTA index c (in launch order), writes 4 int32 to
+ * out[4c..4c+3]: head index, first query tile, number of query tiles (row
+ * stats: the query tiles it owns; sweep: the query tiles it walks), first key
+ * (sweep) or 0.  Returns the number of CTAs; if cap (in
  * int32 elements) is too small, writes nothing and returns -(needed).
  *
  * dilution_attn_debug_tile_mask: the causal mask the kernels apply to the

@@ -42,6 +42,7 @@ _SIGNATURES = {
     "dilution_attn_decode_step": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                   [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
     "dilution_attn_get_error": (_c_int, [_c_void_p, _c_void_p]),
+    "dilution_attn_debug_last_timeout": (_c_int, [_c_void_p, _c_void_p]),
     "dilution_attn_debug_tile_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_void_p, _c_size_t]),
     "dilution_attn_debug_tile_mask": (_c_int, [_c_int, _c_int, _c_int, _c_void_p]),
 }
@@ -230,6 +231,15 @@ def dilution_attn_status_string(status: int) -> str:
 
 def dilution_attn_version() -> int:
     return int(load().dilution_attn_version())
+
+
+def dilution_attn_debug_last_timeout(workspace):
+    """(status, mbarrier shared-memory offset, block, thread) of the workspace's status block."""
+    import numpy as np
+    buf = np.zeros(4, dtype=np.int32)
+    _check(load().dilution_attn_debug_last_timeout(_ptr(workspace), buf.ctypes.data_as(ctypes.c_void_p)),
+           "dilution_attn_debug_last_timeout")
+    return tuple(int(x) for x in buf)
 
 
 def dilution_attn_debug_tile_schedule(BH: int, T: int, kernel: int):

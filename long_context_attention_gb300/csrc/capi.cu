@@ -98,7 +98,8 @@ int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, v
   int *status = reinterpret_cast<int *>(ws);
   float *lse2_ws = reinterpret_cast<float *>(ws + L.lse2_off);
   float *acc = reinterpret_cast<float *>(ws + L.acc_off);
-  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
+  if (dtype == DA_BF16 && eps < 1e-18f) return DA_ERR_UNSUPPORTED;
+  if (cudaMemsetAsync(status, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   const float c2 = logit_scale_log2(tau, d);
   if (dtype == DA_F32) {
     if (launch_fwd_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse2_out, rowsum_out,
@@ -133,7 +134,7 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
-  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   if (launch_decode(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, (int)BH,
                     logit_scale_log2(tau, d), eps, dtype, reinterpret_cast<float *>(ws + L.logit_off),
                     reinterpret_cast<float2 *>(ws + L.ml_off), reinterpret_cast<float *>(ws + L.acc_off), L.nchunk,
@@ -150,6 +151,13 @@ int dilution_attn_get_error(void *workspace, void *stream_) {
   if (cudaMemcpy(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
   if (host != DA_OK && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return DA_ERR_CUDA;
   return host;
+}
+
+int dilution_attn_debug_last_timeout(void *workspace, int32_t *out) {
+  if (workspace == nullptr || out == nullptr) return DA_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaMemcpy(out, workspace, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+  return DA_OK;
 }
 
 int dilution_attn_debug_tile_schedule(int BH, int T, int kernel, int32_t *out, size_t cap) {

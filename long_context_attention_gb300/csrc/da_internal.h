@@ -20,7 +20,7 @@ namespace da {
 
 constexpr int kD = 64;             // head dimension handled by every kernel
 constexpr int kTile = 128;         // query / key tile edge (one TMEM lane per row)
-constexpr int kSpan = 256;         // keys owned by one demand-sweep CTA (two key tiles)
+constexpr int kSpan = 256;         // Tp granule: two 128-row tiles (one row-statistics CTA)
 constexpr int kAccStride = 68;     // fp32 per accumulator row: 64 numerator + rowsum + 3 pad
 constexpr size_t kStatusBytes = 256;
 
@@ -87,12 +87,15 @@ DA_HD TileWork rowstats_work(int cta, int BH, int64_t T) {
   return w;
 }
 
-// Demand sweep: one CTA per span of 256 keys, walking query tiles from the
-// span's diagonal tile to the last tile.  Heads are taken in groups whose fp32
-// accumulators (Tp x 272 B per head) together stay near 64 MB, so the
-// reductions of the CTAs in flight hit L2; inside a group the spans with the
-// most query tiles launch first.
+// Demand sweep: one CTA per span of 384 keys (three 128-key tiles), walking
+// 128-query tiles from the span's first query tile to the end.  Heads are
+// taken in groups whose fp32 accumulators (Tp x 272 B per head) together stay
+// near 64 MB, so the reductions of the CTAs in flight hit L2; inside a group
+// the spans with the most query tiles launch first.
+constexpr int kSweepKeys = 384;
+constexpr int kSweepQTile = 128;
 constexpr int64_t kAccGroupBytes = 64ll << 20;
+DA_HD int sweep_num_spans(int64_t T) { return (int)((t_pad(T) + kSweepKeys - 1) / kSweepKeys); }
 DA_HD int sweep_head_group(int BH, int64_t T) {
   const int64_t per_head = t_pad(T) * kAccStride * 4;
   int64_t hg = kAccGroupBytes / per_head;
@@ -100,10 +103,10 @@ DA_HD int sweep_head_group(int BH, int64_t T) {
   if (hg > BH) hg = BH;
   return (int)hg;
 }
-DA_HD int sweep_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / kSpan); }
+DA_HD int sweep_num_ctas(int BH, int64_t T) { return BH * sweep_num_spans(T); }
 DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
-  const int nqt = (int)(t_pad(T) / kTile);
-  const int nspan = (int)(t_pad(T) / kSpan);
+  const int nqt = (int)(t_pad(T) / kSweepQTile);
+  const int nspan = sweep_num_spans(T);
   const int hg = sweep_head_group(BH, T);
   const int group = cta / (hg * nspan);
   const int h0 = group * hg;
@@ -112,8 +115,8 @@ DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
   TileWork w;
   w.bh = h0 + r % ng;
   const int span = r / ng;                   // span 0 walks every query tile
-  w.key0 = span * kSpan;
-  w.q_tile0 = span * (kSpan / kTile);
+  w.key0 = span * kSweepKeys;
+  w.q_tile0 = w.key0 / kSweepQTile;
   w.n_q_tiles = nqt - w.q_tile0;
   return w;
 }

@@ -57,9 +57,15 @@ struct WaitCtx {
   int *status;               // global status word (workspace)
 };
 
-__device__ __forceinline__ void raise_timeout(const WaitCtx &w) {
+// The first wait that gives up also records where: status[1] = shared-memory
+// offset of its mbarrier, status[2] = block index, status[3] = thread index.
+__device__ __forceinline__ void raise_timeout(const WaitCtx &w, const void *bar) {
   *w.abort_flag = 1;
-  atomicExch(w.status, DA_ERR_TIMEOUT);
+  if (atomicCAS(w.status, DA_OK, DA_ERR_TIMEOUT) == DA_OK) {
+    w.status[1] = (int)smem_u32(bar);
+    w.status[2] = (int)blockIdx.x;
+    w.status[3] = (int)threadIdx.x;
+  }
 }
 
 // try_wait with a suspend-time hint: the thread sleeps until the phase
@@ -83,7 +89,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*w.abort_flag) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
-      raise_timeout(w);
+      raise_timeout(w, bar);
       return false;
     }
   }

@@ -14,7 +14,7 @@
 //     c2 = tau / sqrt(d) * log2(e).  Also zeroes the rows of the fp32
 //     accumulator that the sweep adds into.
 //
-//  sweep_kernel  (one CTA per span of 256 keys, both tiles resident in smem)
+//  sweep_kernel  (one CTA per span of 384 keys, all three tiles resident in smem)
 //     Walks the query tiles from the span's diagonal to the end, in causal
 //     order.  S^T = K Q^T puts keys on TMEM lanes, so each thread owns one key
 //     and carries that key's demand (committed + eps) in a register across
@@ -25,16 +25,17 @@
 //     shares (bf16) are written to shared memory as the MN-major A operand of
 //     a second tcgen05 product, share^T [V | 1]: TMEM columns 0..63 collect
 //     sum_k share_ik v_k and columns 64..79 sum_k share_ik (a constant all-ones
-//     B operand).  An epilogue warpgroup adds each query tile's partials into
-//     acc[row][0..64] with vector fp32 reductions in L2.
+//     block).  An epilogue warpgroup adds each query tile's partials into
+//     acc[row][0..64] with vector fp32 reductions in L2.  The share^T [V | 1]
+//     product is one M = 128, N = 80 instruction per 16 keys.
 //
 //  finalize (fwd_f32.cu) divides the numerator by the row sum.
 //
 // Warp specialisation, all waits bounded (timeout -> DA_ERR_TIMEOUT):
 //   rowstats: warps 0-3 / 4-7 = softmax-statistics warpgroups for the two
 //             query tiles, warp 8 = TMA producer, warp 9 = MMA issuer.
-//   sweep:    warps 0-3 / 4-7 = demand warpgroups (key tiles 0 / 1 of the
-//             span), warps 8-11 = epilogue, warp 12 = TMA, warp 13 = MMA.
+//   sweep:    warps 0-11 = demand warpgroups (key tiles 0..2 of the span),
+//             warps 12-15 = epilogue, warp 16 = TMA, warp 17 = MMA.
 #include "da_internal.h"
 #include "da_ptx.cuh"
 
@@ -110,13 +111,31 @@ struct RowStat {
   }
 };
 
+// Reciprocal on the FMA pipe: a linear seed from the float's bit pattern
+// (integer subtraction from a magic constant, which negates the exponent and
+// approximately inverts the mantissa; max relative error ~5%) refined by two
+// Newton-Raphson steps y <- y (2 - q y), each squaring the relative error
+// (6.6e-6 max after two steps over normal floats).  Two values per packed op.
+__device__ __forceinline__ float2 rcp2_newton(float2 q) {
+  float2 y = make_float2(__int_as_float(0x7EF311C3 - __float_as_int(q.x)),
+                         __int_as_float(0x7EF311C3 - __float_as_int(q.y)));
+  const float2 one = make_float2(1.f, 1.f), nq = make_float2(-q.x, -q.y);
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const float2 e = ffma2(nq, y, one);
+    y = ffma2(y, e, y);
+  }
+  return y;
+}
+
 // Demand step for 32 consecutive queries (columns col0 ..) of one key row:
 //   p = 2^(s*c2 - lse2),  den = (committed + eps) + p,  share = p / den,
 //   committed + eps <- den   (queries in causal order: the exclusive cumsum).
-// nl holds -lse2 of those queries (shared memory, read as float4).  DIAG
-// zeroes the bids of queries before the key (key row > query column).
-template <bool DIAG>
-__device__ __forceinline__ void demand_chunk(const float (&s)[32], const float *nl, int col0, int row, float c2,
+// nl holds -lse2 of those queries (shared memory, read as float4).  MASK
+// zeroes the bids of queries before the key: key row `row` is after query
+// column c when row_eff > c, row_eff = row - (first query - first key).
+template <bool MASK>
+__device__ __forceinline__ void demand_chunk(const float (&s)[32], const float *nl, int col0, int row_eff, float c2,
                                              float &ceps, uint32_t (&pk)[16]) {
   const float4 *nl4 = reinterpret_cast<const float4 *>(nl);
   const float2 c2v = make_float2(c2, c2);
@@ -131,22 +150,30 @@ __device__ __forceinline__ void demand_chunk(const float (&s)[32], const float *
     p[4 * i + 2] = ex2_approx(x1.x);
     p[4 * i + 3] = ex2_approx(x1.y);
   }
-  if (DIAG) {
+  if (MASK) {
 #pragma unroll
     for (int c = 0; c < 32; ++c)
-      if (row > col0 + c) p[c] = 0.f;
+      if (row_eff > col0 + c) p[c] = 0.f;
   }
-  float r[32];
+  float d[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    const float den = ceps + p[c];
-    r[c] = rcp_approx(den);
-    ceps = den;
+    d[c] = ceps + p[c];
+    ceps = d[c];
   }
+  // One reciprocal per pair of consecutive queries: r = 1 / (d0 d1),
+  // share0 = p0 d1 r, share1 = p1 d0 r.  d0, d1 lie in [eps, T + 1], so
+  // d0 d1 stays a normal float for eps >= 1e-18.
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 sh = fmul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(r[2 * i], r[2 * i + 1]));
-    pk[i] = pack_bf16x2(sh.x, sh.y);
+  for (int i = 0; i < 16; i += 2) {
+    const float2 q = fmul2(make_float2(d[2 * i], d[2 * i + 2]), make_float2(d[2 * i + 1], d[2 * i + 3]));
+    const float2 r = rcp2_newton(q);
+    const float2 sh0 =
+        fmul2(fmul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(d[2 * i + 1], d[2 * i])), make_float2(r.x, r.x));
+    const float2 sh1 = fmul2(fmul2(make_float2(p[2 * i + 2], p[2 * i + 3]), make_float2(d[2 * i + 3], d[2 * i + 2])),
+                             make_float2(r.y, r.y));
+    pk[i] = pack_bf16x2(sh0.x, sh0.y);
+    pk[i + 1] = pack_bf16x2(sh1.x, sh1.y);
   }
 }
 
@@ -324,21 +351,44 @@ __global__ void __launch_bounds__(kRsThreads, 2)
 // ============================================================================
 // Demand sweep
 // ============================================================================
-constexpr int kSwThreads = 448;
-constexpr int kSwQStages = 3;
-constexpr uint32_t kShBytes = 2 * 16 * 1024;   // share^T tile: 2 M-blocks x 16 K-groups x 1024 B
-// Shared-memory map (offsets from the 1024-aligned base).
-constexpr uint32_t kSwOffK = 0;                                  // 2 key tiles (resident)
-constexpr uint32_t kSwOffV = kSwOffK + 2 * kTileBytes;           // 2 value tiles (resident)
-constexpr uint32_t kSwOffQ = kSwOffV + 2 * kTileBytes;           // query ring
-constexpr uint32_t kSwOffSh = kSwOffQ + kSwQStages * kTileBytes; // share^T, one per key tile
-constexpr uint32_t kSwOffOnes = kSwOffSh + 2 * kShBytes;         // 16 x 64 bf16 ones (2 KB)
-constexpr uint32_t kSwOffL = kSwOffOnes + 2048;                  // -lse2 ring (512 B per stage)
-constexpr uint32_t kSwOffBar = kSwOffL + kSwQStages * 512;
-constexpr int kSwSmemBytes = kSwOffBar + 256 + 1024;
+// One CTA per span of 384 keys (three 128-key tiles, resident with their
+// values).  For each 128-query tile, in causal order:
+//   S^T_g = K_g Q^T (M = 128 keys, N = 128 queries) into TMEM slot g;
+//   demand warpgroup g turns its slot into shares (bf16, shared memory) = the
+//   MN-major A operand of D[q, 0:80] += share^T [V_g | 1] (M = 128 queries,
+//   N = 80: the value tile and, through the descriptor's leading-byte offset,
+//   a 2 KB block of ones whose product is the share row sum); the epilogue
+//   adds D into acc[row][0..64].
+// Every tcgen05.mma costs at least ~46 cycles on this part and reaches full
+// rate only at M = 128, N >= 128, which is why the query tile is 128 wide and
+// the row sum rides in the same instruction as the value product.
+constexpr int kSwG = kSweepKeys / kTile;        // 3 demand warpgroups, one per key tile
+constexpr int kSwBQ = kSweepQTile;              // 128 queries per tile
+constexpr int kSwWarps = (kSwG + 2) * 4;        // demand WGs, epilogue WG, producer/MMA WG
+constexpr int kSwThreads = kSwWarps * 32;       // 640
+// Register split across warpgroups (setmaxnreg).  The block is launched with
+// 640 x (registers per thread) registers; the split below must not exceed that
+// (checked on the host before every launch).
+constexpr int kSwRegsDemand = 120, kSwRegsEpi = 56, kSwRegsCtl = 48;
+constexpr int kSwRegsNeeded = 128 * (kSwG * kSwRegsDemand + kSwRegsEpi + kSwRegsCtl);
+constexpr int kSwLStages = 2;
+constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key groups x 1 KB
+constexpr uint32_t kSwOffK = 0;
+constexpr uint32_t kSwOffV = kSwOffK + kSwG * kTileBytes;
+constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // one query tile (released early)
+constexpr uint32_t kSwOffSh = kSwOffQ + kTileBytes;
+constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO)
+constexpr uint32_t kSwOffL = kSwOffOnes + 2048;
+constexpr uint32_t kSwOffBar = kSwOffL + kSwLStages * kSwBQ * 4;
+constexpr int kSwSmemBytes = kSwOffBar + 512 + 1024;
+static_assert(kSwSmemBytes <= 232448, "sweep shared memory");
+static_assert(kSwRegsNeeded <= 65536, "sweep register split");
 
-constexpr uint32_t kTmemS = 0;      // S^T of key tile g at columns g*128 .. g*128+127
-constexpr uint32_t kTmemD = 256;    // partials of query tile t at 256 + (t&1)*128: 64 numerator + 16 rowsum
+constexpr uint32_t kTmemD = kSwG * kTile;   // S^T slots at g*128; D (80 columns) after them
+
+__device__ __forceinline__ void regs_inc_demand() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSwRegsDemand)); }
+__device__ __forceinline__ void regs_dec_epi() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsEpi)); }
+__device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsCtl)); }
 
 __global__ void __launch_bounds__(kSwThreads, 1)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -355,45 +405,50 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const float *sL = reinterpret_cast<const float *>(smem + kSwOffL);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSwOffBar);
   uint64_t *kv_full = bars;
-  uint64_t *q_full = bars + 1;
-  uint64_t *q_empty = q_full + kSwQStages;
-  uint64_t *s_full = q_empty + kSwQStages;
-  uint64_t *s_free = s_full + 2;
-  uint64_t *sh_full = s_free + 2;
-  uint64_t *sh_free = sh_full + 2;
-  uint64_t *d_full = sh_free + 2;
-  uint64_t *d_free = d_full + 2;
-  uint64_t *drain = d_free + 2;
+  uint64_t *q_full = kv_full + 1;
+  uint64_t *q_empty = q_full + 1;
+  uint64_t *l_full = q_empty + 1;              // [kSwLStages]
+  uint64_t *l_empty = l_full + kSwLStages;     // [kSwLStages]
+  uint64_t *s_full = l_empty + kSwLStages;     // [g]
+  uint64_t *s_free = s_full + kSwG;            // [g]
+  uint64_t *sh_full = s_free + kSwG;           // [g]
+  uint64_t *sh_free = sh_full + kSwG;          // [g]
+  uint64_t *d_full = sh_free + kSwG;
+  uint64_t *d_free = d_full + 1;
+  uint64_t *drain = d_free + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wg = warp / 4;
+  const int kWarpProd = (kSwG + 1) * 4, kWarpMma = kWarpProd + 1;
   const TileWork w = sweep_work(blockIdx.x, BH, T);
   const int nt = w.n_q_tiles;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < kSwQStages; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1 + 8);   // MMA commit + the 8 demand warps (done with lse2)
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < kSwLStages; ++i) {
+      mbar_init(&l_full[i], 1);
+      mbar_init(&l_empty[i], 4 * kSwG);   // every demand warp is done with that -lse2 stage
     }
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < kSwG; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&s_free[g], 4);
       mbar_init(&sh_full[g], 4);
       mbar_init(&sh_free[g], 1);
-      mbar_init(&d_full[g], 1);
-      mbar_init(&d_free[g], 4);
     }
+    mbar_init(d_full, 1);
+    mbar_init(d_free, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // Constant all-ones B operand for the share row sums.
-  for (int e = threadIdx.x; e < 2048 / 4; e += kSwThreads)
-    reinterpret_cast<uint32_t *>(sOnes)[e] = 0x3F803F80u;
+  // Constant all-ones block: the N = 64..79 part of the value operand.
+  for (int e = threadIdx.x; e < 2048 / 4; e += kSwThreads) reinterpret_cast<uint32_t *>(sOnes)[e] = 0x3F803F80u;
   fence_proxy_async_smem();
-  if (warp == 13) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -402,77 +457,78 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, status};
 
-  if (warp == 12) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (wg == kSwG + 1) {
+    regs_dec_ctl();
+    if (warp == kWarpProd && lane == 0) {
+      // ---------------------------------------------------------- producer
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(kv_full, 4 * kTileBytes);
-      for (int g = 0; g < 2; ++g) {
+      mbar_arrive_expect_tx(kv_full, 2 * kSwG * kTileBytes);
+      for (int g = 0; g < kSwG; ++g) {
         tma_load_3d(sK + g * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
         tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
       }
-      int issued = 0;
+      int q_issued = 0, l_issued = 0;
       for (int t = 0; t < nt; ++t) {
-        const int s = t % kSwQStages;
-        if (!mbar_wait(&q_empty[s], ((t / kSwQStages) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&q_full[s], kTileBytes + 512);
-        const int qrow = (w.q_tile0 + t) * kTile;
-        tma_load_3d(sQ + s * kTileBytes, &tmQ, &q_full[s], 0, qrow, w.bh);
-        bulk_load(smem + kSwOffL + s * 512, nlse2 + (size_t)w.bh * Tp + qrow, 512, &q_full[s]);
-        ++issued;
+        const int qrow = (w.q_tile0 + t) * kSwBQ;
+        const int ls = t % kSwLStages;
+        if (!mbar_wait(&l_empty[ls], ((t / kSwLStages) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&l_full[ls], kSwBQ * 4);
+        bulk_load(smem + kSwOffL + ls * kSwBQ * 4, nlse2 + (size_t)w.bh * Tp + qrow, kSwBQ * 4, &l_full[ls]);
+        ++l_issued;
+        // the query tile's single slot frees as soon as the S products of the previous tile are done
+        if (!mbar_wait(q_empty, (t & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        tma_load_3d(sQ, &tmQ, q_full, 0, qrow, w.bh);
+        ++q_issued;
       }
       if (*abort_flag) {
         drain_wait(kv_full, 0);
-        for (int t = (issued > kSwQStages ? issued - kSwQStages : 0); t < issued; ++t)
-          drain_wait(&q_full[t % kSwQStages], (t / kSwQStages) & 1);
+        if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1);
+        for (int t = (l_issued > kSwLStages ? l_issued - kSwLStages : 0); t < l_issued; ++t)
+          drain_wait(&l_full[t % kSwLStages], (t / kSwLStages) & 1);
       }
-    }
-  } else if (warp == 13) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_s = idesc_bf16(kTile, kTile, false, false);
-      const uint32_t idesc_pv = idesc_bf16(kTile, kD, true, true);
-      const uint32_t idesc_rs = idesc_bf16(kTile, 16, true, false);
-      const uint64_t ones_desc = smem_desc(smem_u32(sOnes), 16, 1024);
+    } else if (warp == kWarpMma && lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      const uint32_t idesc_s = idesc_bf16(kTile, kSwBQ, false, false);
+      const uint32_t idesc_pv = idesc_bf16(kSwBQ, kD + 16, true, true);
+      const uint32_t ones_addr = smem_u32(sOnes);
       auto issue_s = [&](int t) -> bool {
-        const int s = t % kSwQStages;
-        if (!mbar_wait(&q_full[s], (t / kSwQStages) & 1, wc)) return false;
+        if (!mbar_wait(q_full, t & 1, wc)) return false;
         tc_fence_after();
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < kSwG; ++g) {
           if (!mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)
-            mma_bf16(tmem + kTmemS + g * kTile, kmajor_desc(sK + g * kTileBytes, kk),
-                     kmajor_desc(sQ + s * kTileBytes, kk), idesc_s, kk > 0);
+            mma_bf16(tmem + g * kTile, kmajor_desc(sK + g * kTileBytes, kk), kmajor_desc(sQ, kk), idesc_s, kk > 0);
           mma_commit(&s_full[g]);
         }
-        mma_commit(&q_empty[s]);
+        mma_commit(q_empty);
         return true;
       };
       auto issue_pv = [&](int t) -> bool {
-        const int b = t & 1;
-        if (!mbar_wait(&d_free[b], ((t >> 1) & 1) ^ 1, wc)) return false;
+        if (!mbar_wait(d_free, (t & 1) ^ 1, wc)) return false;
         tc_fence_after();
-        const uint32_t dcol = tmem + kTmemD + b * 128;
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < kSwG; ++g) {
           if (!mbar_wait(&sh_full[g], t & 1, wc)) return false;
           tc_fence_after();
+          const uint32_t sh = smem_u32(sSh + g * kShBytes);
+          const uint32_t vg = smem_u32(sV + g * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
-            const uint64_t a = smem_desc(smem_u32(sSh + g * kShBytes) + kk * 2048, 16384, 1024);
-            // V tile as an MN-major B operand: 8-key groups 1 KB apart; one 64-wide N block.
-            const uint64_t bv = smem_desc(smem_u32(sV + g * kTileBytes) + kk * 2048, 8192, 1024);
-            const uint32_t accum = (g > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16(dcol, a, bv, idesc_pv, accum);
-            mma_bf16(dcol + kD, a, ones_desc, idesc_rs, accum);
+            const uint64_t a = smem_desc(sh + kk * 2048, 16384, 1024);
+            // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO away)
+            // = the ones block, of which N = 64..79 are read.
+            const uint32_t vstart = vg + kk * 2048;
+            const uint64_t bv = smem_desc(vstart, ones_addr - vstart, 1024);
+            mma_bf16(tmem + kTmemD, a, bv, idesc_pv, (g > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&sh_free[g]);
         }
-        mma_commit(&d_full[b]);
+        mma_commit(d_full);
         return true;
       };
       if (mbar_wait(kv_full, 0, wc)) {
@@ -486,61 +542,65 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       mma_commit(drain);
       drain_wait(drain, 0);
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ epilogue
+  } else if (wg == kSwG) {
+    // -------------------------------------------------------------- epilogue
+    regs_dec_epi();
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;
     for (int t = 0; t < nt; ++t) {
-      const int b = t & 1;
-      if (!mbar_wait(&d_full[b], (t >> 1) & 1, wc)) break;
+      if (!mbar_wait(d_full, t & 1, wc)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + kTmemD + b * 128 + ((uint32_t)(quarter * 32) << 16);
-      float a0[32], a1[32], rs;
-      tmem_ld32(taddr, a0);
-      tmem_ld32(taddr + 32, a1);
-      tmem_ld1(taddr + kD, rs);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&d_free[b]);
-      const int64_t qi = (int64_t)(w.q_tile0 + t) * kTile + row;
+      const uint32_t taddr = tmem + kTmemD + ((uint32_t)(quarter * 32) << 16);
+      const int64_t qi = (int64_t)(w.q_tile0 + t) * kSwBQ + row;
+      float *dst = acc + ((size_t)w.bh * Tp + qi) * kAccStride;
+      float a[32], rs;
+      tmem_ld32(taddr, a);
+      tmem_wait_ld_r(a);
       if (qi < T) {
-        float *dst = acc + ((size_t)w.bh * Tp + qi) * kAccStride;
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) red_add_v4(dst + c, a0[c], a0[c + 1], a0[c + 2], a0[c + 3]);
+        for (int c = 0; c < 32; c += 4) red_add_v4(dst + c, a[c], a[c + 1], a[c + 2], a[c + 3]);
+      }
+      tmem_ld32(taddr + 32, a);
+      tmem_ld1(taddr + kD, rs);
+      tmem_wait_ld_r(a);
+      tmem_wait_ld();
+      release_tmem(d_free, lane);
+      if (qi < T) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) red_add_v4(dst + 32 + c, a1[c], a1[c + 1], a1[c + 2], a1[c + 3]);
+        for (int c = 0; c < 32; c += 4) red_add_v4(dst + 32 + c, a[c], a[c + 1], a[c + 2], a[c + 3]);
         atomicAdd(dst + kD, rs);
       }
     }
   } else {
-    // -------------------------------------------- demand warpgroups (2 WGs)
-    const int g = warp / 4;
+    // ----------------------------------------------------- demand warpgroups
+    regs_inc_demand();
+    const int g = wg;
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;            // key row inside the key tile
     const int kbase = w.key0 + g * kTile;           // first key of this warpgroup's tile
-    const uint32_t tbase = tmem + kTmemS + g * kTile + ((uint32_t)(quarter * 32) << 16);
-    uint8_t *sh_rows = sSh + g * kShBytes + (row / 8) * 1024 + (row % 8) * 128;
     const int swz = row % 8;
+    const uint32_t tb = tmem + g * kTile + ((uint32_t)(quarter * 32) << 16);
+    uint8_t *sh_row = sSh + g * kShBytes + (row / 8) * 1024 + (row % 8) * 128;
     float ceps = eps;   // committed + eps: demand this key received from earlier queries
-    // 32 shares (bf16 pairs) of query chunk c -> the share^T operand:
-    // 64-query M-block c/2, 16-byte pieces (c%2)*4 .. +3, 128B-swizzled by key row.
+    // 32 shares (bf16 pairs) of query chunk c -> 64-query M-block c/2, 16-byte
+    // pieces (c%2)*4 .. +3 of this key's row, 128B-swizzled by row.
     auto store = [&](const uint32_t (&pk)[16], int c) {
-      uint8_t *dst = sh_rows + (c >> 1) * 16384;
+      uint8_t *dst = sh_row + (c >> 1) * 16384;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         *reinterpret_cast<uint4 *>(dst + ((((c & 1) * 4 + i) ^ swz) * 16)) =
             make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     };
     for (int t = 0; t < nt; ++t) {
-      const int s = t % kSwQStages;
-      const int j = w.q_tile0 + t;
-      const bool all_masked = kbase > j * kTile;    // every key after every query of the tile
-      const bool diag = kbase == j * kTile;
-      if (!mbar_wait(&q_full[s], (t / kSwQStages) & 1, wc)) break;
+      const int ls = t % kSwLStages;
+      const int qlo = (w.q_tile0 + t) * kSwBQ;      // first query of the tile
+      const bool all_masked = kbase > qlo + kSwBQ - 1 || kbase >= T;
+      const bool need_mask = kbase + kTile - 1 > qlo;
+      const int row_eff = row - (qlo - kbase);      // key after query col iff row_eff > col
+      if (!mbar_wait(&l_full[ls], (t / kSwLStages) & 1, wc)) break;
       if (!mbar_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
-      const float *nl = sL + s * 128;   // -lse2 of the tile's 128 queries
+      const float *nl = sL + ls * kSwBQ;   // -lse2 of the tile's queries
       uint32_t pk[16];
       if (all_masked) {
         release_tmem(&s_free[g], lane);
@@ -552,35 +612,35 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       } else {
         // 32-column chunks; the load of chunk c+1 is in flight while chunk c is formed.
         float A[32], B[32];
-        tmem_ld32(tbase, A);
+        tmem_ld32(tb, A);
         tmem_wait_ld_r(A);
-        tmem_ld32(tbase + 32, B);
-        if (diag) demand_chunk<true>(A, nl, 0, row, c2, ceps, pk);
-        else demand_chunk<false>(A, nl, 0, row, c2, ceps, pk);
+        tmem_ld32(tb + 32, B);
+        if (need_mask) demand_chunk<true>(A, nl, 0, row_eff, c2, ceps, pk);
+        else demand_chunk<false>(A, nl, 0, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
         if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
         store(pk, 0);
         tmem_wait_ld_r(B);
-        tmem_ld32(tbase + 64, A);
-        if (diag) demand_chunk<true>(B, nl + 32, 32, row, c2, ceps, pk);
-        else demand_chunk<false>(B, nl + 32, 32, row, c2, ceps, pk);
+        tmem_ld32(tb + 64, A);
+        if (need_mask) demand_chunk<true>(B, nl + 32, 32, row_eff, c2, ceps, pk);
+        else demand_chunk<false>(B, nl + 32, 32, row_eff, c2, ceps, pk);
         store(pk, 1);
         tmem_wait_ld_r(A);
-        tmem_ld32(tbase + 96, B);
-        if (diag) demand_chunk<true>(A, nl + 64, 64, row, c2, ceps, pk);
-        else demand_chunk<false>(A, nl + 64, 64, row, c2, ceps, pk);
+        tmem_ld32(tb + 96, B);
+        if (need_mask) demand_chunk<true>(A, nl + 64, 64, row_eff, c2, ceps, pk);
+        else demand_chunk<false>(A, nl + 64, 64, row_eff, c2, ceps, pk);
         store(pk, 2);
         tmem_wait_ld_r(B);
         release_tmem(&s_free[g], lane);
-        if (diag) demand_chunk<true>(B, nl + 96, 96, row, c2, ceps, pk);
-        else demand_chunk<false>(B, nl + 96, 96, row, c2, ceps, pk);
+        if (need_mask) demand_chunk<true>(B, nl + 96, 96, row_eff, c2, ceps, pk);
+        else demand_chunk<false>(B, nl + 96, 96, row_eff, c2, ceps, pk);
         store(pk, 3);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sh_full[g]);
-        mbar_arrive(&q_empty[s]);
+        mbar_arrive(&l_empty[ls]);
       }
     }
     const int64_t key = (int64_t)kbase + row;
@@ -589,7 +649,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -617,14 +677,14 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [BH, T, 64] bf16 viewed as a 3-D tensor; box = one 128-row tile of one head.
-// Rows past T read as zero.
-static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T) {
+// [BH, T, 64] bf16 viewed as a 3-D tensor; box = one tile of `rows` rows of
+// one head.  Rows past T read as zero.
+static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int rows = kTile) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)T, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)T * kD * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)kTile, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -650,6 +710,13 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
         cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes) !=
             cudaSuccess)
       return DA_ERR_CUDA;
+    // The sweep's warpgroups re-split the block's registers (setmaxnreg); a
+    // split larger than what the block is launched with would never resolve,
+    // so refuse to launch unless the compiled register count covers it.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, sweep_kernel) != cudaSuccess) return DA_ERR_CUDA;
+    if (fa.numRegs * kSwThreads < kSwRegsNeeded || fa.numRegs > kSwRegsDemand || fa.numRegs < kSwRegsEpi)
+      return DA_ERR_UNSUPPORTED;
     if (dev < 64) attr_done[dev] = true;
   }
   const int Tp = (int)t_pad(T);

@@ -42,14 +42,14 @@ def _sched_rowstats(BH, T):
 
 def _sched_sweep(BH, T):
     Tp = -(-T // 256) * 256
-    nqt, nspan = Tp // 128, Tp // 256
+    nqt, nspan = Tp // 128, -(-Tp // 384)
     hg = min(BH, max(1, (64 << 20) // (Tp * 68 * 4)))
     rows = []
     for h0 in range(0, BH, hg):
         heads = list(range(h0, min(BH, h0 + hg)))
         for span in range(nspan):
             for bh in heads:
-                rows.append((bh, 2 * span, nqt - 2 * span, 256 * span))
+                rows.append((bh, 3 * span, nqt - 3 * span, 384 * span))
     return np.array(rows, dtype=np.int32).reshape(-1, 4)
 
 
@@ -60,17 +60,19 @@ def test_tile_schedules_bit_exact(lib, BH, T):
 
 
 def test_tile_schedules_cover_triangle_once():
-    # every (head, key tile, query tile) pair with key tile <= query tile is
-    # visited by exactly one sweep CTA, and every query tile by one row-stats CTA
+    # every (head, key, query) pair with key <= query < Tp is visited by exactly
+    # one sweep CTA (128-key tiles x 128-query tiles), every 128-row query tile
+    # by one row-statistics CTA
     BH, T = 3, 1000
     Tp = 1024
     seen = {}
     for bh, q0, n, key0 in b.dilution_attn_debug_tile_schedule(BH, T, 1):
-        for kt in (key0 // 128, key0 // 128 + 1):
+        for kt in range(key0 // 128, key0 // 128 + 3):
             for qt in range(q0, q0 + n):
-                if kt <= qt:
+                if kt * 128 < Tp and kt * 128 <= qt * 128 + 127:
                     seen[(bh, kt, qt)] = seen.get((bh, kt, qt), 0) + 1
-    want = {(bh, kt, qt) for bh in range(BH) for qt in range(Tp // 128) for kt in range(qt + 1)}
+    want = {(bh, kt, qt) for bh in range(BH) for qt in range(Tp // 128) for kt in range(Tp // 128)
+            if kt * 128 <= qt * 128 + 127}
     assert set(seen) == want and all(v == 1 for v in seen.values())
     rs = b.dilution_attn_debug_tile_schedule(BH, T, 0)
     tiles = sorted((int(r[0]), int(r[1]) + i) for r in rs for i in range(r[2]))
@@ -110,6 +112,8 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, tau=-0.5) == b.DA_ERR_INVALID
     assert _fwd(lib, tau=float("inf")) == b.DA_ERR_INVALID
     assert _fwd(lib, d=128) == b.DA_ERR_UNSUPPORTED
+    assert _fwd(lib, eps=1e-20) == b.DA_ERR_UNSUPPORTED        # bf16 path: eps >= 1e-18
+    assert _fwd(lib, eps=1e-20, dtype=0, ws=None) == b.DA_ERR_WORKSPACE   # fp32 path accepts it
     assert _fwd(lib, T=(1 << 24) + 1) == b.DA_ERR_UNSUPPORTED
     assert _fwd(lib, B=-1) == b.DA_ERR_INVALID
     assert _fwd(lib, dtype=7) == b.DA_ERR_INVALID
