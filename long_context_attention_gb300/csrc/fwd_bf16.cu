@@ -111,23 +111,6 @@ struct RowStat {
   }
 };
 
-// Reciprocal on the FMA pipe: a linear seed from the float's bit pattern
-// (integer subtraction from a magic constant, which negates the exponent and
-// approximately inverts the mantissa; max relative error ~5%) refined by two
-// Newton-Raphson steps y <- y (2 - q y), each squaring the relative error
-// (6.6e-6 max after two steps over normal floats).  Two values per packed op.
-__device__ __forceinline__ float2 rcp2_newton(float2 q) {
-  float2 y = make_float2(__int_as_float(0x7EF311C3 - __float_as_int(q.x)),
-                         __int_as_float(0x7EF311C3 - __float_as_int(q.y)));
-  const float2 one = make_float2(1.f, 1.f), nq = make_float2(-q.x, -q.y);
-#pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const float2 e = ffma2(nq, y, one);
-    y = ffma2(y, e, y);
-  }
-  return y;
-}
-
 // Demand step for 32 consecutive queries (columns col0 ..) of one key row:
 //   p = 2^(s*c2 - lse2),  den = (committed + eps) + p,  share = p / den,
 //   committed + eps <- den   (queries in causal order: the exclusive cumsum).
@@ -163,17 +146,15 @@ __device__ __forceinline__ void demand_chunk(const float (&s)[32], const float *
   }
   // One reciprocal per pair of consecutive queries: r = 1 / (d0 d1),
   // share0 = p0 d1 r, share1 = p1 d0 r.  d0, d1 lie in [eps, T + 1], so
-  // d0 d1 stays a normal float for eps >= 1e-18.
+  // d0 d1 stays a normal float for eps >= 1e-18.  (Measured on GB300: the
+  // MUFU reciprocal of the pair product beats a Newton iteration on the FMA
+  // pipe, whose extra instructions cost more issue slots than they save.)
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const float2 q = fmul2(make_float2(d[2 * i], d[2 * i + 2]), make_float2(d[2 * i + 1], d[2 * i + 3]));
-    const float2 r = rcp2_newton(q);
-    const float2 sh0 =
-        fmul2(fmul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(d[2 * i + 1], d[2 * i])), make_float2(r.x, r.x));
-    const float2 sh1 = fmul2(fmul2(make_float2(p[2 * i + 2], p[2 * i + 3]), make_float2(d[2 * i + 3], d[2 * i + 2])),
-                             make_float2(r.y, r.y));
-    pk[i] = pack_bf16x2(sh0.x, sh0.y);
-    pk[i + 1] = pack_bf16x2(sh1.x, sh1.y);
+  for (int i = 0; i < 16; ++i) {
+    const float r = rcp_approx(d[2 * i] * d[2 * i + 1]);
+    const float2 sh = fmul2(fmul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(d[2 * i + 1], d[2 * i])),
+                            make_float2(r, r));
+    pk[i] = pack_bf16x2(sh.x, sh.y);
   }
 }
 
