@@ -350,7 +350,7 @@ constexpr int kSwThreads = kSwWarps * 32;       // 640
 // Register split across warpgroups (setmaxnreg).  The block is launched with
 // 640 x (registers per thread) registers; the split below must not exceed that
 // (checked on the host before every launch).
-constexpr int kSwRegsDemand = 120, kSwRegsEpi = 56, kSwRegsCtl = 48;
+constexpr int kSwRegsDemand = 120, kSwRegsEpi = 56, kSwRegsCtl = 56;
 constexpr int kSwRegsNeeded = 128 * (kSwG * kSwRegsDemand + kSwRegsEpi + kSwRegsCtl);
 constexpr int kSwLStages = 2;
 constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key groups x 1 KB
@@ -472,52 +472,92 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       }
     } else if (warp == kWarpMma && lane == 0) {
       // -------------------------------------------------------- MMA issuer
+      // Event-driven: each demand warpgroup's S product and share.[V|1]
+      // product are issued as soon as that warpgroup's own barriers allow, so
+      // a fast warpgroup is not held to the slowest one's pace.  Order
+      // constraints: S(t)[g] for all g read the single query slot (reloaded
+      // once all of them completed); PV(t)[g] for all g accumulate into the
+      // one D buffer, which must have been drained of tile t-1.
       const uint32_t idesc_s = idesc_bf16(kTile, kSwBQ, false, false);
       const uint32_t idesc_pv = idesc_bf16(kSwBQ, kD + 16, true, true);
       const uint32_t ones_addr = smem_u32(sOnes);
-      auto issue_s = [&](int t) -> bool {
-        if (!mbar_wait(q_full, t & 1, wc)) return false;
-        tc_fence_after();
+      int s_next[kSwG], pv_next[kSwG];
+      for (int g = 0; g < kSwG; ++g) s_next[g] = pv_next[g] = 0;
+      int q_ready_tile = -1;    // query tile held (and waited for) in the slot
+      int s_issued_tile = 0;    // warpgroups that issued S for tile q_ready_tile
+      int d_tile = -1;          // tile whose products accumulate in D
+      int pv_in_tile = 0;       // warpgroups whose PV of d_tile were issued
+      bool ok = mbar_wait(kv_full, 0, wc);
+      if (ok) tc_fence_after();
+      unsigned long long t_last = globaltimer();
+      int remaining = ok ? 2 * kSwG * nt : 0;
+      while (remaining > 0) {
+        bool progress = false;
         for (int g = 0; g < kSwG; ++g) {
-          if (!mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) return false;
-          tc_fence_after();
+          // S(t)[g] = K_g Q(t)^T into slot g
+          const int ts = s_next[g];
+          if (ts < nt && ts <= q_ready_tile + 1) {
+            bool q_ok = ts == q_ready_tile;
+            if (!q_ok && s_issued_tile == kSwG * (q_ready_tile >= 0) && mbar_try_wait(q_full, ts & 1)) {
+              q_ready_tile = ts;
+              s_issued_tile = 0;
+              q_ok = true;
+            }
+            if (q_ok && mbar_try_wait(&s_free[g], (ts & 1) ^ 1)) {
+              tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_bf16(tmem + g * kTile, kmajor_desc(sK + g * kTileBytes, kk), kmajor_desc(sQ, kk), idesc_s, kk > 0);
-          mma_commit(&s_full[g]);
-        }
-        mma_commit(q_empty);
-        return true;
-      };
-      auto issue_pv = [&](int t) -> bool {
-        if (!mbar_wait(d_free, (t & 1) ^ 1, wc)) return false;
-        tc_fence_after();
-        for (int g = 0; g < kSwG; ++g) {
-          if (!mbar_wait(&sh_full[g], t & 1, wc)) return false;
-          tc_fence_after();
-          const uint32_t sh = smem_u32(sSh + g * kShBytes);
-          const uint32_t vg = smem_u32(sV + g * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
-            const uint64_t a = smem_desc(sh + kk * 2048, 16384, 1024);
-            // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO away)
-            // = the ones block, of which N = 64..79 are read.
-            const uint32_t vstart = vg + kk * 2048;
-            const uint64_t bv = smem_desc(vstart, ones_addr - vstart, 1024);
-            mma_bf16(tmem + kTmemD, a, bv, idesc_pv, (g > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kD / 16; ++kk)
+                mma_bf16(tmem + g * kTile, kmajor_desc(sK + g * kTileBytes, kk), kmajor_desc(sQ, kk), idesc_s, kk > 0);
+              mma_commit(&s_full[g]);
+              ++s_next[g];
+              if (++s_issued_tile == kSwG) mma_commit(q_empty);   // slot free once every S(t) completed
+              --remaining;
+              progress = true;
+            }
           }
-          mma_commit(&sh_free[g]);
+          // PV(t)[g]: D += share^T [V_g | 1]
+          const int tp = pv_next[g];
+          if (tp < nt && tp < s_next[g]) {
+            bool d_ok = tp == d_tile;
+            if (!d_ok && pv_in_tile == 0 && tp == d_tile + 1 && mbar_try_wait(d_free, (tp & 1) ^ 1)) {
+              d_tile = tp;
+              d_ok = true;
+            }
+            if (d_ok && mbar_try_wait(&sh_full[g], tp & 1)) {
+              tc_fence_after();
+              const uint32_t sh = smem_u32(sSh + g * kShBytes);
+              const uint32_t vg = smem_u32(sV + g * kTileBytes);
+              const bool first = pv_in_tile == 0;
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk) {
+                // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
+                const uint64_t a = smem_desc(sh + kk * 2048, 16384, 1024);
+                // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO
+                // away) = the ones block, of which N = 64..79 are read.
+                const uint32_t vstart = vg + kk * 2048;
+                const uint64_t bv = smem_desc(vstart, ones_addr - vstart, 1024);
+                mma_bf16(tmem + kTmemD, a, bv, idesc_pv, (first && kk == 0) ? 0u : 1u);
+              }
+              mma_commit(&sh_free[g]);
+              ++pv_next[g];
+              if (++pv_in_tile == kSwG) {
+                mma_commit(d_full);
+                pv_in_tile = 0;
+              }
+              --remaining;
+              progress = true;
+            }
+          }
         }
-        mma_commit(d_full);
-        return true;
-      };
-      if (mbar_wait(kv_full, 0, wc)) {
-        tc_fence_after();
-        bool ok = issue_s(0);
-        for (int t = 0; ok && t < nt; ++t) {
-          if (t + 1 < nt) ok = issue_s(t + 1);
-          if (ok) ok = issue_pv(t);
+        if (progress) {
+          t_last = globaltimer();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer() - t_last > kWaitLimitNs) {
+            raise_timeout(wc, q_full);
+            break;
+          }
+          __nanosleep(64);
         }
       }
       mma_commit(drain);
