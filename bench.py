@@ -49,7 +49,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=4096, help="query rows of the oracle's CPU sample")
+    ap.add_argument("--decode-ctx", type=int, default=None, help="cached tokens per sequence (default: the workload's)")
+    ap.add_argument("--decode-steps", type=int, default=None, help="decode steps timed (default: the workload's)")
+    ap.add_argument("--decode-only", action="store_true", help="skip the forward measurement")
+    ap.add_argument("--cpu-heads", type=int, default=5, help="full T=16384 heads in the oracle's CPU sample")
     return ap.parse_args(argv)
 
 
@@ -190,17 +193,23 @@ def oracle_sample(q, k, v, rows, tau=1.0, eps=1e-6):
     return flops, dt
 
 
-def cpu_baseline(rows, seed=2):
+def cpu_baseline(heads, seed=2):
+    """The oracle on `heads` full heads (T = 16384) of the benchmark workload,
+    generated on the host with the same recipe (about 10-30 s of CPU work)."""
     import numpy as np
     from long_context_attention_gb300 import inputs
     w = inputs.WORKLOADS["fwd_bf16_t16384"]
-    q, k, v = inputs.make_qkv(1, 1, rows, w.d, q_std=w.q_std, pairs=w.pairs * rows // w.T, seed=seed, dtype="bf16")
-    qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
-    flops, dt = oracle_sample(qh, kh, vh, rows)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"float64 NumPy oracle, 1 head x first {rows} query rows of the 4x12x16384x64 workload "
-                      f"({flops / 1e9:.1f} GFLOP algorithmic, {dt:.1f} s)",
-            "seconds": dt, "cpu_count": os.cpu_count(), "np": np.__version__}
+    q, k, v = inputs.make_qkv(1, heads, w.T, w.d, q_std=w.q_std, pairs=w.pairs, seed=seed, dtype="bf16")
+    tot_f, tot_t = 0, 0.0
+    for h in range(heads):
+        qh, kh, vh = (x[0, h].double().numpy() for x in (q, k, v))
+        f, t = oracle_sample(qh, kh, vh, w.T)
+        tot_f += f
+        tot_t += t
+    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"float64 NumPy oracle (row-blocked), {heads} full heads of 1 x 12 x 16384 x 64 with the "
+                      f"workload's recipe ({tot_f / 1e9:.0f} GFLOP algorithmic, {tot_t:.1f} s)",
+            "seconds": tot_t, "cpu_count": os.cpu_count(), "np": np.__version__}
 
 
 # ---------------------------------------------------------------------- reference arm
@@ -235,15 +244,15 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------ our arm
-def run_decode(torch, b, inputs, dev, warmup, peaks):
+def run_decode(torch, b, inputs, dev, warmup, peaks, ctx=None, n_steps=None):
     """8 independent 131072-token caches (built by an untimed prefill), 256 steps."""
     w = inputs.WORKLOADS["decode_bf16_ctx131072"]
-    B, H, N, d = w.B, w.H, w.T, w.d
-    steps = w.extra["steps"]
+    B, H, N, d = w.B, w.H, ctx or w.T, w.d
+    steps = n_steps or w.extra["steps"]
     from long_context_attention_gb300 import yarn_tau
     tau = yarn_tau(w.tau_scale)
     T_cap = N + steps
-    q, k, v = inputs.make_workload(w, device=dev)
+    q, k, v = inputs.make_workload(w, device=dev, T=N)
     kc = torch.empty(B, H, T_cap, d, dtype=torch.bfloat16, device=dev)
     vc = torch.empty_like(kc)
     kc[:, :, :N] = k
@@ -262,7 +271,7 @@ def run_decode(torch, b, inputs, dev, warmup, peaks):
     torch.cuda.synchronize()
     assert b.dilution_attn_get_error(ws) == b.DA_OK
     pre_ms = e0.elapsed_time(e1)
-    pre = {"workload": "prefill_bf16_t131072_b8", "B": B, "H": H, "T": N, "tau": tau,
+    pre = {"workload": f"prefill_bf16_t{N}_b{B}", "B": B, "H": H, "T": N, "tau": tau,
            "ms": pre_ms, "tflops": fwd_flops(B, H, N, d) / (pre_ms * 1e-3) / 1e12,
            "tokens_per_s": B * N / (pre_ms * 1e-3)}
     dem[:, :, :N] = dem_n
@@ -289,7 +298,7 @@ def run_decode(torch, b, inputs, dev, warmup, peaks):
     keys = sum((N + i + 1) for i in range(steps)) * B * H
     algo_bytes = (4 * d + 8) * keys     # K and V rows (bf16) + demand read and write (fp32)
     gbs = algo_bytes / (ms * 1e-3) / 1e9
-    return pre, {"workload": "decode_bf16_ctx131072", "B": B, "H": H, "n_ctx": N, "steps": steps, "tau": tau,
+    return pre, {"workload": f"decode_bf16_ctx{N}", "B": B, "H": H, "n_ctx": N, "steps": steps, "tau": tau,
                  "ms_per_step": ms / steps, "tokens_per_s": B * steps / (ms * 1e-3),
                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": gbs / peaks["hbm_gbs"], "traffic": None,
@@ -310,6 +319,11 @@ def run_ours(args):
     b.load(build_if_missing=True)
     peaks, peaks_kind = load_peaks()
 
+    if args.decode_only:
+        pre, dec = run_decode(torch, b, inputs, dev, max(3, args.warmup), peaks, args.decode_ctx, args.decode_steps)
+        if rank == 0:
+            print(json.dumps({"decode": dec, "prefill": pre}), flush=True)
+        return 0
     w = inputs.WORKLOADS[args.workload]
     B, H, T, d = w.B, w.H, w.T, w.d
     # each rank is an independent replica with its own seeded batch
@@ -372,8 +386,10 @@ def run_ours(args):
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d, "tau": 1.0, "eps": w.eps,
                        "planted_pairs_per_head": w.pairs, "parallelism": f"replicas{world}",
-                       "l2": f"no flush; inputs {3 * q.numel() * q.element_size() / 1e6:.0f} MB + accumulator "
-                             f"{ws.numel() / 1e6:.0f} MB per step, larger than the 129 MB L2"},
+                       "l2": (f"no flush; inputs {3 * q.numel() * q.element_size() / 1e6:.0f} MB + workspace "
+                              f"{ws.numel() / 1e6:.0f} MB per step"
+                              + (", larger than the 129 MB L2" if 3 * q.numel() * q.element_size() + ws.numel() > 129e6
+                                 else " (fits in L2: small case)"))},
             "tokens_per_s": world * B * T * K / (ms * 1e-3),
             "pct_of_bf16_peak": 100.0 * value / world / peak_t,
             "kernels_ms": kern_ms,
@@ -415,12 +431,12 @@ def run_ours(args):
     del q, k, v, out, ws
     torch.cuda.empty_cache()
     if not args.no_decode:
-        pre, dec = run_decode(torch, b, inputs, dev, max(3, W), peaks)
+        pre, dec = run_decode(torch, b, inputs, dev, max(3, W), peaks, args.decode_ctx, args.decode_steps)
         line["prefill_131072"] = pre
         line["decode"] = dec
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+        line["cpu_baseline"] = cpu_baseline(args.cpu_heads)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
