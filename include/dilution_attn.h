@@ -131,6 +131,37 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Cached decode step that allocates nothing (no counterpart on the pages: an
+ * interface convenience, not part of the method).
+ *
+ * Same arguments, semantics and errors as dilution_attn_decode_step, without
+ * the workspace: scratch comes from a fixed 16 MiB array built into the
+ * library (dilution_attn_decode_noalloc_scratch_bytes()).  It is for callers
+ * that cannot allocate device memory while decoding -- a runtime whose memory
+ * pool is fixed for the duration of a request, or a host that can pass only
+ * the tensors it already owns.  Every GPU that loads the library keeps the
+ * array until the process exits.
+ *   - Returns DA_ERR_WORKSPACE when dilution_attn_decode_workspace_size(B, H,
+ *     T_cap, d) exceeds the array (e.g. 8 x 12 heads fit T_cap up to ~43K).
+ *   - Calls no cudaMalloc/cudaFree; the first call on a device looks up the
+ *     array's device address (cudaGetSymbolAddress), so make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (the
+ *     status word is cleared at the start of each call): calls that overlap on
+ *     the GPU race with each other, so issue them on one stream or order them.
+ *   - dilution_attn_get_error cannot reach the array's status word; timeouts
+ *     of this entry point are not reported.
+ * ---------------------------------------------------------------------- */
+int dilution_attn_decode_step_noalloc(const void *q_new, const void *k_new, const void *v_new,
+                                      void *k_cache, void *v_cache, float *demand,
+                                      int n_ctx, int T_cap, void *out,
+                                      int B, int H, int d, float tau, float eps, int dtype,
+                                      void *stream);
+
+/* Size in bytes of the fixed scratch array of dilution_attn_decode_step_noalloc. */
+size_t dilution_attn_decode_noalloc_scratch_bytes(void);
+
+/* ------------------------------------------------------------------------
  * Synchronises `stream`, reads the status word that kernels of the last call
  * on `workspace` may have set, clears it and returns it (DA_OK if none).
  * Returns DA_ERR_CUDA if the synchronisation or the copy fails.

@@ -41,6 +41,9 @@ _SIGNATURES = {
     "dilution_attn_decode_workspace_size": (_c_size_t, [_c_int] * 4),
     "dilution_attn_decode_step": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                   [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
+    "dilution_attn_decode_step_noalloc": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
+                                          [_c_float, _c_float, _c_int, _c_void_p]),
+    "dilution_attn_decode_noalloc_scratch_bytes": (_c_size_t, []),
     "dilution_attn_get_error": (_c_int, [_c_void_p, _c_void_p]),
     "dilution_attn_debug_last_timeout": (_c_int, [_c_void_p, _c_void_p]),
     "dilution_attn_debug_tile_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_void_p, _c_size_t]),
@@ -218,6 +221,34 @@ def dilution_attn_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_c
     if check:
         _check(st, "dilution_attn_decode_step")
     return out
+
+
+def dilution_attn_decode_step_noalloc(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,
+                                      tau: float = 1.0, eps: float = 1e-6, stream=None, check: bool = True):
+    """dilution_attn_decode_step with the library's fixed scratch array instead of a workspace."""
+    lib = load()
+    _need(q_new, "q_new")
+    B, H, d = q_new.shape
+    _need(k_new, "k_new", q_new.shape, q_new.dtype)
+    _need(v_new, "v_new", q_new.shape, q_new.dtype)
+    _need(k_cache, "k_cache", None, q_new.dtype)
+    T_cap = k_cache.shape[2]
+    _need(k_cache, "k_cache", (B, H, T_cap, d))
+    _need(v_cache, "v_cache", (B, H, T_cap, d), q_new.dtype)
+    _need(demand, "demand", (B, H, T_cap), torch.float32)
+    if out is None:
+        out = torch.empty_like(q_new)
+    _need(out, "out", q_new.shape, q_new.dtype)
+    st = lib.dilution_attn_decode_step_noalloc(_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                               _ptr(demand), int(n_ctx), T_cap, _ptr(out), B, H, d, float(tau),
+                                               float(eps), _dtype_code(q_new), _stream_handle(stream))
+    if check:
+        _check(st, "dilution_attn_decode_step_noalloc")
+    return out
+
+
+def dilution_attn_decode_noalloc_scratch_bytes() -> int:
+    return int(load().dilution_attn_decode_noalloc_scratch_bytes())
 
 
 # ----------------------------------------------------------------------------- misc

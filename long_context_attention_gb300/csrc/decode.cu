@@ -18,6 +18,8 @@
 // scratch (4 B per key) stays mostly in L2.
 #include "da_internal.h"
 
+#include <mutex>
+
 #include <cuda_bf16.h>
 
 namespace da {
@@ -276,4 +278,53 @@ cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_ne
                                 logits, part_ml, part_acc, nchunk, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Decode step without a caller workspace.
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// a runtime that owns a fixed memory pool and forbids allocation during a
+// request, a foreign host (another language's runtime, a plugin) that can hand
+// over only the tensors it already has, or code that must not allocate between
+// decode steps.  For them the scratch lives in this fixed array, which every
+// GPU that loads the library holds until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of g_decode_scratch on the current device, looked up once per
+// device (the array's name in host code is only a host-side handle).
+static int noalloc_scratch(void **ptr) {
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return DA_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return DA_OK;
+}
+
 }  // namespace da
+
+extern "C" int dilution_attn_decode_step_noalloc(const void *q_new, const void *k_new, const void *v_new,
+                                                 void *k_cache, void *v_cache, float *demand, int n_ctx, int T_cap,
+                                                 void *out, int B, int H, int d, float tau, float eps, int dtype,
+                                                 void *stream) {
+  using namespace da;
+  if (B < 0 || H < 0 || T_cap < 0) return DA_ERR_INVALID;
+  const DecWorkspace L = dec_workspace_layout((int64_t)B * H, T_cap);
+  if (L.total > kNoAllocScratchBytes) return DA_ERR_WORKSPACE;   // beyond the fixed scratch
+  void *scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != DA_OK) return st;
+  // The argument checks, the status-word reset and the launches are the
+  // ordinary decode step's, given the fixed array as its workspace.
+  return dilution_attn_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d, tau,
+                                   eps, dtype, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" size_t dilution_attn_decode_noalloc_scratch_bytes(void) { return da::kNoAllocScratchBytes; }
