@@ -104,6 +104,24 @@ int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, v
                                   void *const *events);
 
 /* ------------------------------------------------------------------------
+ * Backward: gradients dq, dk, dv [B,H,T,d] of sum(dout * out) for the
+ * forward above (the page states only that exact gradients exist; they are
+ * the chain rule through the causal softmax, the exclusive column cumsum, the
+ * share and the renormalisation).
+ *   lse2 [B,H,T] fp32: the forward's lse2_out for the same q, k, tau.
+ *   dtype applies to q, k, v, dout, dq, dk, dv; arithmetic is fp32 (column
+ *   sums of the demand in fp64).
+ * workspace: at least dilution_attn_bwd_workspace_size(); errors as for
+ * dilution_attn_fwd.  This version runs on CUDA cores (no tensor cores).
+ * ---------------------------------------------------------------------- */
+size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype);
+
+int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *dout,
+                      const float *lse2, void *dq, void *dk, void *dv,
+                      int B, int H, int T, int d, float tau, float eps, int dtype,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Cached decode step ("DilutionAttention v0.1.0 · results", section "The
  * operator": the ordinary key/value cache plus one running demand total per
  * key and head).

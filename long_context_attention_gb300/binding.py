@@ -38,6 +38,9 @@ _SIGNATURES = {
     "dilution_attn_fwd_with_events": (_c_int, [_c_void_p] * 7 + [_c_int] * 4 + [_c_float, _c_float, _c_int,
                                                                                     _c_void_p, _c_size_t, _c_void_p,
                                                                                     _c_void_p]),
+    "dilution_attn_bwd_workspace_size": (_c_size_t, [_c_int] * 5),
+    "dilution_attn_bwd": (_c_int, [_c_void_p] * 8 + [_c_int] * 4 + [_c_float, _c_float, _c_int, _c_void_p, _c_size_t,
+                                                                        _c_void_p]),
     "dilution_attn_decode_workspace_size": (_c_size_t, [_c_int] * 4),
     "dilution_attn_decode_step": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                   [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
@@ -183,6 +186,37 @@ def dilution_attn_fwd_with_events(q, k, v, out=None, lse2_out=None, rowsum_out=N
     if check:
         _check(st, "dilution_attn_fwd")
     return out
+
+
+# -------------------------------------------------------------------------- backward
+def dilution_attn_bwd_workspace_size(B: int, H: int, T: int, d: int, dtype: int) -> int:
+    return int(load().dilution_attn_bwd_workspace_size(B, H, T, d, dtype))
+
+
+def dilution_attn_bwd(q, k, v, dout, lse2, dq=None, dk=None, dv=None, *, tau: float = 1.0, eps: float = 1e-6,
+                      workspace=None, stream=None, check: bool = True):
+    """Gradients (dq, dk, dv) of sum(dout * out); lse2 is the forward's lse2_out."""
+    lib = load()
+    _need(q, "q")
+    B, H, T, d = q.shape
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _need(t, name, q.shape, q.dtype)
+    _need(lse2, "lse2", (B, H, T), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, name, q.shape, q.dtype)
+    dt = _dtype_code(q)
+    if workspace is None:
+        workspace = torch.empty(max(dilution_attn_bwd_workspace_size(B, H, T, d, dt), 256), dtype=torch.uint8,
+                                device=q.device)
+    st = lib.dilution_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse2), _ptr(dq), _ptr(dk), _ptr(dv), B,
+                               H, T, d, float(tau), float(eps), dt, _ptr(workspace), workspace.numel(),
+                               _stream_handle(stream))
+    if check:
+        _check(st, "dilution_attn_bwd")
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------------------- decode

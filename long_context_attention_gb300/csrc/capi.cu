@@ -15,6 +15,9 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                     float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
                     cudaStream_t stream, cudaEvent_t const *ev);
+cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
+                       void *dk, void *dv, int BH, int T, float c, float c2, float eps, int dtype, double *dtot,
+                       float *rowbuf, float *dq_acc, cudaStream_t stream);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, float c2, float eps, int dtype,
                           float *logits, float2 *part_ml, float *part_acc, int nchunk, cudaStream_t stream);
@@ -109,6 +112,37 @@ int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, v
   }
   return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, c2, eps, lse2_ws, acc, status,
                          stream, ev);
+}
+
+size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
+  (void)d;
+  (void)dtype;
+  if (B < 0 || H < 0 || T < 0) return 0;
+  return bwd_workspace_layout((int64_t)B * H, T).total;
+}
+
+int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
+                      void *dk, void *dv, int B, int H, int T, int d, float tau, float eps, int dtype,
+                      void *workspace, size_t workspace_bytes, void *stream_) {
+  int st = check_common(B, H, T, d, tau, eps, dtype);
+  if (st != DA_OK) return st;
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0 || T == 0) return DA_OK;
+  const void *ptrs[] = {q, k, v, dout, lse2, dq, dk, dv};
+  for (const void *p : ptrs)
+    if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
+  const BwdWorkspace L = bwd_workspace_layout(BH, T);
+  if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+  if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
+  const float c = (float)((double)tau / std::sqrt((double)d));
+  if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, c, logit_scale_log2(tau, d), eps, dtype,
+                 reinterpret_cast<double *>(ws + L.dtot_off), reinterpret_cast<float *>(ws + L.row_off),
+                 reinterpret_cast<float *>(ws + L.dq_off), stream) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
 }
 
 size_t dilution_attn_decode_workspace_size(int B, int H, int T_cap, int d) {

@@ -45,6 +45,23 @@ DA_HD FwdWorkspace fwd_workspace_layout(int64_t BH, int64_t T) {
 }
 
 // ---------------------------------------------------------------------------
+// Backward workspace: [status | column totals [BH][T] fp64 | R, Y, rho, spare
+// [4][BH][T] fp32 | dq accumulator [BH][T][64] fp32]
+// ---------------------------------------------------------------------------
+struct BwdWorkspace {
+  size_t dtot_off, row_off, dq_off, total;
+};
+
+DA_HD BwdWorkspace bwd_workspace_layout(int64_t BH, int64_t T) {
+  BwdWorkspace w;
+  w.dtot_off = kStatusBytes;
+  w.row_off = (size_t)round_up((int64_t)w.dtot_off + BH * T * 8, 256);
+  w.dq_off = (size_t)round_up((int64_t)w.row_off + 4 * BH * T * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.dq_off + BH * T * kD * 4, 256);
+  return w;
+}
+
+// ---------------------------------------------------------------------------
 // Decode workspace: [status | logits [BH][T_cap] | part_ml [BH][nchunk][2] |
 //                    part_acc [BH][nchunk][68]]
 // ---------------------------------------------------------------------------

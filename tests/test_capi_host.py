@@ -143,3 +143,13 @@ def test_decode_argument_validation(lib):
 
 def test_get_error_rejects_null(lib):
     assert lib.dilution_attn_get_error(None, None) == b.DA_ERR_INVALID
+
+
+def test_bwd_argument_validation(lib):
+    def bwd(eps=1e-6, d=64, q=FAKE, ws=FAKE, wsb=1 << 30):
+        return lib.dilution_attn_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 32, d, 1.0, eps, 1, ws, wsb, None)
+    assert bwd(eps=0.0) == b.DA_ERR_INVALID
+    assert bwd(d=128) == b.DA_ERR_UNSUPPORTED
+    assert bwd(q=None) == b.DA_ERR_INVALID
+    assert bwd(ws=None) == b.DA_ERR_WORKSPACE
+    assert b.dilution_attn_bwd_workspace_size(4, 12, 16384, 64, 1) > 4 * 12 * 16384 * 64 * 4
