@@ -49,6 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-train", action="store_true", help="skip the forward+backward training-step timing")
     ap.add_argument("--decode-ctx", type=int, default=None, help="cached tokens per sequence (default: the workload's)")
     ap.add_argument("--decode-steps", type=int, default=None, help="decode steps timed (default: the workload's)")
     ap.add_argument("--decode-only", action="store_true", help="skip the forward measurement")
@@ -306,6 +307,38 @@ def run_decode(torch, b, inputs, dev, warmup, peaks, ctx=None, n_steps=None):
                  "gpu_launches": 3 * steps}
 
 
+def run_train(torch, b, inputs, dev, steps=2):
+    """Forward + backward at the training shape (4 x 12 x 16384 x 64, all N(0,1))."""
+    w = inputs.WORKLOADS["train_bf16_t16384"]
+    B, H, T, d = w.B, w.H, w.T, w.d
+    q, k, v = inputs.make_workload(w, device=dev)
+    g = inputs.make_like((B, H, T, d), seed=w.seed + 1, dtype=w.dtype, device=dev)
+    out = torch.empty_like(q)
+    lse2 = torch.empty(B, H, T, device=dev)
+    fws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=dev)
+    bws = torch.empty(b.dilution_attn_bwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+
+    def step():
+        b.dilution_attn_fwd(q, k, v, out, lse2, workspace=fws)
+        b.dilution_attn_bwd(q, k, v, g, lse2, dq, dk, dv, workspace=bws)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    assert b.dilution_attn_get_error(fws) == b.DA_OK and b.dilution_attn_get_error(bws) == b.DA_OK
+    ms = e0.elapsed_time(e1) / steps
+    fwd_f = fwd_flops(B, H, T, d)
+    return {"workload": "train_bf16_t16384", "B": B, "H": H, "T": T, "steps": steps, "ms_per_step": ms,
+            "tokens_per_s": B * T / (ms * 1e-3), "backward": "CUDA-core version (no tensor cores yet)",
+            "fwd_flop": fwd_f}
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_info()
@@ -430,6 +463,8 @@ def run_ours(args):
 
     del q, k, v, out, ws
     torch.cuda.empty_cache()
+    if not args.no_train:
+        line["train_step"] = run_train(torch, b, inputs, dev)
     if not args.no_decode:
         pre, dec = run_decode(torch, b, inputs, dev, max(3, W), peaks, args.decode_ctx, args.decode_steps)
         line["prefill_131072"] = pre
