@@ -111,21 +111,31 @@ struct RowStat {
   }
 };
 
-// Demand step for 32 consecutive queries (columns col0 ..) of one key row:
+// -lse2 of a 128-query tile is staged as 32 float4 pieces inside the 2 KB
+// block of ones that the share.[V | 1] product reads (see the sweep kernel):
+// that product reads only 16-byte chunks (0 ^ r) and (1 ^ r) of each 128-byte
+// row r of the block's two 1 KB groups (128B swizzle), so chunks 2..5 of every
+// row are free.  Stage s uses group s; piece f (queries 4f .. 4f+3) goes to
+// row f / 4, chunk 2 + f % 4, swizzled like the rest of the row.
+__host__ __device__ constexpr uint32_t lse_piece(int stage, int f) {
+  return (uint32_t)(stage * 1024 + (f >> 2) * 128 + (((2 + (f & 3)) ^ (f >> 2)) << 4));
+}
+
+// Demand step for 32 consecutive queries (columns 32 C ..) of one key row:
 //   p = 2^(s*c2 - lse2),  den = (committed + eps) + p,  share = p / den,
 //   committed + eps <- den   (queries in causal order: the exclusive cumsum).
-// nl holds -lse2 of those queries (shared memory, read as float4).  MASK
+// lst is the -lse2 stage of the tile (pieces laid out by lse_piece).  MASK
 // zeroes the bids of queries before the key: key row `row` is after query
 // column c when row_eff > c, row_eff = row - (first query - first key).
-template <bool MASK>
-__device__ __forceinline__ void demand_chunk(const float (&s)[32], const float *nl, int col0, int row_eff, float c2,
+template <bool MASK, int C>
+__device__ __forceinline__ void demand_chunk(const float (&s)[32], const uint8_t *lst, int row_eff, float c2,
                                              float &ceps, uint32_t (&pk)[16]) {
-  const float4 *nl4 = reinterpret_cast<const float4 *>(nl);
+  constexpr int col0 = 32 * C;
   const float2 c2v = make_float2(c2, c2);
   float p[32];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 l = nl4[i];
+    const float4 l = *reinterpret_cast<const float4 *>(lst + lse_piece(0, 8 * C + i));
     const float2 x0 = ffma2(make_float2(s[4 * i], s[4 * i + 1]), c2v, make_float2(l.x, l.y));
     const float2 x1 = ffma2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2v, make_float2(l.z, l.w));
     p[4 * i] = ex2_approx(x0.x);
@@ -352,17 +362,18 @@ constexpr int kSwThreads = kSwWarps * 32;       // 640
 // (checked on the host before every launch).
 constexpr int kSwRegsDemand = 120, kSwRegsEpi = 56, kSwRegsCtl = 56;
 constexpr int kSwRegsNeeded = 128 * (kSwG * kSwRegsDemand + kSwRegsEpi + kSwRegsCtl);
-constexpr int kSwLStages = 2;
 constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key groups x 1 KB
+constexpr uint32_t kStageBytes = 32 * 32 * 4;   // epilogue reduction box: 32 rows x 32 fp32, 128B-swizzled
 constexpr uint32_t kSwOffK = 0;
 constexpr uint32_t kSwOffV = kSwOffK + kSwG * kTileBytes;
 constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // one query tile (released early)
 constexpr uint32_t kSwOffSh = kSwOffQ + kTileBytes;
-constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO)
-constexpr uint32_t kSwOffL = kSwOffOnes + 2048;
-constexpr uint32_t kSwOffBar = kSwOffL + kSwLStages * kSwBQ * 4;
-constexpr int kSwSmemBytes = kSwOffBar + 512 + 1024;
+constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO); also -lse2
+constexpr uint32_t kSwOffStage = kSwOffOnes + 2048;                 // one box per epilogue warp
+constexpr uint32_t kSwOffBar = kSwOffStage + 4 * kStageBytes;
+constexpr int kSwSmemBytes = kSwOffBar + 512;   // the dynamic shared-memory base is 1024-byte aligned
 static_assert(kSwSmemBytes <= 232448, "sweep shared memory");
+static_assert(kSwOffStage % 1024 == 0, "reduction boxes are 128B-swizzled");
 static_assert(kSwRegsNeeded <= 65536, "sweep register split");
 
 constexpr uint32_t kTmemD = kSwG * kTile;   // S^T slots at g*128; D (80 columns) after them
@@ -373,24 +384,30 @@ __device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sy
 
 __global__ void __launch_bounds__(kSwThreads, 1)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const float *__restrict__ nlse2,
-                 float *__restrict__ acc, float *__restrict__ demand_out, int BH, int T, int Tp, float c2,
-                 float eps, int *status) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align1024(smem_raw);
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmAcc,
+                 const float *__restrict__ nlse2, float *__restrict__ acc, float *__restrict__ demand_out, int BH,
+                 int T, int Tp, float c2, float eps, int *status) {
+  extern __shared__ __align__(1024) uint8_t sw_smem_raw[];
+  // The layout has no slack for re-alignment: every tile, swizzle atom and
+  // reduction box assumes a 1024-byte aligned base.  Refuse (uniformly,
+  // before any barrier) rather than compute with misaligned operands.
+  if (smem_u32(sw_smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(status, DA_OK, DA_ERR_UNSUPPORTED);
+    return;
+  }
+  uint8_t *smem = sw_smem_raw;
   uint8_t *sK = smem + kSwOffK;
   uint8_t *sV = smem + kSwOffV;
   uint8_t *sQ = smem + kSwOffQ;
   uint8_t *sSh = smem + kSwOffSh;
   uint8_t *sOnes = smem + kSwOffOnes;
-  const float *sL = reinterpret_cast<const float *>(smem + kSwOffL);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSwOffBar);
   uint64_t *kv_full = bars;
   uint64_t *q_full = kv_full + 1;
   uint64_t *q_empty = q_full + 1;
-  uint64_t *l_full = q_empty + 1;              // [kSwLStages]
-  uint64_t *l_empty = l_full + kSwLStages;     // [kSwLStages]
-  uint64_t *s_full = l_empty + kSwLStages;     // [g]
+  uint64_t *l_full = q_empty + 1;              // [2] -lse2 stages (in the ones block)
+  uint64_t *l_empty = l_full + 2;              // [2]
+  uint64_t *s_full = l_empty + 2;              // [g]
   uint64_t *s_free = s_full + kSwG;            // [g]
   uint64_t *sh_full = s_free + kSwG;           // [g]
   uint64_t *sh_free = sh_full + kSwG;          // [g]
@@ -410,8 +427,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     mbar_init(kv_full, 1);
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int i = 0; i < kSwLStages; ++i) {
-      mbar_init(&l_full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&l_full[i], 32);          // one cp.async arrival per producer lane
       mbar_init(&l_empty[i], 4 * kSwG);   // every demand warp is done with that -lse2 stage
     }
     for (int g = 0; g < kSwG; ++g) {
@@ -440,35 +457,42 @@ __global__ void __launch_bounds__(kSwThreads, 1)
 
   if (wg == kSwG + 1) {
     regs_dec_ctl();
-    if (warp == kWarpProd && lane == 0) {
+    if (warp == kWarpProd) {
       // ---------------------------------------------------------- producer
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(kv_full, 2 * kSwG * kTileBytes);
-      for (int g = 0; g < kSwG; ++g) {
-        tma_load_3d(sK + g * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
-        tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
+      // Lane 0 issues the TMA loads; all 32 lanes copy the tile's -lse2 (one
+      // 16-byte piece each) with cp.async into its stage.
+      if (lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmAcc);
+        mbar_arrive_expect_tx(kv_full, 2 * kSwG * kTileBytes);
+        for (int g = 0; g < kSwG; ++g) {
+          tma_load_3d(sK + g * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
+          tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
+        }
       }
-      int q_issued = 0, l_issued = 0;
+      const float *lsrc = nlse2 + (size_t)w.bh * Tp + 4 * lane;
+      uint8_t *ldst = sOnes + lse_piece(0, lane);
+      int q_issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int qrow = (w.q_tile0 + t) * kSwBQ;
-        const int ls = t % kSwLStages;
-        if (!mbar_wait(&l_empty[ls], ((t / kSwLStages) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&l_full[ls], kSwBQ * 4);
-        bulk_load(smem + kSwOffL + ls * kSwBQ * 4, nlse2 + (size_t)w.bh * Tp + qrow, kSwBQ * 4, &l_full[ls]);
-        ++l_issued;
+        const int ls = t & 1;
+        if (!mbar_wait(&l_empty[ls], ((t >> 1) & 1) ^ 1, wc)) break;
+        cp_async16(ldst + ls * 1024, lsrc + qrow);
+        cp_async_arrive_noinc(&l_full[ls]);
         // the query tile's single slot frees as soon as the S products of the previous tile are done
         if (!mbar_wait(q_empty, (t & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(q_full, kTileBytes);
-        tma_load_3d(sQ, &tmQ, q_full, 0, qrow, w.bh);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(q_full, kTileBytes);
+          tma_load_3d(sQ, &tmQ, q_full, 0, qrow, w.bh);
+        }
         ++q_issued;
       }
-      if (*abort_flag) {
+      cp_async_wait_all();
+      if (lane == 0 && *abort_flag) {
         drain_wait(kv_full, 0);
         if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1);
-        for (int t = (l_issued > kSwLStages ? l_issued - kSwLStages : 0); t < l_issued; ++t)
-          drain_wait(&l_full[t % kSwLStages], (t / kSwLStages) & 1);
       }
     } else if (warp == kWarpMma && lane == 0) {
       // -------------------------------------------------------- MMA issuer
@@ -565,33 +589,47 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     }
   } else if (wg == kSwG) {
     // -------------------------------------------------------------- epilogue
+    // D -> acc through the copy engine: each warp stages its 32 rows x 32
+    // columns as a 128B-swizzled box and issues a TMA add-reduction into acc
+    // (two boxes per tile); the row sum (column 64) goes by one atomic per row.
     regs_dec_epi();
     const int quarter = warp % 4;
-    const int row = quarter * 32 + lane;
+    uint8_t *stage = smem + kSwOffStage + quarter * kStageBytes;
+    uint8_t *srow = stage + lane * 128;
+    const int swz = lane & 7;
+    auto stage_box = [&](const float (&x)[32], int col0, int grow0) {
+      if (lane == 0) bulk_wait_read_all();   // the previous box has been read
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4 *>(srow + ((j ^ swz) << 4)) =
+            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_2d(&tmAcc, stage, col0, grow0);
+        bulk_commit_group();
+      }
+    };
     for (int t = 0; t < nt; ++t) {
       if (!mbar_wait(d_full, t & 1, wc)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + kTmemD + ((uint32_t)(quarter * 32) << 16);
-      const int64_t qi = (int64_t)(w.q_tile0 + t) * kSwBQ + row;
-      float *dst = acc + ((size_t)w.bh * Tp + qi) * kAccStride;
+      const int qrow0 = (w.q_tile0 + t) * kSwBQ + quarter * 32;   // first query row of this warp's box
+      const int grow0 = w.bh * Tp + qrow0;                        // its row in the [BH * Tp, 68] view of acc
       float a[32], rs;
       tmem_ld32(taddr, a);
       tmem_wait_ld_r(a);
-      if (qi < T) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) red_add_v4(dst + c, a[c], a[c + 1], a[c + 2], a[c + 3]);
-      }
+      stage_box(a, 0, grow0);
       tmem_ld32(taddr + 32, a);
       tmem_ld1(taddr + kD, rs);
       tmem_wait_ld_r(a);
       tmem_wait_ld();
       release_tmem(d_free, lane);
-      if (qi < T) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) red_add_v4(dst + 32 + c, a[c], a[c + 1], a[c + 2], a[c + 3]);
-        atomicAdd(dst + kD, rs);
-      }
+      stage_box(a, 32, grow0);
+      if (qrow0 + lane < T) atomicAdd(acc + ((size_t)grow0 + lane) * kAccStride + kD, rs);
     }
+    if (lane == 0) bulk_wait_all();
   } else {
     // ----------------------------------------------------- demand warpgroups
     regs_inc_demand();
@@ -613,15 +651,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
             make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     };
     for (int t = 0; t < nt; ++t) {
-      const int ls = t % kSwLStages;
+      const int ls = t & 1;
       const int qlo = (w.q_tile0 + t) * kSwBQ;      // first query of the tile
       const bool all_masked = kbase > qlo + kSwBQ - 1 || kbase >= T;
       const bool need_mask = kbase + kTile - 1 > qlo;
       const int row_eff = row - (qlo - kbase);      // key after query col iff row_eff > col
-      if (!mbar_wait(&l_full[ls], (t / kSwLStages) & 1, wc)) break;
+      if (!mbar_wait(&l_full[ls], (t >> 1) & 1, wc)) break;
       if (!mbar_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
-      const float *nl = sL + ls * kSwBQ;   // -lse2 of the tile's queries
+      const uint8_t *lst = sOnes + ls * 1024;   // -lse2 of the tile's queries
       uint32_t pk[16];
       if (all_masked) {
         release_tmem(&s_free[g], lane);
@@ -636,25 +674,25 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         tmem_ld32(tb, A);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 32, B);
-        if (need_mask) demand_chunk<true>(A, nl, 0, row_eff, c2, ceps, pk);
-        else demand_chunk<false>(A, nl, 0, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 0>(A, lst, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 0>(A, lst, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
         if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
         store(pk, 0);
         tmem_wait_ld_r(B);
         tmem_ld32(tb + 64, A);
-        if (need_mask) demand_chunk<true>(B, nl + 32, 32, row_eff, c2, ceps, pk);
-        else demand_chunk<false>(B, nl + 32, 32, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 1>(B, lst, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 1>(B, lst, row_eff, c2, ceps, pk);
         store(pk, 1);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 96, B);
-        if (need_mask) demand_chunk<true>(A, nl + 64, 64, row_eff, c2, ceps, pk);
-        else demand_chunk<false>(A, nl + 64, 64, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 2>(A, lst, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 2>(A, lst, row_eff, c2, ceps, pk);
         store(pk, 2);
         tmem_wait_ld_r(B);
         release_tmem(&s_free[g], lane);
-        if (need_mask) demand_chunk<true>(B, nl + 96, 96, row_eff, c2, ceps, pk);
-        else demand_chunk<false>(B, nl + 96, 96, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 3>(B, lst, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 3>(B, lst, row_eff, c2, ceps, pk);
         store(pk, 3);
       }
       fence_proxy_async_smem();
@@ -712,14 +750,31 @@ static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 accumulator [BH * Tp rows][68] as a 2-D tensor; box = 32 rows x
+// 32 columns, 128B swizzle: the sweep epilogue's reduction box.
+static bool make_acc_map(CUtensorMap *m, float *acc, int64_t rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kAccStride, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kAccStride * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bfloat16 *out, float *rowsum_out,
                                  float *lse2_out, int BH, int T, cudaStream_t stream);
 
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                     float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
                     cudaStream_t stream, cudaEvent_t const *ev) {
-  CUtensorMap tq, tk, tv;
-  if (!make_tile_map(&tq, q, BH, T) || !make_tile_map(&tk, k, BH, T) || !make_tile_map(&tv, v, BH, T))
+  const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
+  if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;   // TMA row coordinates are 32-bit
+  CUtensorMap tq, tk, tv, ta;
+  if (!make_tile_map(&tq, q, BH, T) || !make_tile_map(&tk, k, BH, T) || !make_tile_map(&tv, v, BH, T) ||
+      !make_acc_map(&ta, acc, acc_rows))
     return DA_ERR_CUDA;
   // The shared-memory opt-in is a per-device function attribute.
   static bool attr_done[64] = {};
@@ -748,7 +803,7 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
   rowstats_kernel<<<rowstats_num_ctas(BH, T), kRsThreads, kRsSmemBytes, stream>>>(tq, tk, lse2_ws, acc, BH, T,
                                                                                   Tp, c2, status);
   if (ev[1]) cudaEventRecord(ev[1], stream);
-  sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, lse2_ws, acc, demand_out,
+  sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, lse2_ws, acc, demand_out,
                                                                             BH, T, Tp, c2, eps, status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
   if (ev[2]) cudaEventRecord(ev[2], stream);
