@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--decode-steps", type=int, default=None, help="decode steps timed (default: the workload's)")
     ap.add_argument("--decode-only", action="store_true", help="skip the forward measurement")
     ap.add_argument("--cpu-heads", type=int, default=5, help="full T=16384 heads in the oracle's CPU sample")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (smaller cases for profiling; not a bench line)")
     return ap.parse_args(argv)
 
 
@@ -358,7 +360,7 @@ def run_ours(args):
             print(json.dumps({"decode": dec, "prefill": pre}), flush=True)
         return 0
     w = inputs.WORKLOADS[args.workload]
-    B, H, T, d = w.B, w.H, w.T, w.d
+    B, H, T, d = (args.batch or w.B), w.H, w.T, w.d
     # each rank is an independent replica with its own seeded batch
     q, k, v = inputs.make_qkv(B, H, T, d, q_std=w.q_std, pairs=w.pairs, seed=w.seed + 1000 * rank, dtype=w.dtype,
                               device=dev)

@@ -75,11 +75,30 @@ __device__ __forceinline__ void release_tmem(uint64_t *bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// Online softmax normaliser of one query row in the log2 domain:
-// m = running max of x = s * c2, l = sum 2^(x - m) in four partial sums.
+// Softmax normaliser of one query row in the log2 domain, lse2 = m + log2 l
+// with l = sum 2^(x - m), x = s * c2.  The reference m is updated lazily: a
+// chunk is summed against the current m without waiting for its own maximum,
+// and only a chunk whose sum leaves [0, 2^64] (a score more than 64 above m,
+// or the row's first chunk, where m = -inf) takes the exact path: chunk
+// maximum, rescale of l, terms recomputed.  lse2 is exact for any m; every
+// term stays <= 2^64 and the largest one seen at a rescale is 1, so l neither
+// overflows nor loses its dominant terms.
 struct RowStat {
   float m = -INFINITY;
   float2 l0 = make_float2(0.f, 0.f), l1 = make_float2(0.f, 0.f);
+
+  __device__ __forceinline__ void terms(const float (&s)[32], float c2, float2 &a0, float2 &a1) const {
+    const float2 c2v = make_float2(c2, c2), nm = make_float2(-m, -m);
+    a0 = make_float2(0.f, 0.f);
+    a1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const float2 x0 = ffma2(make_float2(s[2 * j], s[2 * j + 1]), c2v, nm);
+      const float2 x1 = ffma2(make_float2(s[2 * j + 2], s[2 * j + 3]), c2v, nm);
+      a0 = fadd2(a0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
+      a1 = fadd2(a1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
+    }
+  }
 
   // 32 consecutive keys (columns col0 ..) of the row; DIAG masks key > query.
   template <bool DIAG>
@@ -89,25 +108,30 @@ struct RowStat {
       for (int c = 0; c < 32; ++c)
         if (col0 + c > row) s[c] = -INFINITY;
     }
+    float2 a0, a1;
+    if (m != -INFINITY) {
+      terms(s, c2, a0, a1);
+      const float cs = (a0.x + a0.y) + (a1.x + a1.y);
+      if (cs <= 0x1p64f) {   // false for inf / NaN as well
+        l0 = fadd2(l0, a0);
+        l1 = fadd2(l1, a1);
+        return;
+      }
+    }
     float t[11];
 #pragma unroll
     for (int i = 0; i < 10; ++i) t[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
     t[10] = fmaxf(s[30], s[31]);
     const float mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], fmax3(t[8], t[9], t[10])));
-    if (DIAG && mx == -INFINITY) return;   // every key of the chunk is after the query
+    if (mx == -INFINITY) return;   // every key of the chunk is after the query
     const float mn = fmaxf(m, mx * c2);
     const float sc = ex2_approx(m - mn);    // 0 on the first chunk (m = -inf)
     l0 = fmul2(l0, make_float2(sc, sc));
     l1 = fmul2(l1, make_float2(sc, sc));
     m = mn;
-    const float2 c2v = make_float2(c2, c2), nm = make_float2(-mn, -mn);
-#pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-      const float2 x0 = ffma2(make_float2(s[2 * j], s[2 * j + 1]), c2v, nm);
-      const float2 x1 = ffma2(make_float2(s[2 * j + 2], s[2 * j + 3]), c2v, nm);
-      l0 = fadd2(l0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
-      l1 = fadd2(l1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
-    }
+    terms(s, c2, a0, a1);
+    l0 = fadd2(l0, a0);
+    l1 = fadd2(l1, a1);
   }
 };
 

@@ -104,6 +104,14 @@ def test_bf16_tau_and_eps():
     compare(q, k, v, tau=2.5, eps=1e-3)
 
 
+def test_bf16_sharp_logits_rescale():
+    # tau = 6 multiplies the planted logits (~26 in log2 units at tau = 1) to
+    # ~150: a row's later key tiles then score far more than 64 above its first
+    # chunk, which forces the row-statistics pass to rescale its running sum.
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 2, 700, 64, q_std=1.5, pairs=8, seed=41, dtype="bf16"))
+    compare(q, k, v, tau=6.0, eps=1e-6)
+
+
 def test_bf16_rows_of_A_sum_to_one():
     q, k, _ = inputs.make_qkv(2, 3, 1000, 64, q_std=1.5, pairs=16, seed=22, dtype="bf16")
     q, k = q.to(DEV), k.to(DEV)
