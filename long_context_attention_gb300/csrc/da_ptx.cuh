@@ -50,6 +50,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of a phase (mbarrier.try_wait may suspend the thread for
+// a while when the phase is incomplete; test_wait returns at once).  For
+// threads that poll several barriers in turn.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared abort flag + global status word.  A wait returns false when it
 // timed out or when another thread of the CTA already gave up.
 struct WaitCtx {
@@ -185,6 +200,63 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is read from tensor memory,
+// one row per lane with two bf16 per 32-bit column (element 2i in the low
+// half), K-step kk at column offset 8 kk.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Runs of K steps with descriptors advanced by compile-time offsets inside
+// the instruction sequence: only the base descriptors stay live, and each
+// step costs two adds and the MMA.  Step KK adds KK * SA / KK * SB to the A / B
+// descriptor (for A in TMEM: KK * SA columns); the first step accumulates iff
+// acc != 0, the others always do.
+template <long long OA, long long OB>
+__device__ __forceinline__ void mma_bf16_at(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ta, tb;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.s64 ta, %1, %5;\n\t"
+      "add.s64 tb, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ta, tb, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OA), "n"(OB)
+      : "memory");
+}
+template <int OA, long long OB>
+__device__ __forceinline__ void mma_bf16_tmem_a_at(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 ta;\n\t.reg .b64 tb;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.u32 ta, %1, %5;\n\t"
+      "add.s64 tb, %2, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], tb, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(OA), "n"(OB)
+      : "memory");
+}
+template <int KK, int N, long long SA, long long SB, bool TMEM_A>
+struct MmaRun {
+  static __device__ __forceinline__ void go(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
+    if constexpr (TMEM_A)
+      mma_bf16_tmem_a_at<(int)(KK * SA), KK * SB>(d, (uint32_t)a, b, idesc, KK == 0 ? acc0 : 1u);
+    else
+      mma_bf16_at<KK * SA, KK * SB>(d, a, b, idesc, KK == 0 ? acc0 : 1u);
+    MmaRun<KK + 1, N, SA, SB, TMEM_A>::go(d, a, b, idesc, acc0);
+  }
+};
+template <int N, long long SA, long long SB, bool TMEM_A>
+struct MmaRun<N, N, SA, SB, TMEM_A> {
+  static __device__ __forceinline__ void go(uint32_t, uint64_t, uint64_t, uint32_t, uint32_t) {}
+};
+
 // Arrive (once) on an mbarrier when every tcgen05 op issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -221,6 +293,37 @@ __device__ __forceinline__ void tmem_wait_ld_r(float (&r)[32]) {
         "+f"(r[16]), "+f"(r[17]), "+f"(r[18]), "+f"(r[19]), "+f"(r[20]), "+f"(r[21]), "+f"(r[22]), "+f"(r[23]),
         "+f"(r[24]), "+f"(r[25]), "+f"(r[26]), "+f"(r[27]), "+f"(r[28]), "+f"(r[29]), "+f"(r[30]), "+f"(r[31])
       :
+      : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane (32x32b shape).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&u)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]),
+      "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]), "r"(u[16]), "r"(u[17]),
+      "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]),
+      "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Zero 80 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_zero80(uint32_t taddr) {
+  const uint32_t z = 0u;
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], "
+      "{%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2};" ::"r"(taddr),
+      "r"(taddr + 32), "r"(z)
+      : "memory");
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};" ::"r"(
+          taddr + 64),
+      "r"(z)
       : "memory");
 }
 

@@ -35,7 +35,8 @@
 //   rowstats: warps 0-3 / 4-7 = softmax-statistics warpgroups for the two
 //             query tiles, warp 8 = TMA producer, warp 9 = MMA issuer.
 //   sweep:    warps 0-11 = demand warpgroups (key tiles 0..2 of the span),
-//             warps 12-15 = epilogue, warp 16 = TMA, warp 17 = MMA.
+//             warps 12-15 = epilogue, warp 16 = TMA, warps 17-19 = MMA issuers
+//             (one per demand warpgroup).
 #include "da_internal.h"
 #include "da_ptx.cuh"
 
@@ -388,10 +389,10 @@ constexpr int kSwRegsDemand = 120, kSwRegsEpi = 56, kSwRegsCtl = 56;
 constexpr int kSwRegsNeeded = 128 * (kSwG * kSwRegsDemand + kSwRegsEpi + kSwRegsCtl);
 constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key groups x 1 KB
 constexpr uint32_t kStageBytes = 32 * 32 * 4;   // epilogue reduction box: 32 rows x 32 fp32, 128B-swizzled
-constexpr uint32_t kSwOffK = 0;
-constexpr uint32_t kSwOffV = kSwOffK + kSwG * kTileBytes;
-constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // one query tile (released early)
-constexpr uint32_t kSwOffSh = kSwOffQ + kTileBytes;
+constexpr uint32_t kSwOffK = 0;                                    // key tiles 1, 2 (tile 0 is in TMEM)
+constexpr uint32_t kSwOffV = kSwOffK + (kSwG - 1) * kTileBytes;
+constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // two query slots
+constexpr uint32_t kSwOffSh = kSwOffQ + 2 * kTileBytes;
 constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO); also -lse2
 constexpr uint32_t kSwOffStage = kSwOffOnes + 2048;                 // one box per epilogue warp
 constexpr uint32_t kSwOffBar = kSwOffStage + 4 * kStageBytes;
@@ -401,6 +402,11 @@ static_assert(kSwOffStage % 1024 == 0, "reduction boxes are 128B-swizzled");
 static_assert(kSwRegsNeeded <= 65536, "sweep register split");
 
 constexpr uint32_t kTmemD = kSwG * kTile;   // S^T slots at g*128; D (80 columns) after them
+// Key tile 0 as the A operand of its S product, read from TMEM (one key per
+// lane, 32 columns of bf16 pairs): its 16 KB of shared memory hold the second
+// query slot instead.
+constexpr uint32_t kTmemK0 = kTmemD + kD + 16;
+static_assert(kTmemK0 + kD / 2 <= 512, "TMEM columns");
 
 __device__ __forceinline__ void regs_inc_demand() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSwRegsDemand)); }
 __device__ __forceinline__ void regs_dec_epi() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsEpi)); }
@@ -409,7 +415,8 @@ __device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sy
 __global__ void __launch_bounds__(kSwThreads, 1)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmAcc,
-                 const float *__restrict__ nlse2, float *__restrict__ acc, float *__restrict__ demand_out, int BH,
+                 const uint4 *__restrict__ kglob, const float *__restrict__ nlse2, float *__restrict__ acc,
+                 float *__restrict__ demand_out, int BH,
                  int T, int Tp, float c2, float eps, int *status) {
   extern __shared__ __align__(1024) uint8_t sw_smem_raw[];
   // The layout has no slack for re-alignment: every tile, swizzle atom and
@@ -427,9 +434,10 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   uint8_t *sOnes = smem + kSwOffOnes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSwOffBar);
   uint64_t *kv_full = bars;
-  uint64_t *q_full = kv_full + 1;
-  uint64_t *q_empty = q_full + 1;
-  uint64_t *l_full = q_empty + 1;              // [2] -lse2 stages (in the ones block)
+  uint64_t *k0_full = kv_full + 1;             // key tile 0 written to TMEM
+  uint64_t *q_full = k0_full + 1;              // [2] query slots
+  uint64_t *q_empty = q_full + 2;              // [2]
+  uint64_t *l_full = q_empty + 2;              // [2] -lse2 stages (in the ones block)
   uint64_t *l_empty = l_full + 2;              // [2]
   uint64_t *s_full = l_empty + 2;              // [g]
   uint64_t *s_free = s_full + kSwG;            // [g]
@@ -437,8 +445,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   uint64_t *sh_free = sh_full + kSwG;          // [g]
   uint64_t *d_full = sh_free + kSwG;
   uint64_t *d_free = d_full + 1;
-  uint64_t *drain = d_free + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *drain = d_free + 1;                // [g]: per issuer
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + kSwG);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -449,8 +457,11 @@ __global__ void __launch_bounds__(kSwThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(k0_full, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], kSwG);   // one commit per issuer
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&l_full[i], 32);          // one cp.async arrival per producer lane
       mbar_init(&l_empty[i], 4 * kSwG);   // every demand warp is done with that -lse2 stage
@@ -461,9 +472,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       mbar_init(&sh_full[g], 4);
       mbar_init(&sh_free[g], 1);
     }
-    mbar_init(d_full, 1);
-    mbar_init(d_free, 4);
-    mbar_init(drain, 1);
+    mbar_init(d_full, kSwG);   // one commit per issuer
+    mbar_init(d_free, 4);      // phase t: D holds zeros for tile t (the epilogue warps)
+    for (int g = 0; g < kSwG; ++g) mbar_init(&drain[g], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -490,9 +501,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmAcc);
-        mbar_arrive_expect_tx(kv_full, 2 * kSwG * kTileBytes);
+        mbar_arrive_expect_tx(kv_full, (2 * kSwG - 1) * kTileBytes);
         for (int g = 0; g < kSwG; ++g) {
-          tma_load_3d(sK + g * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
+          if (g > 0) tma_load_3d(sK + (g - 1) * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
           tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
         }
       }
@@ -505,111 +516,94 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         if (!mbar_wait(&l_empty[ls], ((t >> 1) & 1) ^ 1, wc)) break;
         cp_async16(ldst + ls * 1024, lsrc + qrow);
         cp_async_arrive_noinc(&l_full[ls]);
-        // the query tile's single slot frees as soon as the S products of the previous tile are done
-        if (!mbar_wait(q_empty, (t & 1) ^ 1, wc)) break;
+        // query slot t % 2 frees once the S products of tile t - 2 are done
+        const int qs = t & 1;
+        if (!mbar_wait(&q_empty[qs], ((t >> 1) & 1) ^ 1, wc)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(q_full, kTileBytes);
-          tma_load_3d(sQ, &tmQ, q_full, 0, qrow, w.bh);
+          mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
+          tma_load_3d(sQ + qs * kTileBytes, &tmQ, &q_full[qs], 0, qrow, w.bh);
         }
         ++q_issued;
       }
       cp_async_wait_all();
       if (lane == 0 && *abort_flag) {
         drain_wait(kv_full, 0);
-        if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1);
+        for (int t = (q_issued > 2 ? q_issued - 2 : 0); t < q_issued; ++t) drain_wait(&q_full[t & 1], (t >> 1) & 1);
       }
-    } else if (warp == kWarpMma && lane == 0) {
-      // -------------------------------------------------------- MMA issuer
-      // Event-driven: each demand warpgroup's S product and share.[V|1]
-      // product are issued as soon as that warpgroup's own barriers allow, so
-      // a fast warpgroup is not held to the slowest one's pace.  Order
-      // constraints: S(t)[g] for all g read the single query slot (reloaded
-      // once all of them completed); PV(t)[g] for all g accumulate into the
-      // one D buffer, which must have been drained of tile t-1.
+    } else if (warp >= kWarpMma && warp < kWarpMma + kSwG && lane == 0) {
+      // ------------------------------------------------------- MMA issuers
+      // One issuing thread per demand warpgroup (warps 17, 18, 19: one per
+      // sub-partition 1..3), each issuing its warpgroup's S and share.[V|1]
+      // products.  A tcgen05.mma issue stream slows to a fraction when other
+      // warps of its sub-partition are busy, and every sub-partition hosts
+      // three demand warps: three streams keep the tensor pipe fed.  All PV
+      // products accumulate into D (the epilogue zeroes it after each drain),
+      // so their order across issuers does not matter; a commit tracks only
+      // its own thread's MMAs, hence q_empty and d_full count one arrival per
+      // issuer.
+      //   S(t)[g] reads query slot t % 2 (reloaded once all S(t) completed);
+      //   PV(t)[g] waits until D holds zeros for tile t (d_free phase t).
+      //   Operand descriptors are built once; a K step advances them by a
+      //   constant inside the issue sequence (MmaRun): K-major tiles +32 bytes
+      //   (+2 in the start field); share^T +2048 bytes (+128); [V | 1] start
+      //   +128 and its leading byte offset to the ones block -128 (field at
+      //   bit 16).
+      const int g = warp - kWarpMma;
+      constexpr long long kStepKm = 2, kStepSh = 128, kStepV = 128 - (128ll << 16);
+      constexpr uint64_t kTileStep = kTileBytes >> 4, kShStep = kShBytes >> 4;
+      constexpr uint64_t kVTileStep = kTileStep - (kTileStep << 16);
       const uint32_t idesc_s = idesc_bf16(kTile, kSwBQ, false, false);
       const uint32_t idesc_pv = idesc_bf16(kSwBQ, kD + 16, true, true);
       const uint32_t ones_addr = smem_u32(sOnes);
-      int s_next[kSwG], pv_next[kSwG];
-      for (int g = 0; g < kSwG; ++g) s_next[g] = pv_next[g] = 0;
-      int q_ready_tile = -1;    // query tile held (and waited for) in the slot
-      int s_issued_tile = 0;    // warpgroups that issued S for tile q_ready_tile
-      int d_tile = -1;          // tile whose products accumulate in D
-      int pv_in_tile = 0;       // warpgroups whose PV of d_tile were issued
-      bool ok = mbar_wait(kv_full, 0, wc);
+      const uint64_t dQ0 = kmajor_desc(sQ, 0), dQ1 = kmajor_desc(sQ + kTileBytes, 0);
+      const uint64_t dKg = kmajor_desc(sK + (g > 0 ? g - 1 : 0) * kTileBytes, 0);   // (tile 0 is read from TMEM)
+      const uint64_t dShg = smem_desc(smem_u32(sSh), 16384, 1024) + g * kShStep;
+      const uint64_t dVg = smem_desc(smem_u32(sV), ones_addr - smem_u32(sV), 1024) + g * kVTileStep;
+      int ts = 0, tp = 0;   // next S / PV tile
+      bool ok = mbar_wait(kv_full, 0, wc) && (g != 0 || mbar_wait(k0_full, 0, wc));
       if (ok) tc_fence_after();
       unsigned long long t_last = globaltimer();
-      int remaining = ok ? 2 * kSwG * nt : 0;
-      while (remaining > 0) {
+      while (ok && (ts < nt || tp < nt)) {
         bool progress = false;
-        for (int g = 0; g < kSwG; ++g) {
-          // S(t)[g] = K_g Q(t)^T into slot g
-          const int ts = s_next[g];
-          if (ts < nt && ts <= q_ready_tile + 1) {
-            bool q_ok = ts == q_ready_tile;
-            if (!q_ok && s_issued_tile == kSwG * (q_ready_tile >= 0) && mbar_try_wait(q_full, ts & 1)) {
-              q_ready_tile = ts;
-              s_issued_tile = 0;
-              q_ok = true;
-            }
-            if (q_ok && mbar_try_wait(&s_free[g], (ts & 1) ^ 1)) {
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk)
-                mma_bf16(tmem + g * kTile, kmajor_desc(sK + g * kTileBytes, kk), kmajor_desc(sQ, kk), idesc_s, kk > 0);
-              mma_commit(&s_full[g]);
-              ++s_next[g];
-              if (++s_issued_tile == kSwG) mma_commit(q_empty);   // slot free once every S(t) completed
-              --remaining;
-              progress = true;
-            }
-          }
-          // PV(t)[g]: D += share^T [V_g | 1]
-          const int tp = pv_next[g];
-          if (tp < nt && tp < s_next[g]) {
-            bool d_ok = tp == d_tile;
-            if (!d_ok && pv_in_tile == 0 && tp == d_tile + 1 && mbar_try_wait(d_free, (tp & 1) ^ 1)) {
-              d_tile = tp;
-              d_ok = true;
-            }
-            if (d_ok && mbar_try_wait(&sh_full[g], tp & 1)) {
-              tc_fence_after();
-              const uint32_t sh = smem_u32(sSh + g * kShBytes);
-              const uint32_t vg = smem_u32(sV + g * kTileBytes);
-              const bool first = pv_in_tile == 0;
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk) {
-                // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
-                const uint64_t a = smem_desc(sh + kk * 2048, 16384, 1024);
-                // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO
-                // away) = the ones block, of which N = 64..79 are read.
-                const uint32_t vstart = vg + kk * 2048;
-                const uint64_t bv = smem_desc(vstart, ones_addr - vstart, 1024);
-                mma_bf16(tmem + kTmemD, a, bv, idesc_pv, (first && kk == 0) ? 0u : 1u);
-              }
-              mma_commit(&sh_free[g]);
-              ++pv_next[g];
-              if (++pv_in_tile == kSwG) {
-                mma_commit(d_full);
-                pv_in_tile = 0;
-              }
-              --remaining;
-              progress = true;
-            }
-          }
+        // S(ts)[g] = K_g Q(ts)^T into slot g
+        if (ts < nt && mbar_test_wait(&q_full[ts & 1], (ts >> 1) & 1) &&
+            mbar_test_wait(&s_free[g], (ts & 1) ^ 1)) {
+          tc_fence_after();
+          const uint64_t dq = (ts & 1) ? dQ1 : dQ0;
+          if (g == 0)
+            MmaRun<0, kD / 16, 8, kStepKm, true>::go(tmem, tmem + kTmemK0, dq, idesc_s, 0u);
+          else
+            MmaRun<0, kD / 16, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg, dq, idesc_s, 0u);
+          mma_commit(&s_full[g]);
+          mma_commit(&q_empty[ts & 1]);
+          ++ts;
+          progress = true;
+        }
+        // PV(tp)[g]: D += share^T [V_g | 1]
+        if (tp < ts && mbar_test_wait(d_free, tp & 1) && mbar_test_wait(&sh_full[g], tp & 1)) {
+          tc_fence_after();
+          // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
+          // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO
+          // away) = the ones block, of which N = 64..79 are read.
+          MmaRun<0, kTile / 16, kStepSh, kStepV, false>::go(tmem + kTmemD, dShg, dVg, idesc_pv, 1u);
+          mma_commit(&sh_free[g]);
+          mma_commit(d_full);
+          ++tp;
+          progress = true;
         }
         if (progress) {
           t_last = globaltimer();
         } else {
           if (*abort_flag) break;
           if (globaltimer() - t_last > kWaitLimitNs) {
-            raise_timeout(wc, q_full);
+            raise_timeout(wc, &s_free[g]);
             break;
           }
           __nanosleep(64);
         }
       }
-      mma_commit(drain);
-      drain_wait(drain, 0);
+      mma_commit(&drain[g]);
+      drain_wait(&drain[g], 0);
     }
   } else if (wg == kSwG) {
     // -------------------------------------------------------------- epilogue
@@ -635,6 +629,12 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         bulk_commit_group();
       }
     };
+    // D starts as zeros (d_free phase 0); after each drain it is zeroed again
+    // before the buffer is handed back, so every PV MMA accumulates.
+    const uint32_t tdrow = tmem + kTmemD + ((uint32_t)(quarter * 32) << 16);
+    tmem_zero80(tdrow);
+    tmem_wait_st();
+    release_tmem(d_free, lane);
     for (int t = 0; t < nt; ++t) {
       if (!mbar_wait(d_full, t & 1, wc)) break;
       tc_fence_after();
@@ -649,6 +649,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       tmem_ld1(taddr + kD, rs);
       tmem_wait_ld_r(a);
       tmem_wait_ld();
+      tmem_zero80(tdrow);
+      tmem_wait_st();
       release_tmem(d_free, lane);
       stage_box(a, 32, grow0);
       if (qrow0 + lane < T) atomicAdd(acc + ((size_t)grow0 + lane) * kAccStride + kD, rs);
@@ -665,6 +667,25 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     const uint32_t tb = tmem + g * kTile + ((uint32_t)(quarter * 32) << 16);
     uint8_t *sh_row = sSh + g * kShBytes + (row / 8) * 1024 + (row % 8) * 128;
     float ceps = eps;   // committed + eps: demand this key received from earlier queries
+    if (g == 0) {
+      // this thread's key row (64 bf16 = 32 words; zeros past T) -> TMEM lane
+      uint32_t kr[32];
+      const int64_t key = (int64_t)kbase + row;
+      const uint4 *src = kglob + ((size_t)w.bh * T + key) * (kD * 2 / 16);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 x = key < T ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        kr[4 * i] = x.x;
+        kr[4 * i + 1] = x.y;
+        kr[4 * i + 2] = x.z;
+        kr[4 * i + 3] = x.w;
+      }
+      tmem_st32(tmem + kTmemK0 + ((uint32_t)(quarter * 32) << 16), kr);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(k0_full);
+    }
     // 32 shares (bf16 pairs) of query chunk c -> 64-query M-block c/2, 16-byte
     // pieces (c%2)*4 .. +3 of this key's row, 128B-swizzled by row.
     auto store = [&](const uint32_t (&pk)[16], int c) {
@@ -827,7 +848,7 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
   rowstats_kernel<<<rowstats_num_ctas(BH, T), kRsThreads, kRsSmemBytes, stream>>>(tq, tk, lse2_ws, acc, BH, T,
                                                                                   Tp, c2, status);
   if (ev[1]) cudaEventRecord(ev[1], stream);
-  sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, lse2_ws, acc, demand_out,
+  sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, static_cast<const uint4 *>(k), lse2_ws, acc, demand_out,
                                                                             BH, T, Tp, c2, eps, status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
   if (ev[2]) cudaEventRecord(ev[2], stream);
