@@ -559,28 +559,30 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const uint64_t dKg = kmajor_desc(sK + (g > 0 ? g - 1 : 0) * kTileBytes, 0);   // (tile 0 is read from TMEM)
       const uint64_t dShg = smem_desc(smem_u32(sSh), 16384, 1024) + g * kShStep;
       const uint64_t dVg = smem_desc(smem_u32(sV), ones_addr - smem_u32(sV), 1024) + g * kVTileStep;
-      int ts = 0, tp = 0;   // next S / PV tile
+      // Per warpgroup the events come in a fixed order: S(t+1) becomes ready
+      // (slot released while tile t is read) before PV(t) (its shares
+      // written), so the issuer walks S(0), S(1), PV(0), S(2), PV(1), ... with
+      // blocking waits, during which it sleeps instead of taking issue slots
+      // from the demand warps of its sub-partition.
       bool ok = mbar_wait(kv_full, 0, wc) && (g != 0 || mbar_wait(k0_full, 0, wc));
       if (ok) tc_fence_after();
-      unsigned long long t_last = globaltimer();
-      while (ok && (ts < nt || tp < nt)) {
-        bool progress = false;
-        // S(ts)[g] = K_g Q(ts)^T into slot g
-        if (ts < nt && mbar_test_wait(&q_full[ts & 1], (ts >> 1) & 1) &&
-            mbar_test_wait(&s_free[g], (ts & 1) ^ 1)) {
+      for (int t = 0; ok && t <= nt; ++t) {
+        if (t < nt) {
+          // S(t)[g] = K_g Q(t)^T into slot g
+          if (!mbar_wait(&q_full[t & 1], (t >> 1) & 1, wc) || !mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) break;
           tc_fence_after();
-          const uint64_t dq = (ts & 1) ? dQ1 : dQ0;
+          const uint64_t dq = (t & 1) ? dQ1 : dQ0;
           if (g == 0)
             MmaRun<0, kD / 16, 8, kStepKm, true>::go(tmem, tmem + kTmemK0, dq, idesc_s, 0u);
           else
             MmaRun<0, kD / 16, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg, dq, idesc_s, 0u);
           mma_commit(&s_full[g]);
-          mma_commit(&q_empty[ts & 1]);
-          ++ts;
-          progress = true;
+          mma_commit(&q_empty[t & 1]);
         }
-        // PV(tp)[g]: D += share^T [V_g | 1]
-        if (tp < ts && mbar_test_wait(d_free, tp & 1) && mbar_test_wait(&sh_full[g], tp & 1)) {
+        if (t >= 1) {
+          // PV(t-1)[g]: D += share^T [V_g | 1] once D holds zeros for tile t-1
+          const int tp = t - 1;
+          if (!mbar_wait(d_free, tp & 1, wc) || !mbar_wait(&sh_full[g], tp & 1, wc)) break;
           tc_fence_after();
           // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
           // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO
@@ -588,18 +590,6 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           MmaRun<0, kTile / 16, kStepSh, kStepV, false>::go(tmem + kTmemD, dShg, dVg, idesc_pv, 1u);
           mma_commit(&sh_free[g]);
           mma_commit(d_full);
-          ++tp;
-          progress = true;
-        }
-        if (progress) {
-          t_last = globaltimer();
-        } else {
-          if (*abort_flag) break;
-          if (globaltimer() - t_last > kWaitLimitNs) {
-            raise_timeout(wc, &s_free[g]);
-            break;
-          }
-          __nanosleep(64);
         }
       }
       mma_commit(&drain[g]);
