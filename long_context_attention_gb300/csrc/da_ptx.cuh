@@ -350,6 +350,18 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// K-major operand without swizzling ("interleaved" layout): 8-row x 16-byte
+// core matrices; lbo = byte offset between the two core matrices of one
+// K = 16 step, sbo = byte offset between consecutive 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format
 // (1 = bf16), 15 A major (1 = MN-major), 16 B major, [17,23) N >> 3,

@@ -136,33 +136,23 @@ struct RowStat {
   }
 };
 
-// -lse2 of a 128-query tile is staged as 32 float4 pieces inside the 2 KB
-// block of ones that the share.[V | 1] product reads (see the sweep kernel):
-// that product reads only 16-byte chunks (0 ^ r) and (1 ^ r) of each 128-byte
-// row r of the block's two 1 KB groups (128B swizzle), so chunks 2..5 of every
-// row are free.  Stage s uses group s; piece f (queries 4f .. 4f+3) goes to
-// row f / 4, chunk 2 + f % 4, swizzled like the rest of the row.
-__host__ __device__ constexpr uint32_t lse_piece(int stage, int f) {
-  return (uint32_t)(stage * 1024 + (f >> 2) * 128 + (((2 + (f & 3)) ^ (f >> 2)) << 4));
-}
-
 // Demand step for 32 consecutive queries (columns 32 C ..) of one key row:
-//   p = 2^(s*c2 - lse2),  den = (committed + eps) + p,  share = p / den,
-//   committed + eps <- den   (queries in causal order: the exclusive cumsum).
-// lst is the -lse2 stage of the tile (pieces laid out by lse_piece).  MASK
-// zeroes the bids of queries before the key: key row `row` is after query
-// column c when row_eff > c, row_eff = row - (first query - first key).
+//   p = 2^x,  den = (committed + eps) + p,  share = p / den,
+//   committed + eps <- den   (queries in causal order: the exclusive cumsum),
+// with x = c2 S' and S' = q.k - lse2 / c2 from the S product (its fifth K
+// step adds the -lse2 / c2 term).  MASK zeroes the bids of queries before
+// the key: key row `row` is after query column c when row_eff > c,
+// row_eff = row - (first query - first key).
 template <bool MASK, int C>
-__device__ __forceinline__ void demand_chunk(const float (&s)[32], const uint8_t *lst, int row_eff, float c2,
-                                             float &ceps, uint32_t (&pk)[16]) {
+__device__ __forceinline__ void demand_chunk(const float (&s)[32], int row_eff, float c2, float &ceps,
+                                             uint32_t (&pk)[16]) {
   constexpr int col0 = 32 * C;
   const float2 c2v = make_float2(c2, c2);
   float p[32];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 l = *reinterpret_cast<const float4 *>(lst + lse_piece(0, 8 * C + i));
-    const float2 x0 = ffma2(make_float2(s[4 * i], s[4 * i + 1]), c2v, make_float2(l.x, l.y));
-    const float2 x1 = ffma2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2v, make_float2(l.z, l.w));
+    const float2 x0 = fmul2(make_float2(s[4 * i], s[4 * i + 1]), c2v);
+    const float2 x1 = fmul2(make_float2(s[4 * i + 2], s[4 * i + 3]), c2v);
     p[4 * i] = ex2_approx(x0.x);
     p[4 * i + 1] = ex2_approx(x0.y);
     p[4 * i + 2] = ex2_approx(x1.x);
@@ -391,15 +381,19 @@ constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key 
 constexpr uint32_t kStageBytes = 32 * 32 * 4;   // epilogue reduction box: 32 rows x 32 fp32, 128B-swizzled
 constexpr uint32_t kSwOffK = 0;                                    // key tiles 1, 2 (tile 0 is in TMEM)
 constexpr uint32_t kSwOffV = kSwOffK + (kSwG - 1) * kTileBytes;
-constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // two query slots
+constexpr uint32_t kExtBytes = 128 * 16 * 2;    // one 128-row x 16 bf16 K-major operand, no swizzle
+constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // the query tile
+constexpr uint32_t kSwOffAExt = kSwOffQ + kTileBytes;              // [1 1 1 0 ..] for every key
+constexpr uint32_t kSwOffBExt = kSwOffAExt + kExtBytes;            // [hi mid lo 0 ..] of -lse2 / c2 per query
 constexpr uint32_t kSwOffSh = kSwOffQ + 2 * kTileBytes;
-constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO); also -lse2
+constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO)
 constexpr uint32_t kSwOffStage = kSwOffOnes + 2048;                 // one box per epilogue warp
 constexpr uint32_t kSwOffBar = kSwOffStage + 4 * kStageBytes;
 constexpr int kSwSmemBytes = kSwOffBar + 512;   // the dynamic shared-memory base is 1024-byte aligned
 static_assert(kSwSmemBytes <= 232448, "sweep shared memory");
 static_assert(kSwOffStage % 1024 == 0, "reduction boxes are 128B-swizzled");
 static_assert(kSwRegsNeeded <= 65536, "sweep register split");
+static_assert(kSwOffBExt + kExtBytes <= kSwOffSh, "extension operands");
 
 constexpr uint32_t kTmemD = kSwG * kTile;   // S^T slots at g*128; D (80 columns) after them
 // Key tile 0 as the A operand of its S product, read from TMEM (one key per
@@ -431,15 +425,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   uint8_t *sV = smem + kSwOffV;
   uint8_t *sQ = smem + kSwOffQ;
   uint8_t *sSh = smem + kSwOffSh;
+  uint8_t *sAExt = smem + kSwOffAExt;
+  uint8_t *sBExt = smem + kSwOffBExt;
   uint8_t *sOnes = smem + kSwOffOnes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSwOffBar);
   uint64_t *kv_full = bars;
   uint64_t *k0_full = kv_full + 1;             // key tile 0 written to TMEM
-  uint64_t *q_full = k0_full + 1;              // [2] query slots
-  uint64_t *q_empty = q_full + 2;              // [2]
-  uint64_t *l_full = q_empty + 2;              // [2] -lse2 stages (in the ones block)
-  uint64_t *l_empty = l_full + 2;              // [2]
-  uint64_t *s_full = l_empty + 2;              // [g]
+  uint64_t *q_full = k0_full + 1;              // query tile and its -lse2 / c2 block loaded
+  uint64_t *q_empty = q_full + 1;              // every S product of the tile completed
+  uint64_t *s_full = q_empty + 1;              // [g]
   uint64_t *s_free = s_full + kSwG;            // [g]
   uint64_t *sh_full = s_free + kSwG;           // [g]
   uint64_t *sh_free = sh_full + kSwG;          // [g]
@@ -458,14 +452,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(k0_full, 4);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], kSwG);   // one commit per issuer
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&l_full[i], 32);          // one cp.async arrival per producer lane
-      mbar_init(&l_empty[i], 4 * kSwG);   // every demand warp is done with that -lse2 stage
-    }
+    mbar_init(q_full, 2);      // the tile's bytes + the producer's -lse2 / c2 block
+    mbar_init(q_empty, kSwG);  // one commit per issuer
     for (int g = 0; g < kSwG; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&s_free[g], 4);
@@ -480,6 +468,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   }
   // Constant all-ones block: the N = 64..79 part of the value operand.
   for (int e = threadIdx.x; e < 2048 / 4; e += kSwThreads) reinterpret_cast<uint32_t *>(sOnes)[e] = 0x3F803F80u;
+  // The fifth K step of S: A_ext rows (every key) = [1 1 1 0 ... 0], B_ext rows
+  // (every query) = [hi mid lo 0 ... 0] of -lse2 / c2 (written per tile), so
+  // S' = q.k - lse2 / c2 and x = c2 S'.  K-major, no swizzle: 8-row groups of
+  // 256 bytes, each the core matrix of K 0..7 followed by that of K 8..15.
+  for (int e = threadIdx.x; e < (int)(kExtBytes / 16); e += kSwThreads) {
+    const bool k_lo = (e & 15) < 8;
+    reinterpret_cast<uint4 *>(sAExt)[e] = k_lo ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4 *>(sBExt)[e] = make_uint4(0u, 0u, 0u, 0u);
+  }
   fence_proxy_async_smem();
   if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, 512);
@@ -494,8 +491,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     regs_dec_ctl();
     if (warp == kWarpProd) {
       // ---------------------------------------------------------- producer
-      // Lane 0 issues the TMA loads; all 32 lanes copy the tile's -lse2 (one
-      // 16-byte piece each) with cp.async into its stage.
+      // Lane 0 issues the TMA loads; once the S products of the previous tile
+      // (which read both the query tile and B_ext) are done, the 32 lanes turn
+      // the tile's -lse2 into B_ext rows, four queries each.
       if (lane == 0) {
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
@@ -507,28 +505,40 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
         }
       }
-      const float *lsrc = nlse2 + (size_t)w.bh * Tp + 4 * lane;
-      uint8_t *ldst = sOnes + lse_piece(0, lane);
+      const float4 *lsrc = reinterpret_cast<const float4 *>(nlse2 + (size_t)w.bh * Tp) + lane;
       int q_issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int qrow = (w.q_tile0 + t) * kSwBQ;
-        const int ls = t & 1;
-        if (!mbar_wait(&l_empty[ls], ((t >> 1) & 1) ^ 1, wc)) break;
-        cp_async16(ldst + ls * 1024, lsrc + qrow);
-        cp_async_arrive_noinc(&l_full[ls]);
-        // query slot t % 2 frees once the S products of tile t - 2 are done
-        const int qs = t & 1;
-        if (!mbar_wait(&q_empty[qs], ((t >> 1) & 1) ^ 1, wc)) break;
+        const float4 nl = __ldg(lsrc + qrow / 4);   // -lse2 of queries qrow + 4 lane .. + 3 (-inf past T)
+        if (!mbar_wait(q_empty, (t & 1) ^ 1, wc)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
-          tma_load_3d(sQ + qs * kTileBytes, &tmQ, &q_full[qs], 0, qrow, w.bh);
+          mbar_arrive_expect_tx(q_full, kTileBytes);
+          tma_load_3d(sQ, &tmQ, q_full, 0, qrow, w.bh);
         }
         ++q_issued;
+        const float nv[4] = {nl.x, nl.y, nl.z, nl.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // -lse2 / c2 as hi + mid + lo bf16 parts (24 significant bits).  Rows
+          // past T get a large finite negative value: their bids vanish, and
+          // the zero K columns of A_ext that meet it stay 0.
+          const float v = fmaxf(nv[j] / c2, -3.0e38f);
+          const __nv_bfloat16 h = __float2bfloat16_rn(v);
+          const float r1 = v - __bfloat162float(h);
+          const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+          const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+          const int q = 4 * lane + j;
+          *reinterpret_cast<uint4 *>(sBExt + (q >> 3) * 256 + (q & 7) * 16) =
+              make_uint4((uint32_t)__bfloat16_as_ushort(h) | ((uint32_t)__bfloat16_as_ushort(m) << 16),
+                         (uint32_t)__bfloat16_as_ushort(l), 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
       }
-      cp_async_wait_all();
       if (lane == 0 && *abort_flag) {
         drain_wait(kv_full, 0);
-        for (int t = (q_issued > 2 ? q_issued - 2 : 0); t < q_issued; ++t) drain_wait(&q_full[t & 1], (t >> 1) & 1);
+        if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1);
       }
     } else if (warp >= kWarpMma && warp < kWarpMma + kSwG && lane == 0) {
       // ------------------------------------------------------- MMA issuers
@@ -555,7 +565,10 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const uint32_t idesc_s = idesc_bf16(kTile, kSwBQ, false, false);
       const uint32_t idesc_pv = idesc_bf16(kSwBQ, kD + 16, true, true);
       const uint32_t ones_addr = smem_u32(sOnes);
-      const uint64_t dQ0 = kmajor_desc(sQ, 0), dQ1 = kmajor_desc(sQ + kTileBytes, 0);
+      const uint64_t dQ = kmajor_desc(sQ, 0);
+      // fifth K step: -lse2 / c2 for every (key, query)
+      const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
+      const uint64_t dBExt = smem_desc_noswizzle(smem_u32(sBExt), 128, 256);
       const uint64_t dKg = kmajor_desc(sK + (g > 0 ? g - 1 : 0) * kTileBytes, 0);   // (tile 0 is read from TMEM)
       const uint64_t dShg = smem_desc(smem_u32(sSh), 16384, 1024) + g * kShStep;
       const uint64_t dVg = smem_desc(smem_u32(sV), ones_addr - smem_u32(sV), 1024) + g * kVTileStep;
@@ -569,15 +582,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       for (int t = 0; ok && t <= nt; ++t) {
         if (t < nt) {
           // S(t)[g] = K_g Q(t)^T into slot g
-          if (!mbar_wait(&q_full[t & 1], (t >> 1) & 1, wc) || !mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) break;
+          if (!mbar_wait(q_full, t & 1, wc) || !mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) break;
           tc_fence_after();
-          const uint64_t dq = (t & 1) ? dQ1 : dQ0;
           if (g == 0)
-            MmaRun<0, kD / 16, 8, kStepKm, true>::go(tmem, tmem + kTmemK0, dq, idesc_s, 0u);
+            MmaRun<0, kD / 16, 8, kStepKm, true>::go(tmem, tmem + kTmemK0, dQ, idesc_s, 0u);
           else
-            MmaRun<0, kD / 16, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg, dq, idesc_s, 0u);
+            MmaRun<0, kD / 16, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg, dQ, idesc_s, 0u);
+          mma_bf16_at<0, 0>(tmem + g * kTile, dAExt, dBExt, idesc_s, 1u);
           mma_commit(&s_full[g]);
-          mma_commit(&q_empty[t & 1]);
+          mma_commit(q_empty);
         }
         if (t >= 1) {
           // PV(t-1)[g]: D += share^T [V_g | 1] once D holds zeros for tile t-1
@@ -686,15 +699,12 @@ __global__ void __launch_bounds__(kSwThreads, 1)
             make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     };
     for (int t = 0; t < nt; ++t) {
-      const int ls = t & 1;
       const int qlo = (w.q_tile0 + t) * kSwBQ;      // first query of the tile
       const bool all_masked = kbase > qlo + kSwBQ - 1 || kbase >= T;
       const bool need_mask = kbase + kTile - 1 > qlo;
       const int row_eff = row - (qlo - kbase);      // key after query col iff row_eff > col
-      if (!mbar_wait(&l_full[ls], (t >> 1) & 1, wc)) break;
       if (!mbar_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
-      const uint8_t *lst = sOnes + ls * 1024;   // -lse2 of the tile's queries
       uint32_t pk[16];
       if (all_masked) {
         release_tmem(&s_free[g], lane);
@@ -709,32 +719,31 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         tmem_ld32(tb, A);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 32, B);
-        if (need_mask) demand_chunk<true, 0>(A, lst, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 0>(A, lst, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 0>(A, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 0>(A, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
         if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
         store(pk, 0);
         tmem_wait_ld_r(B);
         tmem_ld32(tb + 64, A);
-        if (need_mask) demand_chunk<true, 1>(B, lst, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 1>(B, lst, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 1>(B, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 1>(B, row_eff, c2, ceps, pk);
         store(pk, 1);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 96, B);
-        if (need_mask) demand_chunk<true, 2>(A, lst, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 2>(A, lst, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 2>(A, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 2>(A, row_eff, c2, ceps, pk);
         store(pk, 2);
         tmem_wait_ld_r(B);
         release_tmem(&s_free[g], lane);
-        if (need_mask) demand_chunk<true, 3>(B, lst, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 3>(B, lst, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 3>(B, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 3>(B, row_eff, c2, ceps, pk);
         store(pk, 3);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sh_full[g]);
-        mbar_arrive(&l_empty[ls]);
       }
     }
     const int64_t key = (int64_t)kbase + row;
