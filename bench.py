@@ -435,23 +435,57 @@ def run_ours(args):
             "gpu_launches": 3 * K, "clocks": clocks}
 
     if not args.no_e2e:
+        # Host buffers in, result back, every step.  The batch goes through in
+        # chunks on three streams (copy in / compute / copy out), so that the
+        # copies of one chunk overlap the compute of another, as a caller
+        # streaming requests would do; every byte still crosses inside the
+        # timed region.
         Ke = max(1, min(K, 10))
+        nch = 2 if B % 2 == 0 else 1
+        Bc = B // nch
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
-        b.dilution_attn_fwd(dq.copy_(hq), dk.copy_(hk), dv.copy_(hv), out, workspace=ws)
+        wsc = torch.empty(b.dilution_attn_fwd_workspace_size(Bc, H, T, d, b._dtype_code(q)), dtype=torch.uint8,
+                          device=dev)
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(nch)] for _ in range(3))
+        for e in ev_in + ev_cmp + ev_out:
+            e.record()
+
+        def e2e_step():
+            for c in range(nch):
+                sl = slice(c * Bc, (c + 1) * Bc)
+                s_in.wait_event(ev_cmp[c])          # the chunk's inputs are free again
+                with torch.cuda.stream(s_in):
+                    dq[sl].copy_(hq[sl], non_blocking=True)
+                    dk[sl].copy_(hk[sl], non_blocking=True)
+                    dv[sl].copy_(hv[sl], non_blocking=True)
+                ev_in[c].record(s_in)
+                s_cmp.wait_event(ev_in[c])
+                s_cmp.wait_event(ev_out[c])         # the chunk's output was read back
+                b.dilution_attn_fwd(dq[sl], dk[sl], dv[sl], out[sl], workspace=wsc, stream=s_cmp)
+                ev_cmp[c].record(s_cmp)
+                s_out.wait_event(ev_cmp[c])
+                with torch.cuda.stream(s_out):
+                    hout[sl].copy_(out[sl], non_blocking=True)
+                ev_out[c].record(s_out)
+
+        e2e_step()
         torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
-        e0.record()
+        e0.record(cur)
+        for st in (s_in, s_cmp, s_out):
+            st.wait_stream(cur)
         for _ in range(Ke):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            b.dilution_attn_fwd(dq, dk, dv, out, workspace=ws)
-            hout.copy_(out, non_blocking=True)
-        e1.record()
+            e2e_step()
+        for st in (s_in, s_cmp, s_out):
+            cur.wait_stream(st)
+        e1.record(cur)
         torch.cuda.synchronize()
+        assert b.dilution_attn_get_error(wsc) == b.DA_OK
         ems = e0.elapsed_time(e1)
         if world > 1:
             t = torch.tensor([ems], device=dev)
@@ -460,7 +494,9 @@ def run_ours(args):
         line["e2e"] = {"value": world * flops_step * Ke / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                        "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": Ke,
-                       "ms_per_step": ems / Ke}
+                       "ms_per_step": ems / Ke, "chunks": nch,
+                       "overlap": "copy-in, compute and copy-out streams per batch chunk"}
+        del wsc
         del hq, hk, hv, hout, dq, dk, dv
 
     del q, k, v, out, ws

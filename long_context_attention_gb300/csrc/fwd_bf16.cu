@@ -375,7 +375,7 @@ constexpr int kSwThreads = kSwWarps * 32;       // 640
 // Register split across warpgroups (setmaxnreg).  The block is launched with
 // 640 x (registers per thread) registers; the split below must not exceed that
 // (checked on the host before every launch).
-constexpr int kSwRegsDemand = 120, kSwRegsEpi = 56, kSwRegsCtl = 56;
+constexpr int kSwRegsDemand = 128, kSwRegsEpi = 56, kSwRegsCtl = 40;
 constexpr int kSwRegsNeeded = 128 * (kSwG * kSwRegsDemand + kSwRegsEpi + kSwRegsCtl);
 constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key groups x 1 KB
 constexpr uint32_t kStageBytes = 32 * 32 * 4;   // epilogue reduction box: 32 rows x 32 fp32, 128B-swizzled
