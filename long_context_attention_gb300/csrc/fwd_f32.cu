@@ -157,33 +157,61 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
 // 16 threads per row, 4 columns each.
 // split_lse: the workspace holds the row max and log2(l) separately (fp32
 // path); otherwise it holds -lse2 (bf16 path).
+constexpr int kFinRows = 4;
+
 template <typename OutT>
 __global__ void finalize_kernel(const float *__restrict__ acc, const float *__restrict__ lse2_ws,
                                 OutT *__restrict__ out, float *__restrict__ rowsum_out,
                                 float *__restrict__ lse2_out, int BH, int T, int Tp, bool split_lse) {
+  // 16 threads per row (one float4 of the numerator each); every thread
+  // handles kFinRows rows spaced one grid apart, with all loads issued before
+  // any arithmetic so that enough bytes are in flight for HBM rate.
+  const int64_t nrows = (int64_t)BH * T;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t row = g / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x / 16;   // rows per grid
   const int part = (int)(g % 16);
-  if (row >= (int64_t)BH * T) return;
-  const int64_t bh = row / T, i = row % T;
-  const float *ar = acc + ((size_t)bh * Tp + i) * kAccStride;
-  const float rs = ar[kD];
-  const float inv = 1.f / rs;
-  const float4 a = reinterpret_cast<const float4 *>(ar)[part];
-  if constexpr (sizeof(OutT) == 4) {
-    reinterpret_cast<float4 *>(out + row * kD)[part] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-  } else {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t *>(&lo);
-    pk.y = *reinterpret_cast<uint32_t *>(&hi);
-    reinterpret_cast<uint2 *>(out + row * kD)[part] = pk;
+  float rs[kFinRows];
+  float4 a[kFinRows];
+#pragma unroll
+  for (int j = 0; j < kFinRows; ++j) {
+    const int64_t row = g / 16 + j * stride;
+    if (row < nrows) {
+      const int64_t bh = row / T, i = row % T;
+      const float *ar = acc + ((size_t)bh * Tp + i) * kAccStride;
+      rs[j] = __ldg(ar + kD);
+      a[j] = __ldg(reinterpret_cast<const float4 *>(ar) + part);
+    }
   }
-  if (part == 0) {
-    if (rowsum_out) rowsum_out[row] = rs;
-    if (lse2_out) lse2_out[row] = split_lse ? lse2_ws[(size_t)bh * Tp + i] + ar[kD + 1] : -lse2_ws[(size_t)bh * Tp + i];
+#pragma unroll
+  for (int j = 0; j < kFinRows; ++j) {
+    const int64_t row = g / 16 + j * stride;
+    if (row >= nrows) break;
+    const float inv = 1.f / rs[j];
+    if constexpr (sizeof(OutT) == 4) {
+      reinterpret_cast<float4 *>(out + row * kD)[part] =
+          make_float4(a[j].x * inv, a[j].y * inv, a[j].z * inv, a[j].w * inv);
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a[j].x * inv, a[j].y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(a[j].z * inv, a[j].w * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t *>(&lo);
+      pk.y = *reinterpret_cast<uint32_t *>(&hi);
+      reinterpret_cast<uint2 *>(out + row * kD)[part] = pk;
+    }
+    if (part == 0) {
+      const int64_t bh = row / T, i = row % T;
+      if (rowsum_out) rowsum_out[row] = rs[j];
+      if (lse2_out)
+        lse2_out[row] = split_lse ? lse2_ws[(size_t)bh * Tp + i] + acc[((size_t)bh * Tp + i) * kAccStride + kD + 1]
+                                  : -lse2_ws[(size_t)bh * Tp + i];
+    }
   }
+}
+
+// Grid of the finalize pass: 16 threads per row, kFinRows rows per thread.
+static unsigned finalize_blocks(int64_t nrows) {
+  const int64_t threads = (nrows + kFinRows - 1) / kFinRows * 16;
+  return (unsigned)((threads + 255) / 256);
 }
 
 // ------------------------------------------------------------ host launchers
@@ -199,10 +227,9 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
   if (ev[1]) cudaEventRecord(ev[1], stream);
   f32_sweep<<<dim3(Tp / kF32KeysPerCta, BH), kF32KeysPerCta, smem, stream>>>(q, k, v, lse2_ws, acc, demand_out,
                                                                             T, Tp, c2, eps);
-  const int64_t threads = (int64_t)BH * T * 16;
   if (ev[2]) cudaEventRecord(ev[2], stream);
-  finalize_kernel<float><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(acc, lse2_ws, out, rowsum_out,
-                                                                                lse2_out, BH, T, Tp, true);
+  finalize_kernel<float><<<finalize_blocks((int64_t)BH * T), 256, 0, stream>>>(acc, lse2_ws, out, rowsum_out,
+                                                                               lse2_out, BH, T, Tp, true);
   if (ev[3]) cudaEventRecord(ev[3], stream);
   return cudaGetLastError();
 }
@@ -210,8 +237,7 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
 cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bfloat16 *out, float *rowsum_out,
                                  float *lse2_out, int BH, int T, cudaStream_t stream) {
   const int Tp = (int)t_pad(T);
-  const int64_t threads = (int64_t)BH * T * 16;
-  finalize_kernel<__nv_bfloat16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
+  finalize_kernel<__nv_bfloat16><<<finalize_blocks((int64_t)BH * T), 256, 0, stream>>>(
       acc, lse2_ws, out, rowsum_out, lse2_out, BH, T, Tp, false);
   return cudaGetLastError();
 }
