@@ -27,6 +27,18 @@ What it computes, and where each step comes from:
   every query processed so far and is updated after the step's output is
   formed; a newly appended key starts at zero.
 
+* The "earlier demand only" variant (``earlier_only=True``): the results
+  page, in the paragraph after "The operator", describes dividing each bid
+  by the earlier demand alone, which lets every key win its own first query
+  (the key itself) outright.  Reading taken: share = p / (committed + eps);
+  eps keeps the diagonal entry defined.  Forward and cached decode only.
+
+* ``tau`` may be a scalar or an array broadcastable to [B, H] in the batched
+  functions: one logit multiplier per (batch, head), the per-head
+  temperature of "Learning to Focus: Focal Attention for Selective and
+  Scalable Transformers", section "Transformer with Learned Temperature"
+  (learned there, given here as an input).
+
 * The backward pass is not written out on any page (the results page only
   says exact gradients exist).  ``dilution_backward`` is the chain rule through
   the forward above, derived by hand: softmax, exclusive column cumsum,
@@ -116,7 +128,8 @@ def _exclusive_cumsum_cols(p: np.ndarray) -> np.ndarray:
     return committed
 
 
-def dilution_forward_head(q, k, v, tau: float = 1.0, eps: float = 1e-6, full: bool = False):
+def dilution_forward_head(q, k, v, tau: float = 1.0, eps: float = 1e-6, full: bool = False,
+                          earlier_only: bool = False):
     """Dilution attention forward for one (batch, head) slice.
 
     q, k: [T, d]; v: [T, dv].  Returns a dict with
@@ -138,7 +151,7 @@ def dilution_forward_head(q, k, v, tau: float = 1.0, eps: float = 1e-6, full: bo
     lse = m + np.log(np.where(mask, np.exp(z - m[:, None]), 0.0).sum(axis=1))
     p = _causal_softmax(s)
     committed = _exclusive_cumsum_cols(p)
-    share = p / (committed + p + eps)
+    share = p / (committed + eps) if earlier_only else p / (committed + p + eps)
     rowsum = share.sum(axis=1)
     A = share / rowsum[:, None]
     out = A @ v
@@ -148,13 +161,15 @@ def dilution_forward_head(q, k, v, tau: float = 1.0, eps: float = 1e-6, full: bo
     return res
 
 
-def dilution_forward(q, k, v, tau: float = 1.0, eps: float = 1e-6):
+def dilution_forward(q, k, v, tau=1.0, eps: float = 1e-6, earlier_only: bool = False):
     """Batched forward over [B, H, T, d] inputs; heads are independent.
+    ``tau``: scalar or array broadcastable to [B, H].
 
     Returns dict of out [B,H,T,dv], rowsum [B,H,T], demand [B,H,T], lse [B,H,T].
     """
     q = np.asarray(q, dtype=np.float64)
     B, H, T, _ = q.shape
+    taus = np.broadcast_to(np.asarray(tau, dtype=np.float64), (B, H))
     dv = np.shape(v)[-1]
     out = np.empty((B, H, T, dv))
     rowsum = np.empty((B, H, T))
@@ -162,7 +177,7 @@ def dilution_forward(q, k, v, tau: float = 1.0, eps: float = 1e-6):
     lse = np.empty((B, H, T))
     for b in range(B):
         for h in range(H):
-            r = dilution_forward_head(q[b, h], k[b, h], v[b, h], tau, eps)
+            r = dilution_forward_head(q[b, h], k[b, h], v[b, h], float(taus[b, h]), eps, earlier_only=earlier_only)
             out[b, h], rowsum[b, h], demand[b, h], lse[b, h] = r["out"], r["rowsum"], r["demand"], r["lse"]
     return {"out": out, "rowsum": rowsum, "demand": demand, "lse": lse}
 
@@ -171,7 +186,7 @@ def dilution_forward(q, k, v, tau: float = 1.0, eps: float = 1e-6):
 # Forward, one head, row-blocked (for T too large for T x T matrices)
 # ---------------------------------------------------------------------------
 def dilution_forward_rowblocked_head(q, k, v, tau: float = 1.0, eps: float = 1e-6,
-                                     rows: int | None = None, block: int = 1024):
+                                     rows: int | None = None, block: int = 1024, earlier_only: bool = False):
     """Same operator as ``dilution_forward_head``, evaluated block of queries by
     block of queries, carrying the column demand of all earlier blocks.
 
@@ -201,7 +216,7 @@ def dilution_forward_rowblocked_head(q, k, v, tau: float = 1.0, eps: float = 1e-
         p = e / l[:, None]
         lse[i0:i1] = m + np.log(l)
         committed = carried[None, :kk] + _exclusive_cumsum_cols(p)
-        share = p / (committed + p + eps)
+        share = p / (committed + eps) if earlier_only else p / (committed + p + eps)
         rs = share.sum(axis=1)
         out[i0:i1] = (share / rs[:, None]) @ v[:kk]
         rowsum[i0:i1] = rs
@@ -213,7 +228,7 @@ def dilution_forward_rowblocked_head(q, k, v, tau: float = 1.0, eps: float = 1e-
 # Cached decode
 # ---------------------------------------------------------------------------
 def dilution_decode_step_head(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int,
-                              tau: float = 1.0, eps: float = 1e-6):
+                              tau: float = 1.0, eps: float = 1e-6, earlier_only: bool = False):
     """One cached-decode step for one (batch, head).
 
     The cache holds keys/values 0 .. n_ctx-1 and their running demand totals.
@@ -228,23 +243,26 @@ def dilution_decode_step_head(q_new, k_new, v_new, k_cache, v_cache, demand, n_c
     s = logit_scale(q_new.shape[0], tau) * (K @ q_new)
     e = np.exp(s - s.max())
     p = e / e.sum()
-    share = p / (D + p + eps)
+    share = p / (D + eps) if earlier_only else p / (D + p + eps)
     out = (share @ V) / share.sum()
     return out, D + p, K, V
 
 
 def dilution_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int,
-                         tau: float = 1.0, eps: float = 1e-6):
+                         tau=1.0, eps: float = 1e-6, earlier_only: bool = False):
     """Batched decode step: q_new/k_new/v_new [B,H,d]; caches [B,H,>=n_ctx,d];
-    demand [B,H,>=n_ctx].  Returns (out [B,H,dv], demand_new [B,H,n_ctx+1])."""
+    demand [B,H,>=n_ctx]; ``tau`` scalar or broadcastable to [B, H].
+    Returns (out [B,H,dv], demand_new [B,H,n_ctx+1])."""
     q_new = np.asarray(q_new, np.float64)
     B, H, _ = q_new.shape
+    taus = np.broadcast_to(np.asarray(tau, dtype=np.float64), (B, H))
     out = np.empty((B, H, np.shape(v_new)[-1]))
     dn = np.empty((B, H, n_ctx + 1))
     for b in range(B):
         for h in range(H):
             o, dd, _, _ = dilution_decode_step_head(q_new[b, h], k_new[b, h], v_new[b, h], k_cache[b, h],
-                                                   v_cache[b, h], demand[b, h], n_ctx, tau, eps)
+                                                   v_cache[b, h], demand[b, h], n_ctx, float(taus[b, h]), eps,
+                                                   earlier_only)
             out[b, h], dn[b, h] = o, dd
     return out, dn
 
@@ -293,14 +311,17 @@ def dilution_backward_head(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6):
     return dq, dk, dv
 
 
-def dilution_backward(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6):
-    """Batched backward over [B,H,T,d]; returns (dq, dk, dv)."""
+def dilution_backward(q, k, v, dout, tau=1.0, eps: float = 1e-6):
+    """Batched backward over [B,H,T,d]; ``tau`` scalar or broadcastable to
+    [B, H]; returns (dq, dk, dv)."""
     q = np.asarray(q, np.float64)
     B, H, T, d = q.shape
+    taus = np.broadcast_to(np.asarray(tau, dtype=np.float64), (B, H))
     dq = np.empty_like(q)
     dk = np.empty((B, H, T, d))
     dv = np.empty((B, H, T, np.shape(v)[-1]))
     for b in range(B):
         for h in range(H):
-            dq[b, h], dk[b, h], dv[b, h] = dilution_backward_head(q[b, h], k[b, h], v[b, h], dout[b, h], tau, eps)
+            dq[b, h], dk[b, h], dv[b, h] = dilution_backward_head(q[b, h], k[b, h], v[b, h], dout[b, h],
+                                                                  float(taus[b, h]), eps)
     return dq, dk, dv

@@ -244,6 +244,66 @@ def pin_backward_autograd(T=24, d=8, seed=14, tau=1.1, eps=1e-6):
                np.abs(tv.grad.numpy() - dv).max())
 
 
+def pin_earlier_only_brute_force(T=8, d=4, seed=15, tau=0.8, eps=1e-3):
+    """"Earlier demand only": scalar loops with share = bid / (demand + eps),
+    the running demand taken before the current bid is added."""
+    q, k, v = _rand(T, d, seed, dv=3, q_std=2.0)
+    ql, kl, vl = q.tolist(), k.tolist(), v.tolist()
+    c = tau / math.sqrt(d)
+    demand = [0.0] * T
+    outs, shares = [], []
+    for i in range(T):
+        logits = [c * sum(ql[i][t] * kl[j][t] for t in range(d)) for j in range(i + 1)]
+        mx = max(logits)
+        ex = [math.exp(x - mx) for x in logits]
+        z = sum(ex)
+        bids = [x / z for x in ex]
+        sh = [bids[j] / (demand[j] + eps) for j in range(i + 1)]
+        tot = sum(sh)
+        outs.append([sum(sh[j] * vl[j][t] for j in range(i + 1)) / tot for t in range(3)])
+        shares.append(sh + [0.0] * (T - i - 1))
+        for j in range(i + 1):
+            demand[j] += bids[j]
+    r = od.dilution_forward_head(q, k, v, tau, eps, full=True, earlier_only=True)
+    return max(np.abs(r["out"] - np.array(outs)).max() / max(1.0, np.abs(np.array(outs)).max()),
+               np.abs(r["share"] - np.array(shares)).max() / max(1.0, np.abs(np.array(shares)).max()))
+
+
+def pin_earlier_only_uniform_harmonic(T=23, d=8, eps=1e-6, seed=16):
+    """q = 0: p_ik = 1/(i+1), committed_ik = H_i - H_k, so the earlier-only
+    share is 1/((i+1)(H_i - H_k + eps)) (eps alone on the diagonal)."""
+    _, k, v = _rand(T, d, seed)
+    r = od.dilution_forward_head(np.zeros((T, d)), k, v, 1.0, eps, full=True, earlier_only=True)
+    H = [_harmonic(n) for n in range(T + 2)]
+    s_cf = np.zeros((T, T))
+    for i in range(T):
+        for kk in range(i + 1):
+            s_cf[i, kk] = 1.0 / ((i + 1) * (H[i] - H[kk] + eps))
+    out_cf = (s_cf / s_cf.sum(axis=1, keepdims=True)) @ v
+    return max(np.abs(r["share"] / s_cf.max() - s_cf / s_cf.max()).max(), np.abs(r["out"] - out_cf).max())
+
+
+def pin_earlier_only_identity(T=40, d=16, seed=17):
+    """The pages' observation: dividing by earlier demand alone lets each key
+    win its own first query outright, so as eps -> 0 the layer becomes the
+    identity map, out_i -> v_i."""
+    q, k, v = _rand(T, d, seed)
+    r = od.dilution_forward_head(q, k, v, 1.0, 1e-12, earlier_only=True)
+    return np.abs(r["out"] - v).max() * 1e-3   # identity to ~1e-6 relative: scaled into the pin's tolerance
+
+
+def pin_earlier_only_decode_equals_prefill(T=12, d=8, seed=18, tau=1.1, eps=1e-4):
+    q, k, v = _rand(T, d, seed, q_std=1.5)
+    worst = 0.0
+    for n in range(1, T):
+        pre = od.dilution_forward_head(q[:n], k[:n], v[:n], tau, eps, earlier_only=True)
+        out, dn, _, _ = od.dilution_decode_step_head(q[n], k[n], v[n], k[:n], v[:n], pre["demand"], n, tau, eps,
+                                                     earlier_only=True)
+        full = od.dilution_forward_head(q[:n + 1], k[:n + 1], v[:n + 1], tau, eps, earlier_only=True)
+        worst = max(worst, np.abs(out - full["out"][n]).max(), np.abs(dn - full["demand"]).max())
+    return worst
+
+
 FORWARD_PINS = [
     (pin_uniform_bids_harmonic, 1e-12),
     (pin_equal_keys_harmonic, 1e-12),
@@ -255,6 +315,10 @@ FORWARD_PINS = [
     (pin_decode_equals_prefill, 1e-12),
     (pin_rowblocked, 1e-12),
     (pin_lse, 1e-12),
+    (pin_earlier_only_brute_force, 1e-12),
+    (pin_earlier_only_uniform_harmonic, 1e-12),
+    (pin_earlier_only_identity, 1e-6),
+    (pin_earlier_only_decode_equals_prefill, 1e-12),
 ]
 
 
@@ -303,6 +367,26 @@ def test_batched_matches_per_head():
             assert np.array_equal(r["out"][b, h], rh["out"])
     out, dn = od.dilution_decode_step(q[:, :, 0], k[:, :, 0], v[:, :, 0], k, v, np.zeros((2, 3, 10)), 0)
     assert np.allclose(out, v[:, :, 0])
+
+
+def test_tau_per_batch_head_indexing():
+    # one multiplier per (batch, head): each slice equals the scalar-tau result
+    # for its own multiplier (catches a transposed or shared index)
+    rng = np.random.default_rng(19)
+    B, H, T, d = 2, 3, 9, 8
+    q, k, v = (rng.standard_normal((B, H, T, d)) for _ in range(3))
+    taus = np.array([[0.5, 1.0, 1.7], [2.2, 0.9, 1.3]])
+    r = od.dilution_forward(q, k, v, taus, 1e-6)
+    g = rng.standard_normal((B, H, T, d))
+    dq, dk, dv = od.dilution_backward(q, k, v, g, taus, 1e-6)
+    for b in range(B):
+        for h in range(H):
+            one = od.dilution_forward_head(q[b, h], k[b, h], v[b, h], taus[b, h], 1e-6)
+            assert np.abs(r["out"][b, h] - one["out"]).max() < 1e-13
+            bq, bk, bv = od.dilution_backward_head(q[b, h], k[b, h], v[b, h], g[b, h], taus[b, h], 1e-6)
+            assert max(np.abs(dq[b, h] - bq).max(), np.abs(dk[b, h] - bk).max(), np.abs(dv[b, h] - bv).max()) < 1e-12
+    # and the per-head values really differ from a shared one
+    assert np.abs(r["out"][0, 0] - od.dilution_forward_head(q[0, 0], k[0, 0], v[0, 0], 1.0, 1e-6)["out"]).max() > 1e-3
 
 
 def test_backward_finite_differences():
