@@ -60,6 +60,9 @@ extern "C" {
 
 #define DA_MAX_T (1 << 24)
 
+/* Flags of the *_ex entry points (bitwise or; other bits are DA_ERR_INVALID). */
+#define DA_FLAG_EARLIER_DEMAND_ONLY 1   /* share = p / (committed + eps): see below */
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *dilution_attn_status_string(int status);
 
@@ -104,6 +107,39 @@ int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, v
                                   void *const *events);
 
 /* ------------------------------------------------------------------------
+ * Extended forward: dilution_attn_fwd_with_events plus two options.
+ *
+ *   tau_bh  nullable DEVICE pointer to B*H fp32 logit multipliers, index
+ *           b*H + h: head (b, h) uses tau_bh[b*H + h] instead of `tau` (a
+ *           per-head temperature, "Learning to Focus: Focal Attention for
+ *           Selective and Scalable Transformers", section "Transformer with
+ *           Learned Temperature": learned there, an input here).  4-byte
+ *           aligned.  `tau` is still validated but unused when tau_bh is
+ *           given.  Entries must be finite and >= 0; the kernels cannot
+ *           return a synchronous error for device data, so a negative, NaN or
+ *           infinite entry sets DA_ERR_INVALID in the status word
+ *           (dilution_attn_get_error) and that head's results are unspecified.
+ *           The backward and decode calls of the same model must receive the
+ *           same array.
+ *   flags   DA_FLAG_EARLIER_DEMAND_ONLY: the ablation of "DilutionAttention
+ *           v0.1.0 · results" (paragraph after "The operator") that divides
+ *           each bid by the demand of earlier queries alone,
+ *               share_ik = p_ik / (committed_ik + eps),
+ *           so every key's first query (the key itself) gets share p_ii / eps
+ *           and, as eps -> 0, the layer tends to the identity map.  For
+ *           DA_BF16, shares up to 1/eps are fed to the value product in bf16;
+ *           eps >= 1e-18 as for the default operator.
+ *   events  as for dilution_attn_fwd_with_events (nullable).
+ * Other arguments, outputs and errors as for dilution_attn_fwd; unknown flag
+ * bits or a misaligned tau_bh return DA_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
+                         float *lse2_out, float *rowsum_out, float *demand_out,
+                         int B, int H, int T, int d, float tau, const float *tau_bh, float eps,
+                         int flags, int dtype, void *workspace, size_t workspace_bytes, void *stream,
+                         void *const *events);
+
+/* ------------------------------------------------------------------------
  * Backward: gradients dq, dk, dv [B,H,T,d] of sum(dout * out) for the
  * forward above (the page states only that exact gradients exist; they are
  * the chain rule through the causal softmax, the exclusive column cumsum, the
@@ -120,6 +156,16 @@ int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *d
                       const float *lse2, void *dq, void *dk, void *dv,
                       int B, int H, int T, int d, float tau, float eps, int dtype,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward with the options of dilution_attn_fwd_ex: tau_bh (nullable device
+ * [B*H]) and flags (DA_FLAG_EARLIER_DEMAND_ONLY), which must match the
+ * forward that produced lse2.  With the flag, D_jk = committed_jk + eps and
+ * the direct term of dp_jk is dr_jk / D_jk.  Errors as for dilution_attn_bwd
+ * plus those of dilution_attn_fwd_ex for tau_bh and flags. */
+int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void *dout,
+                         const float *lse2, void *dq, void *dk, void *dv,
+                         int B, int H, int T, int d, float tau, const float *tau_bh, float eps,
+                         int flags, int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Cached decode step ("DilutionAttention v0.1.0 · results", section "The
@@ -147,6 +193,18 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
                               int n_ctx, int T_cap, void *out,
                               int B, int H, int d, float tau, float eps, int dtype,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Decode step with the options of dilution_attn_fwd_ex: tau_bh (nullable
+ * device [B*H]) and flags.  With DA_FLAG_EARLIER_DEMAND_ONLY step 3 becomes
+ * share_k = p_k / (demand_k + eps); the demand update is unchanged, so a
+ * cache built by a flagged prefill continues the flagged operator.  Errors as
+ * for dilution_attn_decode_step plus those of dilution_attn_fwd_ex for tau_bh
+ * and flags. */
+int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new,
+                                 void *k_cache, void *v_cache, float *demand,
+                                 int n_ctx, int T_cap, void *out,
+                                 int B, int H, int d, float tau, const float *tau_bh, float eps,
+                                 int flags, int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Cached decode step that allocates nothing (no counterpart on the pages: an

@@ -19,6 +19,7 @@ from . import build as _build
 
 DA_OK, DA_ERR_INVALID, DA_ERR_UNSUPPORTED, DA_ERR_CUDA, DA_ERR_TIMEOUT, DA_ERR_WORKSPACE = range(6)
 DA_F32, DA_BF16 = 0, 1
+DA_FLAG_EARLIER_DEMAND_ONLY = 1
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dilution_attn.h")
 
 _lib = None
@@ -38,12 +39,19 @@ _SIGNATURES = {
     "dilution_attn_fwd_with_events": (_c_int, [_c_void_p] * 7 + [_c_int] * 4 + [_c_float, _c_float, _c_int,
                                                                                     _c_void_p, _c_size_t, _c_void_p,
                                                                                     _c_void_p]),
+    "dilution_attn_fwd_ex": (_c_int, [_c_void_p] * 7 + [_c_int] * 4 + [_c_float, _c_void_p, _c_float, _c_int, _c_int,
+                                                                       _c_void_p, _c_size_t, _c_void_p, _c_void_p]),
     "dilution_attn_bwd_workspace_size": (_c_size_t, [_c_int] * 5),
     "dilution_attn_bwd": (_c_int, [_c_void_p] * 8 + [_c_int] * 4 + [_c_float, _c_float, _c_int, _c_void_p, _c_size_t,
                                                                         _c_void_p]),
+    "dilution_attn_bwd_ex": (_c_int, [_c_void_p] * 8 + [_c_int] * 4 + [_c_float, _c_void_p, _c_float, _c_int, _c_int,
+                                                                       _c_void_p, _c_size_t, _c_void_p]),
     "dilution_attn_decode_workspace_size": (_c_size_t, [_c_int] * 4),
     "dilution_attn_decode_step": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                   [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
+    "dilution_attn_decode_step_ex": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
+                                     [_c_float, _c_void_p, _c_float, _c_int, _c_int, _c_void_p, _c_size_t,
+                                      _c_void_p]),
     "dilution_attn_decode_step_noalloc": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                           [_c_float, _c_float, _c_int, _c_void_p]),
     "dilution_attn_decode_noalloc_scratch_bytes": (_c_size_t, []),
@@ -156,13 +164,7 @@ def _event_handle(e):
     return e.cuda_event
 
 
-def dilution_attn_fwd_with_events(q, k, v, out=None, lse2_out=None, rowsum_out=None, demand_out=None, *,
-                                  tau: float = 1.0, eps: float = 1e-6, workspace=None, stream=None,
-                                  check: bool = True, events=None):
-    """dilution_attn_fwd that also records up to four torch.cuda.Event
-    (timing-enabled) on the stream: before row statistics, before the sweep,
-    before finalize, after finalize."""
-    lib = load()
+def _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace):
     _need(q, "q")
     B, H, T, d = q.shape
     _need(k, "k", q.shape, q.dtype)
@@ -177,14 +179,58 @@ def dilution_attn_fwd_with_events(q, k, v, out=None, lse2_out=None, rowsum_out=N
     need = dilution_attn_fwd_workspace_size(B, H, T, d, dt)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    ev = None
-    if events is not None:
-        ev = (ctypes.c_void_p * 4)(*[_event_handle(e) for e in events])
+    return out, workspace, dt
+
+
+def _events_array(events):
+    if events is None:
+        return None
+    return (ctypes.c_void_p * 4)(*[_event_handle(e) for e in events])
+
+
+def _tau_bh_ptr(tau_bh, B, H):
+    """Marshal an optional per-(batch, head) multiplier tensor: fp32 CUDA, B*H elements."""
+    if tau_bh is None:
+        return None
+    _need(tau_bh, "tau_bh", None, torch.float32)
+    if tau_bh.numel() != B * H:
+        raise ValueError(f"tau_bh has {tau_bh.numel()} elements, expected B*H = {B * H}")
+    return _ptr(tau_bh)
+
+
+def dilution_attn_fwd_with_events(q, k, v, out=None, lse2_out=None, rowsum_out=None, demand_out=None, *,
+                                  tau: float = 1.0, eps: float = 1e-6, workspace=None, stream=None,
+                                  check: bool = True, events=None):
+    """dilution_attn_fwd that also records up to four torch.cuda.Event
+    (timing-enabled) on the stream: before row statistics, before the sweep,
+    before finalize, after finalize."""
+    lib = load()
+    out, workspace, dt = _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace)
+    B, H, T, d = q.shape
     st = lib.dilution_attn_fwd_with_events(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2_out), _ptr(rowsum_out),
                                            _ptr(demand_out), B, H, T, d, float(tau), float(eps), dt,
-                                           _ptr(workspace), workspace.numel(), _stream_handle(stream), ev)
+                                           _ptr(workspace), workspace.numel(), _stream_handle(stream),
+                                           _events_array(events))
     if check:
         _check(st, "dilution_attn_fwd")
+    return out
+
+
+def dilution_attn_fwd_ex(q, k, v, out=None, lse2_out=None, rowsum_out=None, demand_out=None, *,
+                         tau: float = 1.0, tau_bh=None, eps: float = 1e-6, flags: int = 0, workspace=None,
+                         stream=None, check: bool = True, events=None):
+    """Forward with a per-(batch, head) multiplier tensor ``tau_bh`` (fp32 CUDA,
+    B*H elements, index b*H + h; replaces ``tau``) and ``flags``
+    (``DA_FLAG_EARLIER_DEMAND_ONLY``)."""
+    lib = load()
+    out, workspace, dt = _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace)
+    B, H, T, d = q.shape
+    st = lib.dilution_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2_out), _ptr(rowsum_out),
+                                  _ptr(demand_out), B, H, T, d, float(tau), _tau_bh_ptr(tau_bh, B, H), float(eps),
+                                  int(flags), dt, _ptr(workspace), workspace.numel(), _stream_handle(stream),
+                                  _events_array(events))
+    if check:
+        _check(st, "dilution_attn_fwd_ex")
     return out
 
 
@@ -193,10 +239,7 @@ def dilution_attn_bwd_workspace_size(B: int, H: int, T: int, d: int, dtype: int)
     return int(load().dilution_attn_bwd_workspace_size(B, H, T, d, dtype))
 
 
-def dilution_attn_bwd(q, k, v, dout, lse2, dq=None, dk=None, dv=None, *, tau: float = 1.0, eps: float = 1e-6,
-                      workspace=None, stream=None, check: bool = True):
-    """Gradients (dq, dk, dv) of sum(dout * out); lse2 is the forward's lse2_out."""
-    lib = load()
+def _bwd_prepare(q, k, v, dout, lse2, dq, dk, dv, workspace):
     _need(q, "q")
     B, H, T, d = q.shape
     for name, t in (("k", k), ("v", v), ("dout", dout)):
@@ -211,6 +254,15 @@ def dilution_attn_bwd(q, k, v, dout, lse2, dq=None, dk=None, dv=None, *, tau: fl
     if workspace is None:
         workspace = torch.empty(max(dilution_attn_bwd_workspace_size(B, H, T, d, dt), 256), dtype=torch.uint8,
                                 device=q.device)
+    return dq, dk, dv, workspace, dt
+
+
+def dilution_attn_bwd(q, k, v, dout, lse2, dq=None, dk=None, dv=None, *, tau: float = 1.0, eps: float = 1e-6,
+                      workspace=None, stream=None, check: bool = True):
+    """Gradients (dq, dk, dv) of sum(dout * out); lse2 is the forward's lse2_out."""
+    lib = load()
+    dq, dk, dv, workspace, dt = _bwd_prepare(q, k, v, dout, lse2, dq, dk, dv, workspace)
+    B, H, T, d = q.shape
     st = lib.dilution_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse2), _ptr(dq), _ptr(dk), _ptr(dv), B,
                                H, T, d, float(tau), float(eps), dt, _ptr(workspace), workspace.numel(),
                                _stream_handle(stream))
@@ -219,20 +271,26 @@ def dilution_attn_bwd(q, k, v, dout, lse2, dq=None, dk=None, dv=None, *, tau: fl
     return dq, dk, dv
 
 
+def dilution_attn_bwd_ex(q, k, v, dout, lse2, dq=None, dk=None, dv=None, *, tau: float = 1.0, tau_bh=None,
+                         eps: float = 1e-6, flags: int = 0, workspace=None, stream=None, check: bool = True):
+    """dilution_attn_bwd with the ``tau_bh`` and ``flags`` of the matching forward."""
+    lib = load()
+    dq, dk, dv, workspace, dt = _bwd_prepare(q, k, v, dout, lse2, dq, dk, dv, workspace)
+    B, H, T, d = q.shape
+    st = lib.dilution_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse2), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  B, H, T, d, float(tau), _tau_bh_ptr(tau_bh, B, H), float(eps), int(flags), dt,
+                                  _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if check:
+        _check(st, "dilution_attn_bwd_ex")
+    return dq, dk, dv
+
+
 # ---------------------------------------------------------------------------- decode
 def dilution_attn_decode_workspace_size(B: int, H: int, T_cap: int, d: int) -> int:
     return int(load().dilution_attn_decode_workspace_size(B, H, T_cap, d))
 
 
-def dilution_attn_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,
-                              tau: float = 1.0, eps: float = 1e-6, workspace=None, stream=None,
-                              check: bool = True):
-    """One cached decode step; caches [B, H, T_cap, d], demand [B, H, T_cap] fp32.
-
-    Appends k_new/v_new at position n_ctx, updates ``demand`` in place and
-    returns ``out`` [B, H, d].
-    """
-    lib = load()
+def _decode_prepare(q_new, k_new, v_new, k_cache, v_cache, demand, out):
     _need(q_new, "q_new")
     B, H, d = q_new.shape
     _need(k_new, "k_new", q_new.shape, q_new.dtype)
@@ -245,6 +303,20 @@ def dilution_attn_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_c
     if out is None:
         out = torch.empty_like(q_new)
     _need(out, "out", q_new.shape, q_new.dtype)
+    return out, T_cap
+
+
+def dilution_attn_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,
+                              tau: float = 1.0, eps: float = 1e-6, workspace=None, stream=None,
+                              check: bool = True):
+    """One cached decode step; caches [B, H, T_cap, d], demand [B, H, T_cap] fp32.
+
+    Appends k_new/v_new at position n_ctx, updates ``demand`` in place and
+    returns ``out`` [B, H, d].
+    """
+    lib = load()
+    out, T_cap = _decode_prepare(q_new, k_new, v_new, k_cache, v_cache, demand, out)
+    B, H, d = q_new.shape
     if workspace is None:
         workspace = torch.empty(max(dilution_attn_decode_workspace_size(B, H, T_cap, d), 256), dtype=torch.uint8,
                                 device=q_new.device)
@@ -257,22 +329,31 @@ def dilution_attn_decode_step(q_new, k_new, v_new, k_cache, v_cache, demand, n_c
     return out
 
 
+def dilution_attn_decode_step_ex(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,
+                                 tau: float = 1.0, tau_bh=None, eps: float = 1e-6, flags: int = 0, workspace=None,
+                                 stream=None, check: bool = True):
+    """dilution_attn_decode_step with ``tau_bh`` and ``flags`` (see dilution_attn_fwd_ex)."""
+    lib = load()
+    out, T_cap = _decode_prepare(q_new, k_new, v_new, k_cache, v_cache, demand, out)
+    B, H, d = q_new.shape
+    if workspace is None:
+        workspace = torch.empty(max(dilution_attn_decode_workspace_size(B, H, T_cap, d), 256), dtype=torch.uint8,
+                                device=q_new.device)
+    st = lib.dilution_attn_decode_step_ex(_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(demand), int(n_ctx), T_cap, _ptr(out), B, H, d, float(tau),
+                                          _tau_bh_ptr(tau_bh, B, H), float(eps), int(flags), _dtype_code(q_new),
+                                          _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if check:
+        _check(st, "dilution_attn_decode_step_ex")
+    return out
+
+
 def dilution_attn_decode_step_noalloc(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,
                                       tau: float = 1.0, eps: float = 1e-6, stream=None, check: bool = True):
     """dilution_attn_decode_step with the library's fixed scratch array instead of a workspace."""
     lib = load()
-    _need(q_new, "q_new")
+    out, T_cap = _decode_prepare(q_new, k_new, v_new, k_cache, v_cache, demand, out)
     B, H, d = q_new.shape
-    _need(k_new, "k_new", q_new.shape, q_new.dtype)
-    _need(v_new, "v_new", q_new.shape, q_new.dtype)
-    _need(k_cache, "k_cache", None, q_new.dtype)
-    T_cap = k_cache.shape[2]
-    _need(k_cache, "k_cache", (B, H, T_cap, d))
-    _need(v_cache, "v_cache", (B, H, T_cap, d), q_new.dtype)
-    _need(demand, "demand", (B, H, T_cap), torch.float32)
-    if out is None:
-        out = torch.empty_like(q_new)
-    _need(out, "out", q_new.shape, q_new.dtype)
     st = lib.dilution_attn_decode_step_noalloc(_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                                _ptr(demand), int(n_ctx), T_cap, _ptr(out), B, H, d, float(tau),
                                                float(eps), _dtype_code(q_new), _stream_handle(stream))

@@ -3,7 +3,9 @@
 // The pages state only that exact gradients exist ("DilutionAttention v0.1.0
 // · results", last section); the chain rule through the operator of section
 // "The operator" gives, per (batch, head), with c = tau/sqrt(d),
-// D_jk = committed_jk + p_jk + eps, r = share, R_j = sum_k r_jk, A = r / R:
+// D_jk = committed_jk + p_jk + eps, r = share, R_j = sum_k r_jk, A = r / R
+// (the earlier-demand-only variant: D_jk = committed_jk + eps and the direct
+// term of dp_jk is dr_jk / D_jk):
 //
 //   dV_k   = sum_j A_jk g_j                      (g = dout)
 //   dr_jk  = (g_j . v_k - g_j . out_j) / R_j
@@ -72,16 +74,16 @@ struct ColState {
 };
 
 __device__ __forceinline__ float col_step(ColState &cs, float p, float dA, float delta, float rinv, float eps,
-                                          float &a_out) {
+                                          bool earlier, float &a_out) {
   const float cpe = (float)(cs.dtot - cs.srev - (double)p) + eps;   // committed + eps
-  const float den = cpe + p;
+  const float den = earlier ? cpe : cpe + p;
   const float inv = 1.f / den;
   const float r = p * inv;
   a_out = r * rinv;
   const float dr = (dA - delta) * rinv;
   const float inv2 = inv * inv;
   const float dC = -dr * p * inv2;
-  const float dp = dr * cpe * inv2 + cs.grev;
+  const float dp = (earlier ? dr * inv : dr * cpe * inv2) + cs.grev;
   cs.grev += dC;
   cs.srev += (double)p;
   return dp;
@@ -92,10 +94,13 @@ __global__ void __launch_bounds__(kBwKeys)
     bwd_pass(const E *__restrict__ q, const E *__restrict__ k, const E *__restrict__ v, const E *__restrict__ g,
              const float *__restrict__ lse2, double *__restrict__ dtot, float *__restrict__ Rsum,
              float *__restrict__ Ysum, float *__restrict__ rho, float *__restrict__ dq_acc, E *__restrict__ dk_out,
-             E *__restrict__ dv_out, int T, float c, float c2, float eps) {
+             E *__restrict__ dv_out, int T, float c_scalar, HeadScale hs, float eps, bool earlier) {
   extern __shared__ float4 bw_smem_raw[];
   BwdSmem &S = *reinterpret_cast<BwdSmem *>(bw_smem_raw);
   const int bh = blockIdx.y;
+  // natural-log scale c = tau / sqrt(d) of this head (c2 = c log2(e))
+  const float c2 = head_c2(hs, bh, nullptr);
+  const float c = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int key0 = blockIdx.x * kBwKeys;
   const int key = key0 + tid;
@@ -146,13 +151,13 @@ __global__ void __launch_bounds__(kBwKeys)
         }
         const float p = exp2f(sdot * c2 - S.lse2[r]);
         if (PASS == 0) {
-          const float share = p / (((float)csum + p) + eps);
+          const float share = p / ((earlier ? (float)csum : (float)csum + p) + eps);
           csum += (double)p;
           c0 = share;
           c1 = share * dA;
         } else {
           float a;
-          const float dp = col_step(cs, p, dA, S.delta[r], S.rinv[r], eps, a);
+          const float dp = col_step(cs, p, dA, S.delta[r], S.rinv[r], eps, earlier, a);
           if (PASS == 1) {
             c0 = p * dp;
 #pragma unroll
@@ -224,8 +229,8 @@ __global__ void bwd_final(const float *__restrict__ dq_acc, E *__restrict__ dq, 
 
 template <typename E>
 static cudaError_t launch_bwd_t(const void *q, const void *k, const void *v, const void *dout, const float *lse2,
-                                void *dq, void *dk, void *dv, int BH, int T, float c, float c2, float eps,
-                                double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream) {
+                                void *dq, void *dk, void *dv, int BH, int T, float c, HeadScale hs, float eps,
+                                bool earlier, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream) {
   const int64_t rows = (int64_t)BH * T;
   float *Rsum = rowbuf, *Ysum = rowbuf + rows, *rho = rowbuf + 2 * rows;
   const int64_t nz = rows * kD;
@@ -238,22 +243,23 @@ static cudaError_t launch_bwd_t(const void *q, const void *k, const void *v, con
   if (e != cudaSuccess) return e;
   const dim3 grid((T + kBwKeys - 1) / kBwKeys, BH);
   bwd_pass<E, 0><<<grid, kBwKeys, smem, stream>>>((const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2,
-                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, c2, eps);
+                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, hs, eps, earlier);
   bwd_pass<E, 1><<<grid, kBwKeys, smem, stream>>>((const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2,
-                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, c2, eps);
+                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, hs, eps, earlier);
   bwd_pass<E, 2><<<grid, kBwKeys, smem, stream>>>((const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2,
-                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, c2, eps);
+                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, hs, eps, earlier);
   bwd_final<E><<<(unsigned)((nz + 255) / 256), 256, 0, stream>>>(dq_acc, (E *)dq, nz);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
-                       void *dk, void *dv, int BH, int T, float c, float c2, float eps, int dtype, double *dtot,
-                       float *rowbuf, float *dq_acc, cudaStream_t stream) {
+                       void *dk, void *dv, int BH, int T, float c, HeadScale hs, float eps, bool earlier, int dtype,
+                       double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream) {
   if (dtype == DA_BF16)
-    return launch_bwd_t<__nv_bfloat16>(q, k, v, dout, lse2, dq, dk, dv, BH, T, c, c2, eps, dtot, rowbuf, dq_acc,
-                                       stream);
-  return launch_bwd_t<float>(q, k, v, dout, lse2, dq, dk, dv, BH, T, c, c2, eps, dtot, rowbuf, dq_acc, stream);
+    return launch_bwd_t<__nv_bfloat16>(q, k, v, dout, lse2, dq, dk, dv, BH, T, c, hs, eps, earlier, dtot, rowbuf,
+                                       dq_acc, stream);
+  return launch_bwd_t<float>(q, k, v, dout, lse2, dq, dk, dv, BH, T, c, hs, eps, earlier, dtot, rowbuf, dq_acc,
+                             stream);
 }
 
 }  // namespace da

@@ -10,17 +10,19 @@
 
 namespace da {
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
-                           float *rowsum_out, float *demand_out, int BH, int T, float c2, float eps,
-                           float *lse2_ws, float *acc, cudaStream_t stream, cudaEvent_t const *ev);
+                           float *rowsum_out, float *demand_out, int BH, int T, HeadScale hs, float eps,
+                           bool earlier, float *lse2_ws, float *acc, int *status, cudaStream_t stream,
+                           cudaEvent_t const *ev);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
-                    float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
-                    cudaStream_t stream, cudaEvent_t const *ev);
+                    float *demand_out, int BH, int T, HeadScale hs, float eps, bool earlier, float *lse2_ws,
+                    float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev);
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
-                       void *dk, void *dv, int BH, int T, float c, float c2, float eps, int dtype, double *dtot,
-                       float *rowbuf, float *dq_acc, cudaStream_t stream);
+                       void *dk, void *dv, int BH, int T, float c, HeadScale hs, float eps, bool earlier, int dtype,
+                       double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
-                          float *demand, int n_ctx, int T_cap, void *out, int BH, float c2, float eps, int dtype,
-                          float *logits, float2 *part_ml, float *part_acc, int nchunk, cudaStream_t stream);
+                          float *demand, int n_ctx, int T_cap, void *out, int BH, HeadScale hs, float eps,
+                          bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
+                          int *status, cudaStream_t stream);
 }  // namespace da
 
 using namespace da;
@@ -34,6 +36,17 @@ bool aligned16_or_null(const void *p) { return p == nullptr || aligned16(p); }
 
 // Scale applied to q.k in the log2 domain: tau / sqrt(d) * log2(e).
 float logit_scale_log2(float tau, int d) { return (float)((double)tau / std::sqrt((double)d) * kLog2e); }
+
+HeadScale head_scale(float tau, const float *tau_bh, int d) {
+  return HeadScale{tau_bh, logit_scale_log2(tau, d), logit_scale_log2(1.f, d)};
+}
+
+// Options of the *_ex entry points.
+int check_options(const float *tau_bh, int flags) {
+  if ((flags & ~DA_FLAG_EARLIER_DEMAND_ONLY) != 0) return DA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(tau_bh) & 3u) != 0) return DA_ERR_INVALID;
+  return DA_OK;
+}
 
 int check_common(int B, int H, int T, int d, float tau, float eps, int dtype) {
   if (B < 0 || H < 0 || T < 0) return DA_ERR_INVALID;
@@ -62,7 +75,7 @@ const char *dilution_attn_status_string(int status) {
   }
 }
 
-int dilution_attn_version(void) { return 100; }
+int dilution_attn_version(void) { return 101; }
 
 size_t dilution_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype) {
   (void)d;
@@ -74,19 +87,29 @@ size_t dilution_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype) {
 int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                       float *demand_out, int B, int H, int T, int d, float tau, float eps, int dtype,
                       void *workspace, size_t workspace_bytes, void *stream_) {
-  return dilution_attn_fwd_with_events(q, k, v, out, lse2_out, rowsum_out, demand_out, B, H, T, d, tau, eps, dtype,
-                                       workspace, workspace_bytes, stream_, nullptr);
+  return dilution_attn_fwd_ex(q, k, v, out, lse2_out, rowsum_out, demand_out, B, H, T, d, tau, nullptr, eps, 0,
+                              dtype, workspace, workspace_bytes, stream_, nullptr);
 }
 
 int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, void *out, float *lse2_out,
                                   float *rowsum_out, float *demand_out, int B, int H, int T, int d, float tau,
                                   float eps, int dtype, void *workspace, size_t workspace_bytes, void *stream_,
                                   void *const *events) {
+  return dilution_attn_fwd_ex(q, k, v, out, lse2_out, rowsum_out, demand_out, B, H, T, d, tau, nullptr, eps, 0,
+                              dtype, workspace, workspace_bytes, stream_, events);
+}
+
+int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse2_out,
+                         float *rowsum_out, float *demand_out, int B, int H, int T, int d, float tau,
+                         const float *tau_bh, float eps, int flags, int dtype, void *workspace,
+                         size_t workspace_bytes, void *stream_, void *const *events) {
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   if (events != nullptr)
     for (int i = 0; i < 4; ++i) ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   int st = check_common(B, H, T, d, tau, eps, dtype);
+  if (st == DA_OK) st = check_options(tau_bh, flags);
   if (st != DA_OK) return st;
+  const bool earlier = (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0;
   const int64_t BH = (int64_t)B * H;
   if (BH == 0 || T == 0) return DA_OK;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return DA_ERR_INVALID;
@@ -103,15 +126,15 @@ int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, v
   float *acc = reinterpret_cast<float *>(ws + L.acc_off);
   if (dtype == DA_BF16 && eps < 1e-18f) return DA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(status, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
-  const float c2 = logit_scale_log2(tau, d);
+  const HeadScale hs = head_scale(tau, tau_bh, d);
   if (dtype == DA_F32) {
     if (launch_fwd_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse2_out, rowsum_out,
-                       demand_out, (int)BH, T, c2, eps, lse2_ws, acc, stream, ev) != cudaSuccess)
+                       demand_out, (int)BH, T, hs, eps, earlier, lse2_ws, acc, status, stream, ev) != cudaSuccess)
       return DA_ERR_CUDA;
     return DA_OK;
   }
-  return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, c2, eps, lse2_ws, acc, status,
-                         stream, ev);
+  return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, hs, eps, earlier, lse2_ws, acc,
+                         status, stream, ev);
 }
 
 size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
@@ -124,7 +147,15 @@ size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
 int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
                       void *dk, void *dv, int B, int H, int T, int d, float tau, float eps, int dtype,
                       void *workspace, size_t workspace_bytes, void *stream_) {
+  return dilution_attn_bwd_ex(q, k, v, dout, lse2, dq, dk, dv, B, H, T, d, tau, nullptr, eps, 0, dtype, workspace,
+                              workspace_bytes, stream_);
+}
+
+int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void *dout, const float *lse2,
+                         void *dq, void *dk, void *dv, int B, int H, int T, int d, float tau, const float *tau_bh,
+                         float eps, int flags, int dtype, void *workspace, size_t workspace_bytes, void *stream_) {
   int st = check_common(B, H, T, d, tau, eps, dtype);
+  if (st == DA_OK) st = check_options(tau_bh, flags);
   if (st != DA_OK) return st;
   const int64_t BH = (int64_t)B * H;
   if (BH == 0 || T == 0) return DA_OK;
@@ -138,7 +169,8 @@ int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *d
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   const float c = (float)((double)tau / std::sqrt((double)d));
-  if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, c, logit_scale_log2(tau, d), eps, dtype,
+  if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, c, head_scale(tau, tau_bh, d), eps,
+                 (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, dtype,
                  reinterpret_cast<double *>(ws + L.dtot_off), reinterpret_cast<float *>(ws + L.row_off),
                  reinterpret_cast<float *>(ws + L.dq_off), stream) != cudaSuccess)
     return DA_ERR_CUDA;
@@ -155,7 +187,16 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
                               void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
                               float tau, float eps, int dtype, void *workspace, size_t workspace_bytes,
                               void *stream_) {
+  return dilution_attn_decode_step_ex(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d, tau,
+                                      nullptr, eps, 0, dtype, workspace, workspace_bytes, stream_);
+}
+
+int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
+                                 void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
+                                 float tau, const float *tau_bh, float eps, int flags, int dtype, void *workspace,
+                                 size_t workspace_bytes, void *stream_) {
   int st = check_common(B, H, T_cap, d, tau, eps, dtype);
+  if (st == DA_OK) st = check_options(tau_bh, flags);
   if (st != DA_OK) return st;
   if (n_ctx < 0 || n_ctx >= T_cap) return DA_ERR_INVALID;
   const int64_t BH = (int64_t)B * H;
@@ -170,8 +211,9 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   if (launch_decode(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, (int)BH,
-                    logit_scale_log2(tau, d), eps, dtype, reinterpret_cast<float *>(ws + L.logit_off),
-                    reinterpret_cast<float2 *>(ws + L.ml_off), reinterpret_cast<float *>(ws + L.acc_off), L.nchunk,
+                    head_scale(tau, tau_bh, d), eps, (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, dtype,
+                    reinterpret_cast<float *>(ws + L.logit_off), reinterpret_cast<float2 *>(ws + L.ml_off),
+                    reinterpret_cast<float *>(ws + L.acc_off), L.nchunk, reinterpret_cast<int *>(ws),
                     stream) != cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;

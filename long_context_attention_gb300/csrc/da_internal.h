@@ -138,6 +138,31 @@ DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
   return w;
 }
 
+// ---------------------------------------------------------------------------
+// Logit scale of one (batch, head) in the log2 domain, c2 = tau log2(e) /
+// sqrt(d).  tau_bh (device [BH], nullable) holds one multiplier per head;
+// without it every head uses the scalar's c2, formed on the host in double.
+// ---------------------------------------------------------------------------
+struct HeadScale {
+  const float *tau_bh;
+  float c2;        // scalar tau * log2(e) / sqrt(d)
+  float per_tau;   // log2(e) / sqrt(d)
+};
+
+#if defined(__CUDACC__)
+// A negative, NaN or infinite entry records DA_ERR_INVALID in the status word
+// (when given) and yields 0, i.e. uniform bids.
+__device__ __forceinline__ float head_c2(const HeadScale &hs, int bh, int *status) {
+  if (hs.tau_bh == nullptr) return hs.c2;
+  const float t = __ldg(hs.tau_bh + bh);
+  if (!(t >= 0.f && t <= 3.0e38f)) {
+    if (status != nullptr) atomicCAS(status, DA_OK, DA_ERR_INVALID);
+    return 0.f;
+  }
+  return t * hs.per_tau;
+}
+#endif
+
 // Causal mask predicate used by every kernel: query i sees key k iff k <= i
 // and i < T ("DilutionAttention v0.1.0 · results", section "The operator":
 // causal softmax, diagonal included).

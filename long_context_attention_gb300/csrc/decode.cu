@@ -9,7 +9,8 @@
 //                 to a logit scratch, plus one (max, sum 2^(x - max)) per chunk.
 //                 The chunk holding position n_ctx also appends k_new / v_new.
 //   dec_update  : lse2 from the chunk partials; p_k = 2^(x_k - lse2);
-//                 share_k = p_k / (D_k + p_k + eps) with D_{n_ctx} = 0;
+//                 share_k = p_k / (D_k + p_k + eps) with D_{n_ctx} = 0
+//                 (p_k / (D_k + eps) in the earlier-demand-only variant);
 //                 D_k += p_k in place; per-chunk sum_k share_k v_k and sum_k share_k.
 //   dec_combine : out = sum of chunk numerators / sum of chunk row sums
 //                 (fixed order: deterministic).
@@ -72,12 +73,13 @@ template <typename E>
 __global__ void __launch_bounds__(kDecThreads)
     dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
                E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
-               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, float c2) {
+               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, HeadScale hs, int *status) {
   constexpr int LPR = lanes_per_row<E>();          // lanes cooperating on one key
   constexpr int NV = Vec16<E>::N;
   constexpr int KPR = kDecThreads / LPR;           // keys per round
   const int bh = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x;
+  const float c2 = head_c2(hs, bh, (tid == 0 && chunk == 0) ? status : nullptr);
   const int sub = tid % LPR;                       // which 16-byte piece of the row
   const int grp = tid / LPR;
   const int n_keys = n_ctx + 1;
@@ -156,7 +158,7 @@ template <typename E>
 __global__ void __launch_bounds__(kDecThreads)
     dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
                float *__restrict__ demand, float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
-               int nchunk_used, float eps) {
+               int nchunk_used, float eps, bool earlier) {
   constexpr int LPR = lanes_per_row<E>();
   constexpr int NV = Vec16<E>::N;
   constexpr int KPR = kDecThreads / LPR;
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(kDecThreads)
       const int key = k0 + u * KPR;
       if (key >= k_end) continue;
       const float p = exp2f(x[u] - lse2);
-      const float den = dm[u] + p + eps;
+      const float den = (earlier ? dm[u] : dm[u] + p) + eps;
       const float share = p / den;
       if (sub == 0) demand[(size_t)bh * T_cap + key] = dm[u] + p;
       float vf[NV];
@@ -255,27 +257,28 @@ __global__ void dec_combine(const float *__restrict__ part_acc, E *__restrict__ 
 
 template <typename E>
 static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
-                                   void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int BH, float c2,
-                                   float eps, float *logits, float2 *part_ml, float *part_acc, int nchunk,
-                                   cudaStream_t stream) {
+                                   void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int BH,
+                                   HeadScale hs, float eps, bool earlier, float *logits, float2 *part_ml,
+                                   float *part_acc, int nchunk, int *status, cudaStream_t stream) {
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
   dec_logits<E><<<dim3(used, BH), kDecThreads, 0, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
-      T_cap, nchunk, c2);
+      T_cap, nchunk, hs, status);
   dec_update<E><<<dim3(used, BH), kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc,
-                                                           n_ctx, T_cap, nchunk, used, eps);
+                                                           n_ctx, T_cap, nchunk, used, eps, earlier);
   dec_combine<E><<<BH, kD, 0, stream>>>(part_acc, (E *)out, nchunk, used);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
-                          float *demand, int n_ctx, int T_cap, void *out, int BH, float c2, float eps, int dtype,
-                          float *logits, float2 *part_ml, float *part_acc, int nchunk, cudaStream_t stream) {
+                          float *demand, int n_ctx, int T_cap, void *out, int BH, HeadScale hs, float eps,
+                          bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
+                          int *status, cudaStream_t stream) {
   if (dtype == DA_BF16)
-    return launch_decode_t<__nv_bfloat16>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, c2,
-                                          eps, logits, part_ml, part_acc, nchunk, stream);
-  return launch_decode_t<float>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, c2, eps,
-                                logits, part_ml, part_acc, nchunk, stream);
+    return launch_decode_t<__nv_bfloat16>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, hs,
+                                          eps, earlier, logits, part_ml, part_acc, nchunk, status, stream);
+  return launch_decode_t<float>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, hs, eps,
+                                earlier, logits, part_ml, part_acc, nchunk, status, stream);
 }
 
 // ---------------------------------------------------------------------------

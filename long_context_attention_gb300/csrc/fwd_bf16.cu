@@ -138,12 +138,14 @@ struct RowStat {
 
 // Demand step for 32 consecutive queries (columns 32 C ..) of one key row:
 //   p = 2^x,  den = (committed + eps) + p,  share = p / den,
-//   committed + eps <- den   (queries in causal order: the exclusive cumsum),
+//   committed + eps <- (committed + eps) + p
+// (queries in causal order: the exclusive cumsum).  EARLIER (the
+// earlier-demand-only variant) takes den = committed + eps instead.
 // with x = c2 S' and S' = q.k - lse2 / c2 from the S product (its fifth K
 // step adds the -lse2 / c2 term).  MASK zeroes the bids of queries before
 // the key: key row `row` is after query column c when row_eff > c,
 // row_eff = row - (first query - first key).
-template <bool MASK, int C>
+template <bool MASK, int C, bool EARLIER>
 __device__ __forceinline__ void demand_chunk(const float (&s)[32], int row_eff, float c2, float &ceps,
                                              uint32_t (&pk)[16]) {
   constexpr int col0 = 32 * C;
@@ -166,12 +168,18 @@ __device__ __forceinline__ void demand_chunk(const float (&s)[32], int row_eff, 
   float d[32];
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    d[c] = ceps + p[c];
-    ceps = d[c];
+    if (EARLIER) {
+      d[c] = ceps;
+      ceps += p[c];
+    } else {
+      d[c] = ceps + p[c];
+      ceps = d[c];
+    }
   }
   // One reciprocal per pair of consecutive queries: r = 1 / (d0 d1),
   // share0 = p0 d1 r, share1 = p1 d0 r.  d0, d1 lie in [eps, T + 1], so
-  // d0 d1 stays a normal float for eps >= 1e-18.  (Measured on GB300: the
+  // d0 d1 stays a normal float for eps >= 1e-18 (and the shares, at most
+  // 1 / eps, stay finite).  (Measured on GB300: the
   // MUFU reciprocal of the pair product beats a Newton iteration on the FMA
   // pipe, whose extra instructions cost more issue slots than they save.)
 #pragma unroll
@@ -183,6 +191,13 @@ __device__ __forceinline__ void demand_chunk(const float (&s)[32], int row_eff, 
   }
 }
 
+// Logit scale of head bh for both kernels.  Masked logits enter as -inf; a
+// zero scale (tau = 0) would turn them into NaN, so the scale is at least
+// 1e-30, which keeps every finite logit at 0 (uniform bids) and -inf at -inf.
+__device__ __forceinline__ float bf16_c2(const HeadScale &hs, int bh, int *status) {
+  return fmaxf(head_c2(hs, bh, status), 1e-30f);
+}
+
 // ============================================================================
 // Row statistics
 // ============================================================================
@@ -192,7 +207,7 @@ constexpr int kRsSmemBytes = (2 + kRsKStages) * kTileBytes + 256 + 1024;
 
 __global__ void __launch_bounds__(kRsThreads, 2)
     rowstats_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    float *__restrict__ nlse2, float *__restrict__ acc, int BH, int T, int Tp, float c2,
+                    float *__restrict__ nlse2, float *__restrict__ acc, int BH, int T, int Tp, HeadScale hs,
                     int *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -211,6 +226,7 @@ __global__ void __launch_bounds__(kRsThreads, 2)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const TileWork w = rowstats_work(blockIdx.x, BH, T);
   const int n_kt = w.q_tile0 + 2;   // key tiles 0 .. last query tile
+  const float c2 = bf16_c2(hs, w.bh, status);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -406,12 +422,13 @@ __device__ __forceinline__ void regs_inc_demand() { asm volatile("setmaxnreg.inc
 __device__ __forceinline__ void regs_dec_epi() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsEpi)); }
 __device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsCtl)); }
 
+template <bool EARLIER>
 __global__ void __launch_bounds__(kSwThreads, 1)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmAcc,
                  const uint4 *__restrict__ kglob, const float *__restrict__ nlse2, float *__restrict__ acc,
                  float *__restrict__ demand_out, int BH,
-                 int T, int Tp, float c2, float eps, int *status) {
+                 int T, int Tp, HeadScale hs, float eps, int *status) {
   extern __shared__ __align__(1024) uint8_t sw_smem_raw[];
   // The layout has no slack for re-alignment: every tile, swizzle atom and
   // reduction box assumes a 1024-byte aligned base.  Refuse (uniformly,
@@ -448,6 +465,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const int kWarpProd = (kSwG + 1) * 4, kWarpMma = kWarpProd + 1;
   const TileWork w = sweep_work(blockIdx.x, BH, T);
   const int nt = w.n_q_tiles;
+  const float c2 = bf16_c2(hs, w.bh, nullptr);   // the row statistics report bad entries
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -719,25 +737,25 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         tmem_ld32(tb, A);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 32, B);
-        if (need_mask) demand_chunk<true, 0>(A, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 0>(A, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 0, EARLIER>(A, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
         if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
         store(pk, 0);
         tmem_wait_ld_r(B);
         tmem_ld32(tb + 64, A);
-        if (need_mask) demand_chunk<true, 1>(B, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 1>(B, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 1, EARLIER>(B, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 1);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 96, B);
-        if (need_mask) demand_chunk<true, 2>(A, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 2>(A, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 2, EARLIER>(A, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         store(pk, 2);
         tmem_wait_ld_r(B);
         release_tmem(&s_free[g], lane);
-        if (need_mask) demand_chunk<true, 3>(B, row_eff, c2, ceps, pk);
-        else demand_chunk<false, 3>(B, row_eff, c2, ceps, pk);
+        if (need_mask) demand_chunk<true, 3, EARLIER>(B, row_eff, c2, ceps, pk);
+        else demand_chunk<false, 3, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 3);
       }
       fence_proxy_async_smem();
@@ -811,9 +829,25 @@ static bool make_acc_map(CUtensorMap *m, float *acc, int64_t rows) {
 cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bfloat16 *out, float *rowsum_out,
                                  float *lse2_out, int BH, int T, cudaStream_t stream);
 
+// Shared-memory opt-in and register-split check of one sweep instantiation.
+template <bool EARLIER>
+static int prepare_sweep() {
+  if (cudaFuncSetAttribute(sweep_kernel<EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes) !=
+      cudaSuccess)
+    return DA_ERR_CUDA;
+  // The sweep's warpgroups re-split the block's registers (setmaxnreg); a
+  // split larger than what the block is launched with would never resolve,
+  // so refuse to launch unless the compiled register count covers it.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, sweep_kernel<EARLIER>) != cudaSuccess) return DA_ERR_CUDA;
+  if (fa.numRegs * kSwThreads < kSwRegsNeeded || fa.numRegs > kSwRegsDemand || fa.numRegs < kSwRegsEpi)
+    return DA_ERR_UNSUPPORTED;
+  return DA_OK;
+}
+
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
-                    float *demand_out, int BH, int T, float c2, float eps, float *lse2_ws, float *acc, int *status,
-                    cudaStream_t stream, cudaEvent_t const *ev) {
+                    float *demand_out, int BH, int T, HeadScale hs, float eps, bool earlier, float *lse2_ws,
+                    float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev) {
   const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
   if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;   // TMA row coordinates are 32-bit
   CUtensorMap tq, tk, tv, ta;
@@ -826,29 +860,26 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
   if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
   if (dev >= 64 || !attr_done[dev]) {
     if (cudaFuncSetAttribute(rowstats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRsSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes) !=
-            cudaSuccess)
+        cudaSuccess)
       return DA_ERR_CUDA;
-    // The sweep's warpgroups re-split the block's registers (setmaxnreg); a
-    // split larger than what the block is launched with would never resolve,
-    // so refuse to launch unless the compiled register count covers it.
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, sweep_kernel) != cudaSuccess) return DA_ERR_CUDA;
-    if (fa.numRegs * kSwThreads < kSwRegsNeeded || fa.numRegs > kSwRegsDemand || fa.numRegs < kSwRegsEpi)
-      return DA_ERR_UNSUPPORTED;
+    int st = prepare_sweep<false>();
+    if (st == DA_OK) st = prepare_sweep<true>();
+    if (st != DA_OK) return st;
     if (dev < 64) attr_done[dev] = true;
   }
   const int Tp = (int)t_pad(T);
-  // Masked logits enter as -inf; with tau = 0 a zero scale would turn them
-  // into NaN.  1e-30 keeps every finite logit at 0 (uniform bids) and -inf at -inf.
-  if (c2 < 1e-30f) c2 = 1e-30f;
   if (ev[0]) cudaEventRecord(ev[0], stream);
   rowstats_kernel<<<rowstats_num_ctas(BH, T), kRsThreads, kRsSmemBytes, stream>>>(tq, tk, lse2_ws, acc, BH, T,
-                                                                                  Tp, c2, status);
+                                                                                  Tp, hs, status);
   if (ev[1]) cudaEventRecord(ev[1], stream);
-  sweep_kernel<<<sweep_num_ctas(BH, T), kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, static_cast<const uint4 *>(k), lse2_ws, acc, demand_out,
-                                                                            BH, T, Tp, c2, eps, status);
+  const int nsw = sweep_num_ctas(BH, T);
+  const uint4 *kg = static_cast<const uint4 *>(k);
+  if (earlier)
+    sweep_kernel<true><<<nsw, kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out, BH,
+                                                                  T, Tp, hs, eps, status);
+  else
+    sweep_kernel<false><<<nsw, kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
+                                                                   BH, T, Tp, hs, eps, status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
   if (ev[2]) cudaEventRecord(ev[2], stream);
   if (launch_finalize_bf16(acc, lse2_ws, reinterpret_cast<__nv_bfloat16 *>(out), rowsum_out, lse2_out, BH, T,

@@ -9,7 +9,8 @@
 //      queries in causal order, each thread keeps its key's demand from
 //      earlier queries (the exclusive column cumsum) in a register:
 //      p = 2^(x - lse2), share = p / (committed + p + eps), committed += p
-//      (Kahan-compensated).
+//      (Kahan-compensated); the earlier-demand-only variant divides by
+//      committed + eps.
 //      The shares of 32 queries are staged in shared memory and multiplied
 //      by the CTA's 128 value rows; the partial numerators and share row
 //      sums are added (fp32 atomics) into the accumulator acc[row][0..64].
@@ -27,9 +28,10 @@ constexpr int kF32QChunk = 32;
 
 __global__ void __launch_bounds__(kF32RowsPerCta)
     f32_rowstats(const float *__restrict__ q, const float *__restrict__ k, float *__restrict__ lse2,
-                 float *__restrict__ acc, int T, int Tp, float c2) {
+                 float *__restrict__ acc, int T, int Tp, HeadScale hs, int *status) {
   __shared__ float sk[kF32RowsPerCta][kD];
   const int bh = blockIdx.y;
+  const float c2 = head_c2(hs, bh, threadIdx.x == 0 ? status : nullptr);
   const int tid = threadIdx.x;
   const int i = blockIdx.x * kF32RowsPerCta + tid;
   const float *qb = q + (size_t)bh * T * kD;
@@ -87,10 +89,11 @@ struct F32SweepSmem {
 __global__ void __launch_bounds__(kF32KeysPerCta)
     f32_sweep(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
               const float *__restrict__ lse2, float *__restrict__ acc, float *__restrict__ demand_out, int T,
-              int Tp, float c2, float eps) {
+              int Tp, HeadScale hs, float eps, bool earlier) {
   extern __shared__ float4 f32_smem_raw[];
   F32SweepSmem &S = *reinterpret_cast<F32SweepSmem *>(f32_smem_raw);
   const int bh = blockIdx.y;
+  const float c2 = head_c2(hs, bh, nullptr);   // the row statistics report bad entries
   const int tid = threadIdx.x;
   const int key0 = blockIdx.x * kF32KeysPerCta;
   const int key = key0 + tid;
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kF32KeysPerCta)
 #pragma unroll
         for (int t = 0; t < kD; ++t) s = fmaf(S.q[r][t], kr[t], s);
         const float p = exp2f(fmaf(s, c2, -S.m2[r]) - S.ll[r]);
-        share = p / ((committed + p) + eps);
+        share = p / ((earlier ? committed : committed + p) + eps);
         const float y = p - comp;
         const float t2 = committed + y;
         comp = (t2 - committed) - y;
@@ -216,17 +219,18 @@ static unsigned finalize_blocks(int64_t nrows) {
 
 // ------------------------------------------------------------ host launchers
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
-                           float *rowsum_out, float *demand_out, int BH, int T, float c2, float eps,
-                           float *lse2_ws, float *acc, cudaStream_t stream, cudaEvent_t const *ev) {
+                           float *rowsum_out, float *demand_out, int BH, int T, HeadScale hs, float eps,
+                           bool earlier, float *lse2_ws, float *acc, int *status, cudaStream_t stream,
+                           cudaEvent_t const *ev) {
   const int Tp = (int)t_pad(T);
   if (ev[0]) cudaEventRecord(ev[0], stream);
-  f32_rowstats<<<dim3(Tp / kF32RowsPerCta, BH), kF32RowsPerCta, 0, stream>>>(q, k, lse2_ws, acc, T, Tp, c2);
+  f32_rowstats<<<dim3(Tp / kF32RowsPerCta, BH), kF32RowsPerCta, 0, stream>>>(q, k, lse2_ws, acc, T, Tp, hs, status);
   const size_t smem = sizeof(F32SweepSmem);
   cudaError_t e = cudaFuncSetAttribute(f32_sweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (ev[1]) cudaEventRecord(ev[1], stream);
   f32_sweep<<<dim3(Tp / kF32KeysPerCta, BH), kF32KeysPerCta, smem, stream>>>(q, k, v, lse2_ws, acc, demand_out,
-                                                                            T, Tp, c2, eps);
+                                                                            T, Tp, hs, eps, earlier);
   if (ev[2]) cudaEventRecord(ev[2], stream);
   finalize_kernel<float><<<finalize_blocks((int64_t)BH * T), 256, 0, stream>>>(acc, lse2_ws, out, rowsum_out,
                                                                                lse2_out, BH, T, Tp, true);

@@ -31,7 +31,8 @@ What it computes, and where each step comes from:
   page, in the paragraph after "The operator", describes dividing each bid
   by the earlier demand alone, which lets every key win its own first query
   (the key itself) outright.  Reading taken: share = p / (committed + eps);
-  eps keeps the diagonal entry defined.  Forward and cached decode only.
+  eps keeps the diagonal entry defined.  The page trained a model this way,
+  so the backward takes the flag too.
 
 * ``tau`` may be a scalar or an array broadcastable to [B, H] in the batched
   functions: one logit multiplier per (batch, head), the per-head
@@ -278,7 +279,7 @@ def _reverse_exclusive_cumsum_cols(x: np.ndarray) -> np.ndarray:
     return out
 
 
-def dilution_backward_head(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6):
+def dilution_backward_head(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6, earlier_only: bool = False):
     """Gradients (dq, dk, dv) of sum(dout * out) for one head.
 
     With c = tau/sqrt(d), r = share, R = rowsum(share), D = committed + p + eps:
@@ -288,6 +289,8 @@ def dilution_backward_head(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6):
       dp_jk  = dr_jk (committed_jk + eps) / D_jk^2 + sum_{i > j} dC_ik
       ds_jk  = p_jk (dp_jk - sum_k' p_jk' dp_jk')                (softmax)
       dq     = c ds k,   dk = c ds^T q
+    With ``earlier_only`` (share = p / (committed + eps)) D = committed + eps
+    and the direct term of dp is dr_jk / D_jk instead.
     """
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
@@ -295,23 +298,24 @@ def dilution_backward_head(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6):
     g = np.asarray(dout, np.float64)
     T, d = q.shape
     c = logit_scale(d, tau)
-    f = dilution_forward_head(q, k, v, tau, eps, full=True)
+    f = dilution_forward_head(q, k, v, tau, eps, full=True, earlier_only=earlier_only)
     p, C, A, out, R = f["p"], f["committed"], f["A"], f["out"], f["rowsum"]
     mask = np.tril(np.ones((T, T), dtype=bool))
-    Dn = C + p + eps
+    Dn = C + eps if earlier_only else C + p + eps
     dv = A.T @ g
     dA = g @ v.T
     delta = np.sum(g * out, axis=1)
     dr = np.where(mask, (dA - delta[:, None]) / R[:, None], 0.0)
     dC = -dr * p / Dn**2
-    dp = dr * (C + eps) / Dn**2 + _reverse_exclusive_cumsum_cols(dC)
+    direct = dr / Dn if earlier_only else dr * (C + eps) / Dn**2
+    dp = direct + _reverse_exclusive_cumsum_cols(dC)
     ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
     dq = c * (ds @ k)
     dk = c * (ds.T @ q)
     return dq, dk, dv
 
 
-def dilution_backward(q, k, v, dout, tau=1.0, eps: float = 1e-6):
+def dilution_backward(q, k, v, dout, tau=1.0, eps: float = 1e-6, earlier_only: bool = False):
     """Batched backward over [B,H,T,d]; ``tau`` scalar or broadcastable to
     [B, H]; returns (dq, dk, dv)."""
     q = np.asarray(q, np.float64)
@@ -323,5 +327,5 @@ def dilution_backward(q, k, v, dout, tau=1.0, eps: float = 1e-6):
     for b in range(B):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h] = dilution_backward_head(q[b, h], k[b, h], v[b, h], dout[b, h],
-                                                                  float(taus[b, h]), eps)
+                                                                  float(taus[b, h]), eps, earlier_only)
     return dq, dk, dv

@@ -153,3 +153,31 @@ def test_bwd_argument_validation(lib):
     assert bwd(q=None) == b.DA_ERR_INVALID
     assert bwd(ws=None) == b.DA_ERR_WORKSPACE
     assert b.dilution_attn_bwd_workspace_size(4, 12, 16384, 64, 1) > 4 * 12 * 16384 * 64 * 4
+
+
+def test_ex_option_validation(lib):
+    # flags other than DA_FLAG_EARLIER_DEMAND_ONLY and a tau_bh that is not
+    # 4-byte aligned are argument errors; valid options pass on to the
+    # workspace check (the first check that would need a real buffer)
+    MIS2 = ctypes.c_void_p(0x10002)
+    EARLY = b.DA_FLAG_EARLIER_DEMAND_ONLY
+
+    def fwd(tau_bh=None, flags=0, ws=None):
+        return lib.dilution_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, None, None, 1, 2, 8, 64, 1.0, tau_bh, 1e-6,
+                                        flags, 1, ws, 1 << 30, None, None)
+
+    def bwd(tau_bh=None, flags=0):
+        return lib.dilution_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 8, 64, 1.0, tau_bh,
+                                        1e-6, flags, 1, None, 1 << 30, None)
+
+    def dec(tau_bh=None, flags=0):
+        return lib.dilution_attn_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 16, FAKE, 1, 2, 64, 1.0,
+                                                tau_bh, 1e-6, flags, 1, None, 1 << 30, None)
+
+    for call in (fwd, bwd, dec):
+        assert call(flags=2) == b.DA_ERR_INVALID
+        assert call(flags=-1) == b.DA_ERR_INVALID
+        assert call(tau_bh=MIS2) == b.DA_ERR_INVALID
+        assert call(flags=EARLY) == b.DA_ERR_WORKSPACE
+        assert call(tau_bh=MIS, flags=EARLY) == b.DA_ERR_WORKSPACE   # 4-byte aligned is enough
+    assert fwd(flags=EARLY, ws=MIS) == b.DA_ERR_INVALID              # workspace must be 256-byte aligned

@@ -202,14 +202,14 @@ def pin_lse(T=17, d=8, seed=12, tau=0.7):
     return np.abs(r["lse"] - ref).max()
 
 
-def pin_backward_fd(T=16, d=6, seed=13, tau=0.9, eps=1e-3, h=1e-6):
+def pin_backward_fd(T=16, d=6, seed=13, tau=0.9, eps=1e-3, h=1e-6, earlier_only=False):
     """Central finite differences of L = sum(dout * out) in float64."""
     q, k, v = _rand(T, d, seed, dv=5)
     g = np.random.default_rng(seed + 1).standard_normal((T, 5))
-    dq, dk, dv = od.dilution_backward_head(q, k, v, g, tau, eps)
+    dq, dk, dv = od.dilution_backward_head(q, k, v, g, tau, eps, earlier_only=earlier_only)
 
     def L(qq, kk, vv):
-        return float(np.sum(g * od.dilution_forward_head(qq, kk, vv, tau, eps)["out"]))
+        return float(np.sum(g * od.dilution_forward_head(qq, kk, vv, tau, eps, earlier_only=earlier_only)["out"]))
 
     worst = 0.0
     for X, dX, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
@@ -391,6 +391,12 @@ def test_tau_per_batch_head_indexing():
 
 def test_backward_finite_differences():
     assert pin_backward_fd() < 1e-7
+
+
+def test_backward_finite_differences_earlier_only():
+    # eps = 0.05 keeps the diagonal share (p / eps) from swamping the row, so
+    # the off-diagonal terms of the gradient are exercised too
+    assert pin_backward_fd(seed=21, eps=0.05, earlier_only=True) < 1e-7
 
 
 def test_backward_autograd():
