@@ -35,10 +35,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned16_or_null(const void *p) { return p == nullptr || aligned16(p); }
 
 // Scale applied to q.k in the log2 domain: tau / sqrt(d) * log2(e).
-float logit_scale_log2(float tau, int d) { return (float)((double)tau / std::sqrt((double)d) * kLog2e); }
+double log2e_over_sqrt_d(int d) { return kLog2e / std::sqrt((double)d); }
+float logit_scale_log2(float tau, int d) { return (float)((double)tau * log2e_over_sqrt_d(d)); }
 
 HeadScale head_scale(float tau, const float *tau_bh, int d) {
-  return HeadScale{tau_bh, logit_scale_log2(tau, d), logit_scale_log2(1.f, d)};
+  return HeadScale{tau_bh, logit_scale_log2(tau, d), log2e_over_sqrt_d(d)};
 }
 
 // Options of the *_ex entry points.

@@ -141,12 +141,13 @@ DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
 // ---------------------------------------------------------------------------
 // Logit scale of one (batch, head) in the log2 domain, c2 = tau log2(e) /
 // sqrt(d).  tau_bh (device [BH], nullable) holds one multiplier per head;
-// without it every head uses the scalar's c2, formed on the host in double.
+// without it every head uses the scalar's c2.  Both are formed in double and
+// rounded once, so equal multipliers give bit-identical scales.
 // ---------------------------------------------------------------------------
 struct HeadScale {
   const float *tau_bh;
   float c2;        // scalar tau * log2(e) / sqrt(d)
-  float per_tau;   // log2(e) / sqrt(d)
+  double per_tau;  // log2(e) / sqrt(d)
 };
 
 #if defined(__CUDACC__)
@@ -159,7 +160,7 @@ __device__ __forceinline__ float head_c2(const HeadScale &hs, int bh, int *statu
     if (status != nullptr) atomicCAS(status, DA_OK, DA_ERR_INVALID);
     return 0.f;
   }
-  return t * hs.per_tau;
+  return (float)((double)t * hs.per_tau);   // rounded once, as the scalar's c2
 }
 #endif
 
