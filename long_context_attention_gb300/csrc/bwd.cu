@@ -29,7 +29,8 @@
 //          staging of ds, fp32 atomics across key blocks).
 //   bwd_final: dq accumulator -> dq in the output type.
 // This is the straightforward SIMT version (fp32 arithmetic for fp32 and
-// bf16 inputs); the tensor-core version is future work.
+// bf16 inputs), instantiated for d = 64 and d = 128; the tensor-core version
+// is future work.
 #include "da_internal.h"
 
 #include <cuda_bf16.h>
@@ -50,20 +51,21 @@ __device__ __forceinline__ void st_e(E *p, float x) {
   else *p = __float2bfloat16_rn(x);
 }
 
+template <int D>
 struct BwdSmem {
-  float kT[kD][kBwKeys];      // this block's keys, transposed (conflict-free column reads)
-  float vT[kD][kBwKeys];      // and values
-  float q[kBwQ][kD];          // query chunk
-  float g[kBwQ][kD];          // dout chunk
+  float kT[D][kBwKeys];       // this block's keys, transposed (conflict-free column reads)
+  float vT[D][kBwKeys];       // and values
+  float q[kBwQ][D];           // query chunk
+  float g[kBwQ][D];           // dout chunk
   float lse2[kBwQ], rinv[kBwQ], delta[kBwQ], rho[kBwQ];
   float ds[kBwQ][kBwKeys + 1];
   float red[kBwQ][4];         // per-warp partial sums of rho
 };
 
-__global__ void bwd_zero(float *__restrict__ rowbuf, float *__restrict__ dq_acc, int64_t rows) {
+__global__ void bwd_zero(float *__restrict__ rowbuf, float *__restrict__ dq_acc, int64_t rows, int d) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < rows * 4) rowbuf[i] = 0.f;          // R, Y, rho, (spare)
-  if (i < rows * kD) dq_acc[i] = 0.f;
+  if (i < rows * d) dq_acc[i] = 0.f;
 }
 
 // Reverse-walk step for one key at query j: with srev = sum_{i > j} p_ik
@@ -89,14 +91,14 @@ __device__ __forceinline__ float col_step(ColState &cs, float p, float dA, float
   return dp;
 }
 
-template <typename E, int PASS>
+template <typename E, int D, int PASS>
 __global__ void __launch_bounds__(kBwKeys)
     bwd_pass(const E *__restrict__ q, const E *__restrict__ k, const E *__restrict__ v, const E *__restrict__ g,
              const float *__restrict__ lse2, double *__restrict__ dtot, float *__restrict__ Rsum,
              float *__restrict__ Ysum, float *__restrict__ rho, float *__restrict__ dq_acc, E *__restrict__ dk_out,
              E *__restrict__ dv_out, int T, float c_scalar, HeadScale hs, float eps, bool earlier) {
   extern __shared__ float4 bw_smem_raw[];
-  BwdSmem &S = *reinterpret_cast<BwdSmem *>(bw_smem_raw);
+  BwdSmem<D> &S = *reinterpret_cast<BwdSmem<D> *>(bw_smem_raw);
   const int bh = blockIdx.y;
   // natural-log scale c = tau / sqrt(d) of this head (c2 = c log2(e))
   const float c2 = head_c2(hs, bh, nullptr);
@@ -105,27 +107,27 @@ __global__ void __launch_bounds__(kBwKeys)
   const int key0 = blockIdx.x * kBwKeys;
   const int key = key0 + tid;
   const size_t base = (size_t)bh * T;
-  for (int e = tid; e < kBwKeys * kD; e += kBwKeys) {
-    const int kk = e / kD, t = e % kD;
+  for (int e = tid; e < kBwKeys * D; e += kBwKeys) {
+    const int kk = e / D, t = e % D;
     const bool ok = key0 + kk < T;
-    S.kT[t][kk] = ok ? ld_e(k + (base + key0 + kk) * kD + t) : 0.f;
-    S.vT[t][kk] = ok ? ld_e(v + (base + key0 + kk) * kD + t) : 0.f;
+    S.kT[t][kk] = ok ? ld_e(k + (base + key0 + kk) * D + t) : 0.f;
+    S.vT[t][kk] = ok ? ld_e(v + (base + key0 + kk) * D + t) : 0.f;
   }
   double csum = 0.0;   // pass 0: committed (sum of earlier bids) of this key
   ColState cs{(PASS > 0 && key < T) ? dtot[base + key] : 0.0, 0.0, 0.f};
-  float accv[kD];      // dV_k (pass 1) or dK_k / c (pass 2)
+  float accv[D];      // dV_k (pass 1) or dK_k / c (pass 2)
 #pragma unroll
-  for (int t = 0; t < kD; ++t) accv[t] = 0.f;
+  for (int t = 0; t < D; ++t) accv[t] = 0.f;
   const int nchunks = (T - key0 + kBwQ - 1) / kBwQ;
   for (int cc = 0; cc < nchunks; ++cc) {
     const int ci = (PASS == 0) ? cc : nchunks - 1 - cc;   // pass 0 ascends, passes 1-2 descend
     const int q0 = key0 + ci * kBwQ;
     __syncthreads();
-    for (int e = tid; e < kBwQ * kD; e += kBwKeys) {
-      const int r = e / kD, t = e % kD;
+    for (int e = tid; e < kBwQ * D; e += kBwKeys) {
+      const int r = e / D, t = e % D;
       const bool ok = q0 + r < T;
-      S.q[r][t] = ok ? ld_e(q + (base + q0 + r) * kD + t) : 0.f;
-      S.g[r][t] = ok ? ld_e(g + (base + q0 + r) * kD + t) : 0.f;
+      S.q[r][t] = ok ? ld_e(q + (base + q0 + r) * D + t) : 0.f;
+      S.g[r][t] = ok ? ld_e(g + (base + q0 + r) * D + t) : 0.f;
     }
     if (tid < kBwQ) {
       const bool ok = q0 + tid < T;
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kBwKeys)
       if (key < T && key <= j && j < T) {
         float sdot = 0.f, dA = 0.f;
 #pragma unroll 16
-        for (int t = 0; t < kD; ++t) {
+        for (int t = 0; t < D; ++t) {
           sdot = fmaf(S.q[r][t], S.kT[t][tid], sdot);
           dA = fmaf(S.g[r][t], S.vT[t][tid], dA);
         }
@@ -161,12 +163,12 @@ __global__ void __launch_bounds__(kBwKeys)
           if (PASS == 1) {
             c0 = p * dp;
 #pragma unroll
-            for (int t = 0; t < kD; ++t) accv[t] = fmaf(a, S.g[r][t], accv[t]);
+            for (int t = 0; t < D; ++t) accv[t] = fmaf(a, S.g[r][t], accv[t]);
           } else {
             const float ds = p * (dp - S.rho[r]);
             c0 = ds;
 #pragma unroll
-            for (int t = 0; t < kD; ++t) accv[t] = fmaf(ds, S.q[r][t], accv[t]);
+            for (int t = 0; t < D; ++t) accv[t] = fmaf(ds, S.q[r][t], accv[t]);
           }
         }
       }
@@ -197,14 +199,16 @@ __global__ void __launch_bounds__(kBwKeys)
         }
       }
     } else {
-      // dQ_j += c sum_k ds_jk k_k over this block's keys: thread (half, dim).
-      const int dim = tid % kD, half = tid / kD;
-      for (int rq = 0; rq < kBwQ / 2; ++rq) {
-        const int r = half * (kBwQ / 2) + rq;
+      // dQ_j += c sum_k ds_jk k_k over this block's keys: thread (group, dim),
+      // RG = 128 / d row groups of 32 / RG queries.
+      constexpr int RG = kBwKeys / D;
+      const int dim = tid % D, half = tid / D;
+      for (int rq = 0; rq < kBwQ / RG; ++rq) {
+        const int r = half * (kBwQ / RG) + rq;
         if (q0 + r >= T) break;
         float a = 0.f;
         for (int kk = 0; kk < kBwKeys; ++kk) a = fmaf(S.ds[r][kk], S.kT[dim][kk], a);
-        atomicAdd(dq_acc + (base + q0 + r) * kD + dim, c * a);
+        atomicAdd(dq_acc + (base + q0 + r) * D + dim, c * a);
       }
     }
   }
@@ -213,10 +217,10 @@ __global__ void __launch_bounds__(kBwKeys)
       dtot[base + key] = csum;
     } else if (PASS == 1) {
 #pragma unroll
-      for (int t = 0; t < kD; ++t) st_e(dv_out + (base + key) * kD + t, accv[t]);
+      for (int t = 0; t < D; ++t) st_e(dv_out + (base + key) * D + t, accv[t]);
     } else {
 #pragma unroll
-      for (int t = 0; t < kD; ++t) st_e(dk_out + (base + key) * kD + t, c * accv[t]);
+      for (int t = 0; t < D; ++t) st_e(dk_out + (base + key) * D + t, c * accv[t]);
     }
   }
 }
@@ -227,39 +231,42 @@ __global__ void bwd_final(const float *__restrict__ dq_acc, E *__restrict__ dq, 
   if (i < n) st_e(dq + i, dq_acc[i]);
 }
 
-template <typename E>
+template <typename E, int D>
 static cudaError_t launch_bwd_t(const void *q, const void *k, const void *v, const void *dout, const float *lse2,
                                 void *dq, void *dk, void *dv, int BH, int T, float c, HeadScale hs, float eps,
                                 bool earlier, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream) {
   const int64_t rows = (int64_t)BH * T;
   float *Rsum = rowbuf, *Ysum = rowbuf + rows, *rho = rowbuf + 2 * rows;
-  const int64_t nz = rows * kD;
-  bwd_zero<<<(unsigned)((nz + 255) / 256), 256, 0, stream>>>(rowbuf, dq_acc, rows);
-  const size_t smem = sizeof(BwdSmem);
-  cudaError_t e = cudaSuccess;
-  e = cudaFuncSetAttribute(bwd_pass<E, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_pass<E, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_pass<E, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int64_t nz = rows * D;
+  bwd_zero<<<(unsigned)((nz + 255) / 256), 256, 0, stream>>>(rowbuf, dq_acc, rows, D);
+  const size_t smem = sizeof(BwdSmem<D>);
+  cudaError_t e = cudaFuncSetAttribute(bwd_pass<E, D, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_pass<E, D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_pass<E, D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((T + kBwKeys - 1) / kBwKeys, BH);
-  bwd_pass<E, 0><<<grid, kBwKeys, smem, stream>>>((const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2,
-                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, hs, eps, earlier);
-  bwd_pass<E, 1><<<grid, kBwKeys, smem, stream>>>((const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2,
-                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, hs, eps, earlier);
-  bwd_pass<E, 2><<<grid, kBwKeys, smem, stream>>>((const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2,
-                                                  dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, c, hs, eps, earlier);
+#define DA_BWD_ARGS                                                                                              \
+  (const E *)q, (const E *)k, (const E *)v, (const E *)dout, lse2, dtot, Rsum, Ysum, rho, dq_acc, (E *)dk, (E *)dv, T, \
+      c, hs, eps, earlier
+  bwd_pass<E, D, 0><<<grid, kBwKeys, smem, stream>>>(DA_BWD_ARGS);
+  bwd_pass<E, D, 1><<<grid, kBwKeys, smem, stream>>>(DA_BWD_ARGS);
+  bwd_pass<E, D, 2><<<grid, kBwKeys, smem, stream>>>(DA_BWD_ARGS);
+#undef DA_BWD_ARGS
   bwd_final<E><<<(unsigned)((nz + 255) / 256), 256, 0, stream>>>(dq_acc, (E *)dq, nz);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
-                       void *dk, void *dv, int BH, int T, float c, HeadScale hs, float eps, bool earlier, int dtype,
-                       double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream) {
+                       void *dk, void *dv, int BH, int T, int d, float c, HeadScale hs, float eps, bool earlier,
+                       int dtype, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream) {
+#define DA_BWD_LAUNCH_ARGS q, k, v, dout, lse2, dq, dk, dv, BH, T, c, hs, eps, earlier, dtot, rowbuf, dq_acc, stream
   if (dtype == DA_BF16)
-    return launch_bwd_t<__nv_bfloat16>(q, k, v, dout, lse2, dq, dk, dv, BH, T, c, hs, eps, earlier, dtot, rowbuf,
-                                       dq_acc, stream);
-  return launch_bwd_t<float>(q, k, v, dout, lse2, dq, dk, dv, BH, T, c, hs, eps, earlier, dtot, rowbuf, dq_acc,
-                             stream);
+    return d == 128 ? launch_bwd_t<__nv_bfloat16, 128>(DA_BWD_LAUNCH_ARGS)
+                    : launch_bwd_t<__nv_bfloat16, 64>(DA_BWD_LAUNCH_ARGS);
+  return d == 128 ? launch_bwd_t<float, 128>(DA_BWD_LAUNCH_ARGS) : launch_bwd_t<float, 64>(DA_BWD_LAUNCH_ARGS);
+#undef DA_BWD_LAUNCH_ARGS
 }
 
 }  // namespace da

@@ -10,17 +10,17 @@
 
 namespace da {
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *out, float *lse2_out,
-                           float *rowsum_out, float *demand_out, int BH, int T, HeadScale hs, float eps,
+                           float *rowsum_out, float *demand_out, int BH, int T, int d, HeadScale hs, float eps,
                            bool earlier, float *lse2_ws, float *acc, int *status, cudaStream_t stream,
                            cudaEvent_t const *ev);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
-                    float *demand_out, int BH, int T, HeadScale hs, float eps, bool earlier, float *lse2_ws,
+                    float *demand_out, int BH, int T, int d, HeadScale hs, float eps, bool earlier, float *lse2_ws,
                     float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev);
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
-                       void *dk, void *dv, int BH, int T, float c, HeadScale hs, float eps, bool earlier, int dtype,
-                       double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream);
+                       void *dk, void *dv, int BH, int T, int d, float c, HeadScale hs, float eps, bool earlier,
+                       int dtype, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
-                          float *demand, int n_ctx, int T_cap, void *out, int BH, HeadScale hs, float eps,
+                          float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
                           bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
                           int *status, cudaStream_t stream);
 }  // namespace da
@@ -54,7 +54,7 @@ int check_common(int B, int H, int T, int d, float tau, float eps, int dtype) {
   if (!std::isfinite(tau) || tau < 0.f) return DA_ERR_INVALID;
   if (!std::isfinite(eps) || eps <= 0.f) return DA_ERR_INVALID;
   if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_INVALID;
-  if (d != kD) return DA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d)) return DA_ERR_UNSUPPORTED;
   if (T > DA_MAX_T) return DA_ERR_UNSUPPORTED;
   if ((int64_t)B * H > (1 << 24)) return DA_ERR_UNSUPPORTED;
   return DA_OK;
@@ -79,10 +79,9 @@ const char *dilution_attn_status_string(int status) {
 int dilution_attn_version(void) { return 101; }
 
 size_t dilution_attn_fwd_workspace_size(int B, int H, int T, int d, int dtype) {
-  (void)d;
   (void)dtype;
-  if (B < 0 || H < 0 || T < 0) return 0;
-  return fwd_workspace_layout((int64_t)B * H, T).total;
+  if (B < 0 || H < 0 || T < 0 || !head_dim_supported(d)) return 0;
+  return fwd_workspace_layout((int64_t)B * H, T, d).total;
 }
 
 int dilution_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
@@ -117,7 +116,7 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DA_ERR_INVALID;
   if (!aligned16_or_null(lse2_out) || !aligned16_or_null(rowsum_out) || !aligned16_or_null(demand_out))
     return DA_ERR_INVALID;
-  const FwdWorkspace L = fwd_workspace_layout(BH, T);
+  const FwdWorkspace L = fwd_workspace_layout(BH, T, d);
   if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -130,19 +129,18 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
   const HeadScale hs = head_scale(tau, tau_bh, d);
   if (dtype == DA_F32) {
     if (launch_fwd_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse2_out, rowsum_out,
-                       demand_out, (int)BH, T, hs, eps, earlier, lse2_ws, acc, status, stream, ev) != cudaSuccess)
+                       demand_out, (int)BH, T, d, hs, eps, earlier, lse2_ws, acc, status, stream, ev) != cudaSuccess)
       return DA_ERR_CUDA;
     return DA_OK;
   }
-  return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, hs, eps, earlier, lse2_ws, acc,
-                         status, stream, ev);
+  return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, d, hs, eps, earlier, lse2_ws,
+                         acc, status, stream, ev);
 }
 
 size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
-  (void)d;
   (void)dtype;
-  if (B < 0 || H < 0 || T < 0) return 0;
-  return bwd_workspace_layout((int64_t)B * H, T).total;
+  if (B < 0 || H < 0 || T < 0 || !head_dim_supported(d)) return 0;
+  return bwd_workspace_layout((int64_t)B * H, T, d).total;
 }
 
 int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
@@ -163,14 +161,14 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
   const void *ptrs[] = {q, k, v, dout, lse2, dq, dk, dv};
   for (const void *p : ptrs)
     if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
-  const BwdWorkspace L = bwd_workspace_layout(BH, T);
+  const BwdWorkspace L = bwd_workspace_layout(BH, T, d);
   if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   const float c = (float)((double)tau / std::sqrt((double)d));
-  if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, c, head_scale(tau, tau_bh, d), eps,
+  if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, d, c, head_scale(tau, tau_bh, d), eps,
                  (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, dtype,
                  reinterpret_cast<double *>(ws + L.dtot_off), reinterpret_cast<float *>(ws + L.row_off),
                  reinterpret_cast<float *>(ws + L.dq_off), stream) != cudaSuccess)
@@ -179,9 +177,8 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
 }
 
 size_t dilution_attn_decode_workspace_size(int B, int H, int T_cap, int d) {
-  (void)d;
-  if (B < 0 || H < 0 || T_cap < 0) return 0;
-  return dec_workspace_layout((int64_t)B * H, T_cap).total;
+  if (B < 0 || H < 0 || T_cap < 0 || !head_dim_supported(d)) return 0;
+  return dec_workspace_layout((int64_t)B * H, T_cap, d).total;
 }
 
 int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
@@ -205,13 +202,13 @@ int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const voi
   const void *ptrs[] = {q_new, k_new, v_new, k_cache, v_cache, demand, out};
   for (const void *p : ptrs)
     if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
-  const DecWorkspace L = dec_workspace_layout(BH, T_cap);
+  const DecWorkspace L = dec_workspace_layout(BH, T_cap, d);
   if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
-  if (launch_decode(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, (int)BH,
+  if (launch_decode(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, (int)BH, d,
                     head_scale(tau, tau_bh, d), eps, (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, dtype,
                     reinterpret_cast<float *>(ws + L.logit_off), reinterpret_cast<float2 *>(ws + L.ml_off),
                     reinterpret_cast<float *>(ws + L.acc_off), L.nchunk, reinterpret_cast<int *>(ws),
@@ -238,12 +235,13 @@ int dilution_attn_debug_last_timeout(void *workspace, int32_t *out) {
 }
 
 int dilution_attn_debug_tile_schedule(int BH, int T, int kernel, int32_t *out, size_t cap) {
-  if (BH < 0 || T < 0 || (kernel != 0 && kernel != 1)) return -1;
+  if (BH < 0 || T < 0 || kernel < 0 || kernel > 2) return -1;
   if (BH == 0 || T == 0) return 0;
-  const int n = (kernel == 0) ? rowstats_num_ctas(BH, T) : sweep_num_ctas(BH, T);
+  const int d = kernel == 2 ? 128 : 64;   // kernel 1: sweep at d = 64, 2: sweep at d = 128
+  const int n = (kernel == 0) ? rowstats_num_ctas(BH, T) : sweep_num_ctas(BH, T, d);
   if (out == nullptr || cap < (size_t)n * 4) return -n;
   for (int c = 0; c < n; ++c) {
-    const TileWork w = (kernel == 0) ? rowstats_work(c, BH, T) : sweep_work(c, BH, T);
+    const TileWork w = (kernel == 0) ? rowstats_work(c, BH, T) : sweep_work(c, BH, T, d);
     out[4 * c + 0] = w.bh;
     out[4 * c + 1] = w.q_tile0;
     out[4 * c + 2] = w.n_q_tiles;

@@ -18,52 +18,58 @@
 
 namespace da {
 
-constexpr int kD = 64;             // head dimension handled by every kernel
+// Head dimensions: 64 and 128 (every kernel is instantiated for both).
+constexpr int kD = 64;             // the default head dimension
+constexpr int kDMax = 128;
 constexpr int kTile = 128;         // query / key tile edge (one TMEM lane per row)
 constexpr int kSpan = 256;         // Tp granule: two 128-row tiles (one row-statistics CTA)
-constexpr int kAccStride = 68;     // fp32 per accumulator row: 64 numerator + rowsum + 3 pad
 constexpr size_t kStatusBytes = 256;
+
+DA_HD bool head_dim_supported(int d) { return d == 64 || d == 128; }
+// fp32 per accumulator row: d numerator + row sum + 3 pad (16-byte rows).
+DA_HD constexpr int acc_stride(int d) { return d + 4; }
+constexpr int kAccStride = acc_stride(kD);
 
 DA_HD int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 DA_HD int64_t t_pad(int64_t T) { return round_up(T, kSpan); }
 
 // ---------------------------------------------------------------------------
-// Workspace of the forward: [status | lse2 [BH][Tp] | acc [BH][Tp][68]].
+// Workspace of the forward: [status | lse2 [BH][Tp] | acc [BH][Tp][d + 4]].
 // Padded rows (T <= row < Tp) carry lse2 = +inf so their bids are exactly 0.
 // ---------------------------------------------------------------------------
 struct FwdWorkspace {
   size_t lse2_off, acc_off, total;
 };
 
-DA_HD FwdWorkspace fwd_workspace_layout(int64_t BH, int64_t T) {
+DA_HD FwdWorkspace fwd_workspace_layout(int64_t BH, int64_t T, int d) {
   FwdWorkspace w;
   const int64_t Tp = t_pad(T);
   w.lse2_off = kStatusBytes;
   w.acc_off = (size_t)round_up((int64_t)w.lse2_off + BH * Tp * 4, 256);
-  w.total = (size_t)round_up((int64_t)w.acc_off + BH * Tp * kAccStride * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.acc_off + BH * Tp * acc_stride(d) * 4, 256);
   return w;
 }
 
 // ---------------------------------------------------------------------------
 // Backward workspace: [status | column totals [BH][T] fp64 | R, Y, rho, spare
-// [4][BH][T] fp32 | dq accumulator [BH][T][64] fp32]
+// [4][BH][T] fp32 | dq accumulator [BH][T][d] fp32]
 // ---------------------------------------------------------------------------
 struct BwdWorkspace {
   size_t dtot_off, row_off, dq_off, total;
 };
 
-DA_HD BwdWorkspace bwd_workspace_layout(int64_t BH, int64_t T) {
+DA_HD BwdWorkspace bwd_workspace_layout(int64_t BH, int64_t T, int d) {
   BwdWorkspace w;
   w.dtot_off = kStatusBytes;
   w.row_off = (size_t)round_up((int64_t)w.dtot_off + BH * T * 8, 256);
   w.dq_off = (size_t)round_up((int64_t)w.row_off + 4 * BH * T * 4, 256);
-  w.total = (size_t)round_up((int64_t)w.dq_off + BH * T * kD * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.dq_off + BH * T * d * 4, 256);
   return w;
 }
 
 // ---------------------------------------------------------------------------
 // Decode workspace: [status | logits [BH][T_cap] | part_ml [BH][nchunk][2] |
-//                    part_acc [BH][nchunk][68]]
+//                    part_acc [BH][nchunk][d + 4]]
 // ---------------------------------------------------------------------------
 constexpr int kDecChunk = 4096;    // keys per decode CTA
 
@@ -72,13 +78,13 @@ struct DecWorkspace {
   int nchunk;
 };
 
-DA_HD DecWorkspace dec_workspace_layout(int64_t BH, int64_t T_cap) {
+DA_HD DecWorkspace dec_workspace_layout(int64_t BH, int64_t T_cap, int d) {
   DecWorkspace w;
   w.nchunk = (int)((T_cap + kDecChunk - 1) / kDecChunk);
   w.logit_off = kStatusBytes;
   w.ml_off = (size_t)round_up((int64_t)w.logit_off + BH * T_cap * 4, 256);
   w.acc_off = (size_t)round_up((int64_t)w.ml_off + BH * w.nchunk * 2 * 4, 256);
-  w.total = (size_t)round_up((int64_t)w.acc_off + BH * w.nchunk * kAccStride * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.acc_off + BH * w.nchunk * acc_stride(d) * 4, 256);
   return w;
 }
 
@@ -104,27 +110,30 @@ DA_HD TileWork rowstats_work(int cta, int BH, int64_t T) {
   return w;
 }
 
-// Demand sweep: one CTA per span of 384 keys (three 128-key tiles), walking
-// 128-query tiles from the span's first query tile to the end.  Heads are
-// taken in groups whose fp32 accumulators (Tp x 272 B per head) together stay
-// near 64 MB, so the reductions of the CTAs in flight hit L2; inside a group
-// the spans with the most query tiles launch first.
-constexpr int kSweepKeys = 384;
+// Demand sweep: one CTA per span of keys (three 128-key tiles at d = 64, two
+// at d = 128), walking 128-query tiles from the span's first query tile to
+// the end.  Heads are taken in groups whose fp32 accumulators (Tp x (d + 4) x
+// 4 B per head) together stay near 64 MB, so the reductions of the CTAs in
+// flight hit L2; inside a group the spans with the most query tiles launch
+// first.
 constexpr int kSweepQTile = 128;
 constexpr int64_t kAccGroupBytes = 64ll << 20;
-DA_HD int sweep_num_spans(int64_t T) { return (int)((t_pad(T) + kSweepKeys - 1) / kSweepKeys); }
-DA_HD int sweep_head_group(int BH, int64_t T) {
-  const int64_t per_head = t_pad(T) * kAccStride * 4;
+DA_HD int sweep_span_keys(int d) { return d == 64 ? 384 : 256; }
+DA_HD int sweep_num_spans(int64_t T, int d) {
+  return (int)((t_pad(T) + sweep_span_keys(d) - 1) / sweep_span_keys(d));
+}
+DA_HD int sweep_head_group(int BH, int64_t T, int d) {
+  const int64_t per_head = t_pad(T) * acc_stride(d) * 4;
   int64_t hg = kAccGroupBytes / per_head;
   if (hg < 1) hg = 1;
   if (hg > BH) hg = BH;
   return (int)hg;
 }
-DA_HD int sweep_num_ctas(int BH, int64_t T) { return BH * sweep_num_spans(T); }
-DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
+DA_HD int sweep_num_ctas(int BH, int64_t T, int d) { return BH * sweep_num_spans(T, d); }
+DA_HD TileWork sweep_work(int cta, int BH, int64_t T, int d) {
   const int nqt = (int)(t_pad(T) / kSweepQTile);
-  const int nspan = sweep_num_spans(T);
-  const int hg = sweep_head_group(BH, T);
+  const int nspan = sweep_num_spans(T, d);
+  const int hg = sweep_head_group(BH, T, d);
   const int group = cta / (hg * nspan);
   const int h0 = group * hg;
   const int ng = (BH - h0 < hg) ? BH - h0 : hg;    // heads in this (possibly last, smaller) group
@@ -132,7 +141,7 @@ DA_HD TileWork sweep_work(int cta, int BH, int64_t T) {
   TileWork w;
   w.bh = h0 + r % ng;
   const int span = r / ng;                   // span 0 walks every query tile
-  w.key0 = span * kSweepKeys;
+  w.key0 = span * sweep_span_keys(d);
   w.q_tile0 = w.key0 / kSweepQTile;
   w.n_q_tiles = nqt - w.q_tile0;
   return w;

@@ -327,6 +327,18 @@ __device__ __forceinline__ void tmem_zero80(uint32_t taddr) {
       : "memory");
 }
 
+// Zero 64 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_zero64(uint32_t taddr) {
+  const uint32_t z = 0u;
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], "
+      "{%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2,%2};" ::"r"(taddr),
+      "r"(taddr + 32), "r"(z)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, float &r) {
   uint32_t u;
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(u) : "r"(taddr));

@@ -63,18 +63,19 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return r;
 }
 
-// Lanes per row: a row of d = 64 elements is 128 B (bf16) or 256 B (fp32).
-template <typename E>
+// Lanes per row: a row of d elements is 2d bytes (bf16) or 4d bytes (fp32),
+// one 16-byte piece per lane.
+template <typename E, int D>
 constexpr int lanes_per_row() {
-  return kD / Vec16<E>::N;
+  return D / Vec16<E>::N;
 }
 
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kDecThreads)
     dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
                E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
                float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, HeadScale hs, int *status) {
-  constexpr int LPR = lanes_per_row<E>();          // lanes cooperating on one key
+  constexpr int LPR = lanes_per_row<E, D>();       // lanes cooperating on one key
   constexpr int NV = Vec16<E>::N;
   constexpr int KPR = kDecThreads / LPR;           // keys per round
   const int bh = blockIdx.y, chunk = blockIdx.x;
@@ -87,8 +88,8 @@ __global__ void __launch_bounds__(kDecThreads)
   const int k_end = min(k_begin + kDecChunk, n_keys);
 
   float qf[NV];
-  Vec16<E>::to_float(*reinterpret_cast<const uint4 *>(q_new + (size_t)bh * kD + sub * NV), qf);
-  const E *kb = k_cache + (size_t)bh * T_cap * kD;
+  Vec16<E>::to_float(*reinterpret_cast<const uint4 *>(q_new + (size_t)bh * D + sub * NV), qf);
+  const E *kb = k_cache + (size_t)bh * T_cap * D;
   float m = -INFINITY, l = 0.f;
   // Warp-uniform trip count: every lane runs every round (the shuffles below
   // need the full warp); keys past the chunk are predicated off.
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int u = 0; u < kDecUnroll; ++u) {
       const int key = k0 + u * KPR;
       if (key < k_end) {
-        const E *src = (key == n_ctx) ? k_new + (size_t)bh * kD : kb + (size_t)key * kD;
+        const E *src = (key == n_ctx) ? k_new + (size_t)bh * D : kb + (size_t)key * D;
         raw[u] = ld_stream(src + sub * NV);
       } else {
         raw[u] = make_uint4(0, 0, 0, 0);
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(kDecThreads)
     const E *src = (tid < LPR) ? k_new : v_new;
     E *dst = (tid < LPR) ? k_cache : v_cache;
     const int piece = tid % LPR;
-    *reinterpret_cast<uint4 *>(dst + ((size_t)bh * T_cap + n_ctx) * kD + piece * NV) =
-        *reinterpret_cast<const uint4 *>(src + (size_t)bh * kD + piece * NV);
+    *reinterpret_cast<uint4 *>(dst + ((size_t)bh * T_cap + n_ctx) * D + piece * NV) =
+        *reinterpret_cast<const uint4 *>(src + (size_t)bh * D + piece * NV);
   }
   // Block reduction of (m, l): only lane sub == 0 of each group holds data.
   __shared__ float sm[kDecThreads], sl[kDecThreads];
@@ -154,12 +155,12 @@ __global__ void __launch_bounds__(kDecThreads)
   if (tid == 0) part_ml[(size_t)bh * nchunk + chunk] = make_float2(sm[0], sl[0]);
 }
 
-template <typename E>
+template <typename E, int D>
 __global__ void __launch_bounds__(kDecThreads)
     dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
                float *__restrict__ demand, float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
                int nchunk_used, float eps, bool earlier) {
-  constexpr int LPR = lanes_per_row<E>();
+  constexpr int LPR = lanes_per_row<E, D>();
   constexpr int NV = Vec16<E>::N;
   constexpr int KPR = kDecThreads / LPR;
   const int bh = blockIdx.y, chunk = blockIdx.x;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kDecThreads)
   const float lse2 = s_lse2;
   const int k_begin = chunk * kDecChunk;
   const int k_end = min(k_begin + kDecChunk, n_ctx + 1);
-  const E *vb = v_cache + (size_t)bh * T_cap * kD;
+  const E *vb = v_cache + (size_t)bh * T_cap * D;
   float num[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) num[i] = 0.f;
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int u = 0; u < kDecUnroll; ++u) {
       const int key = k0 + u * KPR;
       const bool ok = key < k_end;
-      raw[u] = ok ? ld_stream(vb + (size_t)key * kD + sub * NV) : make_uint4(0, 0, 0, 0);
+      raw[u] = ok ? ld_stream(vb + (size_t)key * D + sub * NV) : make_uint4(0, 0, 0, 0);
       x[u] = ok ? logits[(size_t)bh * T_cap + key] : -INFINITY;
       dm[u] = (ok && key < n_ctx) ? demand[(size_t)bh * T_cap + key] : 0.f;
     }
@@ -225,60 +226,63 @@ __global__ void __launch_bounds__(kDecThreads)
     }
   }
   // Reduce the KPR key groups: partial rows [KPR][64 + 1] in shared memory.
-  __shared__ float sacc[KPR][kD + 1];
+  __shared__ float sacc[KPR][D + 1];
 #pragma unroll
   for (int i = 0; i < NV; ++i) sacc[grp][sub * NV + i] = num[i];
-  if (sub == 0) sacc[grp][kD] = rs;
+  if (sub == 0) sacc[grp][D] = rs;
   __syncthreads();
-  if (tid <= kD) {
+  if (tid <= D) {
     float a = 0.f;
     for (int gi = 0; gi < KPR; ++gi) a += sacc[gi][tid];
-    part_acc[((size_t)bh * nchunk + chunk) * kAccStride + tid] = a;
+    part_acc[((size_t)bh * nchunk + chunk) * acc_stride(D) + tid] = a;
   }
 }
 
-template <typename E>
+template <typename E, int D>
 __global__ void dec_combine(const float *__restrict__ part_acc, E *__restrict__ out, int nchunk, int nchunk_used) {
   const int bh = blockIdx.x;
   const int t = threadIdx.x;   // 0..63
   float a = 0.f, rs = 0.f;
   for (int c = 0; c < nchunk_used; ++c) {
-    const float *pa = part_acc + ((size_t)bh * nchunk + c) * kAccStride;
+    const float *pa = part_acc + ((size_t)bh * nchunk + c) * acc_stride(D);
     a += pa[t];
-    rs += pa[kD];
+    rs += pa[D];
   }
   const float o = a / rs;
   if constexpr (sizeof(E) == 4) {
-    out[(size_t)bh * kD + t] = o;
+    out[(size_t)bh * D + t] = o;
   } else {
-    out[(size_t)bh * kD + t] = __float2bfloat16_rn(o);
+    out[(size_t)bh * D + t] = __float2bfloat16_rn(o);
   }
 }
 
-template <typename E>
+template <typename E, int D>
 static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
                                    void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int BH,
                                    HeadScale hs, float eps, bool earlier, float *logits, float2 *part_ml,
                                    float *part_acc, int nchunk, int *status, cudaStream_t stream) {
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
-  dec_logits<E><<<dim3(used, BH), kDecThreads, 0, stream>>>(
+  dec_logits<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
       T_cap, nchunk, hs, status);
-  dec_update<E><<<dim3(used, BH), kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc,
+  dec_update<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc,
                                                            n_ctx, T_cap, nchunk, used, eps, earlier);
-  dec_combine<E><<<BH, kD, 0, stream>>>(part_acc, (E *)out, nchunk, used);
+  dec_combine<E, D><<<BH, D, 0, stream>>>(part_acc, (E *)out, nchunk, used);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
-                          float *demand, int n_ctx, int T_cap, void *out, int BH, HeadScale hs, float eps,
+                          float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
                           bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
                           int *status, cudaStream_t stream) {
+#define DA_DECODE_ARGS                                                                                          \
+  q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, hs, eps, earlier, logits, part_ml, part_acc, \
+      nchunk, status, stream
   if (dtype == DA_BF16)
-    return launch_decode_t<__nv_bfloat16>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, hs,
-                                          eps, earlier, logits, part_ml, part_acc, nchunk, status, stream);
-  return launch_decode_t<float>(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, hs, eps,
-                                earlier, logits, part_ml, part_acc, nchunk, status, stream);
+    return d == 128 ? launch_decode_t<__nv_bfloat16, 128>(DA_DECODE_ARGS)
+                    : launch_decode_t<__nv_bfloat16, 64>(DA_DECODE_ARGS);
+  return d == 128 ? launch_decode_t<float, 128>(DA_DECODE_ARGS) : launch_decode_t<float, 64>(DA_DECODE_ARGS);
+#undef DA_DECODE_ARGS
 }
 
 // ---------------------------------------------------------------------------
@@ -319,7 +323,8 @@ extern "C" int dilution_attn_decode_step_noalloc(const void *q_new, const void *
                                                  void *stream) {
   using namespace da;
   if (B < 0 || H < 0 || T_cap < 0) return DA_ERR_INVALID;
-  const DecWorkspace L = dec_workspace_layout((int64_t)B * H, T_cap);
+  if (!head_dim_supported(d)) return DA_ERR_UNSUPPORTED;
+  const DecWorkspace L = dec_workspace_layout((int64_t)B * H, T_cap, d);
   if (L.total > kNoAllocScratchBytes) return DA_ERR_WORKSPACE;   // beyond the fixed scratch
   void *scratch = nullptr;
   const int st = noalloc_scratch(&scratch);

@@ -45,7 +45,12 @@
 
 namespace da {
 
-constexpr uint32_t kTileBytes = kTile * kD * 2;   // one 128 x 64 bf16 tile, 128-byte swizzled rows
+// A tile of 128 rows x d bf16 is stored as d / 64 halves of 128 rows x 64
+// (128-byte swizzled rows, 16 KB each): 128 bytes is the widest box a
+// 128-byte swizzle allows.  Half h of a tile starts h * 16 KB after it.
+constexpr uint32_t kHalfBytes = kTile * 64 * 2;
+template <int D>
+constexpr uint32_t tile_bytes() { return kTile * D * 2; }
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   const uint32_t a = smem_u32(p);
@@ -61,11 +66,19 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
-// K-major operand tile: 128 rows x 64 bf16 (128-byte rows, 128B swizzle, as
-// TMA writes it).  8-row groups are 1024 bytes apart; a K step of 16
-// elements advances the start address by 32 bytes inside the swizzle atom.
+// K-major operand tile: 128 rows x 64 bf16 per half (128-byte rows, 128B
+// swizzle, as TMA writes it).  8-row groups are 1024 bytes apart; a K step of
+// 16 elements advances the start address by 32 bytes inside the swizzle atom,
+// and K steps 4.. continue in the next half.
 __device__ __forceinline__ uint64_t kmajor_desc(const uint8_t *tile, int kstep) {
-  return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
+  return smem_desc(smem_u32(tile) + (kstep >> 2) * kHalfBytes + (kstep & 3) * 32, 16, 1024);
+}
+
+// TMA load of one 128-row tile of a [BH, T, d] tensor into `dst`, half by half.
+template <int D>
+__device__ __forceinline__ void tma_load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int row, int bh) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * kHalfBytes, map, bar, h * 64, row, bh);
 }
 
 // After the last tcgen05.ld of a TMEM buffer has completed: hand the buffer
@@ -201,25 +214,41 @@ __device__ __forceinline__ float bf16_c2(const HeadScale &hs, int bh, int *statu
 // ============================================================================
 // Row statistics
 // ============================================================================
+// d = 64: 2 CTAs per SM, one S buffer per query tile (256 TMEM columns);
+// d = 128: the tiles take one SM's shared memory, so one CTA per SM with two
+// S buffers per query tile (512 columns) keeps the tensor pipe busy while a
+// buffer is being reduced.
 constexpr int kRsThreads = 320;
 constexpr int kRsKStages = 4;
-constexpr int kRsSmemBytes = (2 + kRsKStages) * kTileBytes + 256 + 1024;
+template <int D>
+struct RsCfg {
+  static constexpr uint32_t kTB = tile_bytes<D>();
+  static constexpr int kSlots = D == 64 ? 1 : 2;     // S buffers per query tile
+  static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+  static constexpr uint32_t kTmemCols = 2 * kSlots * kTile;
+  static constexpr int kSmemBytes = (2 + kRsKStages) * kTB + 256 + 1024;
+};
 
-__global__ void __launch_bounds__(kRsThreads, 2)
+template <int D>
+__global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
     rowstats_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     float *__restrict__ nlse2, float *__restrict__ acc, int BH, int T, int Tp, HeadScale hs,
                     int *status) {
+  using C = RsCfg<D>;
+  constexpr uint32_t kTB = C::kTB;
+  constexpr int NS = C::kSlots;
+  constexpr int AS = acc_stride(D);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint8_t *sQ = smem;                    // 2 query tiles
-  uint8_t *sK = smem + 2 * kTileBytes;   // K ring
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + kRsKStages) * kTileBytes);
+  uint8_t *sK = smem + 2 * kTB;          // K ring
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (2 + kRsKStages) * kTB);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;
   uint64_t *k_empty = k_full + kRsKStages;
-  uint64_t *s_full = k_empty + kRsKStages;
-  uint64_t *s_free = s_full + 2;
-  uint64_t *drain = s_free + 2;
+  uint64_t *s_full = k_empty + kRsKStages;   // [g * NS + slot]
+  uint64_t *s_free = s_full + 2 * NS;
+  uint64_t *drain = s_free + 2 * NS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -234,7 +263,7 @@ __global__ void __launch_bounds__(kRsThreads, 2)
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
     }
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < 2 * NS; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&s_free[g], 4);
     }
@@ -243,7 +272,7 @@ __global__ void __launch_bounds__(kRsThreads, 2)
     fence_mbar_init();
   }
   if (warp == 9) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
@@ -256,15 +285,15 @@ __global__ void __launch_bounds__(kRsThreads, 2)
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
-      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-      tma_load_3d(sQ, &tmQ, q_full, 0, w.q_tile0 * kTile, w.bh);
-      tma_load_3d(sQ + kTileBytes, &tmQ, q_full, 0, (w.q_tile0 + 1) * kTile, w.bh);
+      mbar_arrive_expect_tx(q_full, 2 * kTB);
+      tma_load_tile<D>(sQ, &tmQ, q_full, w.q_tile0 * kTile, w.bh);
+      tma_load_tile<D>(sQ + kTB, &tmQ, q_full, (w.q_tile0 + 1) * kTile, w.bh);
       int issued = 0;
       for (int kt = 0; kt < n_kt; ++kt) {
         const int s = kt % kRsKStages;
         if (!mbar_wait(&k_empty[s], ((kt / kRsKStages) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&k_full[s], kTileBytes);
-        tma_load_3d(sK + s * kTileBytes, &tmK, &k_full[s], 0, kt * kTile, w.bh);
+        mbar_arrive_expect_tx(&k_full[s], kTB);
+        tma_load_tile<D>(sK + s * kTB, &tmK, &k_full[s], kt * kTile, w.bh);
         ++issued;
       }
       if (*abort_flag) {
@@ -277,7 +306,6 @@ __global__ void __launch_bounds__(kRsThreads, 2)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kTile, kTile, false, false);
-      uint32_t n_free[2] = {0, 0};
       if (mbar_wait(q_full, 0, wc)) {
         tc_fence_after();
         for (int kt = 0; kt < n_kt; ++kt) {
@@ -287,18 +315,18 @@ __global__ void __launch_bounds__(kRsThreads, 2)
           bool ok = true;
           for (int g = 0; g < 2; ++g) {
             if (kt > w.q_tile0 + g) continue;   // key tile entirely after this query tile
-            if (!mbar_wait(&s_free[g], (n_free[g] & 1) ^ 1, wc)) {
+            // key tile kt is use kt / NS of slot kt % NS of query tile g
+            const int slot = g * NS + kt % NS;
+            if (!mbar_wait(&s_free[slot], ((kt / NS) & 1) ^ 1, wc)) {
               ok = false;
               break;
             }
-            ++n_free[g];
             tc_fence_after();
-            const uint32_t d = tmem + g * kTile;
+            const uint32_t d = tmem + slot * kTile;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              mma_bf16(d, kmajor_desc(sQ + g * kTileBytes, kk), kmajor_desc(sK + s * kTileBytes, kk), idesc,
-                       kk > 0);
-            mma_commit(&s_full[g]);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_bf16(d, kmajor_desc(sQ + g * kTB, kk), kmajor_desc(sK + s * kTB, kk), idesc, kk > 0);
+            mma_commit(&s_full[slot]);
           }
           if (!ok) break;
           mma_commit(&k_empty[s]);
@@ -315,9 +343,10 @@ __global__ void __launch_bounds__(kRsThreads, 2)
     const int qt = w.q_tile0 + g;
     const int64_t qi = (int64_t)qt * kTile + row;
     RowStat st;
-    const uint32_t tbase = tmem + g * kTile + ((uint32_t)(quarter * 32) << 16);
     for (int kt = 0; kt <= qt; ++kt) {
-      if (!mbar_wait(&s_full[g], kt & 1, wc)) break;
+      const int slot = g * NS + kt % NS;
+      const uint32_t tbase = tmem + slot * kTile + ((uint32_t)(quarter * 32) << 16);
+      if (!mbar_wait(&s_full[slot], (kt / NS) & 1, wc)) break;
       tc_fence_after();
       // 32-column chunks; the load of chunk c+1 is in flight while chunk c is reduced.
       float A[32], B[32];
@@ -333,7 +362,7 @@ __global__ void __launch_bounds__(kRsThreads, 2)
         tmem_ld32(tbase + 96, B);
         st.chunk<false>(A, 64, row, c2);
         tmem_wait_ld_r(B);
-        release_tmem(&s_free[g], lane);
+        release_tmem(&s_free[slot], lane);
         st.chunk<false>(B, 96, row, c2);
       } else {
         tmem_ld32(tbase, A);
@@ -347,7 +376,7 @@ __global__ void __launch_bounds__(kRsThreads, 2)
         tmem_ld32(tbase + 96, B);
         st.chunk<true>(A, 64, row, c2);
         tmem_wait_ld_r(B);
-        release_tmem(&s_free[g], lane);
+        release_tmem(&s_free[slot], lane);
         st.chunk<true>(B, 96, row, c2);
       }
       if (*abort_flag) break;
@@ -355,9 +384,9 @@ __global__ void __launch_bounds__(kRsThreads, 2)
     if (qi < Tp) {
       // negated, so the sweep forms x - lse2 with one packed fma
       nlse2[(size_t)w.bh * Tp + qi] = (qi < T) ? -(st.m + log2f(st.l0.x + st.l0.y + st.l1.x + st.l1.y)) : -INFINITY;
-      float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)w.bh * Tp + qi) * kAccStride);
+      float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)w.bh * Tp + qi) * AS);
 #pragma unroll
-      for (int t = 0; t < kAccStride / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int t = 0; t < AS / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 
@@ -366,7 +395,7 @@ __global__ void __launch_bounds__(kRsThreads, 2)
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -384,51 +413,71 @@ __global__ void __launch_bounds__(kRsThreads, 2)
 // Every tcgen05.mma costs at least ~46 cycles on this part and reaches full
 // rate only at M = 128, N >= 128, which is why the query tile is 128 wide and
 // the row sum rides in the same instruction as the value product.
-constexpr int kSwG = kSweepKeys / kTile;        // 3 demand warpgroups, one per key tile
 constexpr int kSwBQ = kSweepQTile;              // 128 queries per tile
-constexpr int kSwWarps = (kSwG + 2) * 4;        // demand WGs, epilogue WG, producer/MMA WG
-constexpr int kSwThreads = kSwWarps * 32;       // 640
-// Register split across warpgroups (setmaxnreg).  The block is launched with
-// 640 x (registers per thread) registers; the split below must not exceed that
-// (checked on the host before every launch).
-constexpr int kSwRegsDemand = 128, kSwRegsEpi = 56, kSwRegsCtl = 40;
-constexpr int kSwRegsNeeded = 128 * (kSwG * kSwRegsDemand + kSwRegsEpi + kSwRegsCtl);
 constexpr uint32_t kShBytes = 2 * 16 * 1024;    // share^T: 2 M-blocks x 16 key groups x 1 KB
 constexpr uint32_t kStageBytes = 32 * 32 * 4;   // epilogue reduction box: 32 rows x 32 fp32, 128B-swizzled
-constexpr uint32_t kSwOffK = 0;                                    // key tiles 1, 2 (tile 0 is in TMEM)
-constexpr uint32_t kSwOffV = kSwOffK + (kSwG - 1) * kTileBytes;
 constexpr uint32_t kExtBytes = 128 * 16 * 2;    // one 128-row x 16 bf16 K-major operand, no swizzle
-constexpr uint32_t kSwOffQ = kSwOffV + kSwG * kTileBytes;          // the query tile
-constexpr uint32_t kSwOffAExt = kSwOffQ + kTileBytes;              // [1 1 1 0 ..] for every key
-constexpr uint32_t kSwOffBExt = kSwOffAExt + kExtBytes;            // [hi mid lo 0 ..] of -lse2 / c2 per query
-constexpr uint32_t kSwOffSh = kSwOffQ + 2 * kTileBytes;
-constexpr uint32_t kSwOffOnes = kSwOffSh + kSwG * kShBytes;         // above every V tile (positive LBO)
-constexpr uint32_t kSwOffStage = kSwOffOnes + 2048;                 // one box per epilogue warp
-constexpr uint32_t kSwOffBar = kSwOffStage + 4 * kStageBytes;
-constexpr int kSwSmemBytes = kSwOffBar + 512;   // the dynamic shared-memory base is 1024-byte aligned
-static_assert(kSwSmemBytes <= 232448, "sweep shared memory");
-static_assert(kSwOffStage % 1024 == 0, "reduction boxes are 128B-swizzled");
-static_assert(kSwRegsNeeded <= 65536, "sweep register split");
-static_assert(kSwOffBExt + kExtBytes <= kSwOffSh, "extension operands");
+// Register split across warpgroups (setmaxnreg).  The block is launched with
+// its threads x (registers per thread) registers; the split must not exceed
+// that (checked on the host before every launch).
+constexpr int kSwRegsDemand = 128, kSwRegsEpi = 56;
 
-constexpr uint32_t kTmemD = kSwG * kTile;   // S^T slots at g*128; D (80 columns) after them
-// Key tile 0 as the A operand of its S product, read from TMEM (one key per
-// lane, 32 columns of bf16 pairs): its 16 KB of shared memory hold the second
-// query slot instead.
-constexpr uint32_t kTmemK0 = kTmemD + kD + 16;
-static_assert(kTmemK0 + kD / 2 <= 512, "TMEM columns");
+// Per-head-dimension layout.  d = 64: three demand warpgroups (384-key
+// spans).  d = 128: two (256-key spans), so that the S slots, the
+// accumulators and key tile 0 fit the 512 TMEM columns and the tiles fit
+// 227 KB of shared memory; its value product is split into D[q, 0:80] +=
+// share^T [V_lo | 1] and DHi[q, 0:64] += share^T V_hi.
+template <int D>
+struct SwCfg {
+  static constexpr int kG = D == 64 ? 3 : 2;           // demand warpgroups, one per key tile
+  static constexpr int kWarps = (kG + 2) * 4;         // demand WGs, epilogue WG, producer/MMA WG
+  static constexpr int kThreads = kWarps * 32;        // 640 / 512
+  static constexpr uint32_t kTB = tile_bytes<D>();
+  // control warps: 40 registers at d = 64; the d = 128 issuers keep two more
+  // operand descriptors live
+  static constexpr int kRegsCtl = D == 64 ? 40 : 56;
+  // registers per thread at launch (d = 64: 640 threads leave 96)
+  static constexpr int kRegsLaunch = D == 64 ? 96 : 112;
+  static constexpr int kRegsNeeded = 128 * (kG * kSwRegsDemand + kSwRegsEpi + kRegsCtl);
+  static constexpr uint32_t kOffK = 0;                              // key tiles 1.. (tile 0 is in TMEM)
+  static constexpr uint32_t kOffV = kOffK + (kG - 1) * kTB;
+  static constexpr uint32_t kOffQ = kOffV + kG * kTB;               // the query tile
+  static constexpr uint32_t kOffAExt = kOffQ + kTB;                 // [1 1 1 0 ..] for every key
+  static constexpr uint32_t kOffBExt = kOffAExt + kExtBytes;        // [hi mid lo 0 ..] of -lse2 / c2 per query
+  static constexpr uint32_t kOffSh = D == 64 ? kOffQ + 2 * kTB : kOffBExt + kExtBytes;
+  static constexpr uint32_t kOffOnes = kOffSh + kG * kShBytes;      // above every V tile (positive LBO)
+  static constexpr uint32_t kOffStage = kOffOnes + 2048;            // one box per epilogue warp
+  static constexpr uint32_t kOffBar = kOffStage + 4 * kStageBytes;
+  static constexpr int kSmemBytes = kOffBar + 512;   // the dynamic shared-memory base is 1024-byte aligned
+  // TMEM: S^T slots at g * 128; D (80 columns: values 0..63, row sum at 64);
+  // DHi (d = 128: values 64..127); key tile 0 as the A operand of its S
+  // product (one key per lane, d / 2 columns of bf16 pairs).
+  static constexpr uint32_t kTmemD = kG * kTile;
+  static constexpr uint32_t kTmemDHi = kTmemD + 80;
+  static constexpr uint32_t kTmemK0 = kTmemDHi + (D - 64);
+  static_assert(kSmemBytes <= 232448, "sweep shared memory");
+  static_assert(kOffStage % 1024 == 0, "reduction boxes are 128B-swizzled");
+  static_assert(kRegsNeeded <= 65536, "sweep register split");
+  static_assert(kOffBExt + kExtBytes <= kOffSh, "extension operands");
+  static_assert(kTmemK0 + D / 2 <= 512, "TMEM columns");
+};
 
 __device__ __forceinline__ void regs_inc_demand() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSwRegsDemand)); }
 __device__ __forceinline__ void regs_dec_epi() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsEpi)); }
-__device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSwRegsCtl)); }
+template <int N>
+__device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
-template <bool EARLIER>
-__global__ void __launch_bounds__(kSwThreads, 1)
+template <int D, bool EARLIER>
+__global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::kRegsLaunch)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmAcc,
                  const uint4 *__restrict__ kglob, const float *__restrict__ nlse2, float *__restrict__ acc,
                  float *__restrict__ demand_out, int BH,
                  int T, int Tp, HeadScale hs, float eps, int *status) {
+  using C = SwCfg<D>;
+  constexpr int kG = C::kG;
+  constexpr uint32_t kTB = C::kTB;
+  constexpr int AS = acc_stride(D);
   extern __shared__ __align__(1024) uint8_t sw_smem_raw[];
   // The layout has no slack for re-alignment: every tile, swizzle atom and
   // reduction box assumes a 1024-byte aligned base.  Refuse (uniformly,
@@ -438,32 +487,32 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     return;
   }
   uint8_t *smem = sw_smem_raw;
-  uint8_t *sK = smem + kSwOffK;
-  uint8_t *sV = smem + kSwOffV;
-  uint8_t *sQ = smem + kSwOffQ;
-  uint8_t *sSh = smem + kSwOffSh;
-  uint8_t *sAExt = smem + kSwOffAExt;
-  uint8_t *sBExt = smem + kSwOffBExt;
-  uint8_t *sOnes = smem + kSwOffOnes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSwOffBar);
+  uint8_t *sK = smem + C::kOffK;
+  uint8_t *sV = smem + C::kOffV;
+  uint8_t *sQ = smem + C::kOffQ;
+  uint8_t *sSh = smem + C::kOffSh;
+  uint8_t *sAExt = smem + C::kOffAExt;
+  uint8_t *sBExt = smem + C::kOffBExt;
+  uint8_t *sOnes = smem + C::kOffOnes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *kv_full = bars;
   uint64_t *k0_full = kv_full + 1;             // key tile 0 written to TMEM
   uint64_t *q_full = k0_full + 1;              // query tile and its -lse2 / c2 block loaded
   uint64_t *q_empty = q_full + 1;              // every S product of the tile completed
   uint64_t *s_full = q_empty + 1;              // [g]
-  uint64_t *s_free = s_full + kSwG;            // [g]
-  uint64_t *sh_full = s_free + kSwG;           // [g]
-  uint64_t *sh_free = sh_full + kSwG;          // [g]
-  uint64_t *d_full = sh_free + kSwG;
+  uint64_t *s_free = s_full + kG;            // [g]
+  uint64_t *sh_full = s_free + kG;           // [g]
+  uint64_t *sh_free = sh_full + kG;          // [g]
+  uint64_t *d_full = sh_free + kG;
   uint64_t *d_free = d_full + 1;
   uint64_t *drain = d_free + 1;                // [g]: per issuer
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + kSwG);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + kG);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wg = warp / 4;
-  const int kWarpProd = (kSwG + 1) * 4, kWarpMma = kWarpProd + 1;
-  const TileWork w = sweep_work(blockIdx.x, BH, T);
+  const int kWarpProd = (kG + 1) * 4, kWarpMma = kWarpProd + 1;
+  const TileWork w = sweep_work(blockIdx.x, BH, T, D);
   const int nt = w.n_q_tiles;
   const float c2 = bf16_c2(hs, w.bh, nullptr);   // the row statistics report bad entries
 
@@ -471,26 +520,26 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     mbar_init(kv_full, 1);
     mbar_init(k0_full, 4);
     mbar_init(q_full, 2);      // the tile's bytes + the producer's -lse2 / c2 block
-    mbar_init(q_empty, kSwG);  // one commit per issuer
-    for (int g = 0; g < kSwG; ++g) {
+    mbar_init(q_empty, kG);  // one commit per issuer
+    for (int g = 0; g < kG; ++g) {
       mbar_init(&s_full[g], 1);
       mbar_init(&s_free[g], 4);
       mbar_init(&sh_full[g], 4);
       mbar_init(&sh_free[g], 1);
     }
-    mbar_init(d_full, kSwG);   // one commit per issuer
+    mbar_init(d_full, kG);   // one commit per issuer
     mbar_init(d_free, 4);      // phase t: D holds zeros for tile t (the epilogue warps)
-    for (int g = 0; g < kSwG; ++g) mbar_init(&drain[g], 1);
+    for (int g = 0; g < kG; ++g) mbar_init(&drain[g], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   // Constant all-ones block: the N = 64..79 part of the value operand.
-  for (int e = threadIdx.x; e < 2048 / 4; e += kSwThreads) reinterpret_cast<uint32_t *>(sOnes)[e] = 0x3F803F80u;
+  for (int e = threadIdx.x; e < 2048 / 4; e += C::kThreads) reinterpret_cast<uint32_t *>(sOnes)[e] = 0x3F803F80u;
   // The fifth K step of S: A_ext rows (every key) = [1 1 1 0 ... 0], B_ext rows
   // (every query) = [hi mid lo 0 ... 0] of -lse2 / c2 (written per tile), so
   // S' = q.k - lse2 / c2 and x = c2 S'.  K-major, no swizzle: 8-row groups of
   // 256 bytes, each the core matrix of K 0..7 followed by that of K 8..15.
-  for (int e = threadIdx.x; e < (int)(kExtBytes / 16); e += kSwThreads) {
+  for (int e = threadIdx.x; e < (int)(kExtBytes / 16); e += C::kThreads) {
     const bool k_lo = (e & 15) < 8;
     reinterpret_cast<uint4 *>(sAExt)[e] = k_lo ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4 *>(sBExt)[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -505,8 +554,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, status};
 
-  if (wg == kSwG + 1) {
-    regs_dec_ctl();
+  if (wg == kG + 1) {
+    regs_dec_ctl<C::kRegsCtl>();
     if (warp == kWarpProd) {
       // ---------------------------------------------------------- producer
       // Lane 0 issues the TMA loads; once the S products of the previous tile
@@ -517,10 +566,10 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmAcc);
-        mbar_arrive_expect_tx(kv_full, (2 * kSwG - 1) * kTileBytes);
-        for (int g = 0; g < kSwG; ++g) {
-          if (g > 0) tma_load_3d(sK + (g - 1) * kTileBytes, &tmK, kv_full, 0, w.key0 + g * kTile, w.bh);
-          tma_load_3d(sV + g * kTileBytes, &tmV, kv_full, 0, w.key0 + g * kTile, w.bh);
+        mbar_arrive_expect_tx(kv_full, (2 * kG - 1) * kTB);
+        for (int g = 0; g < kG; ++g) {
+          if (g > 0) tma_load_tile<D>(sK + (g - 1) * kTB, &tmK, kv_full, w.key0 + g * kTile, w.bh);
+          tma_load_tile<D>(sV + g * kTB, &tmV, kv_full, w.key0 + g * kTile, w.bh);
         }
       }
       const float4 *lsrc = reinterpret_cast<const float4 *>(nlse2 + (size_t)w.bh * Tp) + lane;
@@ -530,8 +579,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         const float4 nl = __ldg(lsrc + qrow / 4);   // -lse2 of queries qrow + 4 lane .. + 3 (-inf past T)
         if (!mbar_wait(q_empty, (t & 1) ^ 1, wc)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(q_full, kTileBytes);
-          tma_load_3d(sQ, &tmQ, q_full, 0, qrow, w.bh);
+          mbar_arrive_expect_tx(q_full, kTB);
+          tma_load_tile<D>(sQ, &tmQ, q_full, qrow, w.bh);
         }
         ++q_issued;
         const float nv[4] = {nl.x, nl.y, nl.z, nl.w};
@@ -558,7 +607,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         drain_wait(kv_full, 0);
         if (q_issued > 0) drain_wait(q_full, (q_issued - 1) & 1);
       }
-    } else if (warp >= kWarpMma && warp < kWarpMma + kSwG && lane == 0) {
+    } else if (warp >= kWarpMma && warp < kWarpMma + kG && lane == 0) {
       // ------------------------------------------------------- MMA issuers
       // One issuing thread per demand warpgroup (warps 17, 18, 19: one per
       // sub-partition 1..3), each issuing its warpgroup's S and share.[V|1]
@@ -578,18 +627,21 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       //   bit 16).
       const int g = warp - kWarpMma;
       constexpr long long kStepKm = 2, kStepSh = 128, kStepV = 128 - (128ll << 16);
-      constexpr uint64_t kTileStep = kTileBytes >> 4, kShStep = kShBytes >> 4;
+      constexpr uint64_t kTileStep = kTB >> 4, kShStep = kShBytes >> 4;
       constexpr uint64_t kVTileStep = kTileStep - (kTileStep << 16);
       const uint32_t idesc_s = idesc_bf16(kTile, kSwBQ, false, false);
-      const uint32_t idesc_pv = idesc_bf16(kSwBQ, kD + 16, true, true);
+      const uint32_t idesc_pv = idesc_bf16(kSwBQ, 64 + 16, true, true);
+      const uint32_t idesc_pv_hi = idesc_bf16(kSwBQ, 64, true, true);   // d = 128: value columns 64..127
       const uint32_t ones_addr = smem_u32(sOnes);
       const uint64_t dQ = kmajor_desc(sQ, 0);
       // fifth K step: -lse2 / c2 for every (key, query)
       const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
       const uint64_t dBExt = smem_desc_noswizzle(smem_u32(sBExt), 128, 256);
-      const uint64_t dKg = kmajor_desc(sK + (g > 0 ? g - 1 : 0) * kTileBytes, 0);   // (tile 0 is read from TMEM)
+      const uint64_t dKg = kmajor_desc(sK + (g > 0 ? g - 1 : 0) * kTB, 0);   // (tile 0 is read from TMEM)
       const uint64_t dShg = smem_desc(smem_u32(sSh), 16384, 1024) + g * kShStep;
       const uint64_t dVg = smem_desc(smem_u32(sV), ones_addr - smem_u32(sV), 1024) + g * kVTileStep;
+      // d = 128: the value tile's second half (columns 64..127), one N block.
+      const uint64_t dVg_hi = smem_desc(smem_u32(sV) + kHalfBytes, kHalfBytes, 1024) + g * kTileStep;
       // Per warpgroup the events come in a fixed order: S(t+1) becomes ready
       // (slot released while tile t is read) before PV(t) (its shares
       // written), so the issuer walks S(0), S(1), PV(0), S(2), PV(1), ... with
@@ -602,10 +654,20 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           // S(t)[g] = K_g Q(t)^T into slot g
           if (!mbar_wait(q_full, t & 1, wc) || !mbar_wait(&s_free[g], (t & 1) ^ 1, wc)) break;
           tc_fence_after();
-          if (g == 0)
-            MmaRun<0, kD / 16, 8, kStepKm, true>::go(tmem, tmem + kTmemK0, dQ, idesc_s, 0u);
-          else
-            MmaRun<0, kD / 16, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg, dQ, idesc_s, 0u);
+          // K steps 0..3 read the first 64 columns of Q and K, steps 4..7
+          // (d = 128) the second halves, 16 KB on (8 TMEM columns per step
+          // for key tile 0, which sits in TMEM).
+          constexpr long long kHalfStep = kHalfBytes >> 4;
+          if (g == 0) {
+            MmaRun<0, 4, 8, kStepKm, true>::go(tmem, tmem + C::kTmemK0, dQ, idesc_s, 0u);
+            if constexpr (D == 128)
+              MmaRun<0, 4, 8, kStepKm, true>::go(tmem, tmem + C::kTmemK0 + 32, dQ + kHalfStep, idesc_s, 1u);
+          } else {
+            MmaRun<0, 4, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg, dQ, idesc_s, 0u);
+            if constexpr (D == 128)
+              MmaRun<0, 4, kStepKm, kStepKm, false>::go(tmem + g * kTile, dKg + kHalfStep, dQ + kHalfStep, idesc_s,
+                                                       1u);
+          }
           mma_bf16_at<0, 0>(tmem + g * kTile, dAExt, dBExt, idesc_s, 1u);
           mma_commit(&s_full[g]);
           mma_commit(q_empty);
@@ -618,7 +680,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           // share^T: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB apart (SBO).
           // [V | 1]: MN-major; N block 0 = the value tile's 16 key rows, N block 1 (LBO
           // away) = the ones block, of which N = 64..79 are read.
-          MmaRun<0, kTile / 16, kStepSh, kStepV, false>::go(tmem + kTmemD, dShg, dVg, idesc_pv, 1u);
+          MmaRun<0, kTile / 16, kStepSh, kStepV, false>::go(tmem + C::kTmemD, dShg, dVg, idesc_pv, 1u);
+          if constexpr (D == 128)
+            MmaRun<0, kTile / 16, kStepSh, 128, false>::go(tmem + C::kTmemDHi, dShg, dVg_hi, idesc_pv_hi, 1u);
           mma_commit(&sh_free[g]);
           mma_commit(d_full);
         }
@@ -626,14 +690,15 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       mma_commit(&drain[g]);
       drain_wait(&drain[g], 0);
     }
-  } else if (wg == kSwG) {
+  } else if (wg == kG) {
     // -------------------------------------------------------------- epilogue
     // D -> acc through the copy engine: each warp stages its 32 rows x 32
     // columns as a 128B-swizzled box and issues a TMA add-reduction into acc
-    // (two boxes per tile); the row sum (column 64) goes by one atomic per row.
+    // (d / 32 boxes per tile: D's value columns, then DHi's at d = 128); the
+    // row sum (D column 64, acc column d) goes by one atomic per row.
     regs_dec_epi();
     const int quarter = warp % 4;
-    uint8_t *stage = smem + kSwOffStage + quarter * kStageBytes;
+    uint8_t *stage = smem + C::kOffStage + quarter * kStageBytes;
     uint8_t *srow = stage + lane * 128;
     const int swz = lane & 7;
     auto stage_box = [&](const float (&x)[32], int col0, int grow0) {
@@ -652,29 +717,42 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     };
     // D starts as zeros (d_free phase 0); after each drain it is zeroed again
     // before the buffer is handed back, so every PV MMA accumulates.
-    const uint32_t tdrow = tmem + kTmemD + ((uint32_t)(quarter * 32) << 16);
-    tmem_zero80(tdrow);
+    const uint32_t tdrow = tmem + C::kTmemD + ((uint32_t)(quarter * 32) << 16);
+    auto zero_d = [&]() {
+      tmem_zero80(tdrow);
+      if constexpr (D == 128) tmem_zero64(tdrow + (C::kTmemDHi - C::kTmemD));
+    };
+    zero_d();
     tmem_wait_st();
     release_tmem(d_free, lane);
     for (int t = 0; t < nt; ++t) {
       if (!mbar_wait(d_full, t & 1, wc)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + kTmemD + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t taddr = tmem + C::kTmemD + ((uint32_t)(quarter * 32) << 16);
       const int qrow0 = (w.q_tile0 + t) * kSwBQ + quarter * 32;   // first query row of this warp's box
-      const int grow0 = w.bh * Tp + qrow0;                        // its row in the [BH * Tp, 68] view of acc
+      const int grow0 = w.bh * Tp + qrow0;                        // its row in the [BH * Tp, d + 4] view of acc
       float a[32], rs;
       tmem_ld32(taddr, a);
       tmem_wait_ld_r(a);
       stage_box(a, 0, grow0);
       tmem_ld32(taddr + 32, a);
-      tmem_ld1(taddr + kD, rs);
+      tmem_ld1(taddr + 64, rs);
       tmem_wait_ld_r(a);
       tmem_wait_ld();
-      tmem_zero80(tdrow);
+      if constexpr (D == 128) {
+        stage_box(a, 32, grow0);
+        const uint32_t thi = taddr + (C::kTmemDHi - C::kTmemD);
+        tmem_ld32(thi, a);
+        tmem_wait_ld_r(a);
+        stage_box(a, 64, grow0);
+        tmem_ld32(thi + 32, a);
+        tmem_wait_ld_r(a);
+      }
+      zero_d();
       tmem_wait_st();
       release_tmem(d_free, lane);
-      stage_box(a, 32, grow0);
-      if (qrow0 + lane < T) atomicAdd(acc + ((size_t)grow0 + lane) * kAccStride + kD, rs);
+      stage_box(a, D - 32, grow0);
+      if (qrow0 + lane < T) atomicAdd(acc + ((size_t)grow0 + lane) * AS + D, rs);
     }
     if (lane == 0) bulk_wait_all();
   } else {
@@ -689,19 +767,23 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     uint8_t *sh_row = sSh + g * kShBytes + (row / 8) * 1024 + (row % 8) * 128;
     float ceps = eps;   // committed + eps: demand this key received from earlier queries
     if (g == 0) {
-      // this thread's key row (64 bf16 = 32 words; zeros past T) -> TMEM lane
-      uint32_t kr[32];
+      // this thread's key row (d bf16 = d / 2 words; zeros past T) -> TMEM
+      // lane, 32 columns at a time
       const int64_t key = (int64_t)kbase + row;
-      const uint4 *src = kglob + ((size_t)w.bh * T + key) * (kD * 2 / 16);
+      const uint4 *src = kglob + ((size_t)w.bh * T + key) * (D * 2 / 16);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 x = key < T ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
-        kr[4 * i] = x.x;
-        kr[4 * i + 1] = x.y;
-        kr[4 * i + 2] = x.z;
-        kr[4 * i + 3] = x.w;
+      for (int part = 0; part < D / 64; ++part) {
+        uint32_t kr[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x = key < T ? __ldg(src + 8 * part + i) : make_uint4(0u, 0u, 0u, 0u);
+          kr[4 * i] = x.x;
+          kr[4 * i + 1] = x.y;
+          kr[4 * i + 2] = x.z;
+          kr[4 * i + 3] = x.w;
+        }
+        tmem_st32(tmem + C::kTmemK0 + 32 * part + ((uint32_t)(quarter * 32) << 16), kr);
       }
-      tmem_st32(tmem + kTmemK0 + ((uint32_t)(quarter * 32) << 16), kr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -798,27 +880,27 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [BH, T, 64] bf16 viewed as a 3-D tensor; box = one tile of `rows` rows of
-// one head.  Rows past T read as zero.
-static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int rows = kTile) {
+// [BH, T, d] bf16 viewed as a 3-D tensor; box = 64 columns (one half) of
+// one tile of `rows` rows of one head.  Rows past T read as zero.
+static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d, int rows = kTile) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)T, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)T * kD * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)rows, 1};
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The fp32 accumulator [BH * Tp rows][68] as a 2-D tensor; box = 32 rows x
-// 32 columns, 128B swizzle: the sweep epilogue's reduction box.
-static bool make_acc_map(CUtensorMap *m, float *acc, int64_t rows) {
+// The fp32 accumulator [BH * Tp rows][d + 4] as a 2-D tensor; box = 32 rows
+// x 32 columns, 128B swizzle: the sweep epilogue's reduction box.
+static bool make_acc_map(CUtensorMap *m, float *acc, int64_t rows, int d) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kAccStride, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kAccStride * 4};
+  const cuuint64_t dims[2] = {(cuuint64_t)acc_stride(d), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)acc_stride(d) * 4};
   const cuuint32_t box[2] = {32, 32};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -827,62 +909,83 @@ static bool make_acc_map(CUtensorMap *m, float *acc, int64_t rows) {
 }
 
 cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bfloat16 *out, float *rowsum_out,
-                                 float *lse2_out, int BH, int T, cudaStream_t stream);
+                                 float *lse2_out, int BH, int T, int d, cudaStream_t stream);
 
 // Shared-memory opt-in and register-split check of one sweep instantiation.
-template <bool EARLIER>
+template <int D, bool EARLIER>
 static int prepare_sweep() {
-  if (cudaFuncSetAttribute(sweep_kernel<EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes) !=
+  using C = SwCfg<D>;
+  if (cudaFuncSetAttribute(sweep_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess)
     return DA_ERR_CUDA;
   // The sweep's warpgroups re-split the block's registers (setmaxnreg); a
   // split larger than what the block is launched with would never resolve,
   // so refuse to launch unless the compiled register count covers it.
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, sweep_kernel<EARLIER>) != cudaSuccess) return DA_ERR_CUDA;
-  if (fa.numRegs * kSwThreads < kSwRegsNeeded || fa.numRegs > kSwRegsDemand || fa.numRegs < kSwRegsEpi)
+  if (cudaFuncGetAttributes(&fa, sweep_kernel<D, EARLIER>) != cudaSuccess) return DA_ERR_CUDA;
+  if (fa.numRegs * C::kThreads < C::kRegsNeeded || fa.numRegs > kSwRegsDemand || fa.numRegs < kSwRegsEpi)
     return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
-int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
-                    float *demand_out, int BH, int T, HeadScale hs, float eps, bool earlier, float *lse2_ws,
-                    float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev) {
-  const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
-  if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;   // TMA row coordinates are 32-bit
-  CUtensorMap tq, tk, tv, ta;
-  if (!make_tile_map(&tq, q, BH, T) || !make_tile_map(&tk, k, BH, T) || !make_tile_map(&tv, v, BH, T) ||
-      !make_acc_map(&ta, acc, acc_rows))
+template <int D>
+static int prepare_fwd_bf16() {
+  if (cudaFuncSetAttribute(rowstats_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           RsCfg<D>::kSmemBytes) != cudaSuccess)
     return DA_ERR_CUDA;
+  int st = prepare_sweep<D, false>();
+  if (st == DA_OK) st = prepare_sweep<D, true>();
+  return st;
+}
+
+template <int D>
+static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &ta, const void *k, float *demand_out, int BH, int T, HeadScale hs,
+                             float eps, bool earlier, float *lse2_ws, float *acc, int *status, cudaStream_t stream,
+                             cudaEvent_t const *ev) {
   // The shared-memory opt-in is a per-device function attribute.
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
   if (dev >= 64 || !attr_done[dev]) {
-    if (cudaFuncSetAttribute(rowstats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRsSmemBytes) !=
-        cudaSuccess)
-      return DA_ERR_CUDA;
-    int st = prepare_sweep<false>();
-    if (st == DA_OK) st = prepare_sweep<true>();
+    const int st = prepare_fwd_bf16<D>();
     if (st != DA_OK) return st;
     if (dev < 64) attr_done[dev] = true;
   }
+  using C = SwCfg<D>;
   const int Tp = (int)t_pad(T);
   if (ev[0]) cudaEventRecord(ev[0], stream);
-  rowstats_kernel<<<rowstats_num_ctas(BH, T), kRsThreads, kRsSmemBytes, stream>>>(tq, tk, lse2_ws, acc, BH, T,
-                                                                                  Tp, hs, status);
+  rowstats_kernel<D><<<rowstats_num_ctas(BH, T), kRsThreads, RsCfg<D>::kSmemBytes, stream>>>(tq, tk, lse2_ws, acc,
+                                                                                            BH, T, Tp, hs, status);
   if (ev[1]) cudaEventRecord(ev[1], stream);
-  const int nsw = sweep_num_ctas(BH, T);
+  const int nsw = sweep_num_ctas(BH, T, D);
   const uint4 *kg = static_cast<const uint4 *>(k);
   if (earlier)
-    sweep_kernel<true><<<nsw, kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out, BH,
-                                                                  T, Tp, hs, eps, status);
+    sweep_kernel<D, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
+                                                                       BH, T, Tp, hs, eps, status);
   else
-    sweep_kernel<false><<<nsw, kSwThreads, kSwSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
-                                                                   BH, T, Tp, hs, eps, status);
+    sweep_kernel<D, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc,
+                                                                        demand_out, BH, T, Tp, hs, eps, status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
+                    float *demand_out, int BH, int T, int d, HeadScale hs, float eps, bool earlier, float *lse2_ws,
+                    float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev) {
+  const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
+  if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;   // TMA row coordinates are 32-bit
+  CUtensorMap tq, tk, tv, ta;
+  if (!make_tile_map(&tq, q, BH, T, d) || !make_tile_map(&tk, k, BH, T, d) || !make_tile_map(&tv, v, BH, T, d) ||
+      !make_acc_map(&ta, acc, acc_rows, d))
+    return DA_ERR_CUDA;
+  const int st = d == 128 ? launch_fwd_bf16_t<128>(tq, tk, tv, ta, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
+                                                   acc, status, stream, ev)
+                          : launch_fwd_bf16_t<64>(tq, tk, tv, ta, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
+                                                  acc, status, stream, ev);
+  if (st != DA_OK) return st;
   if (ev[2]) cudaEventRecord(ev[2], stream);
-  if (launch_finalize_bf16(acc, lse2_ws, reinterpret_cast<__nv_bfloat16 *>(out), rowsum_out, lse2_out, BH, T,
+  if (launch_finalize_bf16(acc, lse2_ws, reinterpret_cast<__nv_bfloat16 *>(out), rowsum_out, lse2_out, BH, T, d,
                            stream) != cudaSuccess)
     return DA_ERR_CUDA;
   if (ev[3]) cudaEventRecord(ev[3], stream);

@@ -40,16 +40,20 @@ def _sched_rowstats(BH, T):
     return np.array(rows, dtype=np.int32).reshape(-1, 4)
 
 
-def _sched_sweep(BH, T):
+def _sched_sweep(BH, T, d=64):
+    # spans of 384 keys (three key tiles) at d = 64, 256 (two) at d = 128;
+    # heads grouped so their fp32 accumulators (Tp rows of d + 4) total ~64 MB
+    span_keys = 384 if d == 64 else 256
     Tp = -(-T // 256) * 256
-    nqt, nspan = Tp // 128, -(-Tp // 384)
-    hg = min(BH, max(1, (64 << 20) // (Tp * 68 * 4)))
+    nqt, nspan = Tp // 128, -(-Tp // span_keys)
+    hg = min(BH, max(1, (64 << 20) // (Tp * (d + 4) * 4)))
     rows = []
     for h0 in range(0, BH, hg):
         heads = list(range(h0, min(BH, h0 + hg)))
         for span in range(nspan):
             for bh in heads:
-                rows.append((bh, 3 * span, nqt - 3 * span, 384 * span))
+                q0 = span_keys * span // 128
+                rows.append((bh, q0, nqt - q0, span_keys * span))
     return np.array(rows, dtype=np.int32).reshape(-1, 4)
 
 
@@ -57,17 +61,19 @@ def _sched_sweep(BH, T):
 def test_tile_schedules_bit_exact(lib, BH, T):
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 0), _sched_rowstats(BH, T))
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 1), _sched_sweep(BH, T))
+    assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 2), _sched_sweep(BH, T, 128))
 
 
-def test_tile_schedules_cover_triangle_once():
+@pytest.mark.parametrize("kernel,tiles_per_span", [(1, 3), (2, 2)])
+def test_tile_schedules_cover_triangle_once(kernel, tiles_per_span):
     # every (head, key, query) pair with key <= query < Tp is visited by exactly
-    # one sweep CTA (128-key tiles x 128-query tiles), every 128-row query tile
-    # by one row-statistics CTA
+    # one sweep CTA (128-key tiles x 128-query tiles; kernel 1: d = 64, 2:
+    # d = 128), every 128-row query tile by one row-statistics CTA
     BH, T = 3, 1000
     Tp = 1024
     seen = {}
-    for bh, q0, n, key0 in b.dilution_attn_debug_tile_schedule(BH, T, 1):
-        for kt in range(key0 // 128, key0 // 128 + 3):
+    for bh, q0, n, key0 in b.dilution_attn_debug_tile_schedule(BH, T, kernel):
+        for kt in range(key0 // 128, key0 // 128 + tiles_per_span):
             for qt in range(q0, q0 + n):
                 if kt * 128 < Tp and kt * 128 <= qt * 128 + 127:
                     seen[(bh, kt, qt)] = seen.get((bh, kt, qt), 0) + 1
@@ -89,9 +95,12 @@ def test_tile_mask_bit_exact(lib, T, qt, kt):
 
 def test_workspace_sizes(lib):
     Tp = 16384
-    want = 256 + 48 * Tp * 4
-    want = -(-want // 256) * 256 + 48 * Tp * 68 * 4
-    assert b.dilution_attn_fwd_workspace_size(4, 12, 16384, 64, b.DA_BF16) == want
+    for d in (64, 128):
+        want = 256 + 48 * Tp * 4
+        want = -(-want // 256) * 256 + 48 * Tp * (d + 4) * 4
+        assert b.dilution_attn_fwd_workspace_size(4, 12, 16384, d, b.DA_BF16) == want
+    assert b.dilution_attn_fwd_workspace_size(4, 12, 16384, 96, b.DA_BF16) == 0   # unsupported d
+    assert b.dilution_attn_bwd_workspace_size(1, 1, 100, 128, 1) > 100 * 128 * 4
     assert b.dilution_attn_fwd_workspace_size(0, 12, 16384, 64, b.DA_BF16) == 256
     assert b.dilution_attn_decode_workspace_size(8, 12, 131328, 64) > 8 * 12 * 131328 * 4
 
@@ -111,7 +120,9 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, eps=float("nan")) == b.DA_ERR_INVALID
     assert _fwd(lib, tau=-0.5) == b.DA_ERR_INVALID
     assert _fwd(lib, tau=float("inf")) == b.DA_ERR_INVALID
-    assert _fwd(lib, d=128) == b.DA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=96) == b.DA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256) == b.DA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=128, ws=None) == b.DA_ERR_WORKSPACE      # d = 128 is supported
     assert _fwd(lib, eps=1e-20) == b.DA_ERR_UNSUPPORTED        # bf16 path: eps >= 1e-18
     assert _fwd(lib, eps=1e-20, dtype=0, ws=None) == b.DA_ERR_WORKSPACE   # fp32 path accepts it
     assert _fwd(lib, T=(1 << 24) + 1) == b.DA_ERR_UNSUPPORTED
@@ -149,7 +160,8 @@ def test_bwd_argument_validation(lib):
     def bwd(eps=1e-6, d=64, q=FAKE, ws=FAKE, wsb=1 << 30):
         return lib.dilution_attn_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 32, d, 1.0, eps, 1, ws, wsb, None)
     assert bwd(eps=0.0) == b.DA_ERR_INVALID
-    assert bwd(d=128) == b.DA_ERR_UNSUPPORTED
+    assert bwd(d=96) == b.DA_ERR_UNSUPPORTED
+    assert bwd(d=128, ws=None) == b.DA_ERR_WORKSPACE
     assert bwd(q=None) == b.DA_ERR_INVALID
     assert bwd(ws=None) == b.DA_ERR_WORKSPACE
     assert b.dilution_attn_bwd_workspace_size(4, 12, 16384, 64, 1) > 4 * 12 * 16384 * 64 * 4
