@@ -20,7 +20,7 @@ def run_fwd(q, k, v, tau=1.0, eps=1e-6):
     lse2 = torch.empty(B, H, T, device=DEV)
     rs = torch.empty(B, H, T, device=DEV)
     dem = torch.empty(B, H, T, device=DEV)
-    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, 64, b._dtype_code(q)), dtype=torch.uint8,
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, q.shape[-1], b._dtype_code(q)), dtype=torch.uint8,
                      device=DEV)
     b.dilution_attn_fwd(q, k, v, out, lse2, rs, dem, tau=tau, eps=eps, workspace=ws)
     assert b.dilution_attn_get_error(ws) == b.DA_OK

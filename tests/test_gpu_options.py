@@ -24,7 +24,7 @@ def run_fwd_ex(q, k, v, tau=1.0, tau_bh=None, eps=1e-6, flags=0):
     B, H, T, _ = q.shape
     out = torch.empty_like(q)
     side = [torch.empty(B, H, T, device=DEV) for _ in range(3)]
-    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, 64, b._dtype_code(q)), dtype=torch.uint8,
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, q.shape[-1], b._dtype_code(q)), dtype=torch.uint8,
                      device=DEV)
     b.dilution_attn_fwd_ex(q, k, v, out, *side, tau=tau, tau_bh=tau_bh, eps=eps, flags=flags, workspace=ws)
     assert b.dilution_attn_get_error(ws) == b.DA_OK
