@@ -50,6 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-train", action="store_true", help="skip the forward+backward training-step timing")
+    ap.add_argument("--no-d128", action="store_true", help="skip the head-dimension-128 forward timing")
     ap.add_argument("--decode-ctx", type=int, default=None, help="cached tokens per sequence (default: the workload's)")
     ap.add_argument("--decode-steps", type=int, default=None, help="decode steps timed (default: the workload's)")
     ap.add_argument("--decode-only", action="store_true", help="skip the forward measurement")
@@ -247,6 +248,43 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------ our arm
+def run_fwd_workload(torch, b, inputs, dev, name, steps, warmup, peaks):
+    """Forward of another workload (d = 128): K timed steps with the three
+    kernels' events; returns TFLOP/s, per-kernel ms and the sweep's and row
+    statistics' fractions of the bf16 peak."""
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.make_qkv(w.B, w.H, w.T, w.d, q_std=w.q_std, pairs=w.pairs, seed=w.seed, dtype=w.dtype,
+                              device=dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(w.B, w.H, w.T, w.d, b._dtype_code(q)), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(warmup):
+        b.dilution_attn_fwd(q, k, v, out, workspace=ws)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        b.dilution_attn_fwd_with_events(q, k, v, out, workspace=ws, events=evs[i], check=False)
+    t1.record()
+    torch.cuda.synchronize()
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+    ms = t0.elapsed_time(t1) / steps
+    kern = {n_: statistics.mean(e4[j].elapsed_time(e4[j + 1]) for e4 in evs)
+            for j, n_ in enumerate(("rowstats", "sweep", "finalize"))}
+    fl = fwd_flops(w.B, w.H, w.T, w.d)
+    sw = sweep_flops(w.B, w.H, w.T, w.d)
+    peak = peaks["bf16_tflops"]
+    res = {"workload": name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "steps": steps, "ms_per_step": ms,
+           "tflops": fl / (ms * 1e-3) / 1e12, "pct_of_bf16_peak": 100.0 * fl / (ms * 1e-3) / 1e12 / peak,
+           "tokens_per_s": w.B * w.T / (ms * 1e-3), "kernels_ms": kern,
+           "sweep_frac": sw / (kern["sweep"] * 1e-3) / 1e12 / peak,
+           "rowstats_frac": (fl - sw) / (kern["rowstats"] * 1e-3) / 1e12 / peak, "gpu_launches": 3 * steps}
+    del q, k, v, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_decode(torch, b, inputs, dev, warmup, peaks, ctx=None, n_steps=None):
     """8 independent 131072-token caches (built by an untimed prefill), 256 steps."""
     w = inputs.WORKLOADS["decode_bf16_ctx131072"]
@@ -501,6 +539,9 @@ def run_ours(args):
 
     del q, k, v, out, ws
     torch.cuda.empty_cache()
+    if not args.no_d128 and args.workload != "fwd_bf16_t16384_d128":
+        line["fwd_d128"] = run_fwd_workload(torch, b, inputs, dev, "fwd_bf16_t16384_d128", max(3, min(K, 20)),
+                                            max(3, W), peaks)
     if not args.no_train:
         line["train_step"] = run_train(torch, b, inputs, dev)
     if not args.no_decode:

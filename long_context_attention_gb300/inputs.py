@@ -55,6 +55,9 @@ WORKLOADS = {
                                       tau_scale=8.0, extra={"steps": 256}),
     # training step shape: all N(0,1), upstream gradient N(0,1).
     "train_bf16_t16384": Workload("train_bf16_t16384", 4, 12, 16384, 64, "bf16", 1.0, 0, 4),
+    # the headline shape at head dimension 128 (the head size of the focal-
+    # attention models), same distributions and planted pairs.
+    "fwd_bf16_t16384_d128": Workload("fwd_bf16_t16384_d128", 4, 12, 16384, 128, "bf16", 1.5, 128, 5),
 }
 
 
