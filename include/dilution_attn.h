@@ -27,9 +27,11 @@
  *     before anything is enqueued; kernel-side errors (a bounded wait that
  *     timed out) are written to a status word at the start of the workspace
  *     and read back with dilution_attn_get_error().
- *   - Supported: d == 64; dtype DA_F32 (fp32 in/out, fp32 SIMT arithmetic)
- *     or DA_BF16 (bf16 in/out, bf16 tensor-core products, fp32 accumulation
- *     and fp32 softmax/demand arithmetic).  tau >= 0 and finite; eps > 0 and
+ *   - Supported: d == 64 or d == 128 (other head sizes return
+ *     DA_ERR_UNSUPPORTED and a workspace size of 0); dtype DA_F32 (fp32
+ *     in/out, fp32 SIMT arithmetic) or DA_BF16 (bf16 in/out, bf16
+ *     tensor-core products, fp32 accumulation and fp32 softmax/demand
+ *     arithmetic).  tau >= 0 and finite; eps > 0 and
  *     finite (eps = 0 would make masked and underflowed entries 0/0).
  *     B, H, T >= 0; a call with B*H*T == 0 does nothing and returns DA_OK.
  *     T <= DA_MAX_T.  The DA_BF16 forward needs eps >= 1e-18 (it forms one
@@ -49,7 +51,7 @@ extern "C" {
 /* Status codes returned by every call. */
 #define DA_OK              0
 #define DA_ERR_INVALID     1   /* bad argument: null/misaligned pointer, negative size, eps <= 0, ... */
-#define DA_ERR_UNSUPPORTED 2   /* valid but not implemented: d != 64, T > DA_MAX_T, ...          */
+#define DA_ERR_UNSUPPORTED 2   /* valid but not implemented: d not 64 or 128, T > DA_MAX_T, ...   */
 #define DA_ERR_CUDA        3   /* a CUDA runtime call failed (launch, tensor-map encode, copy)   */
 #define DA_ERR_TIMEOUT     4   /* a kernel's bounded wait expired; results are not valid         */
 #define DA_ERR_WORKSPACE   5   /* workspace pointer null or smaller than the *_workspace_size    */
@@ -255,8 +257,8 @@ int dilution_attn_debug_last_timeout(void *workspace, int32_t *out);
  *
  * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's
  * kernels for a problem of BH = B*H heads and T tokens.  kernel = 0 (row
- * statistics, 128-row query tiles) or 1 (demand sweep, 128-row query tiles,
- * 384-key spans).  For each CTA index c (in launch order), writes 4 int32 to
+ * statistics, 128-row query tiles), 1 (demand sweep at d = 64: 128-row query
+ * tiles, 384-key spans) or 2 (demand sweep at d = 128: 256-key spans).  For each CTA index c (in launch order), writes 4 int32 to
  * out[4c..4c+3]: head index, first query tile, number of query tiles (row
  * stats: the query tiles it owns; sweep: the query tiles it walks), first key
  * (sweep) or 0.  Returns the number of CTAs; if cap (in
