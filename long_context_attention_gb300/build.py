@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdilution_attn.so")
 
-SOURCES = ["capi.cu", "fwd_f32.cu", "fwd_bf16.cu", "decode.cu", "bwd.cu"]
+SOURCES = ["capi.cu", "fwd_f32.cu", "fwd_bf16.cu", "decode.cu", "bwd.cu", "bwd_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

@@ -1,0 +1,814 @@
+// Tensor-core backward of dilution attention (bf16, d = 64).
+//
+// Gradients of sum(dout * out) through the operator of "DilutionAttention
+// v0.1.0 · results", section "The operator" (the page states only that exact
+// gradients exist; the chain rule is written out in bwd.cu).  Per (batch,
+// head), with g = dout, r = share, R_j = sum_k r_jk, D = committed + p + eps
+// (committed + eps for the earlier-demand-only variant):
+//   dA'_jk = g_j . v_k - delta_j,          delta_j = g_j . out_j
+//   dr_jk  = dA'_jk / R_j
+//   dC_jk  = -dr_jk p_jk / D_jk^2          dp_jk = direct_jk + sum_{i > j} dC_ik
+//   direct = dr (committed + eps) / D^2    (dr / D for the variant)
+//   rho_j  = sum_k p_jk dp_jk,             ds_jk = p_jk (dp_jk - rho_j)
+//   dV_k   = sum_j (r_jk / R_j) g_j,  dK_k = c sum_j ds_jk q_j,  dQ_j = c sum_k ds_jk k_k
+//
+// Every pair (j, k) needs the forward running sum down its key column
+// (committed) and the reverse running sum of dC, and rho needs a reduction
+// over all keys before any ds exists.  The passes:
+//   F   the forward demand sweep again (fwd_bf16.cu) from the given lse2; it
+//       writes committed + eps of every key at every 32-query chunk start
+//       (demand checkpoints) and the forward accumulators (numerator, R);
+//   rows  1/R_j and delta_j = g_j . out_j from those accumulators;
+//   B1  key-major, query chunks in reverse order: S = K Q^T and dA' = V G^T -
+//       delta on tcgen05; one thread per key rebuilds committed inside each
+//       chunk from its checkpoint, carries sum_{i > j} dC in a register, and
+//       writes it at every chunk start (reverse checkpoints); rho_j is summed
+//       over the key tile's lanes and added to rho;
+//   KV  key-major: with both checkpoints every chunk is independent; the
+//       threads write A^T = r / R and ds^T (bf16, K-major) to shared memory
+//       and tcgen05 accumulates dV += A^T G and dK += ds^T Q in TMEM;
+//   Q   query-major: for each key tile the threads write ds (MN-major) and
+//       tcgen05 accumulates dQ += ds K in TMEM.
+// S and dA' are formed 64 queries at a time (N = 64) so two CTAs fit an SM;
+// -lse2 / c2 and -delta ride in a fifth K step of their products (the
+// extension operands of the forward sweep).  Every wait is bounded.
+#include "da_internal.h"
+#include "da_ptx.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace da {
+
+namespace {
+
+constexpr int kBtThreads = 192;                    // 4 demand warps, producer, MMA issuer
+constexpr uint32_t kTile16 = kTile * 64 * 2;       // 128 rows x 64 bf16, 128B swizzle
+constexpr uint32_t kHalf16 = 64 * 64 * 2;          // 64 rows x 64 bf16
+constexpr uint32_t kExt128 = 128 * 16 * 2;         // extension operand, 128 rows
+constexpr uint32_t kExt64 = 64 * 16 * 2;           // extension operand, 64 rows
+
+__device__ __forceinline__ uint64_t kdesc(const uint8_t *tile, int kstep) {
+  return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
+}
+
+__device__ __forceinline__ void drain_wait_bt(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 100ull * 1000ull * 1000ull) break;
+  }
+}
+
+__device__ __forceinline__ void release_bt(uint64_t *bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Extension operand rows (K-major, no swizzle: 8-row groups of 256 bytes,
+// each the core matrix of K 0..7 then that of K 8..15): row q = [hi mid lo 0
+// ...] of v, the bf16 parts of an fp32 value (24 significant bits).  Rows of
+// queries past T carry a large finite negative value (their bids vanish).
+__device__ __forceinline__ void put_ext_row(uint8_t *ext, int q, float v) {
+  v = fmaxf(v, -3.0e38f);
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+  *reinterpret_cast<uint4 *>(ext + (q >> 3) * 256 + (q & 7) * 16) =
+      make_uint4((uint32_t)__bfloat16_as_ushort(h) | ((uint32_t)__bfloat16_as_ushort(m) << 16),
+                 (uint32_t)__bfloat16_as_ushort(l), 0u, 0u);
+}
+
+// A_ext: [1 1 1 0 ...] for every one of 128 rows; its zero half K 8..15 too.
+__device__ __forceinline__ void fill_ones_ext(uint8_t *ext, int tid, int nthreads) {
+  for (int e = tid; e < (int)(kExt128 / 16); e += nthreads) {
+    const bool k_lo = (e & 15) < 8;
+    reinterpret_cast<uint4 *>(ext)[e] = k_lo ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- prep / rows
+// -lse2 for the sweep (rows past T: -inf) and zeroed forward accumulators.
+__global__ void bwdtc_prep(const float *__restrict__ lse2, float *__restrict__ nlse2, float *__restrict__ acc,
+                           int BH, int T, int Tp) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= (int64_t)BH * Tp) return;
+  const int64_t bh = row / Tp, i = row % Tp;
+  nlse2[row] = i < T ? -lse2[bh * T + i] : -INFINITY;
+  float4 *ar = reinterpret_cast<float4 *>(acc + row * acc_stride(64));
+#pragma unroll
+  for (int t = 0; t < acc_stride(64) / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// 1/R_j, delta_j = g_j . out_j (out = numerator / R) and rho_j = 0; 16 threads
+// per row.  Rows past T get zeros, so their dr vanish.
+__global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *__restrict__ g,
+                           float *__restrict__ rinv, float *__restrict__ delta, float *__restrict__ rho, int BH,
+                           int T, int Tp) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = t / 16;
+  const int part = (int)(t % 16);
+  const bool live = row < (int64_t)BH * Tp;
+  const int64_t bh = live ? row / Tp : 0, i = live ? row % Tp : 0;
+  float dot = 0.f, inv = 0.f;
+  if (live && i < T) {
+    const float *ar = acc + row * acc_stride(64);
+    inv = 1.f / ar[64];
+    const float4 a = reinterpret_cast<const float4 *>(ar)[part];
+    const uint2 gg = reinterpret_cast<const uint2 *>(g + (bh * T + i) * 64)[part];
+    const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.x));
+    const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.y));
+    dot = (a.x * g01.x + a.y * g01.y) + (a.z * g23.x + a.w * g23.y);
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if (live && part == 0) {
+    rinv[row] = inv;
+    delta[row] = dot * inv;
+    rho[row] = 0.f;
+  }
+}
+
+// ------------------------------------------------------------- chunk engine
+// One key (this thread) against 32 consecutive queries q0 .. q0 + 31 of its
+// column.  In: S' (q.k - lse2 / c2) and dA' (g.v - delta) from TMEM, the
+// chunk's demand checkpoint cpe = committed + eps before q0, 1/R of the
+// queries (shared memory).  Forms, for each query in causal order, p,
+// e = committed + eps before the query, D, then
+//   t = dr / D,  dir = t e / D (t for EARLIER),  dC = -t p / D,
+// leaving p in P, dir in A and dC in E (and, with AT, A = r / R packed as
+// bf16 pairs).  MASK zeroes keys after the query (row_eff > column).
+template <bool MASK, bool EARLIER, bool AT>
+__device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], float (&E)[32], uint32_t (&at)[16],
+                                              int row_eff, int col0, float c2, float cpe, const float *rinv_q) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float p = ex2_approx(P[i] * c2);
+    if (MASK && row_eff > col0 + i) p = 0.f;
+    P[i] = p;
+    E[i] = cpe;   // committed + eps before query i
+    cpe += p;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float e0 = E[2 * i], e1 = E[2 * i + 1];
+    const float p0 = P[2 * i], p1 = P[2 * i + 1];
+    const float d0 = EARLIER ? e0 : e0 + p0, d1 = EARLIER ? e1 : e1 + p1;
+    const float rr = rcp_approx(d0 * d1);
+    const float i0 = d1 * rr, i1 = d0 * rr;   // 1/d0, 1/d1
+    const float2 rq = *reinterpret_cast<const float2 *>(rinv_q + col0 + 2 * i);
+    float dr0 = A[2 * i] * rq.x, dr1 = A[2 * i + 1] * rq.y;
+    if (MASK && row_eff > col0 + 2 * i) dr0 = 0.f;
+    if (MASK && row_eff > col0 + 2 * i + 1) dr1 = 0.f;
+    const float t0 = dr0 * i0, t1 = dr1 * i1;
+    A[2 * i] = EARLIER ? t0 : t0 * e0 * i0;
+    A[2 * i + 1] = EARLIER ? t1 : t1 * e1 * i1;
+    E[2 * i] = -t0 * p0 * i0;
+    E[2 * i + 1] = -t1 * p1 * i1;
+    if (AT) at[i] = pack_bf16x2(p0 * i0 * rq.x, p1 * i1 * rq.y);   // A = r / R
+  }
+}
+
+// Reverse walk of one chunk: dp = dir + grev, grev += dC (queries in reverse
+// order); dp is left in A.
+__device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[32], float &grev) {
+#pragma unroll
+  for (int i = 31; i >= 0; --i) {
+    A[i] += grev;
+    grev += E[i];
+  }
+}
+
+// Sum of X over the 32 lanes, lane l ending with the total of X[l].
+__device__ __forceinline__ float lane_transpose_sum(float (&X)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const bool hi = (lane & off) != 0;
+      const float send = hi ? X[i] : X[i + off];
+      const float keep = hi ? X[i + off] : X[i];
+      X[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return X[0];
+}
+
+// ------------------------------------------------------------ key-major passes
+// One CTA per (head, 128-key tile), two per SM.  Warps 0-3: one thread per
+// key; warp 4: TMA and the per-query extension rows; warp 5: MMA issuer.
+// MODE 0 (B1) walks the key tile's 64-query half tiles from the last one
+// back to the diagonal, MODE 1 (KV) forward.
+constexpr int kModeB1 = 0, kModeKV = 1;
+
+template <int MODE>
+struct KeyCfg {
+  static constexpr uint32_t kOffK = 0, kOffV = kTile16;
+  static constexpr uint32_t kOffQh = 2 * kTile16;                 // [2] half tiles of Q
+  static constexpr uint32_t kOffGh = kOffQh + 2 * kHalf16;        // [2] half tiles of dout
+  static constexpr uint32_t kOffAExt = kOffGh + 2 * kHalf16;
+  static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // [2] -lse2 / c2 rows
+  static constexpr uint32_t kOffBExtA = kOffBExtS + 2 * kExt64;   // [2] -delta rows
+  static constexpr uint32_t kOffRinv = kOffBExtA + 2 * kExt64;    // [2][64] fp32
+  static constexpr uint32_t kOffRho = kOffRinv + 2 * 64 * 4;      // [2][64] fp32 (KV)
+  static constexpr uint32_t kOffRed = kOffRho + 2 * 64 * 4;       // [2][4][64] fp32 (B1)
+  static constexpr uint32_t kOffAT = kOffRed + 2 * 4 * 64 * 4;    // A^T, K-major (KV)
+  static constexpr uint32_t kOffDsT = kOffAT + kTile16;           // ds^T, K-major (KV)
+  static constexpr uint32_t kOffBar = MODE == kModeKV ? kOffDsT + kTile16 : kOffAT;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + re-alignment slack
+  static_assert(kOffAT % 1024 == 0, "swizzled operands");
+};
+
+template <int MODE, bool EARLIER>
+__global__ void __launch_bounds__(kBtThreads, 2)
+    bwdtc_key_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmGh,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const float *__restrict__ nlse2, const float *__restrict__ delta,
+                     const float *__restrict__ rinv, float *__restrict__ rho, const float *__restrict__ cchk,
+                     float *__restrict__ gchk, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int BH,
+                     int T, int Tp, HeadScale hs, float c_scalar, int *status) {
+  using C = KeyCfg<MODE>;
+  extern __shared__ uint8_t bt_smem_raw[];
+  uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
+  uint8_t *sK = smem + C::kOffK, *sV = smem + C::kOffV;
+  uint8_t *sAExt = smem + C::kOffAExt;
+  float *sRinv = reinterpret_cast<float *>(smem + C::kOffRinv);
+  float *sRho = reinterpret_cast<float *>(smem + C::kOffRho);
+  float *sRed = reinterpret_cast<float *>(smem + C::kOffRed);
+  uint8_t *sAT = smem + C::kOffAT, *sDsT = smem + C::kOffDsT;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *kv_full = bars;
+  uint64_t *in_full = bars + 1;      // [2] half tile b loaded and its rows written
+  uint64_t *in_empty = bars + 3;     // [2] its products done and its rows read
+  uint64_t *s_full = bars + 5;       // [2] S / dA' slots (B1: double, KV: slot 0)
+  uint64_t *s_free = bars + 7;       // [2]
+  uint64_t *w_full = bars + 9;       // KV: A^T, ds^T written;  B1: [2] partial rho written
+  uint64_t *w_free = bars + 11;      // KV: dV, dK products done; B1: [2] partial rho read
+  uint64_t *fin = bars + 13;
+  uint64_t *drain = bars + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.x % BH, kt = blockIdx.x / BH;   // the tiles with the most half tiles first
+  const int NH = Tp / 64, hq0 = 2 * kt, n = NH - hq0, NC = Tp / 32;
+  // as in the forward sweep: a scale of at least 1e-30 keeps -inf logits at -inf
+  const float c2 = fmaxf(head_c2(hs, bh, nullptr), 1e-30f);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&in_full[b], 2);    // the tiles' bytes + the producer's rows
+      mbar_init(&in_empty[b], 5);   // the issuer's commit + the four key warps
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], 4);
+      mbar_init(&w_full[b], MODE == kModeKV ? 4 : 4);
+      mbar_init(&w_free[b], MODE == kModeKV ? 1 : 2);
+    }
+    mbar_init(fin, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  fill_ones_ext(sAExt, threadIdx.x, kBtThreads);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, status};
+  auto half_of = [&](int u) { return MODE == kModeB1 ? NH - 1 - u : hq0 + u; };
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQh);
+      prefetch_tmap(&tmGh);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(kv_full, 2 * kTile16);
+      tma_load_3d(sK, &tmK, kv_full, 0, kt * kTile, bh);
+      tma_load_3d(sV, &tmV, kv_full, 0, kt * kTile, bh);
+    }
+    int issued = 0;
+    for (int u = 0; u < n; ++u) {
+      const int b = u & 1, h = half_of(u);
+      if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&in_full[b], 2 * kHalf16);
+        tma_load_3d(smem + C::kOffQh + b * kHalf16, &tmQh, &in_full[b], 0, h * 64, bh);
+        tma_load_3d(smem + C::kOffGh + b * kHalf16, &tmGh, &in_full[b], 0, h * 64, bh);
+      }
+      ++issued;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int qq = lane + 32 * j;
+        const size_t idx = (size_t)bh * Tp + h * 64 + qq;
+        put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, __ldg(nlse2 + idx) / c2);
+        put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -__ldg(delta + idx));
+        sRinv[b * 64 + qq] = __ldg(rinv + idx);
+        if (MODE == kModeKV) sRho[b * 64 + qq] = rho[idx];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&in_full[b]);
+    }
+    if (lane == 0 && *abort_flag) {
+      drain_wait_bt(kv_full, 0);
+      for (int u = (issued > 2 ? issued - 2 : 0); u < issued; ++u) drain_wait_bt(&in_full[u & 1], (u >> 1) & 1);
+    }
+  } else if (warp == 5) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr long long kStepKm = 2;                       // K-major: +32 bytes per K step
+      constexpr long long kStepMn = 128;                     // MN-major: +16 rows (2 KB) per K step
+      const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
+      const uint32_t idesc_kv = idesc_bf16(kTile, 64, false, true);
+      const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
+      const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
+      bool ok = mbar_wait(kv_full, 0, wc);
+      if (ok) tc_fence_after();
+      for (int u = 0; ok && u <= n; ++u) {
+        if (u < n) {
+          const int b = u & 1;
+          const int slot = MODE == kModeB1 ? b : 0;
+          const uint32_t par_free = MODE == kModeB1 ? (((u >> 1) & 1) ^ 1) : ((u & 1) ^ 1);
+          if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(&s_free[slot], par_free, wc)) break;
+          tc_fence_after();
+          const uint64_t dQh = kdesc(smem + C::kOffQh + b * kHalf16, 0);
+          const uint64_t dGh = kdesc(smem + C::kOffGh + b * kHalf16, 0);
+          const uint64_t dBS = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtS + b * kExt64), 128, 256);
+          const uint64_t dBA = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtA + b * kExt64), 128, 256);
+          const uint32_t tS = tmem + slot * 64, tA = tmem + 128 + slot * 64;
+          const uint32_t tSk = MODE == kModeB1 ? tS : tmem, tAk = MODE == kModeB1 ? tA : tmem + 64;
+          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tSk, dK, dQh, idesc_s, 0u);
+          mma_bf16_at<0, 0>(tSk, dAExt, dBS, idesc_s, 1u);
+          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tAk, dV, dGh, idesc_s, 0u);
+          mma_bf16_at<0, 0>(tAk, dAExt, dBA, idesc_s, 1u);
+          mma_commit(&s_full[slot]);
+          if (MODE == kModeB1) mma_commit(&in_empty[b]);
+        }
+        if (MODE == kModeKV && u >= 1) {
+          // dV += A^T G, dK += ds^T Q for half tile u - 1 (its operands: G and Q
+          // of buffer bp as MN-major B, 16 queries = 2 KB per K step)
+          const int up = u - 1, bp = up & 1;
+          if (!mbar_wait(&w_full[0], up & 1, wc)) break;
+          tc_fence_after();
+          const uint64_t dGmn = smem_desc(smem_u32(smem + C::kOffGh + bp * kHalf16), kHalf16, 1024);
+          const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * kHalf16), kHalf16, 1024);
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + 128, kdesc(sAT, 0), dGmn, idesc_kv, up > 0 ? 1u : 0u);
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + 192, kdesc(sDsT, 0), dQmn, idesc_kv, up > 0 ? 1u : 0u);
+          mma_commit(&w_free[0]);
+          mma_commit(&in_empty[bp]);
+          if (u == n) mma_commit(fin);
+        }
+      }
+      mma_commit(drain);
+      drain_wait_bt(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------ key threads
+    const int row = warp * 32 + lane;
+    const int key = kt * kTile + row;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const int swz = row & 7;
+    uint8_t *at_row = sAT + (row >> 3) * 1024 + (row & 7) * 128;
+    uint8_t *ds_row = sDsT + (row >> 3) * 1024 + (row & 7) * 128;
+    float grev = 0.f;   // B1: sum of dC over the queries after the current one
+    bool ok = true;
+    for (int u = 0; ok && u < n; ++u) {
+      const int b = u & 1, h = half_of(u);
+      const int slot = MODE == kModeB1 ? b : 0;
+      const int q0h = h * 64;
+      const bool need_mask = kt * kTile + kTile - 1 > q0h;
+      const int row_eff = key - q0h;
+      const uint32_t par_full = MODE == kModeB1 ? ((u >> 1) & 1) : (u & 1);
+      if (!mbar_wait(&s_full[slot], par_full, wc)) break;
+      tc_fence_after();
+      if (MODE == kModeKV && !mbar_wait(&w_free[0], (u & 1) ^ 1, wc)) break;   // A^T, ds^T of u - 1 consumed
+      if (MODE == kModeB1 && !mbar_wait(&w_free[b], ((u >> 1) & 1) ^ 1, wc)) break;   // partial rho buffer b read
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = MODE == kModeB1 ? 1 - cc : cc;   // B1 walks the chunks backwards
+        float P[32], A[32], E[32];
+        uint32_t at[16];
+        const uint32_t tS = (MODE == kModeB1 ? tmem + slot * 64 : tmem) + lanes + 32 * c;
+        const uint32_t tA = (MODE == kModeB1 ? tmem + 128 + slot * 64 : tmem + 64) + lanes + 32 * c;
+        tmem_ld32(tS, P);
+        tmem_ld32(tA, A);
+        tmem_wait_ld_r(P);
+        tmem_wait_ld_r(A);
+        if (cc == 1) release_bt(&s_free[slot], lane);
+        const size_t ck = ((size_t)bh * NC + (q0h / 32 + c)) * Tp + key;
+        const float cpe = __ldg(cchk + ck);
+        const float *rq = sRinv + b * 64;
+        if (MODE == kModeB1) {
+          if (need_mask) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+          else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+          gchk[ck] = grev;   // sum of dC after the chunk
+          bwd_chunk_rev(A, E, grev);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) P[i] *= A[i];   // p dp
+          sRed[(b * 4 + warp) * 64 + 32 * c + lane] = lane_transpose_sum(P, lane);
+        } else {
+          if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+          else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+          float g0 = __ldg(gchk + ck);
+          bwd_chunk_rev(A, E, g0);
+          uint32_t ds[16];
+          const float *ro = sRho + b * 64 + 32 * c;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 r2 = *reinterpret_cast<const float2 *>(ro + 2 * i);
+            ds[i] = pack_bf16x2(P[2 * i] * (A[2 * i] - r2.x), P[2 * i + 1] * (A[2 * i + 1] - r2.y));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int piece = (4 * c + j) ^ swz;
+            *reinterpret_cast<uint4 *>(at_row + piece * 16) = make_uint4(at[4 * j], at[4 * j + 1], at[4 * j + 2], at[4 * j + 3]);
+            *reinterpret_cast<uint4 *>(ds_row + piece * 16) = make_uint4(ds[4 * j], ds[4 * j + 1], ds[4 * j + 2], ds[4 * j + 3]);
+          }
+        }
+      }
+      if (MODE == kModeKV) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&w_full[0]);
+          mbar_arrive(&in_empty[b]);
+        }
+      } else {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&w_full[b]);
+          mbar_arrive(&in_empty[b]);
+        }
+        // warps 0 and 1 add the four warps' partial sums of the half tile's
+        // 64 queries into rho (one atomic per query and key tile)
+        if (warp < 2) {
+          if (!mbar_wait(&w_full[b], (u >> 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          const int qq = warp * 32 + lane;
+          const float* rd = sRed + b * 4 * 64 + qq;
+          const float sum = (rd[0] + rd[64]) + (rd[128] + rd[192]);
+          if (q0h + qq < T) atomicAdd(rho + (size_t)bh * Tp + q0h + qq, sum);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&w_free[b]);
+        }
+      }
+    }
+    if (MODE == kModeKV && ok && !*abort_flag && mbar_wait(fin, 0, wc)) {
+      tc_fence_after();
+      // dV (TMEM columns 128..191) and dK (192..255) of this key: out in bf16
+      const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
+      if (key < T) {
+        float x[32];
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+          tmem_ld32(tmem + 128 + lanes + 32 * part, x);
+          tmem_wait_ld_r(x);
+          const float sc = part < 2 ? 1.f : cs;
+          __nv_bfloat16 *dst = (part < 2 ? dv : dk) + ((size_t)bh * T + key) * 64 + 32 * (part & 1);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4 *>(dst)[j] =
+                make_uint4(pack_bf16x2(x[8 * j] * sc, x[8 * j + 1] * sc), pack_bf16x2(x[8 * j + 2] * sc, x[8 * j + 3] * sc),
+                           pack_bf16x2(x[8 * j + 4] * sc, x[8 * j + 5] * sc), pack_bf16x2(x[8 * j + 6] * sc, x[8 * j + 7] * sc));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ------------------------------------------------------------ query-major pass
+// One CTA per (head, 128-query tile), two per SM, walking the key tiles up to
+// the diagonal.  Per key tile: S and dA' for the two 64-query halves (one
+// TMEM slot pair, reused), one thread per key writing ds (MN-major, the
+// layout of the forward's share^T), then dQ += ds K (M = 128 queries, N = 64,
+// K = 128 keys) accumulating in TMEM.
+struct QCfg {
+  static constexpr uint32_t kOffQ = 0, kOffG = kTile16, kOffK = 2 * kTile16, kOffV = 3 * kTile16;
+  static constexpr uint32_t kOffDs = 4 * kTile16;                 // 2 M-blocks x 16 key groups x 1 KB
+  static constexpr uint32_t kOffAExt = kOffDs + 2 * 16 * 1024;
+  static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // 128 query rows
+  static constexpr uint32_t kOffBExtA = kOffBExtS + kExt128;
+  static constexpr uint32_t kOffRinv = kOffBExtA + kExt128;       // [128] fp32
+  static constexpr uint32_t kOffRho = kOffRinv + 128 * 4;         // [128] fp32
+  static constexpr uint32_t kOffBar = kOffRho + 128 * 4;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+};
+
+template <bool EARLIER>
+__global__ void __launch_bounds__(kBtThreads, 2)
+    bwdtc_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const float *__restrict__ nlse2, const float *__restrict__ delta, const float *__restrict__ rinv,
+                   const float *__restrict__ rho, const float *__restrict__ cchk, const float *__restrict__ gchk,
+                   __nv_bfloat16 *__restrict__ dq, int BH, int T, int Tp, HeadScale hs, float c_scalar,
+                   int *status) {
+  using C = QCfg;
+  extern __shared__ uint8_t bt_smem_raw[];
+  uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
+  uint8_t *sQ = smem + C::kOffQ, *sG = smem + C::kOffG, *sK = smem + C::kOffK, *sV = smem + C::kOffV;
+  uint8_t *sDs = smem + C::kOffDs, *sAExt = smem + C::kOffAExt;
+  uint8_t *sBExtS = smem + C::kOffBExtS, *sBExtA = smem + C::kOffBExtA;
+  float *sRinv = reinterpret_cast<float *>(smem + C::kOffRinv);
+  float *sRho = reinterpret_cast<float *>(smem + C::kOffRho);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *q_full = bars;           // Q, G tiles and the query rows
+  uint64_t *k_full = bars + 1, *k_empty = bars + 2;
+  uint64_t *v_full = bars + 3, *v_empty = bars + 4;
+  uint64_t *s_full = bars + 5, *s_free = bars + 6;
+  uint64_t *ds_full = bars + 7, *ds_free = bars + 8;
+  uint64_t *fin = bars + 9, *drain = bars + 10;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int NQT = Tp / kTile, NC = Tp / 32;
+  const int bh = blockIdx.x % BH, qt = NQT - 1 - blockIdx.x / BH;   // the most key tiles first
+  const int n = qt + 1;                                              // key tiles 0 .. qt
+  const float c2 = fmaxf(head_c2(hs, bh, nullptr), 1e-30f);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 2);
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 1);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(ds_full, 4);
+    mbar_init(ds_free, 1);
+    mbar_init(fin, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  fill_ones_ext(sAExt, threadIdx.x, kBtThreads);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, status};
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmG);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(q_full, 2 * kTile16);
+      tma_load_3d(sQ, &tmQ, q_full, 0, qt * kTile, bh);
+      tma_load_3d(sG, &tmG, q_full, 0, qt * kTile, bh);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int qq = lane + 32 * j;
+      const size_t idx = (size_t)bh * Tp + qt * kTile + qq;
+      put_ext_row(sBExtS, qq, __ldg(nlse2 + idx) / c2);
+      put_ext_row(sBExtA, qq, -__ldg(delta + idx));
+      sRinv[qq] = __ldg(rinv + idx);
+      sRho[qq] = rho[idx];
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_full);
+    int issued = 0;
+    if (lane == 0) {
+      for (int u = 0; u < n; ++u) {
+        if (!mbar_wait(k_empty, (u & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(k_full, kTile16);
+        tma_load_3d(sK, &tmK, k_full, 0, u * kTile, bh);
+        if (!mbar_wait(v_empty, (u & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(v_full, kTile16);
+        tma_load_3d(sV, &tmV, v_full, 0, u * kTile, bh);
+        ++issued;
+      }
+      if (*abort_flag) {
+        drain_wait_bt(q_full, 0);
+        if (issued > 0) {
+          drain_wait_bt(k_full, (issued - 1) & 1);
+          drain_wait_bt(v_full, (issued - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr long long kStepKm = 2, kStepMn = 128;
+      const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
+      const uint32_t idesc_q = idesc_bf16(kTile, 64, true, true);
+      const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
+      const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
+      // ds: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB
+      // apart (SBO); K as the MN-major B operand (16 keys = 2 KB per K step)
+      const uint64_t dDs = smem_desc(smem_u32(sDs), 16384, 1024);
+      const uint64_t dKmn = smem_desc(smem_u32(sK), kTile16, 1024);
+      bool ok = mbar_wait(q_full, 0, wc);
+      if (ok) tc_fence_after();
+      for (int u = 0; ok && u < n; ++u) {
+        if (!mbar_wait(k_full, u & 1, wc) || !mbar_wait(v_full, u & 1, wc)) break;
+        tc_fence_after();
+        for (int hh = 0; hh < 2; ++hh) {
+          const int it = 2 * u + hh;
+          if (!mbar_wait(s_free, (it & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // the query half: rows 64 hh.. of the Q / G tiles (8 KB on) and of
+          // the extension rows (8 groups of 256 bytes on)
+          const uint64_t dQh = kdesc(sQ + hh * 8192, 0), dGh = kdesc(sG + hh * 8192, 0);
+          const uint64_t dBS = smem_desc_noswizzle(smem_u32(sBExtS) + hh * 2048, 128, 256);
+          const uint64_t dBA = smem_desc_noswizzle(smem_u32(sBExtA) + hh * 2048, 128, 256);
+          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tmem, dK, dQh, idesc_s, 0u);
+          mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
+          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tmem + 64, dV, dGh, idesc_s, 0u);
+          mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
+          mma_commit(s_full);
+        }
+        if (!ok) break;
+        mma_commit(v_empty);
+        if (!mbar_wait(ds_full, u & 1, wc)) break;
+        tc_fence_after();
+        MmaRun<0, kTile / 16, kStepMn, kStepMn, false>::go(tmem + 128, dDs, dKmn, idesc_q, u > 0 ? 1u : 0u);
+        mma_commit(ds_free);
+        mma_commit(k_empty);
+        if (u == n - 1) mma_commit(fin);
+      }
+      mma_commit(drain);
+      drain_wait_bt(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------ key threads
+    const int row = warp * 32 + lane;   // key row of the current key tile
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const int swz = row & 7;
+    uint8_t *ds_row = sDs + (row >> 3) * 1024 + (row & 7) * 128;
+    bool ok = mbar_wait(q_full, 0, wc);
+    for (int u = 0; ok && u < n; ++u) {
+      const int key = u * kTile + row;
+      const bool diag = u == qt;          // keys after queries only on the diagonal tile
+      for (int hh = 0; hh < 2 && ok; ++hh) {
+        const int it = 2 * u + hh;
+        if (!mbar_wait(s_full, it & 1, wc) || (hh == 0 && !mbar_wait(ds_free, (u & 1) ^ 1, wc))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int c = 0; c < 2; ++c) {
+          float P[32], A[32], E[32];
+          uint32_t at[16];
+          tmem_ld32(tmem + lanes + 32 * c, P);
+          tmem_ld32(tmem + 64 + lanes + 32 * c, A);
+          tmem_wait_ld_r(P);
+          tmem_wait_ld_r(A);
+          if (c == 1) release_bt(s_free, lane);
+          const int col0 = 64 * hh + 32 * c;   // first query of the chunk inside the tile
+          const size_t ck = ((size_t)bh * NC + (qt * kTile + col0) / 32) * Tp + key;
+          const float cpe = __ldg(cchk + ck);
+          if (diag) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row, col0, c2, cpe, sRinv);
+          else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row, col0, c2, cpe, sRinv);
+          float g0 = __ldg(gchk + ck);
+          bwd_chunk_rev(A, E, g0);
+          uint32_t ds[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 r2 = *reinterpret_cast<const float2 *>(sRho + col0 + 2 * i);
+            ds[i] = pack_bf16x2(P[2 * i] * (A[2 * i] - r2.x), P[2 * i + 1] * (A[2 * i + 1] - r2.y));
+          }
+          // 32 queries of chunk qc = 2 hh + c -> 64-query M-block qc / 2,
+          // 16-byte pieces (qc % 2) * 4 .. + 3 of this key's row, swizzled
+          const int qc = 2 * hh + c;
+          uint8_t *dst = ds_row + (qc >> 1) * 16384;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(dst + ((((qc & 1) * 4 + j) ^ swz) * 16)) =
+                make_uint4(ds[4 * j], ds[4 * j + 1], ds[4 * j + 2], ds[4 * j + 3]);
+        }
+      }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (ok && !*abort_flag && mbar_wait(fin, 0, wc)) {
+      tc_fence_after();
+      // dQ rows: TMEM lane = query of this warp's quarter
+      const int qi = qt * kTile + warp * 32 + lane;
+      const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
+      float x[32];
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        tmem_ld32(tmem + 128 + lanes + 32 * part, x);
+        tmem_wait_ld_r(x);
+        if (qi < T) {
+          __nv_bfloat16 *dst = dq + ((size_t)bh * T + qi) * 64 + 32 * part;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4 *>(dst)[j] =
+                make_uint4(pack_bf16x2(x[8 * j] * cs, x[8 * j + 1] * cs), pack_bf16x2(x[8 * j + 2] * cs, x[8 * j + 3] * cs),
+                           pack_bf16x2(x[8 * j + 4] * cs, x[8 * j + 5] * cs), pack_bf16x2(x[8 * j + 6] * cs, x[8 * j + 7] * cs));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ------------------------------------------------------------------- host
+bool make_bf16_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d, int rows);
+int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const float *nlse2, float *acc, float *cchk,
+                          int BH, int T, HeadScale hs, float eps, bool earlier, int *status, cudaStream_t stream);
+
+template <bool EARLIER>
+static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, float *rinv, float *rho, float *cchk,
+                         float *gchk, void *dq, void *dk, void *dv, int BH, int T, int Tp, HeadScale hs, float c,
+                         int *status, cudaStream_t stream) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+  if (dev >= 64 || !attr_done[dev]) {
+    if (cudaFuncSetAttribute(bwdtc_key_kernel<kModeB1, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KeyCfg<kModeB1>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwdtc_key_kernel<kModeKV, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KeyCfg<kModeKV>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwdtc_q_kernel<EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             QCfg::kSmemBytes) != cudaSuccess)
+      return DA_ERR_CUDA;
+    if (dev < 64) attr_done[dev] = true;
+  }
+  const int NT = Tp / kTile;
+  const unsigned grid = (unsigned)(NT * BH);
+  // maps: 0 Q (64-row boxes), 1 dout (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout (128)
+  bwdtc_key_kernel<kModeB1, EARLIER><<<grid, kBtThreads, KeyCfg<kModeB1>::kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, nullptr, nullptr, BH, T, Tp, hs, c,
+      status);
+  bwdtc_key_kernel<kModeKV, EARLIER><<<grid, kBtThreads, KeyCfg<kModeKV>::kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk,
+      static_cast<__nv_bfloat16 *>(dk), static_cast<__nv_bfloat16 *>(dv), BH, T, Tp, hs, c, status);
+  bwdtc_q_kernel<EARLIER><<<grid, kBtThreads, QCfg::kSmemBytes, stream>>>(
+      maps[4], maps[5], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, static_cast<__nv_bfloat16 *>(dq),
+      BH, T, Tp, hs, c, status);
+  return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+// The tensor-core backward (bf16, d = 64): the passes in the file header.
+int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
+                       void *dk, void *dv, int BH, int T, HeadScale hs, float c, float eps, bool earlier,
+                       uint8_t *ws, cudaStream_t stream) {
+  const BwdTcWorkspace L = bwd_tc_workspace_layout(BH, T);
+  const int Tp = (int)t_pad(T);
+  const int64_t rows = (int64_t)BH * Tp;
+  int *status = reinterpret_cast<int *>(ws);
+  float *nlse2 = reinterpret_cast<float *>(ws + L.nlse2_off);
+  float *acc = reinterpret_cast<float *>(ws + L.acc_off);
+  float *rinv = reinterpret_cast<float *>(ws + L.rows_off);
+  float *delta = rinv + rows, *rho = delta + rows;
+  float *cchk = reinterpret_cast<float *>(ws + L.cchk_off);
+  float *gchk = reinterpret_cast<float *>(ws + L.gchk_off);
+  CUtensorMap maps[6];
+  if (!make_bf16_tile_map(&maps[0], q, BH, T, 64, 64) || !make_bf16_tile_map(&maps[1], dout, BH, T, 64, 64) ||
+      !make_bf16_tile_map(&maps[2], k, BH, T, 64, kTile) || !make_bf16_tile_map(&maps[3], v, BH, T, 64, kTile) ||
+      !make_bf16_tile_map(&maps[4], q, BH, T, 64, kTile) || !make_bf16_tile_map(&maps[5], dout, BH, T, 64, kTile))
+    return DA_ERR_CUDA;
+  bwdtc_prep<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
+  int st = launch_sweep_bf16_chk(q, k, v, nlse2, acc, cchk, BH, T, hs, eps, earlier, status, stream);
+  if (st != DA_OK) return st;
+  bwdtc_rows<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, stream>>>(
+      acc, static_cast<const __nv_bfloat16 *>(dout), rinv, delta, rho, BH, T, Tp);
+  return earlier ? launch_passes<true>(maps, nlse2, delta, rinv, rho, cchk, gchk, dq, dk, dv, BH, T, Tp, hs, c, status,
+                                       stream)
+                 : launch_passes<false>(maps, nlse2, delta, rinv, rho, cchk, gchk, dq, dk, dv, BH, T, Tp, hs, c,
+                                        status, stream);
+}
+
+}  // namespace da

@@ -19,6 +19,9 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
                        void *dk, void *dv, int BH, int T, int d, float c, HeadScale hs, float eps, bool earlier,
                        int dtype, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream);
+int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
+                       void *dk, void *dv, int BH, int T, HeadScale hs, float c, float eps, bool earlier,
+                       uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
                           bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
@@ -137,9 +140,12 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
                          acc, status, stream, ev);
 }
 
+// bf16 at d = 64 runs the tensor-core backward; every other case the SIMT one.
+static bool bwd_on_tensor_cores(int d, int dtype) { return dtype == DA_BF16 && d == 64; }
+
 size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
-  (void)dtype;
   if (B < 0 || H < 0 || T < 0 || !head_dim_supported(d)) return 0;
+  if (bwd_on_tensor_cores(d, dtype)) return bwd_tc_workspace_layout((int64_t)B * H, T).total;
   return bwd_workspace_layout((int64_t)B * H, T, d).total;
 }
 
@@ -161,13 +167,20 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
   const void *ptrs[] = {q, k, v, dout, lse2, dq, dk, dv};
   for (const void *p : ptrs)
     if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
-  const BwdWorkspace L = bwd_workspace_layout(BH, T, d);
-  if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
+  const size_t need = bwd_on_tensor_cores(d, dtype) ? bwd_tc_workspace_layout(BH, T).total
+                                                   : bwd_workspace_layout(BH, T, d).total;
+  if (workspace == nullptr || workspace_bytes < need) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   if (cudaMemsetAsync(ws, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   const float c = (float)((double)tau / std::sqrt((double)d));
+  if (bwd_on_tensor_cores(d, dtype)) {
+    if ((int64_t)BH * t_pad(T) > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;
+    return launch_bwd_bf16_tc(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, head_scale(tau, tau_bh, d), c, eps,
+                              (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, ws, stream);
+  }
+  const BwdWorkspace L = bwd_workspace_layout(BH, T, d);
   if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, d, c, head_scale(tau, tau_bh, d), eps,
                  (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, dtype,
                  reinterpret_cast<double *>(ws + L.dtot_off), reinterpret_cast<float *>(ws + L.row_off),

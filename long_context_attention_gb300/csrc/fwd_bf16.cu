@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmAcc,
                  const uint4 *__restrict__ kglob, const float *__restrict__ nlse2, float *__restrict__ acc,
-                 float *__restrict__ demand_out, int BH,
+                 float *__restrict__ demand_out, float *__restrict__ cchk, int BH,
                  int T, int Tp, HeadScale hs, float eps, int *status) {
   using C = SwCfg<D>;
   constexpr int kG = C::kG;
@@ -803,10 +803,20 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
       const bool all_masked = kbase > qlo + kSwBQ - 1 || kbase >= T;
       const bool need_mask = kbase + kTile - 1 > qlo;
       const int row_eff = row - (qlo - kbase);      // key after query col iff row_eff > col
+      // Demand checkpoints for the backward (cchk != null): committed + eps of
+      // this key at the start of each 32-query chunk, [bh][chunk][key < Tp]
+      // (the last span can reach past Tp).
+      float *ck = (cchk == nullptr || kbase + row >= Tp)
+                      ? nullptr
+                      : cchk + ((size_t)w.bh * (Tp / 32) + qlo / 32) * Tp + kbase + row;
       if (!mbar_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
       uint32_t pk[16];
       if (all_masked) {
+        if (ck != nullptr) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ck[(size_t)c * Tp] = ceps;
+        }
         release_tmem(&s_free[g], lane);
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
@@ -819,6 +829,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         tmem_ld32(tb, A);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 32, B);
+        if (ck != nullptr) ck[0 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         else demand_chunk<false, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
@@ -826,16 +837,19 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         store(pk, 0);
         tmem_wait_ld_r(B);
         tmem_ld32(tb + 64, A);
+        if (ck != nullptr) ck[1 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         else demand_chunk<false, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 1);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 96, B);
+        if (ck != nullptr) ck[2 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         else demand_chunk<false, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         store(pk, 2);
         tmem_wait_ld_r(B);
         release_tmem(&s_free[g], lane);
+        if (ck != nullptr) ck[3 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 3, EARLIER>(B, row_eff, c2, ceps, pk);
         else demand_chunk<false, 3, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 3);
@@ -892,6 +906,11 @@ static bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// For the backward's kernels.
+bool make_bf16_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d, int rows) {
+  return make_tile_map(m, base, BH, T, d, rows);
 }
 
 // The fp32 accumulator [BH * Tp rows][d + 4] as a 2-D tensor; box = 32 rows
@@ -962,12 +981,44 @@ static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const
   const uint4 *kg = static_cast<const uint4 *>(k);
   if (earlier)
     sweep_kernel<D, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
-                                                                       BH, T, Tp, hs, eps, status);
+                                                                       nullptr, BH, T, Tp, hs, eps, status);
   else
     sweep_kernel<D, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc,
-                                                                        demand_out, BH, T, Tp, hs, eps, status);
+                                                                        demand_out, nullptr, BH, T, Tp, hs, eps,
+                                                                        status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;
+}
+
+// The demand sweep alone (d = 64), for the backward: the caller has written
+// -lse2 to nlse2 and zeroed acc; cchk receives the demand checkpoints.
+int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const float *nlse2, float *acc, float *cchk,
+                          int BH, int T, HeadScale hs, float eps, bool earlier, int *status, cudaStream_t stream) {
+  const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
+  if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tk, tv, ta;
+  if (!make_tile_map(&tq, q, BH, T, 64) || !make_tile_map(&tk, k, BH, T, 64) || !make_tile_map(&tv, v, BH, T, 64) ||
+      !make_acc_map(&ta, acc, acc_rows, 64))
+    return DA_ERR_CUDA;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+  if (dev >= 64 || !attr_done[dev]) {
+    const int st = prepare_fwd_bf16<64>();
+    if (st != DA_OK) return st;
+    if (dev < 64) attr_done[dev] = true;
+  }
+  using C = SwCfg<64>;
+  const int Tp = (int)t_pad(T);
+  const int nsw = sweep_num_ctas(BH, T, 64);
+  const uint4 *kg = static_cast<const uint4 *>(k);
+  if (earlier)
+    sweep_kernel<64, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr, cchk,
+                                                                        BH, T, Tp, hs, eps, status);
+  else
+    sweep_kernel<64, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr,
+                                                                         cchk, BH, T, Tp, hs, eps, status);
+  return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
