@@ -59,6 +59,13 @@ __device__ __forceinline__ void drain_wait_bt(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// Bounded wait whose outcome is the same in every lane of the warp, for waits
+// followed by warp-collective instructions (tcgen05.ld, shuffles): a lane
+// that gave up takes the whole warp with it.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtx &wc) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+}
+
 __device__ __forceinline__ void release_bt(uint64_t *bar, int lane) {
   tc_fence_before();
   __syncwarp();
@@ -389,10 +396,10 @@ __global__ void __launch_bounds__(kBtThreads, 2)
       const bool need_mask = kt * kTile + kTile - 1 > q0h;
       const int row_eff = key - q0h;
       const uint32_t par_full = MODE == kModeB1 ? ((u >> 1) & 1) : (u & 1);
-      if (!mbar_wait(&s_full[slot], par_full, wc)) break;
+      if (!warp_wait(&s_full[slot], par_full, wc)) break;
       tc_fence_after();
-      if (MODE == kModeKV && !mbar_wait(&w_free[0], (u & 1) ^ 1, wc)) break;   // A^T, ds^T of u - 1 consumed
-      if (MODE == kModeB1 && !mbar_wait(&w_free[b], ((u >> 1) & 1) ^ 1, wc)) break;   // partial rho buffer b read
+      if (MODE == kModeKV && !warp_wait(&w_free[0], (u & 1) ^ 1, wc)) break;   // A^T, ds^T of u - 1 consumed
+      if (MODE == kModeB1 && !warp_wait(&w_free[b], ((u >> 1) & 1) ^ 1, wc)) break;   // partial rho buffer b read
       for (int cc = 0; cc < 2; ++cc) {
         const int c = MODE == kModeB1 ? 1 - cc : cc;   // B1 walks the chunks backwards
         float P[32], A[32], E[32];
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         // warps 0 and 1 add the four warps' partial sums of the half tile's
         // 64 queries into rho (one atomic per query and key tile)
         if (warp < 2) {
-          if (!mbar_wait(&w_full[b], (u >> 1) & 1, wc)) {
+          if (!warp_wait(&w_full[b], (u >> 1) & 1, wc)) {
             ok = false;
             break;
           }
@@ -464,16 +471,17 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         }
       }
     }
-    if (MODE == kModeKV && ok && !*abort_flag && mbar_wait(fin, 0, wc)) {
+    if (MODE == kModeKV && ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
       tc_fence_after();
       // dV (TMEM columns 128..191) and dK (192..255) of this key: out in bf16
       const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
-      if (key < T) {
-        float x[32];
+      // (tcgen05.ld is warp-collective: every lane loads, only keys < T store)
+      float x[32];
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          tmem_ld32(tmem + 128 + lanes + 32 * part, x);
-          tmem_wait_ld_r(x);
+      for (int part = 0; part < 4; ++part) {
+        tmem_ld32(tmem + 128 + lanes + 32 * part, x);
+        tmem_wait_ld_r(x);
+        if (key < T) {
           const float sc = part < 2 ? 1.f : cs;
           __nv_bfloat16 *dst = (part < 2 ? dv : dk) + ((size_t)bh * T + key) * 64 + 32 * (part & 1);
 #pragma unroll
@@ -666,13 +674,13 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const int swz = row & 7;
     uint8_t *ds_row = sDs + (row >> 3) * 1024 + (row & 7) * 128;
-    bool ok = mbar_wait(q_full, 0, wc);
+    bool ok = warp_wait(q_full, 0, wc);
     for (int u = 0; ok && u < n; ++u) {
       const int key = u * kTile + row;
       const bool diag = u == qt;          // keys after queries only on the diagonal tile
       for (int hh = 0; hh < 2 && ok; ++hh) {
         const int it = 2 * u + hh;
-        if (!mbar_wait(s_full, it & 1, wc) || (hh == 0 && !mbar_wait(ds_free, (u & 1) ^ 1, wc))) {
+        if (!warp_wait(s_full, it & 1, wc) || (hh == 0 && !warp_wait(ds_free, (u & 1) ^ 1, wc))) {
           ok = false;
           break;
         }
@@ -713,7 +721,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-    if (ok && !*abort_flag && mbar_wait(fin, 0, wc)) {
+    if (ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
       tc_fence_after();
       // dQ rows: TMEM lane = query of this warp's quarter
       const int qi = qt * kTile + warp * 32 + lane;
