@@ -87,6 +87,13 @@ __device__ __forceinline__ void put_ext_row(uint8_t *ext, int q, float v) {
                  (uint32_t)__bfloat16_as_ushort(l), 0u, 0u);
 }
 
+// Zero `bytes` of shared memory (the extension rows' K 8..15 core matrices
+// are never rewritten: they must hold zeros, not stale bits, since 0 x Inf
+// would reach the products).
+__device__ __forceinline__ void zero_smem(uint8_t *p, uint32_t bytes, int tid, int nthreads) {
+  for (uint32_t e = tid; e < bytes / 16; e += nthreads) reinterpret_cast<uint4 *>(p)[e] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // A_ext: [1 1 1 0 ...] for every one of 128 rows; its zero half K 8..15 too.
 __device__ __forceinline__ void fill_ones_ext(uint8_t *ext, int tid, int nthreads) {
   for (int e = tid; e < (int)(kExt128 / 16); e += nthreads) {
@@ -281,6 +288,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     fence_mbar_init();
   }
   fill_ones_ext(sAExt, threadIdx.x, kBtThreads);
+  zero_smem(smem + C::kOffBExtS, 4 * kExt64, threadIdx.x, kBtThreads);   // both buffers of both rows
   fence_proxy_async_smem();
   if (warp == 5) {
     tmem_alloc(tmem_slot, 256);
@@ -569,6 +577,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     fence_mbar_init();
   }
   fill_ones_ext(sAExt, threadIdx.x, kBtThreads);
+  zero_smem(sBExtS, 2 * kExt128, threadIdx.x, kBtThreads);   // both extension row blocks
   fence_proxy_async_smem();
   if (warp == 5) {
     tmem_alloc(tmem_slot, 256);
