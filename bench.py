@@ -347,7 +347,13 @@ def run_decode(torch, b, inputs, dev, warmup, peaks, ctx=None, n_steps=None):
                  "gpu_launches": 3 * steps}
 
 
-def run_train(torch, b, inputs, dev, steps=2):
+def bwd_flops(B, H, T, d):
+    """Algorithmic backward FLOP: the five contractions S = Q K^T, dA = dout V^T,
+    dV = A^T dout, dK = ds^T Q, dQ = ds K over the causal pairs."""
+    return 5 * d * T * (T + 1) * B * H
+
+
+def run_train(torch, b, inputs, dev, steps=5):
     """Forward + backward at the training shape (4 x 12 x 16384 x 64, all N(0,1))."""
     w = inputs.WORKLOADS["train_bf16_t16384"]
     B, H, T, d = w.B, w.H, w.T, w.d
@@ -358,25 +364,35 @@ def run_train(torch, b, inputs, dev, steps=2):
     fws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=dev)
     bws = torch.empty(b.dilution_attn_bwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
 
-    def step():
+    def step(e3=None):
+        if e3:
+            e3[0].record()
         b.dilution_attn_fwd(q, k, v, out, lse2, workspace=fws)
+        if e3:
+            e3[1].record()
         b.dilution_attn_bwd(q, k, v, g, lse2, dq, dk, dv, workspace=bws)
+        if e3:
+            e3[2].record()
 
     step()
     torch.cuda.synchronize()
-    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(steps):
-        step()
+    for i in range(steps):
+        step(ev[i])
     e1.record()
     torch.cuda.synchronize()
     assert b.dilution_attn_get_error(fws) == b.DA_OK and b.dilution_attn_get_error(bws) == b.DA_OK
     ms = e0.elapsed_time(e1) / steps
-    fwd_f = fwd_flops(B, H, T, d)
+    bwd_ms = statistics.mean(e3[1].elapsed_time(e3[2]) for e3 in ev)
+    fwd_f, bwd_f = fwd_flops(B, H, T, d), bwd_flops(B, H, T, d)
     return {"workload": "train_bf16_t16384", "B": B, "H": H, "T": T, "steps": steps, "ms_per_step": ms,
-            "tokens_per_s": B * T / (ms * 1e-3), "backward": "CUDA-core version (no tensor cores yet)",
-            "fwd_flop": fwd_f}
+            "tokens_per_s": B * T / (ms * 1e-3), "bwd_ms": bwd_ms,
+            "tflops": (fwd_f + bwd_f) / (ms * 1e-3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
+            "backward": "tcgen05: forward sweep again with demand checkpoints, a rho pass, a dK/dV pass, a dQ pass",
+            "fwd_flop": fwd_f, "bwd_flop": bwd_f}
 
 
 def run_ours(args):
