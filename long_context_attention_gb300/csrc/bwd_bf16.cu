@@ -151,64 +151,90 @@ __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *_
 // column.  In: S' (q.k - lse2 / c2) and dA' (g.v - delta) from TMEM, the
 // chunk's demand checkpoint cpe = committed + eps before q0, 1/R of the
 // queries (shared memory).  Forms, for each query in causal order, p,
-// e = committed + eps before the query, D, then
-//   t = dr / D,  dir = t e / D (t for EARLIER),  dC = -t p / D,
-// leaving p in P, dir in A and dC in E (and, with AT, A = r / R packed as
-// bf16 pairs).  MASK zeroes keys after the query (row_eff > column).
+// e = committed + eps before the query, D, then with ti = dr / D^2
+//   dir = ti e (dr / D for EARLIER),  -dC = ti p,
+// leaving p in P, dir in A and -dC in E (and, with AT, A = r / R packed as
+// bf16 pairs).  Pairs of queries share one reciprocal, 1 / (D0 D1), and go
+// through the packed f32x2 pipe.  MASK zeroes keys after the query
+// (row_eff > column).
 template <bool MASK, bool EARLIER, bool AT>
 __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], float (&E)[32], uint32_t (&at)[16],
                                               int row_eff, int col0, float c2, float cpe, const float *rinv_q) {
+  const float2 c2v = make_float2(c2, c2);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 x = fmul2(make_float2(P[i], P[i + 1]), c2v);
+    P[i] = ex2_approx(x.x);
+    P[i + 1] = ex2_approx(x.y);
+  }
+  if (MASK) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (row_eff > col0 + i) P[i] = 0.f;
+  }
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    float p = ex2_approx(P[i] * c2);
-    if (MASK && row_eff > col0 + i) p = 0.f;
-    P[i] = p;
     E[i] = cpe;   // committed + eps before query i
-    cpe += p;
+    cpe += P[i];
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float e0 = E[2 * i], e1 = E[2 * i + 1];
-    const float p0 = P[2 * i], p1 = P[2 * i + 1];
-    const float d0 = EARLIER ? e0 : e0 + p0, d1 = EARLIER ? e1 : e1 + p1;
-    const float rr = rcp_approx(d0 * d1);
-    const float i0 = d1 * rr, i1 = d0 * rr;   // 1/d0, 1/d1
+    const float2 e = make_float2(E[2 * i], E[2 * i + 1]);
+    const float2 p = make_float2(P[2 * i], P[2 * i + 1]);
+    const float2 d = EARLIER ? e : fadd2(e, p);
+    const float rr = rcp_approx(d.x * d.y);
+    const float2 inv = fmul2(make_float2(d.y, d.x), make_float2(rr, rr));   // 1/d0, 1/d1
     const float2 rq = *reinterpret_cast<const float2 *>(rinv_q + col0 + 2 * i);
-    float dr0 = A[2 * i] * rq.x, dr1 = A[2 * i + 1] * rq.y;
-    if (MASK && row_eff > col0 + 2 * i) dr0 = 0.f;
-    if (MASK && row_eff > col0 + 2 * i + 1) dr1 = 0.f;
-    const float t0 = dr0 * i0, t1 = dr1 * i1;
-    A[2 * i] = EARLIER ? t0 : t0 * e0 * i0;
-    A[2 * i + 1] = EARLIER ? t1 : t1 * e1 * i1;
-    E[2 * i] = -t0 * p0 * i0;
-    E[2 * i + 1] = -t1 * p1 * i1;
-    if (AT) at[i] = pack_bf16x2(p0 * i0 * rq.x, p1 * i1 * rq.y);   // A = r / R
+    float2 dr = fmul2(make_float2(A[2 * i], A[2 * i + 1]), rq);
+    if (MASK) {
+      if (row_eff > col0 + 2 * i) dr.x = 0.f;
+      if (row_eff > col0 + 2 * i + 1) dr.y = 0.f;
+    }
+    const float2 dri = fmul2(dr, inv);
+    const float2 ti = fmul2(dri, inv);
+    const float2 dir = EARLIER ? dri : fmul2(ti, e);
+    const float2 ndc = fmul2(ti, p);
+    A[2 * i] = dir.x;
+    A[2 * i + 1] = dir.y;
+    E[2 * i] = ndc.x;
+    E[2 * i + 1] = ndc.y;
+    if (AT) {
+      const float2 a = fmul2(fmul2(p, inv), rq);   // A = r / R
+      at[i] = pack_bf16x2(a.x, a.y);
+    }
   }
 }
 
 // Reverse walk of one chunk: dp = dir + grev, grev += dC (queries in reverse
-// order); dp is left in A.
+// order; E holds -dC); dp is left in A.
 __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[32], float &grev) {
 #pragma unroll
   for (int i = 31; i >= 0; --i) {
     A[i] += grev;
-    grev += E[i];
+    grev -= E[i];
   }
 }
 
-// Sum of X over the 32 lanes, lane l ending with the total of X[l].
-__device__ __forceinline__ float lane_transpose_sum(float (&X)[32], int lane) {
+// Column sums of a warp's 32 x 32 block (lane = key, X[i] = query i) through
+// shared memory: each lane writes its row (rows 36 floats apart, 16-byte
+// aligned), then lane l adds up column l.  Returns the sum over the warp's
+// keys for query l.
+__device__ __forceinline__ float warp_column_sum(const float (&X)[32], float *red, int lane) {
+  float *rowp = red + lane * 36;
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<float4 *>(rowp + 4 * j) = make_float4(X[4 * j], X[4 * j + 1], X[4 * j + 2], X[4 * j + 3]);
+  __syncwarp();
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-    for (int i = 0; i < off; ++i) {
-      const bool hi = (lane & off) != 0;
-      const float send = hi ? X[i] : X[i + off];
-      const float keep = hi ? X[i + off] : X[i];
-      X[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
+  for (int r = 0; r < 32; r += 4) {
+    s0 += red[r * 36 + lane];
+    s1 += red[(r + 1) * 36 + lane];
+    s2 += red[(r + 2) * 36 + lane];
+    s3 += red[(r + 3) * 36 + lane];
   }
-  return X[0];
+  __syncwarp();   // the block is free again
+  return (s0 + s1) + (s2 + s3);
 }
 
 // ------------------------------------------------------------ key-major passes
@@ -229,7 +255,8 @@ struct KeyCfg {
   static constexpr uint32_t kOffRinv = kOffBExtA + 2 * kExt64;    // [2][64] fp32
   static constexpr uint32_t kOffRho = kOffRinv + 2 * 64 * 4;      // [2][64] fp32 (KV)
   static constexpr uint32_t kOffRed = kOffRho + 2 * 64 * 4;       // [2][4][64] fp32 (B1)
-  static constexpr uint32_t kOffAT = kOffRed + 2 * 4 * 64 * 4;    // A^T, K-major (KV)
+  static constexpr uint32_t kOffXp = kOffRed + 2 * 4 * 64 * 4;    // [4][32][36] fp32 (B1)
+  static constexpr uint32_t kOffAT = MODE == kModeB1 ? kOffXp + 4 * 32 * 36 * 4 : kOffXp;   // A^T (KV)
   static constexpr uint32_t kOffDsT = kOffAT + kTile16;           // ds^T, K-major (KV)
   static constexpr uint32_t kOffBar = MODE == kModeKV ? kOffDsT + kTile16 : kOffAT;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + re-alignment slack
@@ -252,6 +279,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
   float *sRinv = reinterpret_cast<float *>(smem + C::kOffRinv);
   float *sRho = reinterpret_cast<float *>(smem + C::kOffRho);
   float *sRed = reinterpret_cast<float *>(smem + C::kOffRed);
+  float *sXp = reinterpret_cast<float *>(smem + C::kOffXp);
   uint8_t *sAT = smem + C::kOffAT, *sDsT = smem + C::kOffDsT;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *kv_full = bars;
@@ -428,8 +456,12 @@ __global__ void __launch_bounds__(kBtThreads, 2)
           gchk[ck] = grev;   // sum of dC after the chunk
           bwd_chunk_rev(A, E, grev);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) P[i] *= A[i];   // p dp
-          sRed[(b * 4 + warp) * 64 + 32 * c + lane] = lane_transpose_sum(P, lane);
+          for (int i = 0; i < 32; i += 2) {   // p dp
+            const float2 x = fmul2(make_float2(P[i], P[i + 1]), make_float2(A[i], A[i + 1]));
+            P[i] = x.x;
+            P[i + 1] = x.y;
+          }
+          sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_column_sum(P, sXp + warp * 32 * 36, lane);
         } else {
           if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
           else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
@@ -440,7 +472,9 @@ __global__ void __launch_bounds__(kBtThreads, 2)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float2 r2 = *reinterpret_cast<const float2 *>(ro + 2 * i);
-            ds[i] = pack_bf16x2(P[2 * i] * (A[2 * i] - r2.x), P[2 * i + 1] * (A[2 * i + 1] - r2.y));
+            const float2 x = fmul2(make_float2(P[2 * i], P[2 * i + 1]),
+                                   fadd2(make_float2(A[2 * i], A[2 * i + 1]), make_float2(-r2.x, -r2.y)));
+            ds[i] = pack_bf16x2(x.x, x.y);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -713,7 +747,9 @@ __global__ void __launch_bounds__(kBtThreads, 2)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float2 r2 = *reinterpret_cast<const float2 *>(sRho + col0 + 2 * i);
-            ds[i] = pack_bf16x2(P[2 * i] * (A[2 * i] - r2.x), P[2 * i + 1] * (A[2 * i + 1] - r2.y));
+            const float2 x = fmul2(make_float2(P[2 * i], P[2 * i + 1]),
+                                   fadd2(make_float2(A[2 * i], A[2 * i + 1]), make_float2(-r2.x, -r2.y)));
+            ds[i] = pack_bf16x2(x.x, x.y);
           }
           // 32 queries of chunk qc = 2 hh + c -> 64-query M-block qc / 2,
           // 16-byte pieces (qc % 2) * 4 .. + 3 of this key's row, swizzled
