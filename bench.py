@@ -51,6 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-train", action="store_true", help="skip the forward+backward training-step timing")
     ap.add_argument("--no-d128", action="store_true", help="skip the head-dimension-128 forward timing")
+    ap.add_argument("--train-only", action="store_true", help="time only the training step (profiling)")
+    ap.add_argument("--train-batch", type=int, default=None, help="training-step batch (default: the workload's)")
+    ap.add_argument("--train-t", type=int, default=None, help="training-step sequence length (default: 16384)")
     ap.add_argument("--decode-ctx", type=int, default=None, help="cached tokens per sequence (default: the workload's)")
     ap.add_argument("--decode-steps", type=int, default=None, help="decode steps timed (default: the workload's)")
     ap.add_argument("--decode-only", action="store_true", help="skip the forward measurement")
@@ -353,11 +356,13 @@ def bwd_flops(B, H, T, d):
     return 5 * d * T * (T + 1) * B * H
 
 
-def run_train(torch, b, inputs, dev, steps=5):
-    """Forward + backward at the training shape (4 x 12 x 16384 x 64, all N(0,1))."""
+def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None):
+    """Forward + backward at the training shape (4 x 12 x 16384 x 64, all N(0,1));
+    ``batch`` / ``T`` override it for smaller profiling runs."""
     w = inputs.WORKLOADS["train_bf16_t16384"]
-    B, H, T, d = w.B, w.H, w.T, w.d
-    q, k, v = inputs.make_workload(w, device=dev)
+    B, H, d = batch or w.B, w.H, w.d
+    T = T or w.T
+    q, k, v = inputs.make_workload(w, device=dev, B=B, T=T)
     g = inputs.make_like((B, H, T, d), seed=w.seed + 1, dtype=w.dtype, device=dev)
     out = torch.empty_like(q)
     lse2 = torch.empty(B, H, T, device=dev)
@@ -388,7 +393,8 @@ def run_train(torch, b, inputs, dev, steps=5):
     ms = e0.elapsed_time(e1) / steps
     bwd_ms = statistics.mean(e3[1].elapsed_time(e3[2]) for e3 in ev)
     fwd_f, bwd_f = fwd_flops(B, H, T, d), bwd_flops(B, H, T, d)
-    return {"workload": "train_bf16_t16384", "B": B, "H": H, "T": T, "steps": steps, "ms_per_step": ms,
+    return {"workload": "train_bf16_t16384" if (B, T) == (w.B, w.T) else f"train_bf16_b{B}_t{T}",
+            "B": B, "H": H, "T": T, "steps": steps, "ms_per_step": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "bwd_ms": bwd_ms,
             "tflops": (fwd_f + bwd_f) / (ms * 1e-3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
             "backward": "tcgen05: forward sweep again with demand checkpoints, a rho pass, a dK/dV pass, a dQ pass",
@@ -408,6 +414,11 @@ def run_ours(args):
     b.load(build_if_missing=True)
     peaks, peaks_kind = load_peaks()
 
+    if args.train_only:
+        res = run_train(torch, b, inputs, dev, steps=max(1, args.steps), batch=args.train_batch, T=args.train_t)
+        if rank == 0:
+            print(json.dumps({"train_step": res}), flush=True)
+        return 0
     if args.decode_only:
         pre, dec = run_decode(torch, b, inputs, dev, max(3, args.warmup), peaks, args.decode_ctx, args.decode_steps)
         if rank == 0:
@@ -559,7 +570,7 @@ def run_ours(args):
         line["fwd_d128"] = run_fwd_workload(torch, b, inputs, dev, "fwd_bf16_t16384_d128", max(3, min(K, 20)),
                                             max(3, W), peaks)
     if not args.no_train:
-        line["train_step"] = run_train(torch, b, inputs, dev)
+        line["train_step"] = run_train(torch, b, inputs, dev, batch=args.train_batch, T=args.train_t)
     if not args.no_decode:
         pre, dec = run_decode(torch, b, inputs, dev, max(3, W), peaks, args.decode_ctx, args.decode_steps)
         line["prefill_131072"] = pre
