@@ -424,9 +424,27 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     uint8_t *at_row = sAT + (row >> 3) * 1024 + (row & 7) * 128;
     uint8_t *ds_row = sDsT + (row >> 3) * 1024 + (row & 7) * 128;
     float grev = 0.f;   // B1: sum of dC over the queries after the current one
+    // Checkpoints are read one half tile ahead: they come from DRAM and are
+    // needed at the start of each chunk.
+    auto ck_of = [&](int uu, int c) { return ((size_t)bh * NC + (half_of(uu) * 2 + c)) * Tp + key; };
+    float cpe_n[2], g_n[2] = {0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      cpe_n[c] = __ldg(cchk + ck_of(0, c));
+      if (MODE == kModeKV) g_n[c] = __ldg(gchk + ck_of(0, c));
+    }
     bool ok = true;
     for (int u = 0; ok && u < n; ++u) {
       const int b = u & 1, h = half_of(u);
+      const float cpe_c[2] = {cpe_n[0], cpe_n[1]};
+      const float g_c[2] = {g_n[0], g_n[1]};
+      if (u + 1 < n) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          cpe_n[c] = __ldg(cchk + ck_of(u + 1, c));
+          if (MODE == kModeKV) g_n[c] = __ldg(gchk + ck_of(u + 1, c));
+        }
+      }
       const int slot = MODE == kModeB1 ? b : 0;
       const int q0h = h * 64;
       const bool need_mask = kt * kTile + kTile - 1 > q0h;
@@ -448,7 +466,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         tmem_wait_ld_r(A);
         if (cc == 1) release_bt(&s_free[slot], lane);
         const size_t ck = ((size_t)bh * NC + (q0h / 32 + c)) * Tp + key;
-        const float cpe = __ldg(cchk + ck);
+        const float cpe = cpe_c[c];
         const float *rq = sRinv + b * 64;
         if (MODE == kModeB1) {
           if (need_mask) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
@@ -465,7 +483,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
         } else {
           if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
           else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
-          float g0 = __ldg(gchk + ck);
+          float g0 = g_c[c];
           bwd_chunk_rev(A, E, g0);
           uint32_t ds[16];
           const float *ro = sRho + b * 64 + 32 * c;
@@ -718,11 +736,30 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     const int swz = row & 7;
     uint8_t *ds_row = sDs + (row >> 3) * 1024 + (row & 7) * 128;
     bool ok = warp_wait(q_full, 0, wc);
+    // checkpoints of step it = 2 u + hh (key tile u, query half hh), read one
+    // step ahead
+    auto ck_of = [&](int it, int c) {
+      return ((size_t)bh * NC + (qt * kTile + 64 * (it & 1) + 32 * c) / 32) * Tp + (it >> 1) * kTile + row;
+    };
+    float cpe_n[2], g_n[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      cpe_n[c] = __ldg(cchk + ck_of(0, c));
+      g_n[c] = __ldg(gchk + ck_of(0, c));
+    }
     for (int u = 0; ok && u < n; ++u) {
-      const int key = u * kTile + row;
       const bool diag = u == qt;          // keys after queries only on the diagonal tile
       for (int hh = 0; hh < 2 && ok; ++hh) {
         const int it = 2 * u + hh;
+        const float cpe_c[2] = {cpe_n[0], cpe_n[1]};
+        const float g_c[2] = {g_n[0], g_n[1]};
+        if (it + 1 < 2 * n) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            cpe_n[c] = __ldg(cchk + ck_of(it + 1, c));
+            g_n[c] = __ldg(gchk + ck_of(it + 1, c));
+          }
+        }
         if (!warp_wait(s_full, it & 1, wc) || (hh == 0 && !warp_wait(ds_free, (u & 1) ^ 1, wc))) {
           ok = false;
           break;
@@ -737,11 +774,10 @@ __global__ void __launch_bounds__(kBtThreads, 2)
           tmem_wait_ld_r(A);
           if (c == 1) release_bt(s_free, lane);
           const int col0 = 64 * hh + 32 * c;   // first query of the chunk inside the tile
-          const size_t ck = ((size_t)bh * NC + (qt * kTile + col0) / 32) * Tp + key;
-          const float cpe = __ldg(cchk + ck);
+          const float cpe = cpe_c[c];
           if (diag) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row, col0, c2, cpe, sRinv);
           else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row, col0, c2, cpe, sRinv);
-          float g0 = __ldg(gchk + ck);
+          float g0 = g_c[c];
           bwd_chunk_rev(A, E, g0);
           uint32_t ds[16];
 #pragma unroll
