@@ -424,33 +424,25 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     uint8_t *at_row = sAT + (row >> 3) * 1024 + (row & 7) * 128;
     uint8_t *ds_row = sDsT + (row >> 3) * 1024 + (row & 7) * 128;
     float grev = 0.f;   // B1: sum of dC over the queries after the current one
-    // Checkpoints are read two half tiles ahead: they come from DRAM and are
+    // Checkpoints are read one half tile ahead: they come from DRAM and are
     // needed at the start of each chunk.
     auto ck_of = [&](int uu, int c) { return ((size_t)bh * NC + (half_of(uu) * 2 + c)) * Tp + key; };
-    float cpe_n[2][2], g_n[2][2] = {{0.f, 0.f}, {0.f, 0.f}};   // [half tile u + 1, u + 2][chunk]
+    float cpe_n[2], g_n[2] = {0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int uu = j < n ? j : n - 1;
-        cpe_n[j][c] = __ldg(cchk + ck_of(uu, c));
-        if (MODE == kModeKV) g_n[j][c] = __ldg(gchk + ck_of(uu, c));
-      }
+    for (int c = 0; c < 2; ++c) {
+      cpe_n[c] = __ldg(cchk + ck_of(0, c));
+      if (MODE == kModeKV) g_n[c] = __ldg(gchk + ck_of(0, c));
+    }
     bool ok = true;
     for (int u = 0; ok && u < n; ++u) {
       const int b = u & 1, h = half_of(u);
-      const float cpe_c[2] = {cpe_n[0][0], cpe_n[0][1]};
-      const float g_c[2] = {g_n[0][0], g_n[0][1]};
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        cpe_n[0][c] = cpe_n[1][c];
-        g_n[0][c] = g_n[1][c];
-      }
-      if (u + 2 < n) {
+      const float cpe_c[2] = {cpe_n[0], cpe_n[1]};
+      const float g_c[2] = {g_n[0], g_n[1]};
+      if (u + 1 < n) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          cpe_n[1][c] = __ldg(cchk + ck_of(u + 2, c));
-          if (MODE == kModeKV) g_n[1][c] = __ldg(gchk + ck_of(u + 2, c));
+          cpe_n[c] = __ldg(cchk + ck_of(u + 1, c));
+          if (MODE == kModeKV) g_n[c] = __ldg(gchk + ck_of(u + 1, c));
         }
       }
       const int slot = MODE == kModeB1 ? b : 0;
@@ -749,30 +741,23 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     auto ck_of = [&](int it, int c) {
       return ((size_t)bh * NC + (qt * kTile + 64 * (it & 1) + 32 * c) / 32) * Tp + (it >> 1) * kTile + row;
     };
-    float cpe_n[2][2], g_n[2][2];   // [step it + 1, it + 2][chunk]
+    float cpe_n[2], g_n[2];
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        cpe_n[j][c] = __ldg(cchk + ck_of(j, c));   // n >= 1: steps 0 and 1 always exist
-        g_n[j][c] = __ldg(gchk + ck_of(j, c));
-      }
+    for (int c = 0; c < 2; ++c) {
+      cpe_n[c] = __ldg(cchk + ck_of(0, c));
+      g_n[c] = __ldg(gchk + ck_of(0, c));
+    }
     for (int u = 0; ok && u < n; ++u) {
       const bool diag = u == qt;          // keys after queries only on the diagonal tile
       for (int hh = 0; hh < 2 && ok; ++hh) {
         const int it = 2 * u + hh;
-        const float cpe_c[2] = {cpe_n[0][0], cpe_n[0][1]};
-        const float g_c[2] = {g_n[0][0], g_n[0][1]};
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          cpe_n[0][c] = cpe_n[1][c];
-          g_n[0][c] = g_n[1][c];
-        }
-        if (it + 2 < 2 * n) {
+        const float cpe_c[2] = {cpe_n[0], cpe_n[1]};
+        const float g_c[2] = {g_n[0], g_n[1]};
+        if (it + 1 < 2 * n) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            cpe_n[1][c] = __ldg(cchk + ck_of(it + 2, c));
-            g_n[1][c] = __ldg(gchk + ck_of(it + 2, c));
+            cpe_n[c] = __ldg(cchk + ck_of(it + 1, c));
+            g_n[c] = __ldg(gchk + ck_of(it + 1, c));
           }
         }
         if (!warp_wait(s_full, it & 1, wc) || (hh == 0 && !warp_wait(ds_free, (u & 1) ^ 1, wc))) {
