@@ -59,13 +59,6 @@ __device__ __forceinline__ void drain_wait_bt(uint64_t *bar, uint32_t parity) {
   }
 }
 
-// Bounded wait whose outcome is the same in every lane of the warp, for waits
-// followed by warp-collective instructions (tcgen05.ld, shuffles): a lane
-// that gave up takes the whole warp with it.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtx &wc) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
-}
-
 __device__ __forceinline__ void release_bt(uint64_t *bar, int lane) {
   tc_fence_before();
   __syncwarp();

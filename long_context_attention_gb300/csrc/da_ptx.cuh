@@ -110,6 +110,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   }
 }
 
+// Bounded wait whose outcome is the same in every lane of the warp, for waits
+// followed by warp-collective instructions (tcgen05.ld / st, shuffles): a
+// lane that gave up takes the whole warp with it, so no collective is ever
+// reached by part of a warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, uint64_t *bar, int x, int y,
                                             int z) {

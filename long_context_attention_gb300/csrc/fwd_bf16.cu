@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
     for (int kt = 0; kt <= qt; ++kt) {
       const int slot = g * NS + kt % NS;
       const uint32_t tbase = tmem + slot * kTile + ((uint32_t)(quarter * 32) << 16);
-      if (!mbar_wait(&s_full[slot], (kt / NS) & 1, wc)) break;
+      if (!warp_wait(&s_full[slot], (kt / NS) & 1, wc)) break;
       tc_fence_after();
       // 32-column chunks; the load of chunk c+1 is in flight while chunk c is reduced.
       float A[32], B[32];
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
       for (int t = 0; t < nt; ++t) {
         const int qrow = (w.q_tile0 + t) * kSwBQ;
         const float4 nl = __ldg(lsrc + qrow / 4);   // -lse2 of queries qrow + 4 lane .. + 3 (-inf past T)
-        if (!mbar_wait(q_empty, (t & 1) ^ 1, wc)) break;
+        if (!warp_wait(q_empty, (t & 1) ^ 1, wc)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full, kTB);
           tma_load_tile<D>(sQ, &tmQ, q_full, qrow, w.bh);
@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
     tmem_wait_st();
     release_tmem(d_free, lane);
     for (int t = 0; t < nt; ++t) {
-      if (!mbar_wait(d_full, t & 1, wc)) break;
+      if (!warp_wait(d_full, t & 1, wc)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + C::kTmemD + ((uint32_t)(quarter * 32) << 16);
       const int qrow0 = (w.q_tile0 + t) * kSwBQ + quarter * 32;   // first query row of this warp's box
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
       float *ck = (cchk == nullptr || kbase + row >= Tp)
                       ? nullptr
                       : cchk + ((size_t)w.bh * (Tp / 32) + qlo / 32) * Tp + kbase + row;
-      if (!mbar_wait(&s_full[g], t & 1, wc)) break;
+      if (!warp_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
       uint32_t pk[16];
       if (all_masked) {
@@ -820,7 +820,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         release_tmem(&s_free[g], lane);
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
-        if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
+        if (!warp_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c) store(pk, c);
       } else {
@@ -833,7 +833,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         if (need_mask) demand_chunk<true, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         else demand_chunk<false, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
-        if (!mbar_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
+        if (!warp_wait(&sh_free[g], (t & 1) ^ 1, wc)) break;
         store(pk, 0);
         tmem_wait_ld_r(B);
         tmem_ld32(tb + 64, A);
