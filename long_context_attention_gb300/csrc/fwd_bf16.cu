@@ -467,7 +467,8 @@ __device__ __forceinline__ void regs_dec_epi() { asm volatile("setmaxnreg.dec.sy
 template <int N>
 __device__ __forceinline__ void regs_dec_ctl() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
-template <int D, bool EARLIER>
+// CHK: also write the demand checkpoints (the backward's forward-again pass).
+template <int D, bool EARLIER, bool CHK>
 __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::kRegsLaunch)
     sweep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmAcc,
@@ -806,14 +807,12 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
       // Demand checkpoints for the backward (cchk != null): committed + eps of
       // this key at the start of each 32-query chunk, [bh][chunk][key < Tp]
       // (the last span can reach past Tp).
-      float *ck = (cchk == nullptr || kbase + row >= Tp)
-                      ? nullptr
-                      : cchk + ((size_t)w.bh * (Tp / 32) + qlo / 32) * Tp + kbase + row;
+      float *ck = (!CHK || kbase + row >= Tp) ? nullptr : cchk + ((size_t)w.bh * (Tp / 32) + qlo / 32) * Tp + kbase + row;
       if (!warp_wait(&s_full[g], t & 1, wc)) break;
       tc_fence_after();
       uint32_t pk[16];
       if (all_masked) {
-        if (ck != nullptr) {
+        if (CHK && ck != nullptr) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) ck[(size_t)c * Tp] = ceps;
         }
@@ -829,7 +828,7 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         tmem_ld32(tb, A);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 32, B);
-        if (ck != nullptr) ck[0 * (size_t)Tp] = ceps;
+        if (CHK && ck != nullptr) ck[0 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         else demand_chunk<false, 0, EARLIER>(A, row_eff, c2, ceps, pk);
         // the product of the previous query tile must be done reading this buffer
@@ -837,19 +836,19 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         store(pk, 0);
         tmem_wait_ld_r(B);
         tmem_ld32(tb + 64, A);
-        if (ck != nullptr) ck[1 * (size_t)Tp] = ceps;
+        if (CHK && ck != nullptr) ck[1 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         else demand_chunk<false, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 1);
         tmem_wait_ld_r(A);
         tmem_ld32(tb + 96, B);
-        if (ck != nullptr) ck[2 * (size_t)Tp] = ceps;
+        if (CHK && ck != nullptr) ck[2 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         else demand_chunk<false, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         store(pk, 2);
         tmem_wait_ld_r(B);
         release_tmem(&s_free[g], lane);
-        if (ck != nullptr) ck[3 * (size_t)Tp] = ceps;
+        if (CHK && ck != nullptr) ck[3 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 3, EARLIER>(B, row_eff, c2, ceps, pk);
         else demand_chunk<false, 3, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 3);
@@ -931,17 +930,17 @@ cudaError_t launch_finalize_bf16(const float *acc, const float *lse2_ws, __nv_bf
                                  float *lse2_out, int BH, int T, int d, cudaStream_t stream);
 
 // Shared-memory opt-in and register-split check of one sweep instantiation.
-template <int D, bool EARLIER>
+template <int D, bool EARLIER, bool CHK>
 static int prepare_sweep() {
   using C = SwCfg<D>;
-  if (cudaFuncSetAttribute(sweep_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(sweep_kernel<D, EARLIER, CHK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
     return DA_ERR_CUDA;
   // The sweep's warpgroups re-split the block's registers (setmaxnreg); a
   // split larger than what the block is launched with would never resolve,
   // so refuse to launch unless the compiled register count covers it.
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, sweep_kernel<D, EARLIER>) != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaFuncGetAttributes(&fa, sweep_kernel<D, EARLIER, CHK>) != cudaSuccess) return DA_ERR_CUDA;
   if (fa.numRegs * C::kThreads < C::kRegsNeeded || fa.numRegs > kSwRegsDemand || fa.numRegs < kSwRegsEpi)
     return DA_ERR_UNSUPPORTED;
   return DA_OK;
@@ -952,8 +951,12 @@ static int prepare_fwd_bf16() {
   if (cudaFuncSetAttribute(rowstats_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            RsCfg<D>::kSmemBytes) != cudaSuccess)
     return DA_ERR_CUDA;
-  int st = prepare_sweep<D, false>();
-  if (st == DA_OK) st = prepare_sweep<D, true>();
+  int st = prepare_sweep<D, false, false>();
+  if (st == DA_OK) st = prepare_sweep<D, true, false>();
+  if constexpr (D == 64) {   // the backward's forward-again sweep (d = 64 only)
+    if (st == DA_OK) st = prepare_sweep<D, false, true>();
+    if (st == DA_OK) st = prepare_sweep<D, true, true>();
+  }
   return st;
 }
 
@@ -980,10 +983,10 @@ static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const
   const int nsw = sweep_num_ctas(BH, T, D);
   const uint4 *kg = static_cast<const uint4 *>(k);
   if (earlier)
-    sweep_kernel<D, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
+    sweep_kernel<D, true, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
                                                                        nullptr, BH, T, Tp, hs, eps, status);
   else
-    sweep_kernel<D, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc,
+    sweep_kernel<D, false, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc,
                                                                         demand_out, nullptr, BH, T, Tp, hs, eps,
                                                                         status);
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
@@ -1013,10 +1016,10 @@ int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const flo
   const int nsw = sweep_num_ctas(BH, T, 64);
   const uint4 *kg = static_cast<const uint4 *>(k);
   if (earlier)
-    sweep_kernel<64, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr, cchk,
+    sweep_kernel<64, true, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr, cchk,
                                                                         BH, T, Tp, hs, eps, status);
   else
-    sweep_kernel<64, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr,
+    sweep_kernel<64, false, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr,
                                                                          cchk, BH, T, Tp, hs, eps, status);
   return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
