@@ -1,4 +1,4 @@
-// Tensor-core backward of dilution attention (bf16, d = 64).
+// Tensor-core backward of dilution attention (bf16, d = 64 and d = 128).
 //
 // Gradients of sum(dout * out) through the operator of "DilutionAttention
 // v0.1.0 · results", section "The operator" (the page states only that exact
@@ -29,7 +29,9 @@
 //       and tcgen05 accumulates dV += A^T G and dK += ds^T Q in TMEM;
 //   Q   query-major: for each key tile the threads write ds (MN-major) and
 //       tcgen05 accumulates dQ += ds K in TMEM.
-// S and dA' are formed 64 queries at a time (N = 64) so two CTAs fit an SM;
+// S and dA' are formed 64 queries at a time (N = 64) so two CTAs fit an SM
+// at d = 64 (one at d = 128, where the tiles and the N = 128 accumulators take
+// the SM);
 // -lse2 / c2 and -delta ride in a fifth K step of their products (the
 // extension operands of the forward sweep).  Every wait is bounded.
 #include "da_internal.h"
@@ -43,13 +45,23 @@ namespace da {
 namespace {
 
 constexpr int kBtThreads = 192;                    // 4 demand warps, producer, MMA issuer
-constexpr uint32_t kTile16 = kTile * 64 * 2;       // 128 rows x 64 bf16, 128B swizzle
-constexpr uint32_t kHalf16 = 64 * 64 * 2;          // 64 rows x 64 bf16
+// A tile of R rows x d bf16 is stored as d / 64 column halves of R rows x 64
+// (128-byte swizzled rows), R * 128 bytes each.
+constexpr uint32_t kH128 = kTile * 64 * 2;         // one half of a 128-row tile
+constexpr uint32_t kH64 = 64 * 64 * 2;             // one half of a 64-row tile
 constexpr uint32_t kExt128 = 128 * 16 * 2;         // extension operand, 128 rows
 constexpr uint32_t kExt64 = 64 * 16 * 2;           // extension operand, 64 rows
 
 __device__ __forceinline__ uint64_t kdesc(const uint8_t *tile, int kstep) {
   return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
+}
+
+// TMA load of one R-row tile of a [BH, T, d] tensor, half by half (the maps
+// have 64-column boxes of R rows).
+template <int D, uint32_t HALF>
+__device__ __forceinline__ void load_tile_halves(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int row, int bh) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * HALF, map, bar, h * 64, row, bh);
 }
 
 __device__ __forceinline__ void drain_wait_bt(uint64_t *bar, uint32_t parity) {
@@ -99,19 +111,21 @@ __device__ __forceinline__ void fill_ones_ext(uint8_t *ext, int tid, int nthread
 
 // ---------------------------------------------------------------- prep / rows
 // -lse2 for the sweep (rows past T: -inf) and zeroed forward accumulators.
+template <int D>
 __global__ void bwdtc_prep(const float *__restrict__ lse2, float *__restrict__ nlse2, float *__restrict__ acc,
                            int BH, int T, int Tp) {
   const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= (int64_t)BH * Tp) return;
   const int64_t bh = row / Tp, i = row % Tp;
   nlse2[row] = i < T ? -lse2[bh * T + i] : -INFINITY;
-  float4 *ar = reinterpret_cast<float4 *>(acc + row * acc_stride(64));
+  float4 *ar = reinterpret_cast<float4 *>(acc + row * acc_stride(D));
 #pragma unroll
-  for (int t = 0; t < acc_stride(64) / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t = 0; t < acc_stride(D) / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // 1/R_j, delta_j = g_j . out_j (out = numerator / R) and rho_j = 0; 16 threads
-// per row.  Rows past T get zeros, so their dr vanish.
+// per row, d / 16 columns each.  Rows past T get zeros, so their dr vanish.
+template <int D>
 __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *__restrict__ g,
                            float *__restrict__ rinv, float *__restrict__ delta, float *__restrict__ rho, int BH,
                            int T, int Tp) {
@@ -122,13 +136,16 @@ __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *_
   const int64_t bh = live ? row / Tp : 0, i = live ? row % Tp : 0;
   float dot = 0.f, inv = 0.f;
   if (live && i < T) {
-    const float *ar = acc + row * acc_stride(64);
-    inv = 1.f / ar[64];
-    const float4 a = reinterpret_cast<const float4 *>(ar)[part];
-    const uint2 gg = reinterpret_cast<const uint2 *>(g + (bh * T + i) * 64)[part];
-    const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.x));
-    const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.y));
-    dot = (a.x * g01.x + a.y * g01.y) + (a.z * g23.x + a.w * g23.y);
+    const float *ar = acc + row * acc_stride(D);
+    inv = 1.f / ar[D];
+#pragma unroll
+    for (int j = 0; j < D / 64; ++j) {
+      const float4 a = reinterpret_cast<const float4 *>(ar)[part + 16 * j];
+      const uint2 gg = reinterpret_cast<const uint2 *>(g + (bh * T + i) * D)[part + 16 * j];
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.y));
+      dot += (a.x * g01.x + a.y * g01.y) + (a.z * g23.x + a.w * g23.y);
+    }
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
@@ -237,12 +254,13 @@ __device__ __forceinline__ float warp_column_sum(const float (&X)[32], float *re
 // back to the diagonal, MODE 1 (KV) forward.
 constexpr int kModeB1 = 0, kModeKV = 1;
 
-template <int MODE>
+template <int MODE, int D>
 struct KeyCfg {
-  static constexpr uint32_t kOffK = 0, kOffV = kTile16;
-  static constexpr uint32_t kOffQh = 2 * kTile16;                 // [2] half tiles of Q
-  static constexpr uint32_t kOffGh = kOffQh + 2 * kHalf16;        // [2] half tiles of dout
-  static constexpr uint32_t kOffAExt = kOffGh + 2 * kHalf16;
+  static constexpr uint32_t kTB = kTile * D * 2, kHB = 64 * D * 2;   // 128-row and 64-row tiles
+  static constexpr uint32_t kOffK = 0, kOffV = kTB;
+  static constexpr uint32_t kOffQh = 2 * kTB;                     // [2] 64-query tiles of Q
+  static constexpr uint32_t kOffGh = kOffQh + 2 * kHB;            // [2] 64-query tiles of dout
+  static constexpr uint32_t kOffAExt = kOffGh + 2 * kHB;
   static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // [2] -lse2 / c2 rows
   static constexpr uint32_t kOffBExtA = kOffBExtS + 2 * kExt64;   // [2] -delta rows
   static constexpr uint32_t kOffRinv = kOffBExtA + 2 * kExt64;    // [2][64] fp32
@@ -250,21 +268,35 @@ struct KeyCfg {
   static constexpr uint32_t kOffRed = kOffRho + 2 * 64 * 4;       // [2][4][64] fp32 (B1)
   static constexpr uint32_t kOffXp = kOffRed + 2 * 4 * 64 * 4;    // [4][32][36] fp32 (B1)
   static constexpr uint32_t kOffAT = MODE == kModeB1 ? kOffXp + 4 * 32 * 36 * 4 : kOffXp;   // A^T (KV)
-  static constexpr uint32_t kOffDsT = kOffAT + kTile16;           // ds^T, K-major (KV)
-  static constexpr uint32_t kOffBar = MODE == kModeKV ? kOffDsT + kTile16 : kOffAT;
+  static constexpr uint32_t kOffDsT = kOffAT + kH128;             // ds^T, K-major (KV)
+  static constexpr uint32_t kOffBar = MODE == kModeKV ? kOffDsT + kH128 : kOffAT;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + re-alignment slack
+  // TMEM: S' and dA' slots (B1: two of each), then (KV) dV and dK, d columns each
+  static constexpr uint32_t kTmemDV = 128, kTmemDK = 128 + D;
+  static constexpr uint32_t kTmemCols = (MODE == kModeB1 || D == 64) ? 256 : 512;
+  static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
   static_assert(kOffAT % 1024 == 0, "swizzled operands");
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-template <int MODE, bool EARLIER>
-__global__ void __launch_bounds__(kBtThreads, 2)
+// The K-major S' = K Q^T (or dA' = V G^T) product over d: K steps 0..3 read
+// the first 64 columns of both operands, 4..7 (d = 128) the second halves.
+template <int D>
+__device__ __forceinline__ void mma_over_d(uint32_t dt, uint64_t da, uint32_t half_a, uint64_t db, uint32_t half_b,
+                                           uint32_t idesc) {
+  MmaRun<0, 4, 2, 2, false>::go(dt, da, db, idesc, 0u);
+  if constexpr (D == 128) MmaRun<0, 4, 2, 2, false>::go(dt, da + (half_a >> 4), db + (half_b >> 4), idesc, 1u);
+}
+
+template <int MODE, int D, bool EARLIER>
+__global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
     bwdtc_key_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmGh,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const float *__restrict__ nlse2, const float *__restrict__ delta,
                      const float *__restrict__ rinv, float *__restrict__ rho, const float *__restrict__ cchk,
                      float *__restrict__ gchk, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int BH,
                      int T, int Tp, HeadScale hs, float c_scalar, int *status) {
-  using C = KeyCfg<MODE>;
+  using C = KeyCfg<MODE, D>;
   extern __shared__ uint8_t bt_smem_raw[];
   uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
   uint8_t *sK = smem + C::kOffK, *sV = smem + C::kOffV;
@@ -312,7 +344,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
   zero_smem(smem + C::kOffBExtS, 4 * kExt64, threadIdx.x, kBtThreads);   // both buffers of both rows
   fence_proxy_async_smem();
   if (warp == 5) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
@@ -328,18 +360,18 @@ __global__ void __launch_bounds__(kBtThreads, 2)
       prefetch_tmap(&tmGh);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(kv_full, 2 * kTile16);
-      tma_load_3d(sK, &tmK, kv_full, 0, kt * kTile, bh);
-      tma_load_3d(sV, &tmV, kv_full, 0, kt * kTile, bh);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTB);
+      load_tile_halves<D, kH128>(sK, &tmK, kv_full, kt * kTile, bh);
+      load_tile_halves<D, kH128>(sV, &tmV, kv_full, kt * kTile, bh);
     }
     int issued = 0;
     for (int u = 0; u < n; ++u) {
       const int b = u & 1, h = half_of(u);
       if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&in_full[b], 2 * kHalf16);
-        tma_load_3d(smem + C::kOffQh + b * kHalf16, &tmQh, &in_full[b], 0, h * 64, bh);
-        tma_load_3d(smem + C::kOffGh + b * kHalf16, &tmGh, &in_full[b], 0, h * 64, bh);
+        mbar_arrive_expect_tx(&in_full[b], 2 * C::kHB);
+        load_tile_halves<D, kH64>(smem + C::kOffQh + b * C::kHB, &tmQh, &in_full[b], h * 64, bh);
+        load_tile_halves<D, kH64>(smem + C::kOffGh + b * C::kHB, &tmGh, &in_full[b], h * 64, bh);
       }
       ++issued;
 #pragma unroll
@@ -365,7 +397,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
       constexpr long long kStepKm = 2;                       // K-major: +32 bytes per K step
       constexpr long long kStepMn = 128;                     // MN-major: +16 rows (2 KB) per K step
       const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
-      const uint32_t idesc_kv = idesc_bf16(kTile, 64, false, true);
+      const uint32_t idesc_kv = idesc_bf16(kTile, D, false, true);
       const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
       const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
       bool ok = mbar_wait(kv_full, 0, wc);
@@ -377,29 +409,32 @@ __global__ void __launch_bounds__(kBtThreads, 2)
           const uint32_t par_free = MODE == kModeB1 ? (((u >> 1) & 1) ^ 1) : ((u & 1) ^ 1);
           if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(&s_free[slot], par_free, wc)) break;
           tc_fence_after();
-          const uint64_t dQh = kdesc(smem + C::kOffQh + b * kHalf16, 0);
-          const uint64_t dGh = kdesc(smem + C::kOffGh + b * kHalf16, 0);
+          const uint64_t dQh = kdesc(smem + C::kOffQh + b * C::kHB, 0);
+          const uint64_t dGh = kdesc(smem + C::kOffGh + b * C::kHB, 0);
           const uint64_t dBS = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtS + b * kExt64), 128, 256);
           const uint64_t dBA = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtA + b * kExt64), 128, 256);
           const uint32_t tS = tmem + slot * 64, tA = tmem + 128 + slot * 64;
           const uint32_t tSk = MODE == kModeB1 ? tS : tmem, tAk = MODE == kModeB1 ? tA : tmem + 64;
-          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tSk, dK, dQh, idesc_s, 0u);
+          mma_over_d<D>(tSk, dK, kH128, dQh, kH64, idesc_s);
           mma_bf16_at<0, 0>(tSk, dAExt, dBS, idesc_s, 1u);
-          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tAk, dV, dGh, idesc_s, 0u);
+          mma_over_d<D>(tAk, dV, kH128, dGh, kH64, idesc_s);
           mma_bf16_at<0, 0>(tAk, dAExt, dBA, idesc_s, 1u);
           mma_commit(&s_full[slot]);
           if (MODE == kModeB1) mma_commit(&in_empty[b]);
         }
         if (MODE == kModeKV && u >= 1) {
           // dV += A^T G, dK += ds^T Q for half tile u - 1 (its operands: G and Q
-          // of buffer bp as MN-major B, 16 queries = 2 KB per K step)
+          // of buffer bp as MN-major B, 16 queries = 2 KB per K step, the two
+          // 64-column halves of d = 128 8 KB apart)
           const int up = u - 1, bp = up & 1;
           if (!mbar_wait(&w_full[0], up & 1, wc)) break;
           tc_fence_after();
-          const uint64_t dGmn = smem_desc(smem_u32(smem + C::kOffGh + bp * kHalf16), kHalf16, 1024);
-          const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * kHalf16), kHalf16, 1024);
-          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + 128, kdesc(sAT, 0), dGmn, idesc_kv, up > 0 ? 1u : 0u);
-          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + 192, kdesc(sDsT, 0), dQmn, idesc_kv, up > 0 ? 1u : 0u);
+          const uint64_t dGmn = smem_desc(smem_u32(smem + C::kOffGh + bp * C::kHB), kH64, 1024);
+          const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * C::kHB), kH64, 1024);
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemDV, kdesc(sAT, 0), dGmn, idesc_kv,
+                                                    up > 0 ? 1u : 0u);
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemDK, kdesc(sDsT, 0), dQmn, idesc_kv,
+                                                    up > 0 ? 1u : 0u);
           mma_commit(&w_free[0]);
           mma_commit(&in_empty[bp]);
           if (u == n) mma_commit(fin);
@@ -526,17 +561,18 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     }
     if (MODE == kModeKV && ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
       tc_fence_after();
-      // dV (TMEM columns 128..191) and dK (192..255) of this key: out in bf16
+      // dV (TMEM columns 128 ..) and dK (128 + d ..) of this key: out in bf16
       const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
       // (tcgen05.ld is warp-collective: every lane loads, only keys < T store)
       float x[32];
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        tmem_ld32(tmem + 128 + lanes + 32 * part, x);
+      for (int part = 0; part < D / 16; ++part) {   // d / 32 parts of dV, then of dK
+        tmem_ld32(tmem + C::kTmemDV + lanes + 32 * part, x);
         tmem_wait_ld_r(x);
         if (key < T) {
-          const float sc = part < 2 ? 1.f : cs;
-          __nv_bfloat16 *dst = (part < 2 ? dv : dk) + ((size_t)bh * T + key) * 64 + 32 * (part & 1);
+          const bool is_v = part < D / 32;
+          const float sc = is_v ? 1.f : cs;
+          __nv_bfloat16 *dst = (is_v ? dv : dk) + ((size_t)bh * T + key) * D + 32 * (part % (D / 32));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             reinterpret_cast<uint4 *>(dst)[j] =
@@ -552,7 +588,7 @@ __global__ void __launch_bounds__(kBtThreads, 2)
   if (warp == 5) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -562,9 +598,11 @@ __global__ void __launch_bounds__(kBtThreads, 2)
 // TMEM slot pair, reused), one thread per key writing ds (MN-major, the
 // layout of the forward's share^T), then dQ += ds K (M = 128 queries, N = 64,
 // K = 128 keys) accumulating in TMEM.
+template <int D>
 struct QCfg {
-  static constexpr uint32_t kOffQ = 0, kOffG = kTile16, kOffK = 2 * kTile16, kOffV = 3 * kTile16;
-  static constexpr uint32_t kOffDs = 4 * kTile16;                 // 2 M-blocks x 16 key groups x 1 KB
+  static constexpr uint32_t kTB = kTile * D * 2;
+  static constexpr uint32_t kOffQ = 0, kOffG = kTB, kOffK = 2 * kTB, kOffV = 3 * kTB;
+  static constexpr uint32_t kOffDs = 4 * kTB;                     // 2 M-blocks x 16 key groups x 1 KB
   static constexpr uint32_t kOffAExt = kOffDs + 2 * 16 * 1024;
   static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // 128 query rows
   static constexpr uint32_t kOffBExtA = kOffBExtS + kExt128;
@@ -572,17 +610,19 @@ struct QCfg {
   static constexpr uint32_t kOffRho = kOffRinv + 128 * 4;         // [128] fp32
   static constexpr uint32_t kOffBar = kOffRho + 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-template <bool EARLIER>
-__global__ void __launch_bounds__(kBtThreads, 2)
+template <int D, bool EARLIER>
+__global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
     bwdtc_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const float *__restrict__ nlse2, const float *__restrict__ delta, const float *__restrict__ rinv,
                    const float *__restrict__ rho, const float *__restrict__ cchk, const float *__restrict__ gchk,
                    __nv_bfloat16 *__restrict__ dq, int BH, int T, int Tp, HeadScale hs, float c_scalar,
                    int *status) {
-  using C = QCfg;
+  using C = QCfg<D>;
   extern __shared__ uint8_t bt_smem_raw[];
   uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
   uint8_t *sQ = smem + C::kOffQ, *sG = smem + C::kOffG, *sK = smem + C::kOffK, *sV = smem + C::kOffV;
@@ -640,9 +680,9 @@ __global__ void __launch_bounds__(kBtThreads, 2)
       prefetch_tmap(&tmG);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(q_full, 2 * kTile16);
-      tma_load_3d(sQ, &tmQ, q_full, 0, qt * kTile, bh);
-      tma_load_3d(sG, &tmG, q_full, 0, qt * kTile, bh);
+      mbar_arrive_expect_tx(q_full, 2 * C::kTB);
+      load_tile_halves<D, kH128>(sQ, &tmQ, q_full, qt * kTile, bh);
+      load_tile_halves<D, kH128>(sG, &tmG, q_full, qt * kTile, bh);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -660,11 +700,11 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     if (lane == 0) {
       for (int u = 0; u < n; ++u) {
         if (!mbar_wait(k_empty, (u & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(k_full, kTile16);
-        tma_load_3d(sK, &tmK, k_full, 0, u * kTile, bh);
+        mbar_arrive_expect_tx(k_full, C::kTB);
+        load_tile_halves<D, kH128>(sK, &tmK, k_full, u * kTile, bh);
         if (!mbar_wait(v_empty, (u & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(v_full, kTile16);
-        tma_load_3d(sV, &tmV, v_full, 0, u * kTile, bh);
+        mbar_arrive_expect_tx(v_full, C::kTB);
+        load_tile_halves<D, kH128>(sV, &tmV, v_full, u * kTile, bh);
         ++issued;
       }
       if (*abort_flag) {
@@ -680,13 +720,14 @@ __global__ void __launch_bounds__(kBtThreads, 2)
     if (lane == 0) {
       constexpr long long kStepKm = 2, kStepMn = 128;
       const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
-      const uint32_t idesc_q = idesc_bf16(kTile, 64, true, true);
+      const uint32_t idesc_q = idesc_bf16(kTile, D, true, true);
       const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
       const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
       // ds: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB
-      // apart (SBO); K as the MN-major B operand (16 keys = 2 KB per K step)
+      // apart (SBO); K as the MN-major B operand (16 keys = 2 KB per K step,
+      // its 64-column halves 16 KB apart)
       const uint64_t dDs = smem_desc(smem_u32(sDs), 16384, 1024);
-      const uint64_t dKmn = smem_desc(smem_u32(sK), kTile16, 1024);
+      const uint64_t dKmn = smem_desc(smem_u32(sK), kH128, 1024);
       bool ok = mbar_wait(q_full, 0, wc);
       if (ok) tc_fence_after();
       for (int u = 0; ok && u < n; ++u) {
@@ -704,9 +745,9 @@ __global__ void __launch_bounds__(kBtThreads, 2)
           const uint64_t dQh = kdesc(sQ + hh * 8192, 0), dGh = kdesc(sG + hh * 8192, 0);
           const uint64_t dBS = smem_desc_noswizzle(smem_u32(sBExtS) + hh * 2048, 128, 256);
           const uint64_t dBA = smem_desc_noswizzle(smem_u32(sBExtA) + hh * 2048, 128, 256);
-          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tmem, dK, dQh, idesc_s, 0u);
+          mma_over_d<D>(tmem, dK, kH128, dQh, kH128, idesc_s);
           mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
-          MmaRun<0, 4, kStepKm, kStepKm, false>::go(tmem + 64, dV, dGh, idesc_s, 0u);
+          mma_over_d<D>(tmem + 64, dV, kH128, dGh, kH128, idesc_s);
           mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
           mma_commit(s_full);
         }
@@ -802,11 +843,11 @@ __global__ void __launch_bounds__(kBtThreads, 2)
       const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
       float x[32];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      for (int part = 0; part < D / 32; ++part) {
         tmem_ld32(tmem + 128 + lanes + 32 * part, x);
         tmem_wait_ld_r(x);
         if (qi < T) {
-          __nv_bfloat16 *dst = dq + ((size_t)bh * T + qi) * 64 + 32 * part;
+          __nv_bfloat16 *dst = dq + ((size_t)bh * T + qi) * D + 32 * part;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             reinterpret_cast<uint4 *>(dst)[j] =
@@ -829,45 +870,48 @@ __global__ void __launch_bounds__(kBtThreads, 2)
 // ------------------------------------------------------------------- host
 bool make_bf16_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d, int rows);
 int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const float *nlse2, float *acc, float *cchk,
-                          int BH, int T, HeadScale hs, float eps, bool earlier, int *status, cudaStream_t stream);
+                          int BH, int T, int d, HeadScale hs, float eps, bool earlier, int *status,
+                          cudaStream_t stream);
 
-template <bool EARLIER>
+template <int D, bool EARLIER>
 static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, float *rinv, float *rho, float *cchk,
                          float *gchk, void *dq, void *dk, void *dv, int BH, int T, int Tp, HeadScale hs, float c,
                          int *status, cudaStream_t stream) {
+  using KB1 = KeyCfg<kModeB1, D>;
+  using KKV = KeyCfg<kModeKV, D>;
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
   if (dev >= 64 || !attr_done[dev]) {
-    if (cudaFuncSetAttribute(bwdtc_key_kernel<kModeB1, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KeyCfg<kModeB1>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(bwdtc_key_kernel<kModeKV, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KeyCfg<kModeKV>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(bwdtc_q_kernel<EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             QCfg::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(bwdtc_key_kernel<kModeB1, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KB1::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwdtc_key_kernel<kModeKV, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KKV::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwdtc_q_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             QCfg<D>::kSmemBytes) != cudaSuccess)
       return DA_ERR_CUDA;
     if (dev < 64) attr_done[dev] = true;
   }
   const int NT = Tp / kTile;
   const unsigned grid = (unsigned)(NT * BH);
   // maps: 0 Q (64-row boxes), 1 dout (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout (128)
-  bwdtc_key_kernel<kModeB1, EARLIER><<<grid, kBtThreads, KeyCfg<kModeB1>::kSmemBytes, stream>>>(
+  bwdtc_key_kernel<kModeB1, D, EARLIER><<<grid, kBtThreads, KB1::kSmemBytes, stream>>>(
       maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, nullptr, nullptr, BH, T, Tp, hs, c,
       status);
-  bwdtc_key_kernel<kModeKV, EARLIER><<<grid, kBtThreads, KeyCfg<kModeKV>::kSmemBytes, stream>>>(
+  bwdtc_key_kernel<kModeKV, D, EARLIER><<<grid, kBtThreads, KKV::kSmemBytes, stream>>>(
       maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk,
       static_cast<__nv_bfloat16 *>(dk), static_cast<__nv_bfloat16 *>(dv), BH, T, Tp, hs, c, status);
-  bwdtc_q_kernel<EARLIER><<<grid, kBtThreads, QCfg::kSmemBytes, stream>>>(
+  bwdtc_q_kernel<D, EARLIER><<<grid, kBtThreads, QCfg<D>::kSmemBytes, stream>>>(
       maps[4], maps[5], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, static_cast<__nv_bfloat16 *>(dq),
       BH, T, Tp, hs, c, status);
   return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
-// The tensor-core backward (bf16, d = 64): the passes in the file header.
+// The tensor-core backward (bf16, d = 64 or 128): the passes in the file header.
 int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
-                       void *dk, void *dv, int BH, int T, HeadScale hs, float c, float eps, bool earlier,
+                       void *dk, void *dv, int BH, int T, int d, HeadScale hs, float c, float eps, bool earlier,
                        uint8_t *ws, cudaStream_t stream) {
-  const BwdTcWorkspace L = bwd_tc_workspace_layout(BH, T);
+  const BwdTcWorkspace L = bwd_tc_workspace_layout(BH, T, d);
   const int Tp = (int)t_pad(T);
   const int64_t rows = (int64_t)BH * Tp;
   int *status = reinterpret_cast<int *>(ws);
@@ -878,19 +922,23 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
   float *cchk = reinterpret_cast<float *>(ws + L.cchk_off);
   float *gchk = reinterpret_cast<float *>(ws + L.gchk_off);
   CUtensorMap maps[6];
-  if (!make_bf16_tile_map(&maps[0], q, BH, T, 64, 64) || !make_bf16_tile_map(&maps[1], dout, BH, T, 64, 64) ||
-      !make_bf16_tile_map(&maps[2], k, BH, T, 64, kTile) || !make_bf16_tile_map(&maps[3], v, BH, T, 64, kTile) ||
-      !make_bf16_tile_map(&maps[4], q, BH, T, 64, kTile) || !make_bf16_tile_map(&maps[5], dout, BH, T, 64, kTile))
+  if (!make_bf16_tile_map(&maps[0], q, BH, T, d, 64) || !make_bf16_tile_map(&maps[1], dout, BH, T, d, 64) ||
+      !make_bf16_tile_map(&maps[2], k, BH, T, d, kTile) || !make_bf16_tile_map(&maps[3], v, BH, T, d, kTile) ||
+      !make_bf16_tile_map(&maps[4], q, BH, T, d, kTile) || !make_bf16_tile_map(&maps[5], dout, BH, T, d, kTile))
     return DA_ERR_CUDA;
-  bwdtc_prep<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
-  int st = launch_sweep_bf16_chk(q, k, v, nlse2, acc, cchk, BH, T, hs, eps, earlier, status, stream);
+  const unsigned gp = (unsigned)((rows + 255) / 256), gr = (unsigned)((rows * 16 + 255) / 256);
+  if (d == 128) bwdtc_prep<128><<<gp, 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
+  else bwdtc_prep<64><<<gp, 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
+  int st = launch_sweep_bf16_chk(q, k, v, nlse2, acc, cchk, BH, T, d, hs, eps, earlier, status, stream);
   if (st != DA_OK) return st;
-  bwdtc_rows<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, stream>>>(
-      acc, static_cast<const __nv_bfloat16 *>(dout), rinv, delta, rho, BH, T, Tp);
-  return earlier ? launch_passes<true>(maps, nlse2, delta, rinv, rho, cchk, gchk, dq, dk, dv, BH, T, Tp, hs, c, status,
-                                       stream)
-                 : launch_passes<false>(maps, nlse2, delta, rinv, rho, cchk, gchk, dq, dk, dv, BH, T, Tp, hs, c,
-                                        status, stream);
+  const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(dout);
+  if (d == 128) bwdtc_rows<128><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
+  else bwdtc_rows<64><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
+#define DA_BWD_PASSES_ARGS maps, nlse2, delta, rinv, rho, cchk, gchk, dq, dk, dv, BH, T, Tp, hs, c, status, stream
+  if (d == 128)
+    return earlier ? launch_passes<128, true>(DA_BWD_PASSES_ARGS) : launch_passes<128, false>(DA_BWD_PASSES_ARGS);
+  return earlier ? launch_passes<64, true>(DA_BWD_PASSES_ARGS) : launch_passes<64, false>(DA_BWD_PASSES_ARGS);
+#undef DA_BWD_PASSES_ARGS
 }
 
 }  // namespace da

@@ -20,7 +20,7 @@ cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *
                        void *dk, void *dv, int BH, int T, int d, float c, HeadScale hs, float eps, bool earlier,
                        int dtype, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream);
 int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
-                       void *dk, void *dv, int BH, int T, HeadScale hs, float c, float eps, bool earlier,
+                       void *dk, void *dv, int BH, int T, int d, HeadScale hs, float c, float eps, bool earlier,
                        uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
@@ -140,12 +140,12 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
                          acc, status, stream, ev);
 }
 
-// bf16 at d = 64 runs the tensor-core backward; every other case the SIMT one.
-static bool bwd_on_tensor_cores(int d, int dtype) { return dtype == DA_BF16 && d == 64; }
+// bf16 runs the tensor-core backward; fp32 the SIMT one.
+static bool bwd_on_tensor_cores(int d, int dtype) { return dtype == DA_BF16 && (d == 64 || d == 128); }
 
 size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
   if (B < 0 || H < 0 || T < 0 || !head_dim_supported(d)) return 0;
-  if (bwd_on_tensor_cores(d, dtype)) return bwd_tc_workspace_layout((int64_t)B * H, T).total;
+  if (bwd_on_tensor_cores(d, dtype)) return bwd_tc_workspace_layout((int64_t)B * H, T, d).total;
   return bwd_workspace_layout((int64_t)B * H, T, d).total;
 }
 
@@ -167,7 +167,7 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
   const void *ptrs[] = {q, k, v, dout, lse2, dq, dk, dv};
   for (const void *p : ptrs)
     if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
-  const size_t need = bwd_on_tensor_cores(d, dtype) ? bwd_tc_workspace_layout(BH, T).total
+  const size_t need = bwd_on_tensor_cores(d, dtype) ? bwd_tc_workspace_layout(BH, T, d).total
                                                    : bwd_workspace_layout(BH, T, d).total;
   if (workspace == nullptr || workspace_bytes < need) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
@@ -177,7 +177,7 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
   const float c = (float)((double)tau / std::sqrt((double)d));
   if (bwd_on_tensor_cores(d, dtype)) {
     if ((int64_t)BH * t_pad(T) > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;
-    return launch_bwd_bf16_tc(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, head_scale(tau, tau_bh, d), c, eps,
+    return launch_bwd_bf16_tc(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, d, head_scale(tau, tau_bh, d), c, eps,
                               (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, ws, stream);
   }
   const BwdWorkspace L = bwd_workspace_layout(BH, T, d);

@@ -68,8 +68,8 @@ DA_HD BwdWorkspace bwd_workspace_layout(int64_t BH, int64_t T, int d) {
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core backward workspace (bf16, d = 64):
-// [status | -lse2 [BH][Tp] | acc [BH][Tp][68] | 1/R, delta, rho [3][BH][Tp] |
+// Tensor-core backward workspace (bf16):
+// [status | -lse2 [BH][Tp] | acc [BH][Tp][d + 4] | 1/R, delta, rho [3][BH][Tp] |
 //  demand checkpoints [BH][Tp/32][Tp] | reverse-sum checkpoints [BH][Tp/32][Tp]]
 // The checkpoints hold, for every key and every 32-query chunk at or after
 // the key's sweep span, committed + eps (forward order) and the sum of dC
@@ -79,12 +79,12 @@ struct BwdTcWorkspace {
   size_t nlse2_off, acc_off, rows_off, cchk_off, gchk_off, total;
 };
 
-DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T) {
+DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T, int d) {
   BwdTcWorkspace w;
   const int64_t Tp = t_pad(T);
   w.nlse2_off = kStatusBytes;
   w.acc_off = (size_t)round_up((int64_t)w.nlse2_off + BH * Tp * 4, 256);
-  w.rows_off = (size_t)round_up((int64_t)w.acc_off + BH * Tp * acc_stride(64) * 4, 256);
+  w.rows_off = (size_t)round_up((int64_t)w.acc_off + BH * Tp * acc_stride(d) * 4, 256);
   w.cchk_off = (size_t)round_up((int64_t)w.rows_off + 3 * BH * Tp * 4, 256);
   w.gchk_off = (size_t)round_up((int64_t)w.cchk_off + BH * (Tp / 32) * Tp * 4, 256);
   w.total = (size_t)round_up((int64_t)w.gchk_off + BH * (Tp / 32) * Tp * 4, 256);

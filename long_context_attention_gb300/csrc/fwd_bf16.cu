@@ -953,10 +953,8 @@ static int prepare_fwd_bf16() {
     return DA_ERR_CUDA;
   int st = prepare_sweep<D, false, false>();
   if (st == DA_OK) st = prepare_sweep<D, true, false>();
-  if constexpr (D == 64) {   // the backward's forward-again sweep (d = 64 only)
-    if (st == DA_OK) st = prepare_sweep<D, false, true>();
-    if (st == DA_OK) st = prepare_sweep<D, true, true>();
-  }
+  if (st == DA_OK) st = prepare_sweep<D, false, true>();   // the backward's forward-again sweep
+  if (st == DA_OK) st = prepare_sweep<D, true, true>();
   return st;
 }
 
@@ -993,35 +991,45 @@ static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const
   return DA_OK;
 }
 
-// The demand sweep alone (d = 64), for the backward: the caller has written
-// -lse2 to nlse2 and zeroed acc; cchk receives the demand checkpoints.
-int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const float *nlse2, float *acc, float *cchk,
-                          int BH, int T, HeadScale hs, float eps, bool earlier, int *status, cudaStream_t stream) {
+// The demand sweep alone, for the backward: the caller has written -lse2 to
+// nlse2 and zeroed acc; cchk receives the demand checkpoints.
+template <int D>
+static int launch_sweep_chk_t(const void *q, const void *k, const void *v, const float *nlse2, float *acc,
+                              float *cchk, int BH, int T, HeadScale hs, float eps, bool earlier, int *status,
+                              cudaStream_t stream) {
   const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
   if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv, ta;
-  if (!make_tile_map(&tq, q, BH, T, 64) || !make_tile_map(&tk, k, BH, T, 64) || !make_tile_map(&tv, v, BH, T, 64) ||
-      !make_acc_map(&ta, acc, acc_rows, 64))
+  if (!make_tile_map(&tq, q, BH, T, D) || !make_tile_map(&tk, k, BH, T, D) || !make_tile_map(&tv, v, BH, T, D) ||
+      !make_acc_map(&ta, acc, acc_rows, D))
     return DA_ERR_CUDA;
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
   if (dev >= 64 || !attr_done[dev]) {
-    const int st = prepare_fwd_bf16<64>();
+    const int st = prepare_fwd_bf16<D>();
     if (st != DA_OK) return st;
     if (dev < 64) attr_done[dev] = true;
   }
-  using C = SwCfg<64>;
+  using C = SwCfg<D>;
   const int Tp = (int)t_pad(T);
-  const int nsw = sweep_num_ctas(BH, T, 64);
+  const int nsw = sweep_num_ctas(BH, T, D);
   const uint4 *kg = static_cast<const uint4 *>(k);
   if (earlier)
-    sweep_kernel<64, true, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr, cchk,
-                                                                        BH, T, Tp, hs, eps, status);
+    sweep_kernel<D, true, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr,
+                                                                             cchk, BH, T, Tp, hs, eps, status);
   else
-    sweep_kernel<64, false, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc, nullptr,
-                                                                         cchk, BH, T, Tp, hs, eps, status);
+    sweep_kernel<D, false, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, nlse2, acc,
+                                                                              nullptr, cchk, BH, T, Tp, hs, eps,
+                                                                              status);
   return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const float *nlse2, float *acc, float *cchk,
+                          int BH, int T, int d, HeadScale hs, float eps, bool earlier, int *status,
+                          cudaStream_t stream) {
+  return d == 128 ? launch_sweep_chk_t<128>(q, k, v, nlse2, acc, cchk, BH, T, hs, eps, earlier, status, stream)
+                  : launch_sweep_chk_t<64>(q, k, v, nlse2, acc, cchk, BH, T, hs, eps, earlier, status, stream);
 }
 
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,

@@ -87,7 +87,7 @@ def test_decode_d128(dtype, n_ctx):
     assert torch.equal(kc[:, :, n_ctx], kn) and torch.equal(vc[:, :, n_ctx], vn)
 
 
-@pytest.mark.parametrize("dtype,T,tol", [("f32", 200, 2e-4), ("bf16", 129, 1.5e-2)])
+@pytest.mark.parametrize("dtype,T,tol", [("f32", 200, 2e-4), ("bf16", 129, 1.5e-2), ("bf16", 700, 1.5e-2)])
 def test_bwd_d128(dtype, T, tol):
     q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 2, T, D, q_std=1.5, pairs=4, seed=1500 + T, dtype=dtype))
     g = inputs.make_like((1, 2, T, D), seed=1600 + T, dtype=dtype, device=DEV)
@@ -98,3 +98,22 @@ def test_bwd_d128(dtype, T, tol):
     ref = od.dilution_backward(host64(q), host64(k), host64(v), host64(g), 1.1, 1e-6)
     for gg, rr in zip(got, ref):
         assert float(np.abs(host64(gg) - rr).max() / np.abs(rr).max()) <= tol
+
+
+def test_bwd_d128_options():
+    # tensor-core backward at d = 128 with per-head multipliers and the
+    # earlier-demand-only share
+    taus = np.array([[0.7, 1.3]])
+    B, H, T = 1, 2, 300
+    flags = b.DA_FLAG_EARLIER_DEMAND_ONLY
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(B, H, T, D, q_std=1.5, pairs=4, seed=1700, dtype="bf16"))
+    g = inputs.make_like((B, H, T, D), seed=1701, dtype="bf16", device=DEV)
+    tau_bh = torch.tensor(taus, dtype=torch.float32, device=DEV)
+    lse2 = torch.empty(B, H, T, device=DEV)
+    b.dilution_attn_fwd_ex(q, k, v, None, lse2, tau_bh=tau_bh, eps=1e-6, flags=flags)
+    got = b.dilution_attn_bwd_ex(q, k, v, g, lse2, tau_bh=tau_bh, eps=1e-6, flags=flags)
+    torch.cuda.synchronize()
+    ref = od.dilution_backward(host64(q), host64(k), host64(v), host64(g), taus.astype(np.float32).astype(np.float64),
+                               1e-6, earlier_only=True)
+    for gg, rr in zip(got, ref):
+        assert float(np.abs(host64(gg) - rr).max() / np.abs(rr).max()) <= 1.5e-2
