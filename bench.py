@@ -54,6 +54,7 @@ def parse_args(argv=None):
     ap.add_argument("--train-only", action="store_true", help="time only the training step (profiling)")
     ap.add_argument("--train-batch", type=int, default=None, help="training-step batch (default: the workload's)")
     ap.add_argument("--train-t", type=int, default=None, help="training-step sequence length (default: 16384)")
+    ap.add_argument("--train-d", type=int, default=None, help="training-step head dimension (default: 64)")
     ap.add_argument("--decode-ctx", type=int, default=None, help="cached tokens per sequence (default: the workload's)")
     ap.add_argument("--decode-steps", type=int, default=None, help="decode steps timed (default: the workload's)")
     ap.add_argument("--decode-only", action="store_true", help="skip the forward measurement")
@@ -356,13 +357,13 @@ def bwd_flops(B, H, T, d):
     return 5 * d * T * (T + 1) * B * H
 
 
-def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None):
+def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None, d=None):
     """Forward + backward at the training shape (4 x 12 x 16384 x 64, all N(0,1));
-    ``batch`` / ``T`` override it for smaller profiling runs."""
+    ``batch`` / ``T`` / ``d`` override it (profiling, head dimension 128)."""
     w = inputs.WORKLOADS["train_bf16_t16384"]
-    B, H, d = batch or w.B, w.H, w.d
+    B, H, d = batch or w.B, w.H, d or w.d
     T = T or w.T
-    q, k, v = inputs.make_workload(w, device=dev, B=B, T=T)
+    q, k, v = inputs.make_qkv(B, H, T, d, q_std=w.q_std, pairs=w.pairs, seed=w.seed, dtype=w.dtype, device=dev)
     g = inputs.make_like((B, H, T, d), seed=w.seed + 1, dtype=w.dtype, device=dev)
     out = torch.empty_like(q)
     lse2 = torch.empty(B, H, T, device=dev)
@@ -393,8 +394,8 @@ def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None):
     ms = e0.elapsed_time(e1) / steps
     bwd_ms = statistics.mean(e3[1].elapsed_time(e3[2]) for e3 in ev)
     fwd_f, bwd_f = fwd_flops(B, H, T, d), bwd_flops(B, H, T, d)
-    return {"workload": "train_bf16_t16384" if (B, T) == (w.B, w.T) else f"train_bf16_b{B}_t{T}",
-            "B": B, "H": H, "T": T, "steps": steps, "ms_per_step": ms,
+    return {"workload": "train_bf16_t16384" if (B, T, d) == (w.B, w.T, w.d) else f"train_bf16_b{B}_t{T}_d{d}",
+            "B": B, "H": H, "T": T, "d": d, "steps": steps, "ms_per_step": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "bwd_ms": bwd_ms,
             "tflops": (fwd_f + bwd_f) / (ms * 1e-3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
             "backward": "tcgen05: forward sweep again with demand checkpoints, a rho pass, a dK/dV pass, a dQ pass",
@@ -415,7 +416,8 @@ def run_ours(args):
     peaks, peaks_kind = load_peaks()
 
     if args.train_only:
-        res = run_train(torch, b, inputs, dev, steps=max(1, args.steps), batch=args.train_batch, T=args.train_t)
+        res = run_train(torch, b, inputs, dev, steps=max(1, args.steps), batch=args.train_batch, T=args.train_t,
+                        d=args.train_d)
         if rank == 0:
             print(json.dumps({"train_step": res}), flush=True)
         return 0
