@@ -70,17 +70,15 @@ constexpr int lanes_per_row() {
   return D / Vec16<E>::N;
 }
 
-// One (chunk, head) item of each phase; the kernels below loop over items
-// with a grid of as many CTAs as are resident at once (no tail wave).
 template <typename E, int D>
-__device__ __forceinline__ void dec_logits_item(const E *__restrict__ q_new, const E *__restrict__ k_new,
-                                                const E *__restrict__ v_new, E *__restrict__ k_cache,
-                                                E *__restrict__ v_cache, float *__restrict__ logits,
-                                                float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk,
-                                                const HeadScale &hs, int *status, int bh, int chunk) {
+__global__ void __launch_bounds__(kDecThreads)
+    dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
+               E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
+               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, HeadScale hs, int *status) {
   constexpr int LPR = lanes_per_row<E, D>();       // lanes cooperating on one key
   constexpr int NV = Vec16<E>::N;
   constexpr int KPR = kDecThreads / LPR;           // keys per round
+  const int bh = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x;
   const float c2 = head_c2(hs, bh, (tid == 0 && chunk == 0) ? status : nullptr);
   const int sub = tid % LPR;                       // which 16-byte piece of the row
@@ -158,13 +156,14 @@ __device__ __forceinline__ void dec_logits_item(const E *__restrict__ q_new, con
 }
 
 template <typename E, int D>
-__device__ __forceinline__ void dec_update_item(const E *__restrict__ v_cache, const float *__restrict__ logits,
-                                                const float2 *__restrict__ part_ml, float *__restrict__ demand,
-                                                float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
-                                                int nchunk_used, float eps, bool earlier, int bh, int chunk) {
+__global__ void __launch_bounds__(kDecThreads)
+    dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
+               float *__restrict__ demand, float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
+               int nchunk_used, float eps, bool earlier) {
   constexpr int LPR = lanes_per_row<E, D>();
   constexpr int NV = Vec16<E>::N;
   constexpr int KPR = kDecThreads / LPR;
+  const int bh = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x;
   const int sub = tid % LPR, grp = tid / LPR;
   __shared__ float s_lse2;
@@ -240,31 +239,6 @@ __device__ __forceinline__ void dec_update_item(const E *__restrict__ v_cache, c
 }
 
 template <typename E, int D>
-__global__ void __launch_bounds__(kDecThreads)
-    dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
-               E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
-               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, int nchunk_used, int n_items,
-               HeadScale hs, int *status) {
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    __syncthreads();   // the previous item's shared-memory reductions are done
-    dec_logits_item<E, D>(q_new, k_new, v_new, k_cache, v_cache, logits, part_ml, n_ctx, T_cap, nchunk, hs, status,
-                          it / nchunk_used, it % nchunk_used);
-  }
-}
-
-template <typename E, int D>
-__global__ void __launch_bounds__(kDecThreads, 4)
-    dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
-               float *__restrict__ demand, float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
-               int nchunk_used, int n_items, float eps, bool earlier) {
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    __syncthreads();
-    dec_update_item<E, D>(v_cache, logits, part_ml, demand, part_acc, n_ctx, T_cap, nchunk, nchunk_used, eps,
-                          earlier, it / nchunk_used, it % nchunk_used);
-  }
-}
-
-template <typename E, int D>
 __global__ void dec_combine(const float *__restrict__ part_acc, E *__restrict__ out, int nchunk, int nchunk_used) {
   const int bh = blockIdx.x;
   const int t = threadIdx.x;   // 0..63
@@ -288,27 +262,11 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
                                    HeadScale hs, float eps, bool earlier, float *logits, float2 *part_ml,
                                    float *part_acc, int nchunk, int *status, cudaStream_t stream) {
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
-  const int n_items = used * BH;
-  // Grids of exactly the CTAs that fit at once, looping over the items.
-  static int resident[2][64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident[0][dev] == 0) {
-    int sms = 0, b0 = 0, b1 = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, dec_logits<E, D>, kDecThreads, 0);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, dec_update<E, D>, kDecThreads, 0);
-    if (e != cudaSuccess) return e;
-    resident[0][dev] = sms * (b0 > 0 ? b0 : 1);
-    resident[1][dev] = sms * (b1 > 0 ? b1 : 1);
-  }
-  const int g0 = n_items < resident[0][dev] ? n_items : resident[0][dev];
-  const int g1 = n_items < resident[1][dev] ? n_items : resident[1][dev];
-  dec_logits<E, D><<<g0, kDecThreads, 0, stream>>>((const E *)q_new, (const E *)k_new, (const E *)v_new,
-                                                   (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx, T_cap, nchunk,
-                                                   used, n_items, hs, status);
-  dec_update<E, D><<<g1, kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc, n_ctx,
-                                                   T_cap, nchunk, used, n_items, eps, earlier);
+  dec_logits<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>(
+      (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
+      T_cap, nchunk, hs, status);
+  dec_update<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc,
+                                                           n_ctx, T_cap, nchunk, used, eps, earlier);
   dec_combine<E, D><<<BH, D, 0, stream>>>(part_acc, (E *)out, nchunk, used);
   return cudaGetLastError();
 }
