@@ -220,7 +220,7 @@ int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const voi
  * the tensors it already owns.  Every GPU that loads the library keeps the
  * array until the process exits.
  *   - Returns DA_ERR_WORKSPACE when dilution_attn_decode_workspace_size(B, H,
- *     T_cap, d) exceeds the array (e.g. 8 x 12 heads fit T_cap up to ~43K).
+ *     T_cap, d) exceeds the array (e.g. 8 x 12 heads fit T_cap up to ~42K).
  *   - Calls no cudaMalloc/cudaFree; the first call on a device looks up the
  *     array's device address (cudaGetSymbolAddress), so make that first call
  *     before any stream capture.

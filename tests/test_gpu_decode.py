@@ -54,7 +54,7 @@ def test_decode_equals_longer_prefill(dtype):
         assert torch.equal(kc[:, :, n], k[:, :, n]) and torch.equal(vc[:, :, n], v[:, :, n])
 
 
-@pytest.mark.parametrize("n_ctx", [0, 1, 4095, 4096, 5000])
+@pytest.mark.parametrize("n_ctx", [0, 1, 2047, 2048, 4095, 4096, 5000])
 def test_decode_matches_oracle_step(n_ctx):
     """Arbitrary cache state (random positive demand) -> oracle decode step."""
     B, H, d, T_cap = 2, 2, 64, n_ctx + 16
