@@ -367,18 +367,21 @@ def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None, d=None):
     g = inputs.make_like((B, H, T, d), seed=w.seed + 1, dtype=w.dtype, device=dev)
     out = torch.empty_like(q)
     lse2 = torch.empty(B, H, T, device=dev)
-    fws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=dev)
+    # one workspace: the forward keeps its demand checkpoints and accumulators
+    # there for the backward (DA_FLAG_KEEP_FOR_BACKWARD)
+    keep = b.DA_FLAG_KEEP_FOR_BACKWARD
     bws = torch.empty(b.dilution_attn_bwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=dev)
+    fws = bws
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
 
     def step(e3=None):
         if e3:
             e3[0].record()
-        b.dilution_attn_fwd(q, k, v, out, lse2, workspace=fws)
+        b.dilution_attn_fwd_ex(q, k, v, out, lse2, flags=keep, workspace=bws)
         if e3:
             e3[1].record()
-        b.dilution_attn_bwd(q, k, v, g, lse2, dq, dk, dv, workspace=bws)
+        b.dilution_attn_bwd_ex(q, k, v, g, lse2, dq, dk, dv, flags=keep, workspace=bws)
         if e3:
             e3[2].record()
 
@@ -398,7 +401,7 @@ def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None, d=None):
             "B": B, "H": H, "T": T, "d": d, "steps": steps, "ms_per_step": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "bwd_ms": bwd_ms,
             "tflops": (fwd_f + bwd_f) / (ms * 1e-3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
-            "backward": "tcgen05: forward sweep again with demand checkpoints, a rho pass, a dK/dV pass, a dQ pass",
+            "backward": "tcgen05: the forward keeps its demand checkpoints; a rho pass, a dK/dV pass, a dQ pass",
             "fwd_flop": fwd_f, "bwd_flop": bwd_f}
 
 

@@ -64,6 +64,7 @@ extern "C" {
 
 /* Flags of the *_ex entry points (bitwise or; other bits are DA_ERR_INVALID). */
 #define DA_FLAG_EARLIER_DEMAND_ONLY 1   /* share = p / (committed + eps): see below */
+#define DA_FLAG_KEEP_FOR_BACKWARD   2   /* forward leaves its state for the backward: see below */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *dilution_attn_status_string(int status);
@@ -131,6 +132,14 @@ int dilution_attn_fwd_with_events(const void *q, const void *k, const void *v, v
  *           and, as eps -> 0, the layer tends to the identity map.  For
  *           DA_BF16, shares up to 1/eps are fed to the value product in bf16;
  *           eps >= 1e-18 as for the default operator.
+ *           DA_FLAG_KEEP_FOR_BACKWARD (DA_BF16 only, else DA_ERR_UNSUPPORTED):
+ *           the workspace must be at least dilution_attn_bwd_workspace_size()
+ *           (else DA_ERR_WORKSPACE); the forward also leaves there what the
+ *           backward would otherwise recompute (the demand of every key at
+ *           every 32-query chunk and the unnormalised outputs), so that a
+ *           dilution_attn_bwd_ex with the same flag, the same inputs,
+ *           options and workspace skips that pass.  The caller must not
+ *           touch the workspace in between.
  *   events  as for dilution_attn_fwd_with_events (nullable).
  * Other arguments, outputs and errors as for dilution_attn_fwd; unknown flag
  * bits or a misaligned tau_bh return DA_ERR_INVALID.
@@ -161,7 +170,9 @@ int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *d
 
 /* Backward with the options of dilution_attn_fwd_ex: tau_bh (nullable device
  * [B*H]) and flags (DA_FLAG_EARLIER_DEMAND_ONLY), which must match the
- * forward that produced lse2.  With the flag, D_jk = committed_jk + eps and
+ * forward that produced lse2.  DA_FLAG_KEEP_FOR_BACKWARD (DA_BF16 only):
+ * workspace is the one the forward ran with under the same flag and still
+ * holds its state; lse2 is then not read (but must still be a valid pointer).  With the flag, D_jk = committed_jk + eps and
  * the direct term of dp_jk is dr_jk / D_jk.  Errors as for dilution_attn_bwd
  * plus those of dilution_attn_fwd_ex for tau_bh and flags. */
 int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void *dout,
@@ -201,7 +212,7 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
  * share_k = p_k / (demand_k + eps); the demand update is unchanged, so a
  * cache built by a flagged prefill continues the flagged operator.  Errors as
  * for dilution_attn_decode_step plus those of dilution_attn_fwd_ex for tau_bh
- * and flags. */
+ * and flags (DA_FLAG_KEEP_FOR_BACKWARD is DA_ERR_INVALID here). */
 int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new,
                                  void *k_cache, void *v_cache, float *demand,
                                  int n_ctx, int T_cap, void *out,

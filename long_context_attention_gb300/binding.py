@@ -20,6 +20,7 @@ from . import build as _build
 DA_OK, DA_ERR_INVALID, DA_ERR_UNSUPPORTED, DA_ERR_CUDA, DA_ERR_TIMEOUT, DA_ERR_WORKSPACE = range(6)
 DA_F32, DA_BF16 = 0, 1
 DA_FLAG_EARLIER_DEMAND_ONLY = 1
+DA_FLAG_KEEP_FOR_BACKWARD = 2
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dilution_attn.h")
 
 _lib = None
@@ -164,7 +165,7 @@ def _event_handle(e):
     return e.cuda_event
 
 
-def _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace):
+def _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace, flags=0):
     _need(q, "q")
     B, H, T, d = q.shape
     _need(k, "k", q.shape, q.dtype)
@@ -176,7 +177,8 @@ def _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace):
         if t is not None:
             _need(t, name, (B, H, T), torch.float32)
     dt = _dtype_code(q)
-    need = dilution_attn_fwd_workspace_size(B, H, T, d, dt)
+    need = (dilution_attn_bwd_workspace_size(B, H, T, d, dt) if flags & DA_FLAG_KEEP_FOR_BACKWARD
+            else dilution_attn_fwd_workspace_size(B, H, T, d, dt))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     return out, workspace, dt
@@ -221,9 +223,11 @@ def dilution_attn_fwd_ex(q, k, v, out=None, lse2_out=None, rowsum_out=None, dema
                          stream=None, check: bool = True, events=None):
     """Forward with a per-(batch, head) multiplier tensor ``tau_bh`` (fp32 CUDA,
     B*H elements, index b*H + h; replaces ``tau``) and ``flags``
-    (``DA_FLAG_EARLIER_DEMAND_ONLY``)."""
+    (``DA_FLAG_EARLIER_DEMAND_ONLY``, ``DA_FLAG_KEEP_FOR_BACKWARD``: pass the
+    same ``workspace`` to ``dilution_attn_bwd_ex`` with the same flags; it is
+    allocated backward-sized when omitted)."""
     lib = load()
-    out, workspace, dt = _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace)
+    out, workspace, dt = _fwd_prepare(q, k, v, out, lse2_out, rowsum_out, demand_out, workspace, int(flags))
     B, H, T, d = q.shape
     st = lib.dilution_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse2_out), _ptr(rowsum_out),
                                   _ptr(demand_out), B, H, T, d, float(tau), _tau_bh_ptr(tau_bh, B, H), float(eps),

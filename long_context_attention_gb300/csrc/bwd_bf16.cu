@@ -908,9 +908,12 @@ static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, fl
 }
 
 // The tensor-core backward (bf16, d = 64 or 128): the passes in the file header.
+// have_fwd_state: the workspace already holds -lse2, the forward accumulators
+// and the demand checkpoints of a forward run for these inputs (the forward
+// kept them), so pass F is skipped.
 int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
                        void *dk, void *dv, int BH, int T, int d, HeadScale hs, float c, float eps, bool earlier,
-                       uint8_t *ws, cudaStream_t stream) {
+                       bool have_fwd_state, uint8_t *ws, cudaStream_t stream) {
   const BwdTcWorkspace L = bwd_tc_workspace_layout(BH, T, d);
   const int Tp = (int)t_pad(T);
   const int64_t rows = (int64_t)BH * Tp;
@@ -927,10 +930,12 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
       !make_bf16_tile_map(&maps[4], q, BH, T, d, kTile) || !make_bf16_tile_map(&maps[5], dout, BH, T, d, kTile))
     return DA_ERR_CUDA;
   const unsigned gp = (unsigned)((rows + 255) / 256), gr = (unsigned)((rows * 16 + 255) / 256);
-  if (d == 128) bwdtc_prep<128><<<gp, 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
-  else bwdtc_prep<64><<<gp, 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
-  int st = launch_sweep_bf16_chk(q, k, v, nlse2, acc, cchk, BH, T, d, hs, eps, earlier, status, stream);
-  if (st != DA_OK) return st;
+  if (!have_fwd_state) {
+    if (d == 128) bwdtc_prep<128><<<gp, 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
+    else bwdtc_prep<64><<<gp, 256, 0, stream>>>(lse2, nlse2, acc, BH, T, Tp);
+    const int st = launch_sweep_bf16_chk(q, k, v, nlse2, acc, cchk, BH, T, d, hs, eps, earlier, status, stream);
+    if (st != DA_OK) return st;
+  }
   const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(dout);
   if (d == 128) bwdtc_rows<128><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
   else bwdtc_rows<64><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);

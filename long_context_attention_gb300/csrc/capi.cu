@@ -15,13 +15,13 @@ cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float
                            cudaEvent_t const *ev);
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                     float *demand_out, int BH, int T, int d, HeadScale hs, float eps, bool earlier, float *lse2_ws,
-                    float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev);
+                    float *acc, float *cchk, int *status, cudaStream_t stream, cudaEvent_t const *ev);
 cudaError_t launch_bwd(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
                        void *dk, void *dv, int BH, int T, int d, float c, HeadScale hs, float eps, bool earlier,
                        int dtype, double *dtot, float *rowbuf, float *dq_acc, cudaStream_t stream);
 int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *dout, const float *lse2, void *dq,
                        void *dk, void *dv, int BH, int T, int d, HeadScale hs, float c, float eps, bool earlier,
-                       uint8_t *ws, cudaStream_t stream);
+                       bool have_fwd_state, uint8_t *ws, cudaStream_t stream);
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
                           bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
@@ -45,9 +45,12 @@ HeadScale head_scale(float tau, const float *tau_bh, int d) {
   return HeadScale{tau_bh, logit_scale_log2(tau, d), log2e_over_sqrt_d(d)};
 }
 
+// bf16 runs the tensor-core backward; fp32 the SIMT one.
+bool bwd_on_tensor_cores(int d, int dtype) { return dtype == DA_BF16 && (d == 64 || d == 128); }
+
 // Options of the *_ex entry points.
 int check_options(const float *tau_bh, int flags) {
-  if ((flags & ~DA_FLAG_EARLIER_DEMAND_ONLY) != 0) return DA_ERR_INVALID;
+  if ((flags & ~(DA_FLAG_EARLIER_DEMAND_ONLY | DA_FLAG_KEEP_FOR_BACKWARD)) != 0) return DA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(tau_bh) & 3u) != 0) return DA_ERR_INVALID;
   return DA_OK;
 }
@@ -119,14 +122,22 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DA_ERR_INVALID;
   if (!aligned16_or_null(lse2_out) || !aligned16_or_null(rowsum_out) || !aligned16_or_null(demand_out))
     return DA_ERR_INVALID;
+  // DA_FLAG_KEEP_FOR_BACKWARD: the workspace is a backward workspace whose
+  // leading regions (-lse2, accumulators) are laid out as the forward's; the
+  // sweep also writes the demand checkpoints there.
+  const bool keep = (flags & DA_FLAG_KEEP_FOR_BACKWARD) != 0;
+  if (keep && !bwd_on_tensor_cores(d, dtype)) return DA_ERR_UNSUPPORTED;
   const FwdWorkspace L = fwd_workspace_layout(BH, T, d);
-  if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
+  const BwdTcWorkspace LB = bwd_tc_workspace_layout(BH, T, d);
+  if (keep && (LB.nlse2_off != L.lse2_off || LB.acc_off != L.acc_off)) return DA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < (keep ? LB.total : L.total)) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
   float *lse2_ws = reinterpret_cast<float *>(ws + L.lse2_off);
   float *acc = reinterpret_cast<float *>(ws + L.acc_off);
+  float *cchk = keep ? reinterpret_cast<float *>(ws + LB.cchk_off) : nullptr;
   if (dtype == DA_BF16 && eps < 1e-18f) return DA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(status, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   const HeadScale hs = head_scale(tau, tau_bh, d);
@@ -137,11 +148,8 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
     return DA_OK;
   }
   return launch_fwd_bf16(q, k, v, out, lse2_out, rowsum_out, demand_out, (int)BH, T, d, hs, eps, earlier, lse2_ws,
-                         acc, status, stream, ev);
+                         acc, cchk, status, stream, ev);
 }
-
-// bf16 runs the tensor-core backward; fp32 the SIMT one.
-static bool bwd_on_tensor_cores(int d, int dtype) { return dtype == DA_BF16 && (d == 64 || d == 128); }
 
 size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype) {
   if (B < 0 || H < 0 || T < 0 || !head_dim_supported(d)) return 0;
@@ -162,6 +170,8 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
   int st = check_common(B, H, T, d, tau, eps, dtype);
   if (st == DA_OK) st = check_options(tau_bh, flags);
   if (st != DA_OK) return st;
+  const bool keep = (flags & DA_FLAG_KEEP_FOR_BACKWARD) != 0;
+  if (keep && !bwd_on_tensor_cores(d, dtype)) return DA_ERR_UNSUPPORTED;
   const int64_t BH = (int64_t)B * H;
   if (BH == 0 || T == 0) return DA_OK;
   const void *ptrs[] = {q, k, v, dout, lse2, dq, dk, dv};
@@ -178,7 +188,7 @@ int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void
   if (bwd_on_tensor_cores(d, dtype)) {
     if ((int64_t)BH * t_pad(T) > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;
     return launch_bwd_bf16_tc(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, d, head_scale(tau, tau_bh, d), c, eps,
-                              (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, ws, stream);
+                              (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, keep, ws, stream);
   }
   const BwdWorkspace L = bwd_workspace_layout(BH, T, d);
   if (launch_bwd(q, k, v, dout, lse2, dq, dk, dv, (int)BH, T, d, c, head_scale(tau, tau_bh, d), eps,
@@ -209,6 +219,7 @@ int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const voi
   int st = check_common(B, H, T_cap, d, tau, eps, dtype);
   if (st == DA_OK) st = check_options(tau_bh, flags);
   if (st != DA_OK) return st;
+  if ((flags & DA_FLAG_KEEP_FOR_BACKWARD) != 0) return DA_ERR_INVALID;   // no backward of a decode step
   if (n_ctx < 0 || n_ctx >= T_cap) return DA_ERR_INVALID;
   const int64_t BH = (int64_t)B * H;
   if (BH == 0) return DA_OK;

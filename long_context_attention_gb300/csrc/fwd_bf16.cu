@@ -961,8 +961,8 @@ static int prepare_fwd_bf16() {
 template <int D>
 static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                              const CUtensorMap &ta, const void *k, float *demand_out, int BH, int T, HeadScale hs,
-                             float eps, bool earlier, float *lse2_ws, float *acc, int *status, cudaStream_t stream,
-                             cudaEvent_t const *ev) {
+                             float eps, bool earlier, float *lse2_ws, float *acc, float *cchk, int *status,
+                             cudaStream_t stream, cudaEvent_t const *ev) {
   // The shared-memory opt-in is a per-device function attribute.
   static bool attr_done[64] = {};
   int dev = 0;
@@ -980,13 +980,16 @@ static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const
   if (ev[1]) cudaEventRecord(ev[1], stream);
   const int nsw = sweep_num_ctas(BH, T, D);
   const uint4 *kg = static_cast<const uint4 *>(k);
-  if (earlier)
-    sweep_kernel<D, true, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc, demand_out,
-                                                                       nullptr, BH, T, Tp, hs, eps, status);
-  else
-    sweep_kernel<D, false, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, ta, kg, lse2_ws, acc,
-                                                                        demand_out, nullptr, BH, T, Tp, hs, eps,
-                                                                        status);
+  // cchk != null: also keep the demand checkpoints for a later backward
+#define DA_SWEEP_ARGS tq, tk, tv, ta, kg, lse2_ws, acc, demand_out, cchk, BH, T, Tp, hs, eps, status
+  if (cchk != nullptr) {
+    if (earlier) sweep_kernel<D, true, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(DA_SWEEP_ARGS);
+    else sweep_kernel<D, false, true><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(DA_SWEEP_ARGS);
+  } else {
+    if (earlier) sweep_kernel<D, true, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(DA_SWEEP_ARGS);
+    else sweep_kernel<D, false, false><<<nsw, C::kThreads, C::kSmemBytes, stream>>>(DA_SWEEP_ARGS);
+  }
+#undef DA_SWEEP_ARGS
   if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
   return DA_OK;
 }
@@ -1034,7 +1037,7 @@ int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const flo
 
 int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, float *lse2_out, float *rowsum_out,
                     float *demand_out, int BH, int T, int d, HeadScale hs, float eps, bool earlier, float *lse2_ws,
-                    float *acc, int *status, cudaStream_t stream, cudaEvent_t const *ev) {
+                    float *acc, float *cchk, int *status, cudaStream_t stream, cudaEvent_t const *ev) {
   const int64_t acc_rows = (int64_t)BH * (int64_t)t_pad(T);
   if (acc_rows > 0x7FFFFFFF) return DA_ERR_UNSUPPORTED;   // TMA row coordinates are 32-bit
   CUtensorMap tq, tk, tv, ta;
@@ -1042,9 +1045,9 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
       !make_acc_map(&ta, acc, acc_rows, d))
     return DA_ERR_CUDA;
   const int st = d == 128 ? launch_fwd_bf16_t<128>(tq, tk, tv, ta, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
-                                                   acc, status, stream, ev)
+                                                   acc, cchk, status, stream, ev)
                           : launch_fwd_bf16_t<64>(tq, tk, tv, ta, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
-                                                  acc, status, stream, ev);
+                                                  acc, cchk, status, stream, ev);
   if (st != DA_OK) return st;
   if (ev[2]) cudaEventRecord(ev[2], stream);
   if (launch_finalize_bf16(acc, lse2_ws, reinterpret_cast<__nv_bfloat16 *>(out), rowsum_out, lse2_out, BH, T, d,

@@ -187,9 +187,30 @@ def test_ex_option_validation(lib):
                                                 tau_bh, 1e-6, flags, 1, None, 1 << 30, None)
 
     for call in (fwd, bwd, dec):
-        assert call(flags=2) == b.DA_ERR_INVALID
+        assert call(flags=4) == b.DA_ERR_INVALID
         assert call(flags=-1) == b.DA_ERR_INVALID
         assert call(tau_bh=MIS2) == b.DA_ERR_INVALID
         assert call(flags=EARLY) == b.DA_ERR_WORKSPACE
         assert call(tau_bh=MIS, flags=EARLY) == b.DA_ERR_WORKSPACE   # 4-byte aligned is enough
     assert fwd(flags=EARLY, ws=MIS) == b.DA_ERR_INVALID              # workspace must be 256-byte aligned
+
+
+def test_keep_for_backward_validation(lib):
+    # the forward-state flag: bf16 only, and the forward then needs a
+    # backward-sized workspace; a decode step rejects it
+    KEEP = b.DA_FLAG_KEEP_FOR_BACKWARD
+
+    def fwd(dtype=1, wsb=1 << 40, ws=FAKE):
+        return lib.dilution_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, None, None, None, 1, 2, 1000, 64, 1.0, None, 1e-6,
+                                        KEEP, dtype, ws, wsb, None, None)
+
+    assert fwd(dtype=0) == b.DA_ERR_UNSUPPORTED
+    need_bwd = b.dilution_attn_bwd_workspace_size(1, 2, 1000, 64, 1)
+    need_fwd = b.dilution_attn_fwd_workspace_size(1, 2, 1000, 64, 1)
+    assert need_bwd > need_fwd
+    assert fwd(wsb=need_fwd) == b.DA_ERR_WORKSPACE
+    assert fwd(ws=None) == b.DA_ERR_WORKSPACE
+    assert lib.dilution_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 8, 64, 1.0, None, 1e-6,
+                                    KEEP, 0, FAKE, 1 << 30, None) == b.DA_ERR_UNSUPPORTED
+    assert lib.dilution_attn_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 16, FAKE, 1, 2, 64, 1.0, None,
+                                            1e-6, KEEP, 1, FAKE, 1 << 30, None) == b.DA_ERR_INVALID

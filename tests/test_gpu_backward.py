@@ -93,3 +93,26 @@ def test_bwd_argument_errors():
     with pytest.raises(b.DilutionAttnError) as ei:
         b.dilution_attn_bwd(q, k, v, q, lse2, eps=0.0)
     assert ei.value.status == b.DA_ERR_INVALID
+
+
+@pytest.mark.parametrize("d,T", [(64, 300), (64, 1000), (128, 300)])
+def test_bwd_with_forward_state(d, T):
+    """DA_FLAG_KEEP_FOR_BACKWARD: the forward leaves its demand checkpoints and
+    accumulators in a backward-sized workspace and the backward skips its own
+    forward pass; same gradients as the stand-alone backward."""
+    keep = b.DA_FLAG_KEEP_FOR_BACKWARD
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 2, T, d, q_std=1.5, pairs=4, seed=T + d, dtype="bf16"))
+    g = inputs.make_like((1, 2, T, d), seed=3000 + T, dtype="bf16", device=DEV)
+    lse2 = torch.empty(1, 2, T, device=DEV)
+    ws = torch.empty(b.dilution_attn_bwd_workspace_size(1, 2, T, d, b.DA_BF16), dtype=torch.uint8, device=DEV)
+    out = b.dilution_attn_fwd_ex(q, k, v, None, lse2, flags=keep, workspace=ws)
+    kept = b.dilution_attn_bwd_ex(q, k, v, g, lse2, flags=keep, workspace=ws)
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+    alone = b.dilution_attn_bwd(q, k, v, g, lse2)
+    plain_out = b.dilution_attn_fwd(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain_out)   # the flag changes nothing the forward returns
+    ref = od.dilution_backward(host64(q), host64(k), host64(v), host64(g), 1.0, 1e-6)
+    for gk, ga, rr in zip(kept, alone, ref):
+        assert rel_to_max(host64(gk), rr) <= 1.5e-2
+        assert rel_to_max(host64(gk), host64(ga)) <= 1e-2
