@@ -36,6 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 SWEEP_SOURCES = ["long_context_attention_gb300/csrc/fwd_bf16.cu", "long_context_attention_gb300/csrc/da_ptx.cuh",
                  "long_context_attention_gb300/csrc/da_internal.h"]
 SWEEP_PROFILE = os.path.join(ROOT, "profiles", "sweep_kernel_fwd_bf16_t16384.md")
+DECODE_SOURCES = ["long_context_attention_gb300/csrc/decode.cu", "long_context_attention_gb300/csrc/da_internal.h"]
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_bf16_ctx131072.md")
 
 
 # --------------------------------------------------------------------------- helpers
@@ -84,19 +86,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def sources_hash():
+def sources_hash(sources=None):
     h = hashlib.sha256()
-    for rel in SWEEP_SOURCES:
+    for rel in sources or SWEEP_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per sweep launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+def profiled_traffic(profile=None, sources=None):
+    """DRAM bytes per launch (per step for the decode) from a committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
     try:
-        text = open(SWEEP_PROFILE).read()
+        text = open(profile or SWEEP_PROFILE).read()
     except OSError:
         return None
     vals = {}
@@ -105,7 +107,7 @@ def profiled_traffic():
         if ":" in line:
             key, _, val = line.partition(":")
             vals[key.strip().strip("`")] = val.strip().strip("`")
-    if vals.get("kernel_source_hash") != sources_hash():
+    if vals.get("kernel_source_hash") != sources_hash(sources):
         return None
     try:
         return float(vals["traffic_bytes_per_launch_full_size"])
@@ -346,7 +348,8 @@ def run_decode(torch, b, inputs, dev, warmup, peaks, ctx=None, n_steps=None):
     return pre, {"workload": f"decode_bf16_ctx{N}", "B": B, "H": H, "n_ctx": N, "steps": steps, "tau": tau,
                  "ms_per_step": ms / steps, "tokens_per_s": B * steps / (ms * 1e-3),
                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                              "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                              "frac": gbs / peaks["hbm_gbs"],
+                              "traffic": profiled_traffic(DECODE_PROFILE, DECODE_SOURCES),
                               "bytes_per_step": algo_bytes / steps},
                  "gpu_launches": 3 * steps}
 
