@@ -18,6 +18,7 @@
 // per 128-byte row), the demand is read and written once; the fp32 logit
 // scratch (4 B per key) stays mostly in L2.
 #include "da_internal.h"
+#include "da_ptx.cuh"
 
 #include <mutex>
 
@@ -155,18 +156,51 @@ __global__ void __launch_bounds__(kDecThreads)
   if (tid == 0) part_ml[(size_t)bh * nchunk + chunk] = make_float2(sm[0], sl[0]);
 }
 
+// The value rows of a chunk stream through a ring of shared-memory stages
+// filled by bulk asynchronous copies that one producer warp issues, so the
+// bytes in flight do not sit in registers (the update otherwise keeps too few
+// in flight to reach HBM rate at its occupancy).  Logits and demand (8 B per
+// key against the row's 128) are read directly, one stage ahead.  A chunk's
+// tail shorter than a stage is read directly too.
 template <typename E, int D>
-__global__ void __launch_bounds__(kDecThreads)
+struct DecRing {
+  static constexpr int kRowBytes = D * (int)sizeof(E);
+  static constexpr int kStageKeys = 8192 / kRowBytes;   // 64 keys for bf16 rows of 64
+  static constexpr int kStages = 4;
+  static constexpr int kThreads = kDecThreads + 32;     // consumers + the producer warp
+};
+
+template <typename E, int D>
+__global__ void __launch_bounds__(DecRing<E, D>::kThreads)
     dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
                float *__restrict__ demand, float *__restrict__ part_acc, int n_ctx, int T_cap, int nchunk,
-               int nchunk_used, float eps, bool earlier) {
+               int nchunk_used, float eps, bool earlier, int *status) {
+  using R = DecRing<E, D>;
   constexpr int LPR = lanes_per_row<E, D>();
   constexpr int NV = Vec16<E>::N;
-  constexpr int KPR = kDecThreads / LPR;
+  constexpr int KPR = kDecThreads / LPR;                // keys per round of the consumers
+  constexpr int SK = R::kStageKeys, RPS = SK / KPR;     // rounds per stage
+  static_assert(SK % KPR == 0, "stage of whole rounds");
   const int bh = blockIdx.y, chunk = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const bool producer = warp == kDecThreads / 32;
   const int sub = tid % LPR, grp = tid / LPR;
+  __shared__ __align__(128) uint8_t ring[R::kStages][SK * R::kRowBytes];
+  __shared__ uint64_t full[R::kStages], empty[R::kStages];
+  __shared__ int abort_word;
   __shared__ float s_lse2;
+  const int k_begin = chunk * kDecChunk;
+  const int k_end = min(k_begin + kDecChunk, n_ctx + 1);
+  const int n_stage = (k_end - k_begin) / SK;           // whole stages through the ring
+  const E *vb = v_cache + (size_t)bh * T_cap * D;
+  if (tid == 0) {
+    for (int st = 0; st < R::kStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kDecThreads / 32);
+    }
+    abort_word = 0;
+    fence_mbar_init();
+  }
   if (tid < 32) {
     // Combine the per-chunk (max, sum) pairs of this head into lse2.
     float m = -INFINITY, l = 0.f;
@@ -191,45 +225,87 @@ __global__ void __launch_bounds__(kDecThreads)
   }
   __syncthreads();
   const float lse2 = s_lse2;
-  const int k_begin = chunk * kDecChunk;
-  const int k_end = min(k_begin + kDecChunk, n_ctx + 1);
-  const E *vb = v_cache + (size_t)bh * T_cap * D;
+  const WaitCtx wc{reinterpret_cast<volatile int *>(&abort_word), status};
   float num[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) num[i] = 0.f;
   float rs = 0.f;
-  for (int r0 = k_begin; r0 < k_end; r0 += KPR * kDecUnroll) {
-    const int k0 = r0 + grp;
-    uint4 raw[kDecUnroll];
-    float x[kDecUnroll], dm[kDecUnroll];
+
+  // one key: its bid, share against the demand, demand update, share * v
+  auto consume = [&](int key, const uint4 &raw, float x, float dm) {
+    const float p = exp2f(x - lse2);
+    const float den = (earlier ? dm : dm + p) + eps;
+    const float share = p / den;
+    if (sub == 0) demand[(size_t)bh * T_cap + key] = dm + p;
+    float vf[NV];
+    Vec16<E>::to_float(raw, vf);
 #pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const int key = k0 + u * KPR;
-      const bool ok = key < k_end;
-      raw[u] = ok ? ld_stream(vb + (size_t)key * D + sub * NV) : make_uint4(0, 0, 0, 0);
-      x[u] = ok ? logits[(size_t)bh * T_cap + key] : -INFINITY;
-      dm[u] = (ok && key < n_ctx) ? demand[(size_t)bh * T_cap + key] : 0.f;
+    for (int i = 0; i < NV; ++i) num[i] = fmaf(share, vf[i], num[i]);
+    rs += share;
+  };
+
+  if (producer) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int st = 0; st < n_stage; ++st) {
+        const int slot = st % R::kStages;
+        if (!mbar_wait(&empty[slot], ((st / R::kStages) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&full[slot], SK * R::kRowBytes);
+        bulk_load(ring[slot], vb + (size_t)(k_begin + st * SK) * D, SK * R::kRowBytes, &full[slot]);
+        ++issued;
+      }
+      if (abort_word) {   // let the copies in flight land before the CTA exits
+        for (int st = (issued > R::kStages ? issued - R::kStages : 0); st < issued; ++st) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(&full[st % R::kStages], (st / R::kStages) & 1))
+            if (globaltimer() - t0 > 100ull * 1000ull * 1000ull) break;
+        }
+      }
     }
+  } else {
+    // logits and demand of this thread's keys, one stage ahead
+    float xn[RPS], dn[RPS];
+    auto fetch = [&](int st, float (&x)[RPS], float (&d)[RPS]) {
 #pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const int key = k0 + u * KPR;
-      if (key >= k_end) continue;
-      const float p = exp2f(x[u] - lse2);
-      const float den = (earlier ? dm[u] : dm[u] + p) + eps;
-      const float share = p / den;
-      if (sub == 0) demand[(size_t)bh * T_cap + key] = dm[u] + p;
-      float vf[NV];
-      Vec16<E>::to_float(raw[u], vf);
+      for (int r = 0; r < RPS; ++r) {
+        const int key = k_begin + st * SK + r * KPR + grp;
+        x[r] = logits[(size_t)bh * T_cap + key];
+        d[r] = key < n_ctx ? demand[(size_t)bh * T_cap + key] : 0.f;
+      }
+    };
+    if (n_stage > 0) fetch(0, xn, dn);
+    for (int st = 0; st < n_stage; ++st) {
+      const int slot = st % R::kStages;
+      float xc[RPS], dc[RPS];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) num[i] = fmaf(share, vf[i], num[i]);
-      rs += share;
+      for (int r = 0; r < RPS; ++r) {
+        xc[r] = xn[r];
+        dc[r] = dn[r];
+      }
+      if (st + 1 < n_stage) fetch(st + 1, xn, dn);
+      if (!mbar_wait(&full[slot], (st / R::kStages) & 1, wc)) break;
+#pragma unroll
+      for (int r = 0; r < RPS; ++r) {
+        const int kl = r * KPR + grp;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(ring[slot] + kl * R::kRowBytes + sub * 16);
+        consume(k_begin + st * SK + kl, raw, xc[r], dc[r]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    // the tail of the chunk, read directly
+    for (int key = k_begin + n_stage * SK + grp; key < k_end; key += KPR) {
+      const uint4 raw = ld_stream(vb + (size_t)key * D + sub * NV);
+      consume(key, raw, logits[(size_t)bh * T_cap + key], key < n_ctx ? demand[(size_t)bh * T_cap + key] : 0.f);
     }
   }
-  // Reduce the KPR key groups: partial rows [KPR][64 + 1] in shared memory.
+  // Reduce the KPR key groups: partial rows [KPR][d + 1] in shared memory.
   __shared__ float sacc[KPR][D + 1];
+  if (!producer) {
 #pragma unroll
-  for (int i = 0; i < NV; ++i) sacc[grp][sub * NV + i] = num[i];
-  if (sub == 0) sacc[grp][D] = rs;
+    for (int i = 0; i < NV; ++i) sacc[grp][sub * NV + i] = num[i];
+    if (sub == 0) sacc[grp][D] = rs;
+  }
   __syncthreads();
   if (tid <= D) {
     float a = 0.f;
@@ -265,8 +341,8 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
   dec_logits<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
       T_cap, nchunk, hs, status);
-  dec_update<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>((const E *)v_cache, logits, part_ml, demand, part_acc,
-                                                           n_ctx, T_cap, nchunk, used, eps, earlier);
+  dec_update<E, D><<<dim3(used, BH), DecRing<E, D>::kThreads, 0, stream>>>(
+      (const E *)v_cache, logits, part_ml, demand, part_acc, n_ctx, T_cap, nchunk, used, eps, earlier, status);
   dec_combine<E, D><<<BH, D, 0, stream>>>(part_acc, (E *)out, nchunk, used);
   return cudaGetLastError();
 }
