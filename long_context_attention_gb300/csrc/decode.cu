@@ -14,9 +14,10 @@
 //                 D_k += p_k in place; per-chunk sum_k share_k v_k and sum_k share_k.
 //   dec_combine : out = sum of chunk numerators / sum of chunk row sums
 //                 (fixed order: deterministic).
-// Memory: K, V bf16 rows are read once each with 16-byte vector loads (8 lanes
-// per 128-byte row), the demand is read and written once; the fp32 logit
-// scratch (4 B per key) stays mostly in L2.
+// Memory: K and V rows are read once each, streamed into shared memory by
+// bulk copies (8 consumer lanes per 128-byte bf16 row read them from there),
+// the demand is read and written once; the fp32 logit scratch (4 B per key)
+// stays mostly in L2.
 #include "da_internal.h"
 #include "da_ptx.cuh"
 
@@ -27,7 +28,6 @@
 namespace da {
 
 constexpr int kDecThreads = 256;
-constexpr int kDecUnroll = 4;                       // keys per 8-lane group per round
 
 template <typename E>
 struct Vec16;   // 16 bytes of one row: 8 bf16 or 4 fp32 elements
@@ -71,53 +71,111 @@ constexpr int lanes_per_row() {
   return D / Vec16<E>::N;
 }
 
+// Cache rows stream through a ring of shared-memory stages filled by bulk
+// asynchronous copies that one producer warp issues, so the bytes in flight
+// do not sit in registers (with register-held loads both streaming kernels
+// keep too few bytes in flight per SM to reach HBM rate at their occupancy).
+// Whole stages go through the ring; a chunk's tail shorter than a stage is
+// read directly.  Every wait is bounded: a timeout records DA_ERR_TIMEOUT in
+// the status block and the CTA finishes without waiting further.
 template <typename E, int D>
-__global__ void __launch_bounds__(kDecThreads)
+struct DecRing {
+  static constexpr int kRowBytes = D * (int)sizeof(E);
+  static constexpr int kStageKeys = 8192 / kRowBytes;   // 64 keys for bf16 rows of 64
+  static constexpr int kStages = 4;
+  static constexpr int kConsumerWarps = kDecThreads / 32;
+  static constexpr int kThreads = kDecThreads + 32;     // consumers + the producer warp
+
+  __align__(128) uint8_t stage[kStages][kStageKeys * kRowBytes];
+  uint64_t full[kStages], empty[kStages];
+  int abort_word;
+
+  // one thread, before a __syncthreads
+  __device__ __forceinline__ void init() {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __device__ __forceinline__ WaitCtx wait_ctx(int *status) {
+    return WaitCtx{reinterpret_cast<volatile int *>(&abort_word), status};
+  }
+  // Producer lane: stages 0 .. n_stage - 1 of the rows starting at `rows`.
+  __device__ __forceinline__ void produce(const E *rows, int n_stage, const WaitCtx &wc) {
+    int issued = 0;
+    for (int st = 0; st < n_stage; ++st) {
+      const int s = st % kStages;
+      if (!mbar_wait(&empty[s], ((st / kStages) & 1) ^ 1, wc)) break;
+      mbar_arrive_expect_tx(&full[s], kStageKeys * kRowBytes);
+      bulk_load(stage[s], rows + (size_t)st * kStageKeys * D, kStageKeys * kRowBytes, &full[s]);
+      ++issued;
+    }
+    if (abort_word) {   // let the copies in flight land before the CTA exits
+      for (int st = (issued > kStages ? issued - kStages : 0); st < issued; ++st) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(&full[st % kStages], (st / kStages) & 1))
+          if (globaltimer() - t0 > 100ull * 1000ull * 1000ull) break;
+      }
+    }
+  }
+  // Consumer warp: wait until stage st has landed (same outcome in every
+  // lane, so shuffles may follow), read it, then hand its slot back.
+  __device__ __forceinline__ bool ready(int st, const WaitCtx &wc) {
+    return warp_wait(&full[st % kStages], (st / kStages) & 1, wc);
+  }
+  __device__ __forceinline__ const uint8_t *slot(int st) const { return stage[st % kStages]; }
+  __device__ __forceinline__ void release(int st, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st % kStages]);
+  }
+};
+
+template <typename E, int D>
+__global__ void __launch_bounds__(DecRing<E, D>::kThreads)
     dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
                E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
                float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, HeadScale hs, int *status) {
+  using R = DecRing<E, D>;
   constexpr int LPR = lanes_per_row<E, D>();       // lanes cooperating on one key
   constexpr int NV = Vec16<E>::N;
-  constexpr int KPR = kDecThreads / LPR;           // keys per round
+  constexpr int KPR = kDecThreads / LPR;           // keys per round of the consumers
+  constexpr int SK = R::kStageKeys, RPS = SK / KPR;
+  static_assert(SK % KPR == 0, "stage of whole rounds");
   const int bh = blockIdx.y, chunk = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const bool producer = warp == R::kConsumerWarps;
+  __shared__ R ring;
   const float c2 = head_c2(hs, bh, (tid == 0 && chunk == 0) ? status : nullptr);
   const int sub = tid % LPR;                       // which 16-byte piece of the row
   const int grp = tid / LPR;
-  const int n_keys = n_ctx + 1;
   const int k_begin = chunk * kDecChunk;
-  const int k_end = min(k_begin + kDecChunk, n_keys);
-
-  float qf[NV];
-  Vec16<E>::to_float(*reinterpret_cast<const uint4 *>(q_new + (size_t)bh * D + sub * NV), qf);
+  const int k_end = min(k_begin + kDecChunk, n_ctx + 1);
+  // Whole stages of cached rows before n_ctx go through the ring; key n_ctx
+  // (taken from k_new) and the rest of the chunk are read directly.
+  const int n_stage = (min(k_end, n_ctx) - k_begin) / SK;
   const E *kb = k_cache + (size_t)bh * T_cap * D;
+  if (tid == 0) ring.init();
+  __syncthreads();
+  const WaitCtx wc = ring.wait_ctx(status);
   float m = -INFINITY, l = 0.f;
-  // Warp-uniform trip count: every lane runs every round (the shuffles below
-  // need the full warp); keys past the chunk are predicated off.
-  for (int r0 = k_begin; r0 < k_end; r0 += KPR * kDecUnroll) {
-    const int k0 = r0 + grp;
-    uint4 raw[kDecUnroll];
-#pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const int key = k0 + u * KPR;
-      if (key < k_end) {
-        const E *src = (key == n_ctx) ? k_new + (size_t)bh * D : kb + (size_t)key * D;
-        raw[u] = ld_stream(src + sub * NV);
-      } else {
-        raw[u] = make_uint4(0, 0, 0, 0);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const int key = k0 + u * KPR;
+  if (producer) {
+    if (lane == 0) ring.produce(kb + (size_t)k_begin * D, n_stage, wc);
+  } else {
+    float qf[NV];
+    Vec16<E>::to_float(*reinterpret_cast<const uint4 *>(q_new + (size_t)bh * D + sub * NV), qf);
+    // One key per lane group; every lane of the warp runs it (shuffles), and
+    // a key past the chunk (ok = false) leaves the statistics alone.
+    auto consume = [&](int key, const uint4 &raw, bool ok) {
       float kf[NV];
-      Vec16<E>::to_float(raw[u], kf);
+      Vec16<E>::to_float(raw, kf);
       float s = 0.f;
 #pragma unroll
       for (int i = 0; i < NV; ++i) s = fmaf(qf[i], kf[i], s);
 #pragma unroll
       for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (key < k_end) {
+      if (ok) {
         const float x = s * c2;
         if (sub == 0) logits[(size_t)bh * T_cap + key] = x;
         if (x > m) {
@@ -127,6 +185,24 @@ __global__ void __launch_bounds__(kDecThreads)
           l += exp2f(x - m);
         }
       }
+    };
+    for (int st = 0; st < n_stage; ++st) {
+      if (!ring.ready(st, wc)) break;
+      const uint8_t *stg = ring.slot(st);
+#pragma unroll
+      for (int r = 0; r < RPS; ++r) {
+        const int kl = r * KPR + grp;
+        consume(k_begin + st * SK + kl, *reinterpret_cast<const uint4 *>(stg + kl * R::kRowBytes + sub * 16), true);
+      }
+      ring.release(st, lane);
+    }
+    // the tail, with a warp-uniform trip count
+    for (int r0 = k_begin + n_stage * SK; r0 < k_end; r0 += KPR) {
+      const int key = r0 + grp;
+      const bool ok = key < k_end;
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (ok) raw = ld_stream(((key == n_ctx) ? k_new + (size_t)bh * D : kb + (size_t)key * D) + sub * NV);
+      consume(key, raw, ok);
     }
   }
   // Append the new key/value at position n_ctx (done by the chunk holding it).
@@ -137,10 +213,12 @@ __global__ void __launch_bounds__(kDecThreads)
     *reinterpret_cast<uint4 *>(dst + ((size_t)bh * T_cap + n_ctx) * D + piece * NV) =
         *reinterpret_cast<const uint4 *>(src + (size_t)bh * D + piece * NV);
   }
-  // Block reduction of (m, l): only lane sub == 0 of each group holds data.
+  // Block reduction of (m, l): only lane sub == 0 of each consumer group holds data.
   __shared__ float sm[kDecThreads], sl[kDecThreads];
-  sm[tid] = (sub == 0) ? m : -INFINITY;
-  sl[tid] = (sub == 0) ? l : 0.f;
+  if (tid < kDecThreads) {
+    sm[tid] = (sub == 0) ? m : -INFINITY;
+    sl[tid] = (sub == 0) ? l : 0.f;
+  }
   __syncthreads();
   for (int stride = kDecThreads / 2; stride > 0; stride >>= 1) {
     if (tid < stride) {
@@ -156,20 +234,6 @@ __global__ void __launch_bounds__(kDecThreads)
   if (tid == 0) part_ml[(size_t)bh * nchunk + chunk] = make_float2(sm[0], sl[0]);
 }
 
-// The value rows of a chunk stream through a ring of shared-memory stages
-// filled by bulk asynchronous copies that one producer warp issues, so the
-// bytes in flight do not sit in registers (the update otherwise keeps too few
-// in flight to reach HBM rate at its occupancy).  Logits and demand (8 B per
-// key against the row's 128) are read directly, one stage ahead.  A chunk's
-// tail shorter than a stage is read directly too.
-template <typename E, int D>
-struct DecRing {
-  static constexpr int kRowBytes = D * (int)sizeof(E);
-  static constexpr int kStageKeys = 8192 / kRowBytes;   // 64 keys for bf16 rows of 64
-  static constexpr int kStages = 4;
-  static constexpr int kThreads = kDecThreads + 32;     // consumers + the producer warp
-};
-
 template <typename E, int D>
 __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
     dec_update(const E *__restrict__ v_cache, const float *__restrict__ logits, const float2 *__restrict__ part_ml,
@@ -183,24 +247,15 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
   static_assert(SK % KPR == 0, "stage of whole rounds");
   const int bh = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const bool producer = warp == kDecThreads / 32;
+  const bool producer = warp == R::kConsumerWarps;
   const int sub = tid % LPR, grp = tid / LPR;
-  __shared__ __align__(128) uint8_t ring[R::kStages][SK * R::kRowBytes];
-  __shared__ uint64_t full[R::kStages], empty[R::kStages];
-  __shared__ int abort_word;
+  __shared__ R ring;
   __shared__ float s_lse2;
   const int k_begin = chunk * kDecChunk;
   const int k_end = min(k_begin + kDecChunk, n_ctx + 1);
   const int n_stage = (k_end - k_begin) / SK;           // whole stages through the ring
   const E *vb = v_cache + (size_t)bh * T_cap * D;
-  if (tid == 0) {
-    for (int st = 0; st < R::kStages; ++st) {
-      mbar_init(&full[st], 1);
-      mbar_init(&empty[st], kDecThreads / 32);
-    }
-    abort_word = 0;
-    fence_mbar_init();
-  }
+  if (tid == 0) ring.init();
   if (tid < 32) {
     // Combine the per-chunk (max, sum) pairs of this head into lse2.
     float m = -INFINITY, l = 0.f;
@@ -225,7 +280,7 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
   }
   __syncthreads();
   const float lse2 = s_lse2;
-  const WaitCtx wc{reinterpret_cast<volatile int *>(&abort_word), status};
+  const WaitCtx wc = ring.wait_ctx(status);
   float num[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) num[i] = 0.f;
@@ -245,23 +300,7 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
   };
 
   if (producer) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int st = 0; st < n_stage; ++st) {
-        const int slot = st % R::kStages;
-        if (!mbar_wait(&empty[slot], ((st / R::kStages) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&full[slot], SK * R::kRowBytes);
-        bulk_load(ring[slot], vb + (size_t)(k_begin + st * SK) * D, SK * R::kRowBytes, &full[slot]);
-        ++issued;
-      }
-      if (abort_word) {   // let the copies in flight land before the CTA exits
-        for (int st = (issued > R::kStages ? issued - R::kStages : 0); st < issued; ++st) {
-          const unsigned long long t0 = globaltimer();
-          while (!mbar_try_wait(&full[st % R::kStages], (st / R::kStages) & 1))
-            if (globaltimer() - t0 > 100ull * 1000ull * 1000ull) break;
-        }
-      }
-    }
+    if (lane == 0) ring.produce(vb + (size_t)k_begin * D, n_stage, wc);
   } else {
     // logits and demand of this thread's keys, one stage ahead
     float xn[RPS], dn[RPS];
@@ -275,7 +314,6 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
     };
     if (n_stage > 0) fetch(0, xn, dn);
     for (int st = 0; st < n_stage; ++st) {
-      const int slot = st % R::kStages;
       float xc[RPS], dc[RPS];
 #pragma unroll
       for (int r = 0; r < RPS; ++r) {
@@ -283,15 +321,15 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
         dc[r] = dn[r];
       }
       if (st + 1 < n_stage) fetch(st + 1, xn, dn);
-      if (!mbar_wait(&full[slot], (st / R::kStages) & 1, wc)) break;
+      if (!ring.ready(st, wc)) break;
+      const uint8_t *stg = ring.slot(st);
 #pragma unroll
       for (int r = 0; r < RPS; ++r) {
         const int kl = r * KPR + grp;
-        const uint4 raw = *reinterpret_cast<const uint4 *>(ring[slot] + kl * R::kRowBytes + sub * 16);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(stg + kl * R::kRowBytes + sub * 16);
         consume(k_begin + st * SK + kl, raw, xc[r], dc[r]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
+      ring.release(st, lane);
     }
     // the tail of the chunk, read directly
     for (int key = k_begin + n_stage * SK + grp; key < k_end; key += KPR) {
@@ -338,7 +376,7 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
                                    HeadScale hs, float eps, bool earlier, float *logits, float2 *part_ml,
                                    float *part_acc, int nchunk, int *status, cudaStream_t stream) {
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
-  dec_logits<E, D><<<dim3(used, BH), kDecThreads, 0, stream>>>(
+  dec_logits<E, D><<<dim3(used, BH), DecRing<E, D>::kThreads, 0, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
       T_cap, nchunk, hs, status);
   dec_update<E, D><<<dim3(used, BH), DecRing<E, D>::kThreads, 0, stream>>>(
