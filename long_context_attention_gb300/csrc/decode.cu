@@ -78,15 +78,23 @@ constexpr int lanes_per_row() {
 // Whole stages go through the ring; a chunk's tail shorter than a stage is
 // read directly.  Every wait is bounded: a timeout records DA_ERR_TIMEOUT in
 // the status block and the CTA finishes without waiting further.
+// Measured on GB300 (8 x 12 caches of 131072, step time): two 32 KB stages
+// 0.508 ms, two 16 KB 0.515, three 16 KB 0.526, four 8 KB 0.555, six 8 KB
+// 0.608, eight 4 KB 0.762; 512 consumer threads instead of 256 was slower.
+// The stages live in dynamic shared memory (dec_ring_smem), the barriers in
+// the kernel's static shared memory.
+extern __shared__ __align__(128) uint8_t dec_ring_smem[];
+
 template <typename E, int D>
 struct DecRing {
   static constexpr int kRowBytes = D * (int)sizeof(E);
-  static constexpr int kStageKeys = 8192 / kRowBytes;   // 64 keys for bf16 rows of 64
-  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = 32768;
+  static constexpr int kStageKeys = kStageBytes / kRowBytes;   // 256 keys for bf16 rows of 64
+  static constexpr int kStages = 2;
+  static constexpr int kDynSmemBytes = kStages * kStageBytes;
   static constexpr int kConsumerWarps = kDecThreads / 32;
-  static constexpr int kThreads = kDecThreads + 32;     // consumers + the producer warp
+  static constexpr int kThreads = kDecThreads + 32;            // consumers + the producer warp
 
-  __align__(128) uint8_t stage[kStages][kStageKeys * kRowBytes];
   uint64_t full[kStages], empty[kStages];
   int abort_word;
 
@@ -108,8 +116,8 @@ struct DecRing {
     for (int st = 0; st < n_stage; ++st) {
       const int s = st % kStages;
       if (!mbar_wait(&empty[s], ((st / kStages) & 1) ^ 1, wc)) break;
-      mbar_arrive_expect_tx(&full[s], kStageKeys * kRowBytes);
-      bulk_load(stage[s], rows + (size_t)st * kStageKeys * D, kStageKeys * kRowBytes, &full[s]);
+      mbar_arrive_expect_tx(&full[s], kStageBytes);
+      bulk_load(dec_ring_smem + s * kStageBytes, rows + (size_t)st * kStageKeys * D, kStageBytes, &full[s]);
       ++issued;
     }
     if (abort_word) {   // let the copies in flight land before the CTA exits
@@ -125,7 +133,7 @@ struct DecRing {
   __device__ __forceinline__ bool ready(int st, const WaitCtx &wc) {
     return warp_wait(&full[st % kStages], (st / kStages) & 1, wc);
   }
-  __device__ __forceinline__ const uint8_t *slot(int st) const { return stage[st % kStages]; }
+  __device__ __forceinline__ const uint8_t *slot(int st) const { return dec_ring_smem + (st % kStages) * kStageBytes; }
   __device__ __forceinline__ void release(int st, int lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st % kStages]);
@@ -375,11 +383,24 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
                                    void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int BH,
                                    HeadScale hs, float eps, bool earlier, float *logits, float2 *part_ml,
                                    float *part_acc, int nchunk, int *status, cudaStream_t stream) {
+  using R = DecRing<E, D>;
+  // The ring's shared-memory opt-in is a per-device function attribute.
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(dec_logits<E, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         R::kDynSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(dec_update<E, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, R::kDynSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_done[dev] = true;
+  }
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
-  dec_logits<E, D><<<dim3(used, BH), DecRing<E, D>::kThreads, 0, stream>>>(
+  dec_logits<E, D><<<dim3(used, BH), R::kThreads, R::kDynSmemBytes, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
       T_cap, nchunk, hs, status);
-  dec_update<E, D><<<dim3(used, BH), DecRing<E, D>::kThreads, 0, stream>>>(
+  dec_update<E, D><<<dim3(used, BH), R::kThreads, R::kDynSmemBytes, stream>>>(
       (const E *)v_cache, logits, part_ml, demand, part_acc, n_ctx, T_cap, nchunk, used, eps, earlier, status);
   dec_combine<E, D><<<BH, D, 0, stream>>>(part_acc, (E *)out, nchunk, used);
   return cudaGetLastError();
