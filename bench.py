@@ -36,7 +36,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 SWEEP_SOURCES = ["long_context_attention_gb300/csrc/fwd_bf16.cu", "long_context_attention_gb300/csrc/da_ptx.cuh",
                  "long_context_attention_gb300/csrc/da_internal.h"]
 SWEEP_PROFILE = os.path.join(ROOT, "profiles", "sweep_kernel_fwd_bf16_t16384.md")
-DECODE_SOURCES = ["long_context_attention_gb300/csrc/decode.cu", "long_context_attention_gb300/csrc/da_internal.h"]
+DECODE_SOURCES = ["long_context_attention_gb300/csrc/decode.cu", "long_context_attention_gb300/csrc/da_internal.h",
+                  "long_context_attention_gb300/csrc/da_ptx.cuh"]
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_bf16_ctx131072.md")
 
 

@@ -71,6 +71,18 @@ constexpr int lanes_per_row() {
   return D / Vec16<E>::N;
 }
 
+// Bulk copy global -> shared with an L2 evict-first policy, for rows read
+// exactly once: their lines are the first to go, so the logit scratch and the
+// demand written by the same step stay in L2.
+__device__ __forceinline__ void bulk_load_stream(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n\t}"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Cache rows stream through a ring of shared-memory stages filled by bulk
 // asynchronous copies that one producer warp issues, so the bytes in flight
 // do not sit in registers (with register-held loads both streaming kernels
@@ -117,7 +129,7 @@ struct DecRing {
       const int s = st % kStages;
       if (!mbar_wait(&empty[s], ((st / kStages) & 1) ^ 1, wc)) break;
       mbar_arrive_expect_tx(&full[s], kStageBytes);
-      bulk_load(dec_ring_smem + s * kStageBytes, rows + (size_t)st * kStageKeys * D, kStageBytes, &full[s]);
+      bulk_load_stream(dec_ring_smem + s * kStageBytes, rows + (size_t)st * kStageKeys * D, kStageBytes, &full[s]);
       ++issued;
     }
     if (abort_word) {   // let the copies in flight land before the CTA exits
