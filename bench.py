@@ -77,6 +77,32 @@ def sweep_flops(B, H, T, d):
     return 2 * d * T * (T + 1) * B * H
 
 
+# Special-function-unit (MUFU) results the forward issues per causal pair:
+# one exponential in the row statistics; one exponential and one reciprocal per
+# pair of queries in the sweep.  Peak: 32 MUFU results per SM per clock (an
+# isolated ex2 loop reached 29.6 on GB300), times the SM count and clock.
+SFU_PER_PAIR = {"rowstats": 1.0, "sweep": 1.5}
+SFU_PER_SM_CLK = 32
+
+
+def sfu_report(B, H, T, kern_ms, n_sm, sm_mhz):
+    """Achieved MUFU results/s of the two forward kernels and of the step."""
+    pairs = T * (T + 1) // 2 * B * H
+    peak = SFU_PER_SM_CLK * n_sm * sm_mhz * 1e6 / 1e12
+    out = {"unit": "Tops/s", "peak": peak, "peak_source": f"{SFU_PER_SM_CLK}/SM/clk x {n_sm} SMs x {sm_mhz:.0f} MHz",
+           "ops_per_pair": SFU_PER_PAIR}
+    tot_ops, tot_ms = 0.0, 0.0
+    for k_, per in SFU_PER_PAIR.items():
+        ops = per * pairs
+        out[k_] = {"achieved": ops / (kern_ms[k_] * 1e-3) / 1e12}
+        out[k_]["frac"] = out[k_]["achieved"] / peak
+        tot_ops += ops
+        tot_ms += kern_ms[k_]
+    out["achieved"] = tot_ops / (tot_ms * 1e-3) / 1e12
+    out["frac"] = out["achieved"] / peak
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -506,6 +532,8 @@ def run_ours(args):
                          "unit": "TFLOP/s", "frac": sweep_tf / peak_t, "traffic": profiled_traffic(),
                          "peak_source": f"{peaks_kind} {'sustained' if timed_s > 1.0 else 'burst'} bf16",
                          "rowstats_achieved": rs_tf, "rowstats_frac": rs_tf / peak_t},
+            "sfu": sfu_report(B, H, T, kern_ms, torch.cuda.get_device_properties(dev).multi_processor_count,
+                              clocks.get("sm_max_mhz") or 2070.0),
             "gpu_launches": 3 * K, "clocks": clocks}
 
     if not args.no_e2e:
