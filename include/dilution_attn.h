@@ -86,7 +86,11 @@ int dilution_attn_version(void);
  *              ("DilutionAttention v0.1.0 · results", section "The operator",
  *              cached decoding).
  * workspace: device scratch of at least dilution_attn_fwd_workspace_size()
- * bytes; its first 256 bytes hold the status word.  Every call overwrites the
+ * bytes; its first 256 bytes hold the status word.  For bf16 inputs, int32
+ * word 4 of that block counts the rows whose softmax normaliser the
+ * tensor-core pass handed to an exact per-row recomputation (its running sum
+ * overflowed: a logit more than ~106 log2 units above the maximum of the
+ * row's first 32 keys); diagnostic only.  Every call overwrites the
  * workspace, so concurrent calls on different streams need distinct
  * workspaces.  Errors: DA_ERR_INVALID, DA_ERR_UNSUPPORTED, DA_ERR_WORKSPACE,
  * DA_ERR_CUDA (launch failure).

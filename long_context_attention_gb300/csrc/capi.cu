@@ -139,7 +139,7 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
   float *acc = reinterpret_cast<float *>(ws + L.acc_off);
   float *cchk = keep ? reinterpret_cast<float *>(ws + LB.cchk_off) : nullptr;
   if (dtype == DA_BF16 && eps < 1e-18f) return DA_ERR_UNSUPPORTED;
-  if (cudaMemsetAsync(status, 0, 4 * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, kStatusWordsReset * sizeof(int), stream) != cudaSuccess) return DA_ERR_CUDA;
   const HeadScale hs = head_scale(tau, tau_bh, d);
   if (dtype == DA_F32) {
     if (launch_fwd_f32((const float *)q, (const float *)k, (const float *)v, (float *)out, lse2_out, rowsum_out,

@@ -24,6 +24,11 @@ constexpr int kDMax = 128;
 constexpr int kTile = 128;         // query / key tile edge (one TMEM lane per row)
 constexpr int kSpan = 256;         // Tp granule: two 128-row tiles (one row-statistics CTA)
 constexpr size_t kStatusBytes = 256;
+// Status block words: [0] status code, [1..3] where a bounded wait gave up,
+// [4] rows the row-statistics pass marked for exact recomputation.  Words
+// 0..kStatusWordsReset-1 are cleared before every call.
+constexpr int kStatusRowsRedo = 4;
+constexpr int kStatusWordsReset = 8;
 
 DA_HD bool head_dim_supported(int d) { return d == 64 || d == 128; }
 // fp32 per accumulator row: d numerator + row sum + 3 pad (16-byte rows).

@@ -90,29 +90,16 @@ __device__ __forceinline__ void release_tmem(uint64_t *bar, int lane) {
 }
 
 // Softmax normaliser of one query row in the log2 domain, lse2 = m + log2 l
-// with l = sum 2^(x - m), x = s * c2.  The reference m is updated lazily: a
-// chunk is summed against the current m without waiting for its own maximum,
-// and only a chunk whose sum leaves [0, 2^64] (a score more than 64 above m,
-// or the row's first chunk, where m = -inf) takes the exact path: chunk
-// maximum, rescale of l, terms recomputed.  lse2 is exact for any m; every
-// term stays <= 2^64 and the largest one seen at a rescale is 1, so l neither
-// overflows nor loses its dominant terms.
+// with l = sum 2^(x - m), x = s * c2.  The reference m is the maximum of the
+// row's first 32-key chunk (so l >= 1); every later chunk is summed against
+// it without a check.  lse2 is exact for any m as long as l stays finite: a
+// row whose sum passes 2^120 (a logit more than ~106 above that first
+// maximum; fp32 overflows at 2^128) is marked and recomputed exactly by
+// rowstats_fixup_kernel.  Terms below 2^-126 flush to zero, which is
+// negligible against l >= 1.
 struct RowStat {
   float m = -INFINITY;
   float2 l0 = make_float2(0.f, 0.f), l1 = make_float2(0.f, 0.f);
-
-  __device__ __forceinline__ void terms(const float (&s)[32], float c2, float2 &a0, float2 &a1) const {
-    const float2 c2v = make_float2(c2, c2), nm = make_float2(-m, -m);
-    a0 = make_float2(0.f, 0.f);
-    a1 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-      const float2 x0 = ffma2(make_float2(s[2 * j], s[2 * j + 1]), c2v, nm);
-      const float2 x1 = ffma2(make_float2(s[2 * j + 2], s[2 * j + 3]), c2v, nm);
-      a0 = fadd2(a0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
-      a1 = fadd2(a1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
-    }
-  }
 
   // 32 consecutive keys (columns col0 ..) of the row; DIAG masks key > query.
   template <bool DIAG>
@@ -122,30 +109,30 @@ struct RowStat {
       for (int c = 0; c < 32; ++c)
         if (col0 + c > row) s[c] = -INFINITY;
     }
-    float2 a0, a1;
-    if (m != -INFINITY) {
-      terms(s, c2, a0, a1);
-      const float cs = (a0.x + a0.y) + (a1.x + a1.y);
-      if (cs <= 0x1p64f) {   // false for inf / NaN as well
-        l0 = fadd2(l0, a0);
-        l1 = fadd2(l1, a1);
-        return;
-      }
-    }
-    float t[11];
+    if (m == -INFINITY) {   // the row's first chunk: its maximum becomes the reference
+      float t[11];
 #pragma unroll
-    for (int i = 0; i < 10; ++i) t[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-    t[10] = fmaxf(s[30], s[31]);
-    const float mx = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], fmax3(t[8], t[9], t[10])));
-    if (mx == -INFINITY) return;   // every key of the chunk is after the query
-    const float mn = fmaxf(m, mx * c2);
-    const float sc = ex2_approx(m - mn);    // 0 on the first chunk (m = -inf)
-    l0 = fmul2(l0, make_float2(sc, sc));
-    l1 = fmul2(l1, make_float2(sc, sc));
-    m = mn;
-    terms(s, c2, a0, a1);
-    l0 = fadd2(l0, a0);
-    l1 = fadd2(l1, a1);
+      for (int i = 0; i < 10; ++i) t[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+      t[10] = fmaxf(s[30], s[31]);
+      const float mx =
+          fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], fmax3(t[8], t[9], t[10])));
+      if (mx == -INFINITY) return;   // every key of the chunk is after the query
+      m = mx * c2;
+    }
+    const float2 c2v = make_float2(c2, c2), nm = make_float2(-m, -m);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const float2 x0 = ffma2(make_float2(s[2 * j], s[2 * j + 1]), c2v, nm);
+      const float2 x1 = ffma2(make_float2(s[2 * j + 2], s[2 * j + 3]), c2v, nm);
+      l0 = fadd2(l0, make_float2(ex2_approx(x0.x), ex2_approx(x0.y)));
+      l1 = fadd2(l1, make_float2(ex2_approx(x1.x), ex2_approx(x1.y)));
+    }
+  }
+
+  // -lse2 of the row, or NaN when the sum left [1, 2^120] (inf or NaN included).
+  __device__ __forceinline__ float neg_lse2() const {
+    const float l = (l0.x + l0.y) + (l1.x + l1.y);
+    return l <= 0x1p120f ? -(m + log2f(l)) : NAN;
   }
 };
 
@@ -306,6 +293,7 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kTile, kTile, false, false);
+      const uint64_t dQ0 = kmajor_desc(sQ, 0), dQ1 = kmajor_desc(sQ + kTB, 0), dK0 = kmajor_desc(sK, 0);
       if (mbar_wait(q_full, 0, wc)) {
         tc_fence_after();
         for (int kt = 0; kt < n_kt; ++kt) {
@@ -323,9 +311,10 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
             }
             tc_fence_after();
             const uint32_t d = tmem + slot * kTile;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16(d, kmajor_desc(sQ + g * kTB, kk), kmajor_desc(sK + s * kTB, kk), idesc, kk > 0);
+            const uint64_t dQg = g ? dQ1 : dQ0;
+            const uint64_t dKs = dK0 + (uint64_t)s * (kTB >> 4);
+            MmaRun<0, 4, 2, 2, false>::go(d, dQg, dKs, idesc, 0u);
+            if constexpr (D == 128) MmaRun<0, 4, 2, 2, false>::go(d, dQg + (kHalfBytes >> 4), dKs + (kHalfBytes >> 4), idesc, 1u);
             mma_commit(&s_full[slot]);
           }
           if (!ok) break;
@@ -383,7 +372,12 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
     }
     if (qi < Tp) {
       // negated, so the sweep forms x - lse2 with one packed fma
-      nlse2[(size_t)w.bh * Tp + qi] = (qi < T) ? -(st.m + log2f(st.l0.x + st.l0.y + st.l1.x + st.l1.y)) : -INFINITY;
+      float v = -INFINITY;
+      if (qi < T) {
+        v = st.neg_lse2();
+        if (v != v) atomicAdd(status + kStatusRowsRedo, 1);   // marked for rowstats_fixup_kernel
+      }
+      nlse2[(size_t)w.bh * Tp + qi] = v;
       float4 *ar = reinterpret_cast<float4 *>(acc + ((size_t)w.bh * Tp + qi) * AS);
 #pragma unroll
       for (int t = 0; t < AS / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -396,6 +390,73 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Exact recomputation of the rows that rowstats_kernel marked (their running
+// sum overflowed: a logit more than ~106 above the maximum of the row's first
+// 32 keys).  One warp per marked row: each lane walks keys lane, lane + 32, ...
+// <= the query with an exact running maximum, then the lanes' (max, sum)
+// pairs are merged.  Exits at once when no row was marked, which is the case
+// for any input whose logits stay within ~106 (log2 units) of each row's
+// first-chunk maximum.
+template <int D>
+__global__ void __launch_bounds__(256) rowstats_fixup_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                             const __nv_bfloat16 *__restrict__ k,
+                                                             float *__restrict__ nlse2, int BH, int T, int Tp,
+                                                             HeadScale hs, int *status) {
+  // nothing marked, or the pass gave up (rows it did not reach are not valid marks)
+  const volatile int *vs = status;
+  if (vs[kStatusRowsRedo] == 0 || vs[0] != DA_OK) return;
+  __shared__ float sq[8][D];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t nrows = (int64_t)BH * Tp;
+  const int64_t nwarps = (int64_t)gridDim.x * 8;
+  for (int64_t base = ((int64_t)blockIdx.x * 8 + warp) * 32; base < nrows; base += nwarps * 32) {
+    const bool marked = base + lane < nrows && nlse2[base + lane] != nlse2[base + lane];
+    uint32_t todo = __ballot_sync(0xffffffffu, marked);
+    while (todo != 0u) {
+      const int64_t r = base + (__ffs(todo) - 1);
+      todo &= todo - 1u;
+      const int bh = (int)(r / Tp);
+      const int64_t i = r % Tp;
+      if (i >= T) continue;       // padded rows are never marked
+      const float c2 = bf16_c2(hs, bh, nullptr);
+      for (int t = lane; t < D; t += 32) sq[warp][t] = __bfloat162float(q[((size_t)bh * T + i) * D + t]);
+      __syncwarp();
+      float m = -INFINITY, l = 0.f;
+      for (int64_t key = lane; key <= i; key += 32) {
+        const uint4 *kr = reinterpret_cast<const uint4 *>(k + ((size_t)bh * T + key) * D);
+        float dot = 0.f;
+#pragma unroll
+        for (int t = 0; t < D / 8; ++t) {
+          const uint4 u = __ldg(kr + t);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+            dot = fmaf(sq[warp][8 * t + 2 * e], kv.x, dot);
+            dot = fmaf(sq[warp][8 * t + 2 * e + 1], kv.y, dot);
+          }
+        }
+        const float x = dot * c2;
+        if (x > m) {
+          l = l * ex2_approx(m - x) + 1.f;
+          m = x;
+        } else {
+          l += ex2_approx(x - m);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o), lo = __shfl_xor_sync(0xffffffffu, l, o);
+        const float mn = fmaxf(m, mo);
+        l = (mn == -INFINITY) ? 0.f : l * ex2_approx(m - mn) + lo * ex2_approx(mo - mn);
+        m = mn;
+      }
+      if (lane == 0) nlse2[r] = -(m + log2f(l));
+      __syncwarp();
+    }
   }
 }
 
@@ -958,9 +1019,12 @@ static int prepare_fwd_bf16() {
   return st;
 }
 
+// Blocks of the fix-up pass (two per SM of a GB300; grid-stride over rows).
+constexpr int kFixupBlocks = 304;
 template <int D>
 static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const CUtensorMap &ta, const void *k, float *demand_out, int BH, int T, HeadScale hs,
+                             const CUtensorMap &ta, const void *q, const void *k, float *demand_out, int BH, int T,
+                             HeadScale hs,
                              float eps, bool earlier, float *lse2_ws, float *acc, float *cchk, int *status,
                              cudaStream_t stream, cudaEvent_t const *ev) {
   // The shared-memory opt-in is a per-device function attribute.
@@ -977,6 +1041,9 @@ static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const
   if (ev[0]) cudaEventRecord(ev[0], stream);
   rowstats_kernel<D><<<rowstats_num_ctas(BH, T), kRsThreads, RsCfg<D>::kSmemBytes, stream>>>(tq, tk, lse2_ws, acc,
                                                                                             BH, T, Tp, hs, status);
+  rowstats_fixup_kernel<D><<<kFixupBlocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(q),
+                                                              static_cast<const __nv_bfloat16 *>(k), lse2_ws, BH, T,
+                                                              Tp, hs, status);
   if (ev[1]) cudaEventRecord(ev[1], stream);
   const int nsw = sweep_num_ctas(BH, T, D);
   const uint4 *kg = static_cast<const uint4 *>(k);
@@ -1044,9 +1111,9 @@ int launch_fwd_bf16(const void *q, const void *k, const void *v, void *out, floa
   if (!make_tile_map(&tq, q, BH, T, d) || !make_tile_map(&tk, k, BH, T, d) || !make_tile_map(&tv, v, BH, T, d) ||
       !make_acc_map(&ta, acc, acc_rows, d))
     return DA_ERR_CUDA;
-  const int st = d == 128 ? launch_fwd_bf16_t<128>(tq, tk, tv, ta, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
+  const int st = d == 128 ? launch_fwd_bf16_t<128>(tq, tk, tv, ta, q, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
                                                    acc, cchk, status, stream, ev)
-                          : launch_fwd_bf16_t<64>(tq, tk, tv, ta, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
+                          : launch_fwd_bf16_t<64>(tq, tk, tv, ta, q, k, demand_out, BH, T, hs, eps, earlier, lse2_ws,
                                                   acc, cchk, status, stream, ev);
   if (st != DA_OK) return st;
   if (ev[2]) cudaEventRecord(ev[2], stream);

@@ -106,8 +106,9 @@ def test_bf16_tau_and_eps():
 
 def test_bf16_sharp_logits_rescale():
     # tau = 6 multiplies the planted logits (~26 in log2 units at tau = 1) to
-    # ~150: a row's later key tiles then score far more than 64 above its first
-    # chunk, which forces the row-statistics pass to rescale its running sum.
+    # ~150: a row whose planted key lies beyond its first 32 keys then scores
+    # far above that chunk's maximum, overflows the unchecked running sum and
+    # is recomputed by the fix-up pass.
     q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 2, 700, 64, q_std=1.5, pairs=8, seed=41, dtype="bf16"))
     compare(q, k, v, tau=6.0, eps=1e-6)
 
@@ -209,3 +210,50 @@ def test_bf16_tau_zero_uniform_bids():
     for (bb, hh), r in ref.items():
         check_head([x[bb, hh] for x in got], r, "bf16")
     assert np.abs(got[1][0, 0] - np.log2(np.arange(1, T + 1))).max() < 2e-3
+
+
+def _status_words(ws):
+    torch.cuda.synchronize()
+    return ws[:32].view(torch.int32).cpu().tolist()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_overflowing_rows_recomputed(d):
+    """The row-statistics pass sums each row against the maximum of its first
+    32 keys without further checks; a row whose later logit lies far above that
+    (here ~185 log2 units at d = 64) overflows the running sum, is marked, and
+    is recomputed exactly by the fix-up pass (status word 4 counts the marked
+    rows).  Marked and ordinary rows both match the oracle."""
+    B, H, T = 1, 2, 300
+    g = torch.Generator().manual_seed(70 + d)
+    q = torch.randn(B, H, T, d, generator=g) * 1.5
+    k = torch.randn(B, H, T, d, generator=g)
+    v = torch.randn(B, H, T, d, generator=g)
+    big = [50, 100, 200, 299]
+    k[:, :, 40] = 4.0          # key 40 sits in the second 32-key chunk of every row
+    for i in big:
+        q[:, :, i] = 4.0       # q_i . k_40 = 16 d
+    q, k, v = (x.to(torch.bfloat16).to(DEV) for x in (q, k, v))
+    out = torch.empty_like(q)
+    lse2, rs, dem = (torch.empty(B, H, T, device=DEV) for _ in range(3))
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b._dtype_code(q)), dtype=torch.uint8,
+                     device=DEV)
+    b.dilution_attn_fwd(q, k, v, out, lse2, rs, dem, workspace=ws)
+    words = _status_words(ws)
+    assert words[0] == b.DA_OK
+    assert words[4] == B * H * len(big)
+    got = [host64(x) for x in (out, lse2, rs, dem)]
+    ref = oracle_forward(q, k, v, 1.0, 1e-6)
+    for (bb, hh), r in ref.items():
+        check_head([x[bb, hh] for x in got], r, "bf16")
+    assert np.all(got[1][0, :, big] > 150.0)
+
+
+def test_bf16_ordinary_rows_not_marked():
+    """Planted retrieval pairs at tau = 1 stay well inside the unchecked range:
+    no row is marked for recomputation."""
+    q, k, v = (x.to(DEV) for x in inputs.make_qkv(1, 4, 1500, 64, q_std=1.5, pairs=16, seed=33, dtype="bf16"))
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(1, 4, 1500, 64, 1), dtype=torch.uint8, device=DEV)
+    b.dilution_attn_fwd(q, k, v, workspace=ws)
+    words = _status_words(ws)
+    assert words[0] == b.DA_OK and words[4] == 0
