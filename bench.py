@@ -142,6 +142,24 @@ def profiled_traffic(profile=None, sources=None):
         return None
 
 
+def max_over_ranks(x, device=None):
+    """The largest value of x over the ranks of the default process group
+    (x itself when no group is initialised): every replica's timing is taken
+    and the slowest one defines the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(seed, rank):
+    """Seed of rank `rank`'s independent replica batch."""
+    return seed + 1000 * rank
+
+
 def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -462,8 +480,8 @@ def run_ours(args):
     w = inputs.WORKLOADS[args.workload]
     B, H, T, d = (args.batch or w.B), w.H, w.T, w.d
     # each rank is an independent replica with its own seeded batch
-    q, k, v = inputs.make_qkv(B, H, T, d, q_std=w.q_std, pairs=w.pairs, seed=w.seed + 1000 * rank, dtype=w.dtype,
-                              device=dev)
+    q, k, v = inputs.make_qkv(B, H, T, d, q_std=w.q_std, pairs=w.pairs, seed=replica_seed(w.seed, rank),
+                              dtype=w.dtype, device=dev)
     out = torch.empty_like(q)
     ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b._dtype_code(q)), dtype=torch.uint8,
                      device=dev)
@@ -496,11 +514,7 @@ def run_ours(args):
         barrier()
         w1 = time.time()
     assert b.dilution_attn_get_error(ws) == b.DA_OK
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     per = {"rowstats": [], "sweep": [], "finalize": []}
     for e4 in evs:
         per["rowstats"].append(e4[0].elapsed_time(e4[1]))
@@ -588,11 +602,7 @@ def run_ours(args):
         e1.record(cur)
         torch.cuda.synchronize()
         assert b.dilution_attn_get_error(wsc) == b.DA_OK
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
         line["e2e"] = {"value": world * flops_step * Ke / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                        "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": Ke,
