@@ -294,7 +294,12 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kTile, kTile, false, false);
       const uint64_t dQ0 = kmajor_desc(sQ, 0), dQ1 = kmajor_desc(sQ + kTB, 0), dK0 = kmajor_desc(sK, 0);
-      if (mbar_wait(q_full, 0, wc)) {
+      auto kt_slot = [](int g, int kt) { return g * NS + kt % NS; };
+      // d = 64 (two CTAs per SM, four reduction warps per sub-partition):
+      // key tile by key tile, query tile 0 then 1, with blocking waits that
+      // leave the issue slots to the reduction warps (polling both slots, as
+      // at d = 128, measured 0.958 -> 0.989 ms here).
+      if (D == 64 && mbar_wait(q_full, 0, wc)) {
         tc_fence_after();
         for (int kt = 0; kt < n_kt; ++kt) {
           const int s = kt % kRsKStages;
@@ -319,6 +324,59 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
           }
           if (!ok) break;
           mma_commit(&k_empty[s]);
+        }
+      }
+      // d = 128 (one CTA per SM, two reduction warps per sub-partition): the
+      // two query tiles' S products are issued as soon as each one's slot is
+      // free, whichever comes first, so that neither tile's reduction waits
+      // on the other's (measured: 1.43 -> 1.38 ms at 4x12x16384x128).  Query tile g uses key tiles 0 .. q_tile0 + g;
+      // a key stage goes back to the producer once every query tile that uses
+      // it has been issued (the commit covers all earlier products).  A query
+      // tile runs at most one ring's depth ahead of the other, so no barrier
+      // is polled more than one phase ahead.
+      if (D == 128 && mbar_wait(q_full, 0, wc)) {
+        tc_fence_after();
+        const int lim[2] = {w.q_tile0 + 1, w.q_tile0 + 2};
+        int nx[2] = {0, 0}, kdone = 0;
+        unsigned long long idle0 = 0;
+        while (nx[0] < lim[0] || nx[1] < lim[1]) {
+          bool progressed = false;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int kt = nx[g];
+            if (kt >= lim[g]) continue;
+            const int s = kt % kRsKStages;
+            const int slot = g * NS + kt % NS;
+            if (!mbar_test_wait(&k_full[s], (kt / kRsKStages) & 1) ||
+                !mbar_test_wait(&s_free[slot], ((kt / NS) & 1) ^ 1))
+              continue;
+            tc_fence_after();
+            const uint32_t d = tmem + slot * kTile;
+            const uint64_t dQg = g ? dQ1 : dQ0;
+            const uint64_t dKs = dK0 + (uint64_t)s * (kTB >> 4);
+            MmaRun<0, 4, 2, 2, false>::go(d, dQg, dKs, idesc, 0u);
+            if constexpr (D == 128) MmaRun<0, 4, 2, 2, false>::go(d, dQg + (kHalfBytes >> 4), dKs + (kHalfBytes >> 4), idesc, 1u);
+            mma_commit(&s_full[slot]);
+            ++nx[g];
+            progressed = true;
+          }
+          while (kdone < n_kt && (nx[0] > kdone || kdone >= lim[0]) && nx[1] > kdone) {
+            mma_commit(&k_empty[kdone % kRsKStages]);
+            ++kdone;
+          }
+          if (progressed) {
+            idle0 = 0;
+            continue;
+          }
+          if (*abort_flag) break;
+          const unsigned long long now = globaltimer();
+          if (idle0 == 0) {
+            idle0 = now;
+          } else if (now - idle0 > kWaitLimitNs) {
+            raise_timeout(wc, nx[0] < lim[0] ? &s_free[kt_slot(0, nx[0])] : &s_free[kt_slot(1, nx[1])]);
+            break;
+          }
+          __nanosleep(32);
         }
       }
       mma_commit(drain);
