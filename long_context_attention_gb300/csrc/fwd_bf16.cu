@@ -959,14 +959,14 @@ __global__ void __launch_bounds__(SwCfg<D>::kThreads, 1) __maxnreg__(SwCfg<D>::k
         if (need_mask) demand_chunk<true, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         else demand_chunk<false, 1, EARLIER>(B, row_eff, c2, ceps, pk);
         store(pk, 1);
-        tmem_wait_ld_r(A);
         tmem_ld32(tb + 96, B);
+        tmem_wait_ld_r(A);
+        tmem_wait_ld_r(B);
+        release_tmem(&s_free[g], lane);   // the next tile's S runs while the last two chunks are formed
         if (CHK && ck != nullptr) ck[2 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         else demand_chunk<false, 2, EARLIER>(A, row_eff, c2, ceps, pk);
         store(pk, 2);
-        tmem_wait_ld_r(B);
-        release_tmem(&s_free[g], lane);
         if (CHK && ck != nullptr) ck[3 * (size_t)Tp] = ceps;
         if (need_mask) demand_chunk<true, 3, EARLIER>(B, row_eff, c2, ceps, pk);
         else demand_chunk<false, 3, EARLIER>(B, row_eff, c2, ceps, pk);
