@@ -718,7 +718,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
   } else if (warp == 5) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr long long kStepKm = 2, kStepMn = 128;
+      constexpr long long kStepMn = 128;
       const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
       const uint32_t idesc_q = idesc_bf16(kTile, D, true, true);
       const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
