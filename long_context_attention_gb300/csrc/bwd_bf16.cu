@@ -367,6 +367,17 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
     int issued = 0;
     for (int u = 0; u < n; ++u) {
       const int b = u & 1, h = half_of(u);
+      // the half tile's per-query values are read before waiting for the
+      // buffer, so their global-memory latency overlaps that wait
+      float nl[2], de[2], ri[2], rh[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const size_t idx = (size_t)bh * Tp + h * 64 + lane + 32 * j;
+        nl[j] = __ldg(nlse2 + idx);
+        de[j] = __ldg(delta + idx);
+        ri[j] = __ldg(rinv + idx);
+        rh[j] = MODE == kModeKV ? __ldg(rho + idx) : 0.f;
+      }
       if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&in_full[b], 2 * C::kHB);
@@ -377,11 +388,10 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int qq = lane + 32 * j;
-        const size_t idx = (size_t)bh * Tp + h * 64 + qq;
-        put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, __ldg(nlse2 + idx) / c2);
-        put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -__ldg(delta + idx));
-        sRinv[b * 64 + qq] = __ldg(rinv + idx);
-        if (MODE == kModeKV) sRho[b * 64 + qq] = rho[idx];
+        put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, nl[j] / c2);
+        put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -de[j]);
+        sRinv[b * 64 + qq] = ri[j];
+        if (MODE == kModeKV) sRho[b * 64 + qq] = rh[j];
       }
       fence_proxy_async_smem();
       __syncwarp();
