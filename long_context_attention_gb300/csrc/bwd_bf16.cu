@@ -611,9 +611,11 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
 template <int D>
 struct QCfg {
   static constexpr uint32_t kTB = kTile * D * 2;
-  static constexpr uint32_t kOffQ = 0, kOffG = kTB, kOffK = 2 * kTB, kOffV = 3 * kTB;
-  static constexpr uint32_t kOffDs = 4 * kTB;                     // 2 M-blocks x 16 key groups x 1 KB
-  static constexpr uint32_t kOffAExt = kOffDs + 2 * 16 * 1024;
+  // two key-tile buffers (tile u in buffer u % 2), one value tile, and ds of
+  // one 64-query half (16 key groups x 1 KB)
+  static constexpr uint32_t kOffQ = 0, kOffG = kTB, kOffK = 2 * kTB, kOffV = 4 * kTB;
+  static constexpr uint32_t kOffDs = 5 * kTB;
+  static constexpr uint32_t kOffAExt = kOffDs + 16 * 1024;
   static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // 128 query rows
   static constexpr uint32_t kOffBExtA = kOffBExtS + kExt128;
   static constexpr uint32_t kOffRinv = kOffBExtA + kExt128;       // [128] fp32
@@ -621,6 +623,10 @@ struct QCfg {
   static constexpr uint32_t kOffBar = kOffRho + 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+  // TMEM: S' (64 columns), dA' (64), then dQ as two M = 64 accumulators
+  // (queries 0..63 and 64..127 of the tile), d columns each
+  static constexpr uint32_t kTmemDQ = 128;
+  static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -642,12 +648,12 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
   float *sRho = reinterpret_cast<float *>(smem + C::kOffRho);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *q_full = bars;           // Q, G tiles and the query rows
-  uint64_t *k_full = bars + 1, *k_empty = bars + 2;
-  uint64_t *v_full = bars + 3, *v_empty = bars + 4;
-  uint64_t *s_full = bars + 5, *s_free = bars + 6;
-  uint64_t *ds_full = bars + 7, *ds_free = bars + 8;
-  uint64_t *fin = bars + 9, *drain = bars + 10;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+  uint64_t *k_full = bars + 1, *k_empty = bars + 3;   // [2]: key buffer u % 2
+  uint64_t *v_full = bars + 5, *v_empty = bars + 6;
+  uint64_t *s_full = bars + 7, *s_free = bars + 8;
+  uint64_t *ds_full = bars + 9, *ds_free = bars + 10;   // per step it = 2 u + half
+  uint64_t *fin = bars + 11, *drain = bars + 12;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -658,8 +664,10 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 2);
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
     mbar_init(v_full, 1);
     mbar_init(v_empty, 1);
     mbar_init(s_full, 1);
@@ -675,7 +683,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
   zero_smem(sBExtS, 2 * kExt128, threadIdx.x, kBtThreads);   // both extension row blocks
   fence_proxy_async_smem();
   if (warp == 5) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
@@ -709,9 +717,10 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
     int issued = 0;
     if (lane == 0) {
       for (int u = 0; u < n; ++u) {
-        if (!mbar_wait(k_empty, (u & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(k_full, C::kTB);
-        load_tile_halves<D, kH128>(sK, &tmK, k_full, u * kTile, bh);
+        const int kb = u & 1;
+        if (!mbar_wait(&k_empty[kb], ((u >> 1) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&k_full[kb], C::kTB);
+        load_tile_halves<D, kH128>(sK + kb * C::kTB, &tmK, &k_full[kb], u * kTile, bh);
         if (!mbar_wait(v_empty, (u & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(v_full, C::kTB);
         load_tile_halves<D, kH128>(sV, &tmV, v_full, u * kTile, bh);
@@ -719,10 +728,9 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
       }
       if (*abort_flag) {
         drain_wait_bt(q_full, 0);
-        if (issued > 0) {
-          drain_wait_bt(k_full, (issued - 1) & 1);
-          drain_wait_bt(v_full, (issued - 1) & 1);
-        }
+        for (int u = (issued > 2 ? issued - 2 : 0); u <= issued && u < n; ++u)   // key loads possibly in flight
+          drain_wait_bt(&k_full[u & 1], (u >> 1) & 1);
+        if (issued > 0) drain_wait_bt(v_full, (issued - 1) & 1);
       }
     }
   } else if (warp == 5) {
@@ -730,45 +738,58 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
     if (lane == 0) {
       constexpr long long kStepMn = 128;
       const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
-      const uint32_t idesc_q = idesc_bf16(kTile, D, true, true);
-      const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
+      const uint32_t idesc_q = idesc_bf16(64, D, true, true);   // one 64-query half: M = 64
+      const uint64_t dV = kdesc(sV, 0);
       const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
-      // ds: MN-major, 64-query blocks 16 KB apart (LBO), 8-key groups 1 KB
-      // apart (SBO); K as the MN-major B operand (16 keys = 2 KB per K step,
-      // its 64-column halves 16 KB apart)
+      // ds: MN-major, one 64-query block, 8-key groups 1 KB apart (SBO); K as
+      // the MN-major B operand (16 keys = 2 KB per K step, its 64-column
+      // halves 16 KB apart)
       const uint64_t dDs = smem_desc(smem_u32(sDs), 16384, 1024);
-      const uint64_t dKmn = smem_desc(smem_u32(sK), kH128, 1024);
+      // Steps it = 2 u + hh (key tile u, query half hh).  The events of the
+      // key threads come in the order: slot of step it released (its S' and
+      // dA' loaded), ds of step it written, slot of step it + 1 released ...;
+      // so the issuer walks S(0), S(1), dQ(0), S(2), dQ(1), ... with blocking
+      // waits.  dQ(it) adds ds K(u) into the half's accumulator; key tile u's
+      // buffer goes back to the producer after dQ(2 u + 1), so tile u + 1
+      // (the other buffer) has been loading all along.
+      auto issue_s = [&](int it) -> bool {
+        const int u = it >> 1, hh = it & 1;
+        if (hh == 0 && (!mbar_wait(&k_full[u & 1], (u >> 1) & 1, wc) || !mbar_wait(v_full, u & 1, wc)))
+          return false;
+        if (!mbar_wait(s_free, (it & 1) ^ 1, wc)) return false;
+        tc_fence_after();
+        // the query half: rows 64 hh.. of the Q / G tiles (8 KB on) and of
+        // the extension rows (8 groups of 256 bytes on)
+        const uint64_t dK = kdesc(sK + (u & 1) * C::kTB, 0);
+        const uint64_t dQh = kdesc(sQ + hh * 8192, 0), dGh = kdesc(sG + hh * 8192, 0);
+        const uint64_t dBS = smem_desc_noswizzle(smem_u32(sBExtS) + hh * 2048, 128, 256);
+        const uint64_t dBA = smem_desc_noswizzle(smem_u32(sBExtA) + hh * 2048, 128, 256);
+        mma_over_d<D>(tmem, dK, kH128, dQh, kH128, idesc_s);
+        mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
+        mma_over_d<D>(tmem + 64, dV, kH128, dGh, kH128, idesc_s);
+        mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
+        mma_commit(s_full);
+        if (hh == 1) mma_commit(v_empty);
+        return true;
+      };
+      auto issue_dq = [&](int it) -> bool {
+        const int u = it >> 1, hh = it & 1;
+        if (!mbar_wait(ds_full, it & 1, wc)) return false;
+        tc_fence_after();
+        const uint64_t dKmn = smem_desc(smem_u32(sK + (u & 1) * C::kTB), kH128, 1024);
+        MmaRun<0, kTile / 16, kStepMn, kStepMn, false>::go(tmem + C::kTmemDQ + hh * D, dDs, dKmn, idesc_q,
+                                                          u > 0 ? 1u : 0u);
+        mma_commit(ds_free);
+        if (hh == 1) mma_commit(&k_empty[u & 1]);
+        if (it == 2 * n - 1) mma_commit(fin);
+        return true;
+      };
       bool ok = mbar_wait(q_full, 0, wc);
       if (ok) tc_fence_after();
-      for (int u = 0; ok && u < n; ++u) {
-        if (!mbar_wait(k_full, u & 1, wc) || !mbar_wait(v_full, u & 1, wc)) break;
-        tc_fence_after();
-        for (int hh = 0; hh < 2; ++hh) {
-          const int it = 2 * u + hh;
-          if (!mbar_wait(s_free, (it & 1) ^ 1, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // the query half: rows 64 hh.. of the Q / G tiles (8 KB on) and of
-          // the extension rows (8 groups of 256 bytes on)
-          const uint64_t dQh = kdesc(sQ + hh * 8192, 0), dGh = kdesc(sG + hh * 8192, 0);
-          const uint64_t dBS = smem_desc_noswizzle(smem_u32(sBExtS) + hh * 2048, 128, 256);
-          const uint64_t dBA = smem_desc_noswizzle(smem_u32(sBExtA) + hh * 2048, 128, 256);
-          mma_over_d<D>(tmem, dK, kH128, dQh, kH128, idesc_s);
-          mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
-          mma_over_d<D>(tmem + 64, dV, kH128, dGh, kH128, idesc_s);
-          mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
-          mma_commit(s_full);
-        }
-        if (!ok) break;
-        mma_commit(v_empty);
-        if (!mbar_wait(ds_full, u & 1, wc)) break;
-        tc_fence_after();
-        MmaRun<0, kTile / 16, kStepMn, kStepMn, false>::go(tmem + 128, dDs, dKmn, idesc_q, u > 0 ? 1u : 0u);
-        mma_commit(ds_free);
-        mma_commit(k_empty);
-        if (u == n - 1) mma_commit(fin);
+      ok = ok && issue_s(0);
+      for (int it = 0; ok && it < 2 * n; ++it) {
+        if (it + 1 < 2 * n && !issue_s(it + 1)) break;
+        if (!issue_dq(it)) break;
       }
       mma_commit(drain);
       drain_wait_bt(drain, 0);
@@ -804,7 +825,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
             g_n[c] = __ldg(gchk + ck_of(it + 1, c));
           }
         }
-        if (!warp_wait(s_full, it & 1, wc) || (hh == 0 && !warp_wait(ds_free, (u & 1) ^ 1, wc))) {
+        if (!warp_wait(s_full, it & 1, wc)) {
           ok = false;
           break;
         }
@@ -831,38 +852,46 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
                                    fadd2(make_float2(A[2 * i], A[2 * i + 1]), make_float2(-r2.x, -r2.y)));
             ds[i] = pack_bf16x2(x.x, x.y);
           }
-          // 32 queries of chunk qc = 2 hh + c -> 64-query M-block qc / 2,
-          // 16-byte pieces (qc % 2) * 4 .. + 3 of this key's row, swizzled
-          const int qc = 2 * hh + c;
-          uint8_t *dst = ds_row + (qc >> 1) * 16384;
+          // the previous step's dQ product must be done reading the ds buffer
+          if (c == 0 && !warp_wait(ds_free, (it & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          // 32 queries of chunk c of this half -> 16-byte pieces c * 4 .. + 3
+          // of this key's 128-byte row of the half's ds block, swizzled
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4 *>(dst + ((((qc & 1) * 4 + j) ^ swz) * 16)) =
+            *reinterpret_cast<uint4 *>(ds_row + (((c * 4 + j) ^ swz) * 16)) =
                 make_uint4(ds[4 * j], ds[4 * j + 1], ds[4 * j + 2], ds[4 * j + 3]);
         }
+        if (!ok) break;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
       }
-      if (!ok) break;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
     }
     if (ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
       tc_fence_after();
-      // dQ rows: TMEM lane = query of this warp's quarter
-      const int qi = qt * kTile + warp * 32 + lane;
+      // dQ rows: an M = 64 accumulator keeps row m on TMEM lane
+      // (m / 16) * 32 + m % 16, so lane l < 16 of warp w holds row 16 w + l
+      // of each half's accumulator
       const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
       float x[32];
 #pragma unroll
-      for (int part = 0; part < D / 32; ++part) {
-        tmem_ld32(tmem + 128 + lanes + 32 * part, x);
-        tmem_wait_ld_r(x);
-        if (qi < T) {
-          __nv_bfloat16 *dst = dq + ((size_t)bh * T + qi) * D + 32 * part;
+      for (int hh = 0; hh < 2; ++hh) {
+        const int qi = qt * kTile + 64 * hh + 16 * warp + lane;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            reinterpret_cast<uint4 *>(dst)[j] =
-                make_uint4(pack_bf16x2(x[8 * j] * cs, x[8 * j + 1] * cs), pack_bf16x2(x[8 * j + 2] * cs, x[8 * j + 3] * cs),
-                           pack_bf16x2(x[8 * j + 4] * cs, x[8 * j + 5] * cs), pack_bf16x2(x[8 * j + 6] * cs, x[8 * j + 7] * cs));
+        for (int part = 0; part < D / 32; ++part) {
+          tmem_ld32(tmem + C::kTmemDQ + hh * D + lanes + 32 * part, x);
+          tmem_wait_ld_r(x);
+          if (lane < 16 && qi < T) {
+            __nv_bfloat16 *dst = dq + ((size_t)bh * T + qi) * D + 32 * part;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              reinterpret_cast<uint4 *>(dst)[j] =
+                  make_uint4(pack_bf16x2(x[8 * j] * cs, x[8 * j + 1] * cs), pack_bf16x2(x[8 * j + 2] * cs, x[8 * j + 3] * cs),
+                             pack_bf16x2(x[8 * j + 4] * cs, x[8 * j + 5] * cs), pack_bf16x2(x[8 * j + 6] * cs, x[8 * j + 7] * cs));
+          }
         }
       }
     }
@@ -873,7 +902,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
   if (warp == 5) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
