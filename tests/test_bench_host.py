@@ -1,0 +1,52 @@
+"""Host-side arithmetic of the benchmark, checked on the CPU.
+
+The reported numbers are algorithmic work divided by measured time, so the
+work formulas, the special-function-unit peak and the rule that a committed
+DRAM-traffic figure is used only while the kernel source is unchanged are
+pinned here against values worked out by hand.
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_forward_work_counts_three_contractions_over_causal_pairs():
+    # 4 x 12 heads of T = 16384, d = 64: causal pairs 16384 * 16385 / 2 per head,
+    # 2 d FLOP per pair per contraction, three contractions
+    pairs = 16384 * 16385 // 2 * 48
+    assert bench.fwd_flops(4, 12, 16384, 64) == 3 * 2 * 64 * pairs == 2474052157440
+    assert bench.sweep_flops(4, 12, 16384, 64) * 3 == bench.fwd_flops(4, 12, 16384, 64) * 2
+    assert bench.fwd_flops(1, 1, 1, 64) == 3 * 2 * 64   # one query, one pair
+
+
+def test_backward_work_is_five_contractions():
+    assert bench.bwd_flops(4, 12, 16384, 64) * 3 == bench.fwd_flops(4, 12, 16384, 64) * 5
+
+
+def test_sfu_peak_and_fractions():
+    # 32 results per SM per clock x 152 SMs x 2070 MHz = 10.06848 T/s
+    r = bench.sfu_report(1, 1, 3, {"rowstats": 1.0, "sweep": 2.0}, 152, 2070.0)
+    assert abs(r["peak"] - 10.06848) < 1e-9
+    pairs = 6   # T = 3: 3 * 4 / 2
+    assert abs(r["rowstats"]["achieved"] - 1.0 * pairs / 1e-3 / 1e12) < 1e-18
+    assert abs(r["sweep"]["achieved"] - 1.5 * pairs / 2e-3 / 1e12) < 1e-18
+    assert abs(r["achieved"] - 2.5 * pairs / 3e-3 / 1e12) < 1e-18
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-15
+
+
+def test_traffic_figure_only_for_the_profiled_source(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    rel = os.path.relpath(src, bench.ROOT)
+    prof = tmp_path / "p.md"
+    prof.write_text("kernel_source_hash: `%s`\n\ntraffic_bytes_per_launch_full_size: `12345`\n"
+                    % bench.sources_hash([rel]))
+    assert bench.profiled_traffic(str(prof), [rel]) == 12345.0
+    src.write_text("kernel v2\n")          # the kernel changed since the capture
+    assert bench.profiled_traffic(str(prof), [rel]) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md"), [rel]) is None
+
