@@ -214,3 +214,30 @@ def test_keep_for_backward_validation(lib):
                                     KEEP, 0, FAKE, 1 << 30, None) == b.DA_ERR_UNSUPPORTED
     assert lib.dilution_attn_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 16, FAKE, 1, 2, 64, 1.0, None,
                                             1e-6, KEEP, 1, FAKE, 1 << 30, None) == b.DA_ERR_INVALID
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """The public header is a C ABI: it compiles as C99 (and C++) on its own,
+    with no CUDA or PyTorch types, and a C program links against the library's
+    exported version symbol."""
+    import os
+    import shutil
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("gcc not available")
+    hdr = os.path.join(root, "include", "dilution_attn.h")
+    src = tmp_path / "use.c"
+    src.write_text('#include "%s"\nint main(void) { return dilution_attn_version() > 0 ? 0 : 1; }\n' % hdr)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-c", str(src), "-o", str(tmp_path / "use.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    lib = b.lib_path()
+    r = subprocess.run([cc, str(tmp_path / "use.o"), lib, "-o", str(tmp_path / "use"),
+                        "-Wl,-rpath," + os.path.dirname(lib)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    if shutil.which("g++"):
+        r = subprocess.run(["g++", "-std=c++17", "-Wall", "-Werror", "-x", "c++", "-c", str(src), "-o",
+                            str(tmp_path / "use_cpp.o")], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
