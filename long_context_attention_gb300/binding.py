@@ -132,6 +132,11 @@ def _need(t, name, shape=None, dtype=None):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device and takes its per-device
+        # set-up (and the no-alloc scratch address) from it
+        raise ValueError(f"{name} is on {t.device} but the current device is cuda:{torch.cuda.current_device()}; "
+                         f"call inside torch.cuda.device({t.device})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):

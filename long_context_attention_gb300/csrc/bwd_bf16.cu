@@ -918,19 +918,19 @@ static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, fl
                          int *status, cudaStream_t stream) {
   using KB1 = KeyCfg<kModeB1, D>;
   using KKV = KeyCfg<kModeKV, D>;
-  static bool attr_done[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
-  if (dev >= 64 || !attr_done[dev]) {
-    if (cudaFuncSetAttribute(bwdtc_key_kernel<kModeB1, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KB1::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(bwdtc_key_kernel<kModeKV, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KKV::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(bwdtc_q_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             QCfg<D>::kSmemBytes) != cudaSuccess)
-      return DA_ERR_CUDA;
-    if (dev < 64) attr_done[dev] = true;
-  }
+  // The shared-memory opt-in is a per-device function attribute.
+  static PerDeviceOnce once;
+  const int prep = once.run([] {
+    return (cudaFuncSetAttribute(bwdtc_key_kernel<kModeB1, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 KB1::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(bwdtc_key_kernel<kModeKV, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 KKV::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(bwdtc_q_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 QCfg<D>::kSmemBytes) != cudaSuccess)
+               ? DA_ERR_CUDA
+               : DA_OK;
+  });
+  if (prep != DA_OK) return prep;
   const int NT = Tp / kTile;
   const unsigned grid = (unsigned)(NT * BH);
   // maps: 0 Q (64-row boxes), 1 dout (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout (128)

@@ -212,20 +212,39 @@ int dilution_attn_decode_step(const void *q_new, const void *k_new, const void *
                                       nullptr, eps, 0, dtype, workspace, workspace_bytes, stream_);
 }
 
-int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
-                                 void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
-                                 float tau, const float *tau_bh, float eps, int flags, int dtype, void *workspace,
-                                 size_t workspace_bytes, void *stream_) {
+}  // extern "C"
+
+namespace da {
+// Argument checks of a decode step that need no workspace: sizes, tau, eps,
+// dtype, options, n_ctx and the tensor pointers.  Returns DA_OK, or the status
+// the step returns for them (B * H == 0 passes: the step then does nothing).
+int check_decode_step_args(const void *q_new, const void *k_new, const void *v_new, const void *k_cache,
+                           const void *v_cache, const float *demand, int n_ctx, int T_cap, const void *out, int B,
+                           int H, int d, float tau, const float *tau_bh, float eps, int flags, int dtype) {
   int st = check_common(B, H, T_cap, d, tau, eps, dtype);
   if (st == DA_OK) st = check_options(tau_bh, flags);
   if (st != DA_OK) return st;
   if ((flags & DA_FLAG_KEEP_FOR_BACKWARD) != 0) return DA_ERR_INVALID;   // no backward of a decode step
   if (n_ctx < 0 || n_ctx >= T_cap) return DA_ERR_INVALID;
-  const int64_t BH = (int64_t)B * H;
-  if (BH == 0) return DA_OK;
+  if ((int64_t)B * H == 0) return DA_OK;
   const void *ptrs[] = {q_new, k_new, v_new, k_cache, v_cache, demand, out};
   for (const void *p : ptrs)
     if (p == nullptr || !aligned16(p)) return DA_ERR_INVALID;
+  return DA_OK;
+}
+}  // namespace da
+
+extern "C" {
+
+int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
+                                 void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
+                                 float tau, const float *tau_bh, float eps, int flags, int dtype, void *workspace,
+                                 size_t workspace_bytes, void *stream_) {
+  const int st = check_decode_step_args(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d,
+                                        tau, tau_bh, eps, flags, dtype);
+  if (st != DA_OK) return st;
+  const int64_t BH = (int64_t)B * H;
+  if (BH == 0) return DA_OK;
   const DecWorkspace L = dec_workspace_layout(BH, T_cap, d);
   if (workspace == nullptr || workspace_bytes < L.total) return DA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DA_ERR_INVALID;

@@ -3,8 +3,10 @@
 // schedule functions, so the debug export reproduces the kernels' order.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -144,7 +146,11 @@ DA_HD TileWork rowstats_work(int cta, int BH, int64_t T) {
 // the end.  Heads are taken in groups whose fp32 accumulators (Tp x (d + 4) x
 // 4 B per head) together stay near 64 MB, so the reductions of the CTAs in
 // flight hit L2; inside a group the spans with the most query tiles launch
-// first.
+// first.  When BH is not a multiple of the group size, the smaller remainder
+// group goes FIRST: launched last, its long first spans would start after
+// every other group and run alone at the end (4 x 12 x 16384: groups 15, 15,
+// 15, 3 leave ~7 % of the SM time idle in a greedy list-scheduling model; 3,
+// 15, 15, 15 leave ~0.5 %).
 constexpr int kSweepQTile = 128;
 constexpr int64_t kAccGroupBytes = 64ll << 20;
 DA_HD int sweep_span_keys(int d) { return d == 64 ? 384 : 256; }
@@ -163,9 +169,16 @@ DA_HD TileWork sweep_work(int cta, int BH, int64_t T, int d) {
   const int nqt = (int)(t_pad(T) / kSweepQTile);
   const int nspan = sweep_num_spans(T, d);
   const int hg = sweep_head_group(BH, T, d);
-  const int group = cta / (hg * nspan);
-  const int h0 = group * hg;
-  const int ng = (BH - h0 < hg) ? BH - h0 : hg;    // heads in this (possibly last, smaller) group
+  const int ngroups = (BH + hg - 1) / hg;
+  const int first = BH - (ngroups - 1) * hg;       // heads in group 0 (1 .. hg)
+  int h0, ng;
+  if (cta < first * nspan) {
+    h0 = 0;
+    ng = first;
+  } else {
+    h0 = first + (cta - first * nspan) / (hg * nspan) * hg;
+    ng = hg;
+  }
   const int r = cta - h0 * nspan;
   TileWork w;
   w.bh = h0 + r % ng;
@@ -201,6 +214,30 @@ __device__ __forceinline__ float head_c2(const HeadScale &hs, int bh, int *statu
   return (float)((double)t * hs.per_tau);   // rounded once, as the scalar's c2
 }
 #endif
+
+// One-time set-up per device (function attributes such as the shared-memory
+// opt-in are per device).  Several host threads may make their first call on
+// a device at the same time: the set-up runs under a lock, once, and later
+// calls see the flag without locking.  `setup` returns a da status; a failed
+// set-up is retried by the next call.  Devices past the table's 64 entries
+// run the set-up on every call.
+struct PerDeviceOnce {
+  std::mutex mu;
+  std::atomic<bool> done[64] = {};
+
+  template <typename F>
+  int run(F &&setup) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return setup();
+    if (done[dev].load(std::memory_order_acquire)) return DA_OK;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev].load(std::memory_order_relaxed)) return DA_OK;
+    const int st = setup();
+    if (st == DA_OK) done[dev].store(true, std::memory_order_release);
+    return st;
+  }
+};
 
 // Causal mask predicate used by every kernel: query i sees key k iff k <= i
 // and i < T ("DilutionAttention v0.1.0 · results", section "The operator":

@@ -397,17 +397,16 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
                                    float *part_acc, int nchunk, int *status, cudaStream_t stream) {
   using R = DecRing<E, D>;
   // The ring's shared-memory opt-in is a per-device function attribute.
-  static bool attr_done[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(dec_logits<E, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         R::kDynSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(dec_update<E, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, R::kDynSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done[dev] = true;
-  }
+  static PerDeviceOnce once;
+  const int prep = once.run([] {
+    return (cudaFuncSetAttribute(dec_logits<E, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, R::kDynSmemBytes) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(dec_update<E, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, R::kDynSmemBytes) !=
+                cudaSuccess)
+               ? DA_ERR_CUDA
+               : DA_OK;
+  });
+  if (prep != DA_OK) return cudaErrorInvalidDeviceFunction;
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
   dec_logits<E, D><<<dim3(used, BH), R::kThreads, R::kDynSmemBytes, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
@@ -417,6 +416,10 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
   dec_combine<E, D><<<BH, D, 0, stream>>>(part_acc, (E *)out, nchunk, used);
   return cudaGetLastError();
 }
+
+int check_decode_step_args(const void *q_new, const void *k_new, const void *v_new, const void *k_cache,
+                           const void *v_cache, const float *demand, int n_ctx, int T_cap, const void *out, int B,
+                           int H, int d, float tau, const float *tau_bh, float eps, int flags, int dtype);
 
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
@@ -469,8 +472,11 @@ extern "C" int dilution_attn_decode_step_noalloc(const void *q_new, const void *
                                                  void *out, int B, int H, int d, float tau, float eps, int dtype,
                                                  void *stream) {
   using namespace da;
-  if (B < 0 || H < 0 || T_cap < 0) return DA_ERR_INVALID;
-  if (!head_dim_supported(d)) return DA_ERR_UNSUPPORTED;
+  // The ordinary step's argument checks come first, so a bad argument is
+  // reported as such whatever the size; then the size against the array.
+  const int chk = check_decode_step_args(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d,
+                                         tau, nullptr, eps, 0, dtype);
+  if (chk != DA_OK) return chk;
   const DecWorkspace L = dec_workspace_layout((int64_t)B * H, T_cap, d);
   if (L.total > kNoAllocScratchBytes) return DA_ERR_WORKSPACE;   // beyond the fixed scratch
   void *scratch = nullptr;

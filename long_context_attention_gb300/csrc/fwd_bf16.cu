@@ -1077,6 +1077,14 @@ static int prepare_fwd_bf16() {
   return st;
 }
 
+// The per-device set-up of the forward kernels of head dimension D, shared
+// by the forward and the backward's forward-again sweep.
+template <int D>
+static PerDeviceOnce &fwd_bf16_once() {
+  static PerDeviceOnce once;
+  return once;
+}
+
 // Blocks of the fix-up pass (two per SM of a GB300; grid-stride over rows).
 constexpr int kFixupBlocks = 304;
 template <int D>
@@ -1086,14 +1094,8 @@ static int launch_fwd_bf16_t(const CUtensorMap &tq, const CUtensorMap &tk, const
                              float eps, bool earlier, float *lse2_ws, float *acc, float *cchk, int *status,
                              cudaStream_t stream, cudaEvent_t const *ev) {
   // The shared-memory opt-in is a per-device function attribute.
-  static bool attr_done[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
-  if (dev >= 64 || !attr_done[dev]) {
-    const int st = prepare_fwd_bf16<D>();
-    if (st != DA_OK) return st;
-    if (dev < 64) attr_done[dev] = true;
-  }
+  const int prep = fwd_bf16_once<D>().run(prepare_fwd_bf16<D>);
+  if (prep != DA_OK) return prep;
   using C = SwCfg<D>;
   const int Tp = (int)t_pad(T);
   if (ev[0]) cudaEventRecord(ev[0], stream);
@@ -1131,14 +1133,8 @@ static int launch_sweep_chk_t(const void *q, const void *k, const void *v, const
   if (!make_tile_map(&tq, q, BH, T, D) || !make_tile_map(&tk, k, BH, T, D) || !make_tile_map(&tv, v, BH, T, D) ||
       !make_acc_map(&ta, acc, acc_rows, D))
     return DA_ERR_CUDA;
-  static bool attr_done[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
-  if (dev >= 64 || !attr_done[dev]) {
-    const int st = prepare_fwd_bf16<D>();
-    if (st != DA_OK) return st;
-    if (dev < 64) attr_done[dev] = true;
-  }
+  const int prep = fwd_bf16_once<D>().run(prepare_fwd_bf16<D>);
+  if (prep != DA_OK) return prep;
   using C = SwCfg<D>;
   const int Tp = (int)t_pad(T);
   const int nsw = sweep_num_ctas(BH, T, D);

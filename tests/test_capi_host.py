@@ -47,9 +47,12 @@ def _sched_sweep(BH, T, d=64):
     Tp = -(-T // 256) * 256
     nqt, nspan = Tp // 128, -(-Tp // span_keys)
     hg = min(BH, max(1, (64 << 20) // (Tp * (d + 4) * 4)))
+    # group sizes: the remainder (BH mod hg, if any) first, then full groups
+    sizes = ([BH % hg] if BH % hg else []) + [hg] * (BH // hg)
+    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(int)
     rows = []
-    for h0 in range(0, BH, hg):
-        heads = list(range(h0, min(BH, h0 + hg)))
+    for h0, n in zip(starts, sizes):
+        heads = list(range(h0, h0 + n))
         for span in range(nspan):
             for bh in heads:
                 q0 = span_keys * span // 128
@@ -150,6 +153,25 @@ def test_decode_argument_validation(lib):
     assert _dec(lib, k_cache=None) == b.DA_ERR_INVALID
     assert _dec(lib, k_cache=MIS) == b.DA_ERR_INVALID
     assert _dec(lib, wsb=16) == b.DA_ERR_WORKSPACE
+
+
+def test_noalloc_decode_checks_arguments_before_its_scratch_size(lib):
+    # a call that is both malformed and too large for the fixed scratch array
+    # reports the malformed argument; a well-formed oversize call reports the
+    # size (both before any CUDA call)
+    big = 1 << 17   # 8 x 12 heads of 131072 keys need ~50 MB of scratch
+
+    def call(n_ctx=4, T_cap=big, dtype=1, q=FAKE, d=64, eps=1e-6):
+        return lib.dilution_attn_decode_step_noalloc(q, FAKE, FAKE, FAKE, FAKE, FAKE, n_ctx, T_cap, FAKE, 8, 12, d,
+                                                     1.0, eps, dtype, None)
+
+    assert call(dtype=7) == b.DA_ERR_INVALID
+    assert call(n_ctx=big) == b.DA_ERR_INVALID
+    assert call(q=None) == b.DA_ERR_INVALID
+    assert call(q=MIS) == b.DA_ERR_INVALID
+    assert call(eps=0.0) == b.DA_ERR_INVALID
+    assert call(d=96) == b.DA_ERR_UNSUPPORTED
+    assert call() == b.DA_ERR_WORKSPACE
 
 
 def test_get_error_rejects_null(lib):
