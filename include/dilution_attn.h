@@ -268,6 +268,32 @@ int dilution_attn_get_error(void *workspace, void *stream);
 int dilution_attn_debug_last_timeout(void *workspace, int32_t *out);
 
 /* ------------------------------------------------------------------------
+ * Test hook of the bounded waits (diagnostic only; no counterpart on the
+ * pages).  Runs one decode step like dilution_attn_decode_step (same
+ * arguments, tau_bh = NULL, flags = 0), except that
+ *   - in the first kernel's block for key chunk `stall_chunk` (2048 keys per
+ *     chunk) of head stall_bh (= b*H + h), one consumer warp keeps the first
+ *     ring stage it read instead of handing it back, so the block's copy
+ *     producer waits for a shared-memory slot that is never freed (the chunk
+ *     needs at least three 256-key stages of cached keys before n_ctx);
+ *   - every wait of that kernel gives up after wait_limit_ns (1e3 .. 1e9 ns).
+ * The waits that run out record DA_ERR_TIMEOUT and their place
+ * (dilution_attn_debug_last_timeout: status, barrier offset, block index =
+ * stall_chunk, thread index) in the workspace status word; the blocks that
+ * gave up finish without waiting further, so the call completes and the
+ * device stays usable.  The step's outputs, the appended cache row and the
+ * demand are then unspecified.  Errors: those of dilution_attn_decode_step,
+ * and DA_ERR_INVALID for a wait_limit_ns outside the range, a negative
+ * stall_chunk or a stall_bh outside [0, B*H).
+ * ---------------------------------------------------------------------- */
+int dilution_attn_debug_decode_stall(const void *q_new, const void *k_new, const void *v_new,
+                                     void *k_cache, void *v_cache, float *demand,
+                                     int n_ctx, int T_cap, void *out,
+                                     int B, int H, int d, float tau, float eps, int dtype,
+                                     void *workspace, size_t workspace_bytes, void *stream,
+                                     int stall_chunk, int stall_bh, long long wait_limit_ns);
+
+/* ------------------------------------------------------------------------
  * Host-only introspection of integer artefacts (no GPU needed).
  *
  * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's

@@ -56,6 +56,9 @@ _SIGNATURES = {
     "dilution_attn_decode_step_noalloc": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                           [_c_float, _c_float, _c_int, _c_void_p]),
     "dilution_attn_decode_noalloc_scratch_bytes": (_c_size_t, []),
+    "dilution_attn_debug_decode_stall": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
+                                         [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p, _c_int, _c_int,
+                                          ctypes.c_longlong]),
     "dilution_attn_get_error": (_c_int, [_c_void_p, _c_void_p]),
     "dilution_attn_debug_last_timeout": (_c_int, [_c_void_p, _c_void_p]),
     "dilution_attn_debug_tile_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_void_p, _c_size_t]),
@@ -373,6 +376,27 @@ def dilution_attn_decode_step_noalloc(q_new, k_new, v_new, k_cache, v_cache, dem
 
 def dilution_attn_decode_noalloc_scratch_bytes() -> int:
     return int(load().dilution_attn_decode_noalloc_scratch_bytes())
+
+
+def dilution_attn_debug_decode_stall(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,
+                                     tau: float = 1.0, eps: float = 1e-6, workspace=None, stream=None,
+                                     stall_chunk: int = 0, stall_bh: int = 0, wait_limit_ns: int = 2_000_000):
+    """Test hook of the bounded waits: a decode step in which one block's ring
+    slot is never handed back (see the header).  Returns (status, out); the
+    kernel-side outcome is read with dilution_attn_debug_last_timeout /
+    dilution_attn_get_error on ``workspace``."""
+    lib = load()
+    out, T_cap = _decode_prepare(q_new, k_new, v_new, k_cache, v_cache, demand, out)
+    B, H, d = q_new.shape
+    if workspace is None:
+        workspace = torch.empty(max(dilution_attn_decode_workspace_size(B, H, T_cap, d), 256), dtype=torch.uint8,
+                                device=q_new.device)
+    st = lib.dilution_attn_debug_decode_stall(_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                              _ptr(demand), int(n_ctx), T_cap, _ptr(out), B, H, d, float(tau),
+                                              float(eps), _dtype_code(q_new), _ptr(workspace), workspace.numel(),
+                                              _stream_handle(stream), int(stall_chunk), int(stall_bh),
+                                              int(wait_limit_ns))
+    return int(st), out
 
 
 # ----------------------------------------------------------------------------- misc

@@ -25,7 +25,7 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
                           bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
-                          int *status, cudaStream_t stream);
+                          int *status, DecDebug dbg, cudaStream_t stream);
 }  // namespace da
 
 using namespace da;
@@ -33,6 +33,8 @@ using namespace da;
 namespace {
 
 constexpr double kLog2e = 1.4426950408889634;
+// The kernels' bounded-wait limit (1 s), as the host sees it.
+constexpr unsigned long long kWaitLimitNsHost = 1000ull * 1000ull * 1000ull;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned16_or_null(const void *p) { return p == nullptr || aligned16(p); }
@@ -234,12 +236,12 @@ int check_decode_step_args(const void *q_new, const void *k_new, const void *v_n
 }
 }  // namespace da
 
-extern "C" {
-
-int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
-                                 void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
-                                 float tau, const float *tau_bh, float eps, int flags, int dtype, void *workspace,
-                                 size_t workspace_bytes, void *stream_) {
+namespace {
+// The decode step behind dilution_attn_decode_step_ex and its test hook.
+int decode_step_impl(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                     float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d, float tau,
+                     const float *tau_bh, float eps, int flags, int dtype, void *workspace, size_t workspace_bytes,
+                     void *stream_, DecDebug dbg) {
   const int st = check_decode_step_args(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d,
                                         tau, tau_bh, eps, flags, dtype);
   if (st != DA_OK) return st;
@@ -254,10 +256,32 @@ int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const voi
   if (launch_decode(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, (int)BH, d,
                     head_scale(tau, tau_bh, d), eps, (flags & DA_FLAG_EARLIER_DEMAND_ONLY) != 0, dtype,
                     reinterpret_cast<float *>(ws + L.logit_off), reinterpret_cast<float2 *>(ws + L.ml_off),
-                    reinterpret_cast<float *>(ws + L.acc_off), L.nchunk, reinterpret_cast<int *>(ws),
+                    reinterpret_cast<float *>(ws + L.acc_off), L.nchunk, reinterpret_cast<int *>(ws), dbg,
                     stream) != cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
+                                 void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H, int d,
+                                 float tau, const float *tau_bh, float eps, int flags, int dtype, void *workspace,
+                                 size_t workspace_bytes, void *stream_) {
+  return decode_step_impl(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d, tau, tau_bh, eps,
+                          flags, dtype, workspace, workspace_bytes, stream_, DecDebug{kWaitLimitNsHost, -1, -1});
+}
+
+int dilution_attn_debug_decode_stall(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
+                                     void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int B, int H,
+                                     int d, float tau, float eps, int dtype, void *workspace, size_t workspace_bytes,
+                                     void *stream_, int stall_chunk, int stall_bh, long long wait_limit_ns) {
+  if (wait_limit_ns < 1000 || wait_limit_ns > (long long)kWaitLimitNsHost) return DA_ERR_INVALID;
+  if (stall_chunk < 0 || stall_bh < 0 || (int64_t)stall_bh >= (int64_t)B * H) return DA_ERR_INVALID;
+  return decode_step_impl(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, B, H, d, tau, nullptr,
+                          eps, 0, dtype, workspace, workspace_bytes, stream_,
+                          DecDebug{(unsigned long long)wait_limit_ns, stall_chunk, stall_bh});
 }
 
 int dilution_attn_get_error(void *workspace, void *stream_) {

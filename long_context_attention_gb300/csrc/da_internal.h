@@ -104,6 +104,16 @@ DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T, int d) {
 // ---------------------------------------------------------------------------
 constexpr int kDecChunk = 2048;    // keys per decode CTA (measured: 2048 beats 1024 and 4096)
 
+// Test hook of the decode step's bounded waits: in the first kernel's block
+// (chunk stall_chunk, head stall_bh), consumer warp 0 keeps its hand-off of
+// ring stage 0, so the block's copy producer waits for a slot that is never
+// freed; every wait of that kernel gives up after wait_limit_ns.  The
+// ordinary step passes stall_chunk = -1 and the 1 s limit.
+struct DecDebug {
+  unsigned long long wait_limit_ns;
+  int stall_chunk, stall_bh;
+};
+
 struct DecWorkspace {
   size_t logit_off, ml_off, acc_off, total;
   int nchunk;

@@ -70,6 +70,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 struct WaitCtx {
   volatile int *abort_flag;  // shared memory
   int *status;               // global status word (workspace)
+  unsigned long long limit_ns = kWaitLimitNs;   // shortened only by the decode test hook
 };
 
 // The first wait that gives up also records where: status[1] = shared-memory
@@ -103,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*w.abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > w.limit_ns) {
       raise_timeout(w, bar);
       return false;
     }

@@ -119,8 +119,8 @@ struct DecRing {
     abort_word = 0;
     fence_mbar_init();
   }
-  __device__ __forceinline__ WaitCtx wait_ctx(int *status) {
-    return WaitCtx{reinterpret_cast<volatile int *>(&abort_word), status};
+  __device__ __forceinline__ WaitCtx wait_ctx(int *status, unsigned long long limit_ns = kWaitLimitNs) {
+    return WaitCtx{reinterpret_cast<volatile int *>(&abort_word), status, limit_ns};
   }
   // Producer lane: stages 0 .. n_stage - 1 of the rows starting at `rows`.
   __device__ __forceinline__ void produce(const E *rows, int n_stage, const WaitCtx &wc) {
@@ -146,9 +146,10 @@ struct DecRing {
     return warp_wait(&full[st % kStages], (st / kStages) & 1, wc);
   }
   __device__ __forceinline__ const uint8_t *slot(int st) const { return dec_ring_smem + (st % kStages) * kStageBytes; }
-  __device__ __forceinline__ void release(int st, int lane) {
+  // keep = true (the test hook only): the warp does not hand the slot back.
+  __device__ __forceinline__ void release(int st, int lane, bool keep = false) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st % kStages]);
+    if (lane == 0 && !keep) mbar_arrive(&empty[st % kStages]);
   }
 };
 
@@ -156,7 +157,8 @@ template <typename E, int D>
 __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
     dec_logits(const E *__restrict__ q_new, const E *__restrict__ k_new, const E *__restrict__ v_new,
                E *__restrict__ k_cache, E *__restrict__ v_cache, float *__restrict__ logits,
-               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, HeadScale hs, int *status) {
+               float2 *__restrict__ part_ml, int n_ctx, int T_cap, int nchunk, HeadScale hs, int *status,
+               DecDebug dbg) {
   using R = DecRing<E, D>;
   constexpr int LPR = lanes_per_row<E, D>();       // lanes cooperating on one key
   constexpr int NV = Vec16<E>::N;
@@ -178,7 +180,8 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
   const E *kb = k_cache + (size_t)bh * T_cap * D;
   if (tid == 0) ring.init();
   __syncthreads();
-  const WaitCtx wc = ring.wait_ctx(status);
+  const WaitCtx wc = ring.wait_ctx(status, dbg.wait_limit_ns);
+  const bool stall = warp == 0 && chunk == dbg.stall_chunk && bh == dbg.stall_bh;   // test hook
   float m = -INFINITY, l = 0.f;
   if (producer) {
     if (lane == 0) ring.produce(kb + (size_t)k_begin * D, n_stage, wc);
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(DecRing<E, D>::kThreads)
         const int kl = r * KPR + grp;
         consume(k_begin + st * SK + kl, *reinterpret_cast<const uint4 *>(stg + kl * R::kRowBytes + sub * 16), true);
       }
-      ring.release(st, lane);
+      ring.release(st, lane, stall && st == 0);
     }
     // the tail, with a warp-uniform trip count
     for (int r0 = k_begin + n_stage * SK; r0 < k_end; r0 += KPR) {
@@ -394,7 +397,7 @@ template <typename E, int D>
 static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const void *v_new, void *k_cache,
                                    void *v_cache, float *demand, int n_ctx, int T_cap, void *out, int BH,
                                    HeadScale hs, float eps, bool earlier, float *logits, float2 *part_ml,
-                                   float *part_acc, int nchunk, int *status, cudaStream_t stream) {
+                                   float *part_acc, int nchunk, int *status, DecDebug dbg, cudaStream_t stream) {
   using R = DecRing<E, D>;
   // The ring's shared-memory opt-in is a per-device function attribute.
   static PerDeviceOnce once;
@@ -410,7 +413,7 @@ static cudaError_t launch_decode_t(const void *q_new, const void *k_new, const v
   const int used = (n_ctx + 1 + kDecChunk - 1) / kDecChunk;
   dec_logits<E, D><<<dim3(used, BH), R::kThreads, R::kDynSmemBytes, stream>>>(
       (const E *)q_new, (const E *)k_new, (const E *)v_new, (E *)k_cache, (E *)v_cache, logits, part_ml, n_ctx,
-      T_cap, nchunk, hs, status);
+      T_cap, nchunk, hs, status, dbg);
   dec_update<E, D><<<dim3(used, BH), R::kThreads, R::kDynSmemBytes, stream>>>(
       (const E *)v_cache, logits, part_ml, demand, part_acc, n_ctx, T_cap, nchunk, used, eps, earlier, status);
   dec_combine<E, D><<<BH, D, 0, stream>>>(part_acc, (E *)out, nchunk, used);
@@ -424,10 +427,10 @@ int check_decode_step_args(const void *q_new, const void *k_new, const void *v_n
 cudaError_t launch_decode(const void *q_new, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                           float *demand, int n_ctx, int T_cap, void *out, int BH, int d, HeadScale hs, float eps,
                           bool earlier, int dtype, float *logits, float2 *part_ml, float *part_acc, int nchunk,
-                          int *status, cudaStream_t stream) {
+                          int *status, DecDebug dbg, cudaStream_t stream) {
 #define DA_DECODE_ARGS                                                                                          \
   q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx, T_cap, out, BH, hs, eps, earlier, logits, part_ml, part_acc, \
-      nchunk, status, stream
+      nchunk, status, dbg, stream
   if (dtype == DA_BF16)
     return d == 128 ? launch_decode_t<__nv_bfloat16, 128>(DA_DECODE_ARGS)
                     : launch_decode_t<__nv_bfloat16, 64>(DA_DECODE_ARGS);
