@@ -62,8 +62,15 @@ def test_prefill_config_t131072():
     T = w.T
     out, lse2, rs, dem = _fwd_all(q, k, v, tau, w.eps)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse2).all()
+    # Unit demand per query: each head's demand totals T.  The totals are fp32
+    # running sums over up to T bids, and a bid below half an ulp of its key's
+    # running total is absorbed, so the sum falls short by a margin that grows
+    # with T: a CPU replay of exact bids added in fp32 in query order loses
+    # 1.3e-5 T on this workload (at most 3e-4 of any key's total, inside the
+    # per-key demand tolerance of 1e-3).  The bound is ten times below that
+    # per-key tolerance.
     err = (dem.double().sum(-1) - T).abs().max().item()
-    assert err <= 1e-5 * T, err
+    assert err <= 1e-4 * T, err
     heads = [(0, 0), (0, 11)]
     n = 4096
     ref = oracle_forward(q, k, v, tau, w.eps, rows=n, heads=heads)
