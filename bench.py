@@ -268,29 +268,51 @@ def cpu_baseline(heads, seed=2):
 
 
 # ---------------------------------------------------------------------- reference arm
+def workload_config(args, w, B, world, ws_bytes):
+    """The ``config`` object of both arms: the workload and how the timed steps
+    treat the L2 (no flush; the per-step inputs and workspace exceed it)."""
+    in_bytes = 3 * B * w.H * w.T * w.d * (2 if w.dtype == "bf16" else 4)
+    l2 = (f"no flush; inputs {in_bytes / 1e6:.0f} MB + workspace {ws_bytes / 1e6:.0f} MB per step"
+          + (", larger than the 129 MB L2" if in_bytes + ws_bytes > 129e6 else " (fits in L2: small case)"))
+    return {"workload": args.workload, "B": B, "H": w.H, "T": w.T, "d": w.d, "tau": 1.0, "eps": w.eps,
+            "planted_pairs_per_head": w.pairs, "parallelism": f"replicas{world}", "l2": l2}
+
+
 def run_reference(args):
+    """The oracle as it stands, on the host cores, on this arm's workload.  Each
+    timed step is one whole (batch, head) slice of the workload (all T query
+    rows of one of its B x H independent heads, taken in turn); its TFLOP/s is
+    that head's algorithmic FLOP over the step's time, the same unit as the GPU
+    arm's whole-batch figure.  Warm-up steps run the first 1024 rows of a head."""
     rank, world, _ = dist_info()
     if rank != 0:
         return 0
+    from long_context_attention_gb300 import binding as b
     from long_context_attention_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
-    rows = 2048
-    q, k, v = inputs.make_qkv(1, 1, rows, w.d, q_std=w.q_std, pairs=max(1, w.pairs * rows // w.T), seed=w.seed,
-                              dtype=w.dtype)
-    qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
-    for _ in range(args.warmup):
-        oracle_sample(qh, kh, vh, rows)
+    B = args.batch or w.B
+    q, k, v = inputs.make_qkv(B, w.H, w.T, w.d, q_std=w.q_std, pairs=w.pairs, seed=w.seed, dtype=w.dtype)
+    heads = [(bb, hh) for bb in range(B) for hh in range(w.H)]
+
+    def head(j):
+        bb, hh = heads[j % len(heads)]
+        return (x[bb, hh].double().numpy() for x in (q, k, v))
+
+    for j in range(args.warmup):
+        oracle_sample(*head(j), rows=min(1024, w.T))
     tot_f, tot_t = 0, 0.0
-    for _ in range(args.steps):
-        f, t = oracle_sample(qh, kh, vh, rows)
+    for j in range(args.steps):
+        f, t = oracle_sample(*head(j), rows=w.T)
         tot_f += f
         tot_t += t
     val = tot_f / tot_t / 1e12
-    sample = f"float64 NumPy oracle, 1 head x first {rows} query rows per step ({args.workload} shape)"
+    sample = (f"float64 NumPy oracle (row-blocked), one whole head of the {args.workload} workload per step "
+              f"({args.steps} heads, all {w.T} query rows each, {tot_t:.1f} s)")
+    ws_bytes = b.dilution_attn_fwd_workspace_size(B, w.H, w.T, w.d, b.DA_BF16 if w.dtype == "bf16" else b.DA_F32)
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "tau": 1.0, "eps": w.eps},
+            "config": workload_config(args, w, B, world, ws_bytes),
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -533,12 +555,7 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.workload, "B": B, "H": H, "T": T, "d": d, "tau": 1.0, "eps": w.eps,
-                       "planted_pairs_per_head": w.pairs, "parallelism": f"replicas{world}",
-                       "l2": (f"no flush; inputs {3 * q.numel() * q.element_size() / 1e6:.0f} MB + workspace "
-                              f"{ws.numel() / 1e6:.0f} MB per step"
-                              + (", larger than the 129 MB L2" if 3 * q.numel() * q.element_size() + ws.numel() > 129e6
-                                 else " (fits in L2: small case)"))},
+            "config": workload_config(args, w, B, world, ws.numel()),
             "tokens_per_s": world * B * T * K / (ms * 1e-3),
             "pct_of_bf16_peak": 100.0 * value / world / peak_t,
             "kernels_ms": kern_ms,

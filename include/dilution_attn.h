@@ -80,7 +80,9 @@ int dilution_attn_version(void);
  *   lse2_out   [B,H,T] fp32, nullable: log2 of the softmax normaliser of the
  *              scaled logits, log2(sum_{k<=i} 2^(s_ik * log2 e)); the bid is
  *              p_ik = 2^(s_ik*log2 e - lse2_i).
- *   rowsum_out [B,H,T] fp32, nullable: sum_k share_ik (before renormalising).
+ *   rowsum_out [B,H,T] fp32, nullable: R_i = sum_k share_ik, the normaliser
+ *              of row i of A = share / R (whose rows therefore sum to 1 by
+ *              construction); out_i = sum_k share_ik v_k / R_i.
  *   demand_out [B,H,T] fp32, nullable: column totals sum_i p_ik over all T
  *              queries -- the decode demand cache after prefill
  *              ("DilutionAttention v0.1.0 · results", section "The operator",
@@ -160,10 +162,12 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
  * the chain rule through the causal softmax, the exclusive column cumsum, the
  * share and the renormalisation).
  *   lse2 [B,H,T] fp32: the forward's lse2_out for the same q, k, tau.
- *   dtype applies to q, k, v, dout, dq, dk, dv; arithmetic is fp32 (column
- *   sums of the demand in fp64).
+ *   dtype applies to q, k, v, dout, dq, dk, dv.  DA_BF16 runs on tcgen05
+ *   tensor cores (bf16 products, fp32 accumulation and fp32 demand
+ *   arithmetic, the demand recomputed from checkpoints every 32 queries);
+ *   DA_F32 runs on CUDA cores in fp32 (column sums of the demand in fp64).
  * workspace: at least dilution_attn_bwd_workspace_size(); errors as for
- * dilution_attn_fwd.  This version runs on CUDA cores (no tensor cores).
+ * dilution_attn_fwd.
  * ---------------------------------------------------------------------- */
 size_t dilution_attn_bwd_workspace_size(int B, int H, int T, int d, int dtype);
 

@@ -286,10 +286,16 @@ def pin_earlier_only_uniform_harmonic(T=23, d=8, eps=1e-6, seed=16):
 def pin_earlier_only_identity(T=40, d=16, seed=17):
     """The pages' observation: dividing by earlier demand alone lets each key
     win its own first query outright, so as eps -> 0 the layer becomes the
-    identity map, out_i -> v_i."""
+    identity map, out_i -> v_i.  The diagonal share is p_ii / eps while every
+    other share stays bounded, so the deviation shrinks in proportion to eps:
+    returns max |out - v| at eps = 1e-12 (bound 1e-8 in the table; ~4e-9 for
+    these inputs) after checking that a hundredfold smaller eps gives a
+    hundredfold smaller deviation (within 10 %)."""
     q, k, v = _rand(T, d, seed)
-    r = od.dilution_forward_head(q, k, v, 1.0, 1e-12, earlier_only=True)
-    return np.abs(r["out"] - v).max() * 1e-3   # identity to ~1e-6 relative: scaled into the pin's tolerance
+    err = [np.abs(od.dilution_forward_head(q, k, v, 1.0, e, earlier_only=True)["out"] - v).max()
+           for e in (1e-10, 1e-12)]
+    assert 90.0 < err[0] / err[1] < 110.0, err
+    return err[1]
 
 
 def pin_earlier_only_decode_equals_prefill(T=12, d=8, seed=18, tau=1.1, eps=1e-4):
@@ -317,7 +323,7 @@ FORWARD_PINS = [
     (pin_lse, 1e-12),
     (pin_earlier_only_brute_force, 1e-12),
     (pin_earlier_only_uniform_harmonic, 1e-12),
-    (pin_earlier_only_identity, 1e-6),
+    (pin_earlier_only_identity, 1e-8),
     (pin_earlier_only_decode_equals_prefill, 1e-12),
 ]
 
