@@ -14,25 +14,28 @@
 //
 // Every pair (j, k) needs the forward running sum down its key column
 // (committed) and the reverse running sum of dC, and rho needs a reduction
-// over all keys before any ds exists.  The passes:
+// over all keys before any ds exists.  Since ds = p (dp - rho),
+//   dK_k = c (sum_j u_jk q_j - sum_j p_jk rho_j q_j),  u = p dp,
+// and only the second sum needs rho.  The passes:
 //   F   the forward demand sweep again (fwd_bf16.cu) from the given lse2; it
 //       writes committed + eps of every key at every 32-query chunk start
 //       (demand checkpoints) and the forward accumulators (numerator, R);
 //   rows  1/R_j and delta_j = g_j . out_j from those accumulators;
-//   B1  key-major, query chunks in reverse order: S = K Q^T and dA' = V G^T -
+//   R   key-major, query chunks in reverse order: S = K Q^T and dA' = V G^T -
 //       delta on tcgen05; one thread per key rebuilds committed inside each
 //       chunk from its checkpoint, carries sum_{i > j} dC in a register, and
-//       writes it at every chunk start (reverse checkpoints); rho_j is summed
-//       over the key tile's lanes and added to rho;
-//   KV  key-major: with both checkpoints every chunk is independent; the
-//       threads write A^T = r / R and ds^T (bf16, K-major) to shared memory
-//       and tcgen05 accumulates dV += A^T G and dK += ds^T Q in TMEM;
-//   Q   query-major: for each key tile the threads write ds (MN-major) and
-//       tcgen05 accumulates dQ += ds K in TMEM.
+//       writes it at every chunk start (reverse checkpoints); it forms
+//       A = r / R and u = p dp, tcgen05 accumulates dV += A^T G and dK1 +=
+//       u^T Q in TMEM, and rho_j (the sum of u over the key tile's lanes) is
+//       added to rho;
+//   L   key-major, no demand: the bids p again (S product, one exponential
+//       per pair), dK2 += (p rho)^T Q on tcgen05, dK = c (dK1 - dK2);
+//   Q   query-major: with both checkpoints every chunk is independent; for
+//       each key tile the threads write ds (MN-major) and tcgen05 accumulates
+//       dQ += ds K in TMEM.
 // S and dA' are formed 64 queries at a time (N = 64) so two CTAs fit an SM
-// at d = 64 (one at d = 128, where the tiles and the N = 128 accumulators take
-// the SM);
-// -lse2 / c2 and -delta ride in a fifth K step of their products (the
+// at d = 64 (R at d = 128: one, its tiles and N = 128 accumulators take the
+// SM); -lse2 / c2 and -delta ride in a fifth K step of their products (the
 // extension operands of the forward sweep).  Every wait is bounded.
 #include "da_internal.h"
 #include "da_ptx.cuh"
@@ -51,6 +54,8 @@ constexpr uint32_t kH128 = kTile * 64 * 2;         // one half of a 128-row tile
 constexpr uint32_t kH64 = 64 * 64 * 2;             // one half of a 64-row tile
 constexpr uint32_t kExt128 = 128 * 16 * 2;         // extension operand, 128 rows
 constexpr uint32_t kExt64 = 64 * 16 * 2;           // extension operand, 64 rows
+
+constexpr uint32_t round_up_c(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
 
 __device__ __forceinline__ uint64_t kdesc(const uint8_t *tile, int kstep) {
   return smem_desc(smem_u32(tile) + kstep * 32, 16, 1024);
@@ -225,58 +230,52 @@ __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[3
   }
 }
 
-// Column sums of a warp's 32 x 32 block (lane = key, X[i] = query i) through
-// shared memory: each lane writes its row (rows 36 floats apart, 16-byte
-// aligned), then lane l adds up column l.  Returns the sum over the warp's
-// keys for query l.
-__device__ __forceinline__ float warp_column_sum(const float (&X)[32], float *red, int lane) {
-  float *rowp = red + lane * 36;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    *reinterpret_cast<float4 *>(rowp + 4 * j) = make_float4(X[4 * j], X[4 * j + 1], X[4 * j + 2], X[4 * j + 3]);
-  __syncwarp();
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-  for (int r = 0; r < 32; r += 4) {
-    s0 += red[r * 36 + lane];
-    s1 += red[(r + 1) * 36 + lane];
-    s2 += red[(r + 2) * 36 + lane];
-    s3 += red[(r + 3) * 36 + lane];
-  }
-  __syncwarp();   // the block is free again
-  return (s0 + s1) + (s2 + s3);
-}
-
 // ------------------------------------------------------------ key-major passes
-// One CTA per (head, 128-key tile), two per SM.  Warps 0-3: one thread per
-// key; warp 4: TMA and the per-query extension rows; warp 5: MMA issuer.
-// MODE 0 (B1) walks the key tile's 64-query half tiles from the last one
-// back to the diagonal, MODE 1 (KV) forward.
-constexpr int kModeB1 = 0, kModeKV = 1;
+// One CTA per (head, 128-key tile), two per SM at d = 64.  Warps 0-3: one
+// thread per key; warp 4: TMA and the per-query extension rows; warp 5: MMA
+// issuer.
+//
+// R (bwdtc_rev_kernel) walks the key tile's 64-query half tiles from the last
+// one back to the diagonal.  Per half tile: S' = K Q^T and dA' = V G^T - delta
+// on tcgen05; one thread per key rebuilds committed inside each 32-query
+// chunk from its demand checkpoint, carries the reverse sum of dC (writing it
+// at every chunk start: the reverse checkpoints), and forms
+//   A = r / R (bf16, for dV),   u = p dp (bf16, for dK1; fp32 for rho);
+// the products dV += A^T G and dK1 += u^T Q accumulate in TMEM, and the
+// key tile's partial sums of u (rho_j = sum_k p_jk dp_jk) go to rho.
+// Because ds = p (dp - rho),
+//   dK_k = c sum_j ds_jk q_j = c (sum_j u_jk q_j - sum_j p_jk rho_j q_j),
+// so the rest of dK needs rho but not the demand: L (bwdtc_dk2_kernel) forms
+// the bids p again (S' product, one exponential per pair) and accumulates
+// dK2 += (p rho)^T Q, then writes dK = c (dK1 - dK2).
+constexpr int kModeRev = 0, kModeDk2 = 1;
 
 template <int MODE, int D>
 struct KeyCfg {
   static constexpr uint32_t kTB = kTile * D * 2, kHB = 64 * D * 2;   // 128-row and 64-row tiles
-  static constexpr uint32_t kOffK = 0, kOffV = kTB;
-  static constexpr uint32_t kOffQh = 2 * kTB;                     // [2] 64-query tiles of Q
-  static constexpr uint32_t kOffGh = kOffQh + 2 * kHB;            // [2] 64-query tiles of dout
-  static constexpr uint32_t kOffAExt = kOffGh + 2 * kHB;
-  static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // [2] -lse2 / c2 rows
-  static constexpr uint32_t kOffBExtA = kOffBExtS + 2 * kExt64;   // [2] -delta rows
-  static constexpr uint32_t kOffRinv = kOffBExtA + 2 * kExt64;    // [2][64] fp32
-  static constexpr uint32_t kOffRho = kOffRinv + 2 * 64 * 4;      // [2][64] fp32 (KV)
-  static constexpr uint32_t kOffRed = kOffRho + 2 * 64 * 4;       // [2][4][64] fp32 (B1)
-  static constexpr uint32_t kOffXp = kOffRed + 2 * 4 * 64 * 4;    // [4][32][36] fp32 (B1)
-  static constexpr uint32_t kOffAT = MODE == kModeB1 ? kOffXp + 4 * 32 * 36 * 4 : kOffXp;   // A^T (KV)
-  static constexpr uint32_t kOffDsT = kOffAT + kH128;             // ds^T, K-major (KV)
-  static constexpr uint32_t kOffBar = MODE == kModeKV ? kOffDsT + kH128 : kOffAT;
+  static constexpr bool kRev = MODE == kModeRev;
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kOffK + kTB;                          // R only
+  static constexpr uint32_t kOffQh = kRev ? kOffV + kTB : kOffK + kTB;    // [2] 64-query tiles of Q
+  static constexpr uint32_t kOffGh = kOffQh + 2 * kHB;                    // [2] 64-query tiles of dout (R)
+  static constexpr uint32_t kOffAExt = kRev ? kOffGh + 2 * kHB : kOffGh;
+  static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;               // [2] -lse2 / c2 rows
+  static constexpr uint32_t kOffBExtA = kOffBExtS + 2 * kExt64;           // [2] -delta rows (R)
+  static constexpr uint32_t kOffRows = kOffBExtA + (kRev ? 2 * kExt64 : 0);   // [2][64] fp32: 1/R (R), rho (L)
+  static constexpr uint32_t kOffRed = kOffRows + 2 * 64 * 4;              // [2][4][64] fp32 partial rho (R)
+  static constexpr uint32_t kOffOp = round_up_c(kOffRed + (kRev ? 2 * 4 * 64 * 4 : 0), 1024);
+  // R: A^T and u^T (bf16, K-major: 128 keys x 64 queries, 128B-swizzled);
+  // L: two buffers of (p rho)^T
+  static constexpr uint32_t kOffBar = kOffOp + 2 * kH128;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + re-alignment slack
-  // TMEM: S' and dA' slots (B1: two of each), then (KV) dV and dK, d columns each
-  static constexpr uint32_t kTmemDV = 128, kTmemDK = 128 + D;
-  static constexpr uint32_t kTmemCols = (MODE == kModeB1 || D == 64) ? 256 : 512;
-  static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
-  static_assert(kOffAT % 1024 == 0, "swizzled operands");
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  // TMEM: S' (and dA'), then the accumulators (d columns each):
+  //   R: S' 0..63, dA' 64..127, dV, dK1;   L: S' 0..63, dK2
+  // (L at d = 64 runs three CTAs per SM: 128 columns each)
+  static constexpr uint32_t kTmemAcc0 = kRev ? 128 : 64, kTmemAcc1 = kTmemAcc0 + D;
+  static constexpr uint32_t kTmemCols = kRev ? (D == 128 ? 512 : 256) : (D == 128 ? 256 : 128);
+  static constexpr int kCtasPerSm = kRev ? (D == 128 ? 1 : 2) : (D == 128 ? 2 : 3);
+  static_assert(kOffOp % 1024 == 0, "swizzled operands");
+  static_assert(kSmemBytes * kCtasPerSm <= 232448, "shared memory");
 };
 
 // The K-major S' = K Q^T (or dA' = V G^T) product over d: K steps 0..3 read
@@ -288,32 +287,51 @@ __device__ __forceinline__ void mma_over_d(uint32_t dt, uint64_t da, uint32_t ha
   if constexpr (D == 128) MmaRun<0, 4, 2, 2, false>::go(dt, da + (half_a >> 4), db + (half_b >> 4), idesc, 1u);
 }
 
-template <int MODE, int D, bool EARLIER>
-__global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
-    bwdtc_key_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmGh,
+// Sum over the warp's 32 keys (lanes) of X[i] for each query i by recursive
+// halving: in each round a lane keeps one half of its values (by one bit of
+// its lane index), sends the other half to the lane that differs in that bit
+// and adds what it receives; lane l ends with the sum for query l.  X is
+// clobbered.
+__device__ __forceinline__ float warp_reduce_scatter32(float (&X)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = up ? X[i] : X[i + off];
+      const float keep = up ? X[i + off] : X[i];
+      X[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return X[0];
+}
+
+template <int D, bool EARLIER>
+__global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
+    bwdtc_rev_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmGh,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const float *__restrict__ nlse2, const float *__restrict__ delta,
                      const float *__restrict__ rinv, float *__restrict__ rho, const float *__restrict__ cchk,
-                     float *__restrict__ gchk, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int BH,
-                     int T, int Tp, HeadScale hs, float c_scalar, int *status) {
-  using C = KeyCfg<MODE, D>;
+                     float *__restrict__ gchk, float *__restrict__ dk1, __nv_bfloat16 *__restrict__ dv, int BH,
+                     int T, int Tp, HeadScale hs, int *status) {
+  using C = KeyCfg<kModeRev, D>;
   extern __shared__ uint8_t bt_smem_raw[];
   uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
   uint8_t *sK = smem + C::kOffK, *sV = smem + C::kOffV;
   uint8_t *sAExt = smem + C::kOffAExt;
-  float *sRinv = reinterpret_cast<float *>(smem + C::kOffRinv);
-  float *sRho = reinterpret_cast<float *>(smem + C::kOffRho);
+  float *sRinv = reinterpret_cast<float *>(smem + C::kOffRows);
   float *sRed = reinterpret_cast<float *>(smem + C::kOffRed);
-  float *sXp = reinterpret_cast<float *>(smem + C::kOffXp);
-  uint8_t *sAT = smem + C::kOffAT, *sDsT = smem + C::kOffDsT;
+  uint8_t *sAT = smem + C::kOffOp, *sUT = smem + C::kOffOp + kH128;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *kv_full = bars;
   uint64_t *in_full = bars + 1;      // [2] half tile b loaded and its rows written
   uint64_t *in_empty = bars + 3;     // [2] its products done and its rows read
-  uint64_t *s_full = bars + 5;       // [2] S / dA' slots (B1: double, KV: slot 0)
-  uint64_t *s_free = bars + 7;       // [2]
-  uint64_t *w_full = bars + 9;       // KV: A^T, ds^T written;  B1: [2] partial rho written
-  uint64_t *w_free = bars + 11;      // KV: dV, dK products done; B1: [2] partial rho read
+  uint64_t *s_full = bars + 5;       // S' / dA' slot
+  uint64_t *s_free = bars + 6;
+  uint64_t *x_full = bars + 7;       // A^T, u^T of the half tile written
+  uint64_t *x_free = bars + 8;       // dV, dK1 products of the half tile done
+  uint64_t *r_full = bars + 9;       // [2] partial rho written
+  uint64_t *r_free = bars + 11;      // [2] partial rho read
   uint64_t *fin = bars + 13;
   uint64_t *drain = bars + 14;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
@@ -330,11 +348,13 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&in_full[b], 2);    // the tiles' bytes + the producer's rows
       mbar_init(&in_empty[b], 5);   // the issuer's commit + the four key warps
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
-      mbar_init(&w_full[b], MODE == kModeKV ? 4 : 4);
-      mbar_init(&w_free[b], MODE == kModeKV ? 1 : 2);
+      mbar_init(&r_full[b], 4);
+      mbar_init(&r_free[b], 2);
     }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(x_full, 4);
+    mbar_init(x_free, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -351,7 +371,7 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, status};
-  auto half_of = [&](int u) { return MODE == kModeB1 ? NH - 1 - u : hq0 + u; };
+  auto half_of = [&](int u) { return NH - 1 - u; };
 
   if (warp == 4) {
     // ---------------------------------------------------------- producer
@@ -369,14 +389,13 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
       const int b = u & 1, h = half_of(u);
       // the half tile's per-query values are read before waiting for the
       // buffer, so their global-memory latency overlaps that wait
-      float nl[2], de[2], ri[2], rh[2];
+      float nl[2], de[2], ri[2];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const size_t idx = (size_t)bh * Tp + h * 64 + lane + 32 * j;
         nl[j] = __ldg(nlse2 + idx);
         de[j] = __ldg(delta + idx);
         ri[j] = __ldg(rinv + idx);
-        rh[j] = MODE == kModeKV ? __ldg(rho + idx) : 0.f;
       }
       if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
       if (lane == 0) {
@@ -391,7 +410,6 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
         put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, nl[j] / c2);
         put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -de[j]);
         sRinv[b * 64 + qq] = ri[j];
-        if (MODE == kModeKV) sRho[b * 64 + qq] = rh[j];
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -403,11 +421,16 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
     }
   } else if (warp == 5) {
     // -------------------------------------------------------- MMA issuer
+    // S'(u), dA'(u) into the slot, then the products of half tile u - 1:
+    // dV += A^T G and dK1 += u^T Q (A^T, u^T: K-major A operands, 16
+    // queries = 32 bytes per K step; G and Q of buffer bp as MN-major B, 16
+    // queries = 2 KB per K step, the two 64-column halves of d = 128 8 KB
+    // apart).
     if (lane == 0) {
       constexpr long long kStepKm = 2;                       // K-major: +32 bytes per K step
       constexpr long long kStepMn = 128;                     // MN-major: +16 rows (2 KB) per K step
       const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
-      const uint32_t idesc_kv = idesc_bf16(kTile, D, false, true);
+      const uint32_t idesc_acc = idesc_bf16(kTile, D, false, true);
       const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
       const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
       bool ok = mbar_wait(kv_full, 0, wc);
@@ -415,37 +438,29 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
       for (int u = 0; ok && u <= n; ++u) {
         if (u < n) {
           const int b = u & 1;
-          const int slot = MODE == kModeB1 ? b : 0;
-          const uint32_t par_free = MODE == kModeB1 ? (((u >> 1) & 1) ^ 1) : ((u & 1) ^ 1);
-          if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(&s_free[slot], par_free, wc)) break;
+          if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(s_free, (u & 1) ^ 1, wc)) break;
           tc_fence_after();
           const uint64_t dQh = kdesc(smem + C::kOffQh + b * C::kHB, 0);
           const uint64_t dGh = kdesc(smem + C::kOffGh + b * C::kHB, 0);
           const uint64_t dBS = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtS + b * kExt64), 128, 256);
           const uint64_t dBA = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtA + b * kExt64), 128, 256);
-          const uint32_t tS = tmem + slot * 64, tA = tmem + 128 + slot * 64;
-          const uint32_t tSk = MODE == kModeB1 ? tS : tmem, tAk = MODE == kModeB1 ? tA : tmem + 64;
-          mma_over_d<D>(tSk, dK, kH128, dQh, kH64, idesc_s);
-          mma_bf16_at<0, 0>(tSk, dAExt, dBS, idesc_s, 1u);
-          mma_over_d<D>(tAk, dV, kH128, dGh, kH64, idesc_s);
-          mma_bf16_at<0, 0>(tAk, dAExt, dBA, idesc_s, 1u);
-          mma_commit(&s_full[slot]);
-          if (MODE == kModeB1) mma_commit(&in_empty[b]);
+          mma_over_d<D>(tmem, dK, kH128, dQh, kH64, idesc_s);
+          mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
+          mma_over_d<D>(tmem + 64, dV, kH128, dGh, kH64, idesc_s);
+          mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
+          mma_commit(s_full);
         }
-        if (MODE == kModeKV && u >= 1) {
-          // dV += A^T G, dK += ds^T Q for half tile u - 1 (its operands: G and Q
-          // of buffer bp as MN-major B, 16 queries = 2 KB per K step, the two
-          // 64-column halves of d = 128 8 KB apart)
+        if (u >= 1) {
           const int up = u - 1, bp = up & 1;
-          if (!mbar_wait(&w_full[0], up & 1, wc)) break;
+          if (!mbar_wait(x_full, up & 1, wc)) break;
           tc_fence_after();
           const uint64_t dGmn = smem_desc(smem_u32(smem + C::kOffGh + bp * C::kHB), kH64, 1024);
           const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * C::kHB), kH64, 1024);
-          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemDV, kdesc(sAT, 0), dGmn, idesc_kv,
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc0, kdesc(sAT, 0), dGmn, idesc_acc,
                                                     up > 0 ? 1u : 0u);
-          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemDK, kdesc(sDsT, 0), dQmn, idesc_kv,
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc1, kdesc(sUT, 0), dQmn, idesc_acc,
                                                     up > 0 ? 1u : 0u);
-          mma_commit(&w_free[0]);
+          mma_commit(x_free);
           mma_commit(&in_empty[bp]);
           if (u == n) mma_commit(fin);
         }
@@ -460,134 +475,335 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<MODE, D>::kCtasPerSm)
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const int swz = row & 7;
     uint8_t *at_row = sAT + (row >> 3) * 1024 + (row & 7) * 128;
-    uint8_t *ds_row = sDsT + (row >> 3) * 1024 + (row & 7) * 128;
-    float grev = 0.f;   // B1: sum of dC over the queries after the current one
+    uint8_t *ut_row = sUT + (row >> 3) * 1024 + (row & 7) * 128;
+    float grev = 0.f;   // sum of dC over the queries after the current one
     // Checkpoints are read one half tile ahead: they come from DRAM and are
     // needed at the start of each chunk.
     auto ck_of = [&](int uu, int c) { return ((size_t)bh * NC + (half_of(uu) * 2 + c)) * Tp + key; };
-    float cpe_n[2], g_n[2] = {0.f, 0.f};
+    float cpe_n[2];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      cpe_n[c] = __ldg(cchk + ck_of(0, c));
-      if (MODE == kModeKV) g_n[c] = __ldg(gchk + ck_of(0, c));
-    }
+    for (int c = 0; c < 2; ++c) cpe_n[c] = __ldg(cchk + ck_of(0, c));
     bool ok = true;
     for (int u = 0; ok && u < n; ++u) {
       const int b = u & 1, h = half_of(u);
       const float cpe_c[2] = {cpe_n[0], cpe_n[1]};
-      const float g_c[2] = {g_n[0], g_n[1]};
       if (u + 1 < n) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          cpe_n[c] = __ldg(cchk + ck_of(u + 1, c));
-          if (MODE == kModeKV) g_n[c] = __ldg(gchk + ck_of(u + 1, c));
-        }
+        for (int c = 0; c < 2; ++c) cpe_n[c] = __ldg(cchk + ck_of(u + 1, c));
       }
-      const int slot = MODE == kModeB1 ? b : 0;
       const int q0h = h * 64;
       const bool need_mask = kt * kTile + kTile - 1 > q0h;
       const int row_eff = key - q0h;
-      const uint32_t par_full = MODE == kModeB1 ? ((u >> 1) & 1) : (u & 1);
-      if (!warp_wait(&s_full[slot], par_full, wc)) break;
+      if (!warp_wait(s_full, u & 1, wc)) break;
       tc_fence_after();
-      if (MODE == kModeKV && !warp_wait(&w_free[0], (u & 1) ^ 1, wc)) break;   // A^T, ds^T of u - 1 consumed
-      if (MODE == kModeB1 && !warp_wait(&w_free[b], ((u >> 1) & 1) ^ 1, wc)) break;   // partial rho buffer b read
+      // partial rho buffer b read
+      if (!warp_wait(&r_free[b], ((u >> 1) & 1) ^ 1, wc)) break;
       for (int cc = 0; cc < 2; ++cc) {
-        const int c = MODE == kModeB1 ? 1 - cc : cc;   // B1 walks the chunks backwards
+        const int c = 1 - cc;   // the chunks backwards
         float P[32], A[32], E[32];
         uint32_t at[16];
-        const uint32_t tS = (MODE == kModeB1 ? tmem + slot * 64 : tmem) + lanes + 32 * c;
-        const uint32_t tA = (MODE == kModeB1 ? tmem + 128 + slot * 64 : tmem + 64) + lanes + 32 * c;
-        tmem_ld32(tS, P);
-        tmem_ld32(tA, A);
+        tmem_ld32(tmem + lanes + 32 * c, P);
+        tmem_ld32(tmem + 64 + lanes + 32 * c, A);
         tmem_wait_ld_r(P);
         tmem_wait_ld_r(A);
-        if (cc == 1) release_bt(&s_free[slot], lane);
+        if (cc == 1) release_bt(s_free, lane);
         const size_t ck = ((size_t)bh * NC + (q0h / 32 + c)) * Tp + key;
         const float cpe = cpe_c[c];
         const float *rq = sRinv + b * 64;
-        if (MODE == kModeB1) {
-          if (need_mask) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
-          else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
-          gchk[ck] = grev;   // sum of dC after the chunk
-          bwd_chunk_rev(A, E, grev);
+        if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+        else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+        gchk[ck] = grev;   // sum of dC after the chunk
+        bwd_chunk_rev(A, E, grev);
+        uint32_t ut[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {   // p dp
-            const float2 x = fmul2(make_float2(P[i], P[i + 1]), make_float2(A[i], A[i + 1]));
-            P[i] = x.x;
-            P[i + 1] = x.y;
-          }
-          sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_column_sum(P, sXp + warp * 32 * 36, lane);
-        } else {
-          if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
-          else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
-          float g0 = g_c[c];
-          bwd_chunk_rev(A, E, g0);
-          uint32_t ds[16];
-          const float *ro = sRho + b * 64 + 32 * c;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 r2 = *reinterpret_cast<const float2 *>(ro + 2 * i);
-            const float2 x = fmul2(make_float2(P[2 * i], P[2 * i + 1]),
-                                   fadd2(make_float2(A[2 * i], A[2 * i + 1]), make_float2(-r2.x, -r2.y)));
-            ds[i] = pack_bf16x2(x.x, x.y);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int piece = (4 * c + j) ^ swz;
-            *reinterpret_cast<uint4 *>(at_row + piece * 16) = make_uint4(at[4 * j], at[4 * j + 1], at[4 * j + 2], at[4 * j + 3]);
-            *reinterpret_cast<uint4 *>(ds_row + piece * 16) = make_uint4(ds[4 * j], ds[4 * j + 1], ds[4 * j + 2], ds[4 * j + 3]);
-          }
+        for (int i = 0; i < 32; i += 2) {   // u = p dp
+          const float2 x = fmul2(make_float2(P[i], P[i + 1]), make_float2(A[i], A[i + 1]));
+          P[i] = x.x;
+          P[i + 1] = x.y;
+          ut[i / 2] = pack_bf16x2(x.x, x.y);
         }
+        // the previous half tile's products must be done reading A^T, u^T
+        // (checked once the first chunk is formed, so they run meanwhile)
+        if (cc == 0 && !warp_wait(x_free, (u & 1) ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int piece = (4 * c + j) ^ swz;
+          *reinterpret_cast<uint4 *>(at_row + piece * 16) = make_uint4(at[4 * j], at[4 * j + 1], at[4 * j + 2], at[4 * j + 3]);
+          *reinterpret_cast<uint4 *>(ut_row + piece * 16) = make_uint4(ut[4 * j], ut[4 * j + 1], ut[4 * j + 2], ut[4 * j + 3]);
+        }
+        sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_reduce_scatter32(P, lane);
       }
-      if (MODE == kModeKV) {
-        fence_proxy_async_smem();
+      if (!ok) break;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(x_full);
+        mbar_arrive(&r_full[b]);
+        mbar_arrive(&in_empty[b]);
+      }
+      // warps 0 and 1 add the four warps' partial sums of the half tile's
+      // 64 queries into rho (one atomic per query and key tile)
+      if (warp < 2) {
+        if (!warp_wait(&r_full[b], (u >> 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        const int qq = warp * 32 + lane;
+        const float *rd = sRed + b * 4 * 64 + qq;
+        const float sum = (rd[0] + rd[64]) + (rd[128] + rd[192]);
+        if (q0h + qq < T) atomicAdd(rho + (size_t)bh * Tp + q0h + qq, sum);
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&w_full[0]);
-          mbar_arrive(&in_empty[b]);
-        }
-      } else {
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&w_full[b]);
-          mbar_arrive(&in_empty[b]);
-        }
-        // warps 0 and 1 add the four warps' partial sums of the half tile's
-        // 64 queries into rho (one atomic per query and key tile)
-        if (warp < 2) {
-          if (!warp_wait(&w_full[b], (u >> 1) & 1, wc)) {
-            ok = false;
-            break;
-          }
-          const int qq = warp * 32 + lane;
-          const float* rd = sRed + b * 4 * 64 + qq;
-          const float sum = (rd[0] + rd[64]) + (rd[128] + rd[192]);
-          if (q0h + qq < T) atomicAdd(rho + (size_t)bh * Tp + q0h + qq, sum);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&w_free[b]);
-        }
+        if (lane == 0) mbar_arrive(&r_free[b]);
       }
     }
-    if (MODE == kModeKV && ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
+    if (ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
       tc_fence_after();
-      // dV (TMEM columns 128 ..) and dK (128 + d ..) of this key: out in bf16
-      const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
+      // dV (TMEM columns 128 ..) of this key out in bf16; dK1 (128 + d ..) in
+      // fp32 for the pass that completes dK
       // (tcgen05.ld is warp-collective: every lane loads, only keys < T store)
       float x[32];
 #pragma unroll
-      for (int part = 0; part < D / 16; ++part) {   // d / 32 parts of dV, then of dK
-        tmem_ld32(tmem + C::kTmemDV + lanes + 32 * part, x);
+      for (int part = 0; part < D / 16; ++part) {   // d / 32 parts of dV, then of dK1
+        tmem_ld32(tmem + C::kTmemAcc0 + lanes + 32 * part, x);
         tmem_wait_ld_r(x);
         if (key < T) {
-          const bool is_v = part < D / 32;
-          const float sc = is_v ? 1.f : cs;
-          __nv_bfloat16 *dst = (is_v ? dv : dk) + ((size_t)bh * T + key) * D + 32 * (part % (D / 32));
+          const int col = 32 * (part % (D / 32));
+          if (part < D / 32) {
+            __nv_bfloat16 *dst = dv + ((size_t)bh * T + key) * D + col;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 4; ++j)
+              reinterpret_cast<uint4 *>(dst)[j] =
+                  make_uint4(pack_bf16x2(x[8 * j], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                             pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(dk1 + ((size_t)bh * T + key) * D + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// L: dK2 = sum_j p_jk rho_j q_j, then dK = c (dK1 - dK2).  Half tiles in
+// forward order; one S' slot (the key threads read both chunks at once and
+// hand it back), (p rho)^T buffers double-buffered.
+template <int D>
+__global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeDk2, D>::kCtasPerSm)
+    bwdtc_dk2_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmK,
+                     const float *__restrict__ nlse2, const float *__restrict__ rho, const float *__restrict__ dk1,
+                     __nv_bfloat16 *__restrict__ dk, int BH, int T, int Tp, HeadScale hs, float c_scalar,
+                     int *status) {
+  using C = KeyCfg<kModeDk2, D>;
+  extern __shared__ uint8_t bt_smem_raw[];
+  uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
+  uint8_t *sK = smem + C::kOffK;
+  uint8_t *sAExt = smem + C::kOffAExt;
+  float *sRho = reinterpret_cast<float *>(smem + C::kOffRows);
+  uint8_t *sPT = smem + C::kOffOp;   // [2] (p rho)^T, K-major
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *k_full = bars;
+  uint64_t *in_full = bars + 1;      // [2] half tile b loaded and its rows written
+  uint64_t *in_empty = bars + 3;     // [2] its products done and its rows read
+  uint64_t *s_full = bars + 5;       // S' slot
+  uint64_t *s_free = bars + 7;
+  uint64_t *x_full = bars + 9;       // [2] (p rho)^T written
+  uint64_t *x_free = bars + 11;      // [2] its product done
+  uint64_t *fin = bars + 13;
+  uint64_t *drain = bars + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.x % BH, kt = blockIdx.x / BH;   // the tiles with the most half tiles first
+  const int NH = Tp / 64, hq0 = 2 * kt, n = NH - hq0;
+  const float c2 = fmaxf(head_c2(hs, bh, nullptr), 1e-30f);
+
+  if (threadIdx.x == 0) {
+    mbar_init(k_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&in_full[b], 2);
+      mbar_init(&in_empty[b], 5);   // the issuer's commit + the four key warps
+      mbar_init(&x_full[b], 4);
+      mbar_init(&x_free[b], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(fin, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  fill_ones_ext(sAExt, threadIdx.x, kBtThreads);
+  zero_smem(smem + C::kOffBExtS, 2 * kExt64, threadIdx.x, kBtThreads);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtx wc{abort_flag, status};
+
+  if (warp == 4) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQh);
+      prefetch_tmap(&tmK);
+      mbar_arrive_expect_tx(k_full, C::kTB);
+      load_tile_halves<D, kH128>(sK, &tmK, k_full, kt * kTile, bh);
+    }
+    int issued = 0;
+    for (int u = 0; u < n; ++u) {
+      const int b = u & 1, h = hq0 + u;
+      float nl[2], rh[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const size_t idx = (size_t)bh * Tp + h * 64 + lane + 32 * j;
+        nl[j] = __ldg(nlse2 + idx);
+        rh[j] = __ldg(rho + idx);
+      }
+      if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&in_full[b], C::kHB);
+        load_tile_halves<D, kH64>(smem + C::kOffQh + b * C::kHB, &tmQh, &in_full[b], h * 64, bh);
+      }
+      ++issued;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int qq = lane + 32 * j;
+        put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, nl[j] / c2);
+        sRho[b * 64 + qq] = rh[j];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&in_full[b]);
+    }
+    if (lane == 0 && *abort_flag) {
+      drain_wait_bt(k_full, 0);
+      for (int u = (issued > 2 ? issued - 2 : 0); u < issued; ++u) drain_wait_bt(&in_full[u & 1], (u >> 1) & 1);
+    }
+  } else if (warp == 5) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr long long kStepKm = 2, kStepMn = 128;
+      const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
+      const uint32_t idesc_acc = idesc_bf16(kTile, D, false, true);
+      const uint64_t dK = kdesc(sK, 0);
+      const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
+      bool ok = mbar_wait(k_full, 0, wc);
+      if (ok) tc_fence_after();
+      for (int u = 0; ok && u <= n; ++u) {
+        if (u < n) {
+          const int b = u & 1;
+          if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(s_free, (u & 1) ^ 1, wc)) break;
+          tc_fence_after();
+          const uint64_t dQh = kdesc(smem + C::kOffQh + b * C::kHB, 0);
+          const uint64_t dBS = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtS + b * kExt64), 128, 256);
+          mma_over_d<D>(tmem, dK, kH128, dQh, kH64, idesc_s);
+          mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
+          mma_commit(s_full);
+        }
+        if (u >= 1) {
+          const int up = u - 1, bp = up & 1;
+          if (!mbar_wait(&x_full[bp], (up >> 1) & 1, wc)) break;
+          tc_fence_after();
+          const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * C::kHB), kH64, 1024);
+          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc0, kdesc(sPT + bp * kH128, 0), dQmn,
+                                                    idesc_acc, up > 0 ? 1u : 0u);
+          mma_commit(&x_free[bp]);
+          mma_commit(&in_empty[bp]);
+          if (u == n) mma_commit(fin);
+        }
+      }
+      mma_commit(drain);
+      drain_wait_bt(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------ key threads
+    const int row = warp * 32 + lane;
+    const int key = kt * kTile + row;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const int swz = row & 7;
+    const float2 c2v = make_float2(c2, c2);
+    bool ok = true;
+    for (int u = 0; ok && u < n; ++u) {
+      const int b = u & 1, h = hq0 + u;
+      const int q0h = h * 64;
+      const bool need_mask = kt * kTile + kTile - 1 > q0h;
+      const int row_eff = key - q0h;
+      uint8_t *pt_row = sPT + b * kH128 + (row >> 3) * 1024 + (row & 7) * 128;
+      if (!warp_wait(s_full, u & 1, wc) || !warp_wait(&x_free[b], ((u >> 1) & 1) ^ 1, wc)) break;
+      tc_fence_after();
+      float P0[32], P1[32];
+      tmem_ld32(tmem + lanes, P0);
+      tmem_ld32(tmem + lanes + 32, P1);
+      tmem_wait_ld_r(P0);
+      tmem_wait_ld_r(P1);
+      release_bt(s_free, lane);
+      const float *rq = sRho + b * 64;
+      auto chunk = [&](float (&P)[32], int c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x = fmul2(make_float2(P[i], P[i + 1]), c2v);
+          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          if (need_mask) {
+            if (row_eff > 32 * c + i) p0 = 0.f;
+            if (row_eff > 32 * c + i + 1) p1 = 0.f;
+          }
+          const float2 r2 = *reinterpret_cast<const float2 *>(rq + 32 * c + i);
+          const float2 pr = fmul2(make_float2(p0, p1), r2);
+          pk[i / 2] = pack_bf16x2(pr.x, pr.y);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4 *>(pt_row + (((4 * c + j) ^ swz) * 16)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      };
+      chunk(P0, 0);
+      chunk(P1, 1);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&x_full[b]);
+        mbar_arrive(&in_empty[b]);
+      }
+    }
+    if (ok && __all_sync(0xffffffffu, !*abort_flag) && warp_wait(fin, 0, wc)) {
+      tc_fence_after();
+      // dK = c (dK1 - dK2) of this key, out in bf16
+      const float cs = hs.tau_bh == nullptr ? c_scalar : c2 * 0.69314718055994531f;
+      float x[32];
+#pragma unroll
+      for (int part = 0; part < D / 32; ++part) {
+        tmem_ld32(tmem + C::kTmemAcc0 + lanes + 32 * part, x);
+        tmem_wait_ld_r(x);
+        if (key < T) {
+          const float4 *src = reinterpret_cast<const float4 *>(dk1 + ((size_t)bh * T + key) * D + 32 * part);
+          __nv_bfloat16 *dst = dk + ((size_t)bh * T + key) * D + 32 * part;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 a0 = __ldg(src + 2 * j), a1 = __ldg(src + 2 * j + 1);
             reinterpret_cast<uint4 *>(dst)[j] =
-                make_uint4(pack_bf16x2(x[8 * j] * sc, x[8 * j + 1] * sc), pack_bf16x2(x[8 * j + 2] * sc, x[8 * j + 3] * sc),
-                           pack_bf16x2(x[8 * j + 4] * sc, x[8 * j + 5] * sc), pack_bf16x2(x[8 * j + 6] * sc, x[8 * j + 7] * sc));
+                make_uint4(pack_bf16x2((a0.x - x[8 * j]) * cs, (a0.y - x[8 * j + 1]) * cs),
+                           pack_bf16x2((a0.z - x[8 * j + 2]) * cs, (a0.w - x[8 * j + 3]) * cs),
+                           pack_bf16x2((a1.x - x[8 * j + 4]) * cs, (a1.y - x[8 * j + 5]) * cs),
+                           pack_bf16x2((a1.z - x[8 * j + 6]) * cs, (a1.w - x[8 * j + 7]) * cs));
+          }
         }
       }
     }
@@ -914,17 +1130,17 @@ int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const flo
 
 template <int D, bool EARLIER>
 static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, float *rinv, float *rho, float *cchk,
-                         float *gchk, void *dq, void *dk, void *dv, int BH, int T, int Tp, HeadScale hs, float c,
-                         int *status, cudaStream_t stream) {
-  using KB1 = KeyCfg<kModeB1, D>;
-  using KKV = KeyCfg<kModeKV, D>;
+                         float *gchk, float *dk1, void *dq, void *dk, void *dv, int BH, int T, int Tp, HeadScale hs,
+                         float c, int *status, cudaStream_t stream) {
+  using CR = KeyCfg<kModeRev, D>;
+  using CL = KeyCfg<kModeDk2, D>;
   // The shared-memory opt-in is a per-device function attribute.
   static PerDeviceOnce once;
   const int prep = once.run([] {
-    return (cudaFuncSetAttribute(bwdtc_key_kernel<kModeB1, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 KB1::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(bwdtc_key_kernel<kModeKV, D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 KKV::kSmemBytes) != cudaSuccess ||
+    return (cudaFuncSetAttribute(bwdtc_rev_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CR::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(bwdtc_dk2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CL::kSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(bwdtc_q_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  QCfg<D>::kSmemBytes) != cudaSuccess)
                ? DA_ERR_CUDA
@@ -934,12 +1150,11 @@ static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, fl
   const int NT = Tp / kTile;
   const unsigned grid = (unsigned)(NT * BH);
   // maps: 0 Q (64-row boxes), 1 dout (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout (128)
-  bwdtc_key_kernel<kModeB1, D, EARLIER><<<grid, kBtThreads, KB1::kSmemBytes, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, nullptr, nullptr, BH, T, Tp, hs, c,
-      status);
-  bwdtc_key_kernel<kModeKV, D, EARLIER><<<grid, kBtThreads, KKV::kSmemBytes, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk,
-      static_cast<__nv_bfloat16 *>(dk), static_cast<__nv_bfloat16 *>(dv), BH, T, Tp, hs, c, status);
+  bwdtc_rev_kernel<D, EARLIER><<<grid, kBtThreads, CR::kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, dk1,
+      static_cast<__nv_bfloat16 *>(dv), BH, T, Tp, hs, status);
+  bwdtc_dk2_kernel<D><<<grid, kBtThreads, CL::kSmemBytes, stream>>>(
+      maps[0], maps[2], nlse2, rho, dk1, static_cast<__nv_bfloat16 *>(dk), BH, T, Tp, hs, c, status);
   bwdtc_q_kernel<D, EARLIER><<<grid, kBtThreads, QCfg<D>::kSmemBytes, stream>>>(
       maps[4], maps[5], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, static_cast<__nv_bfloat16 *>(dq),
       BH, T, Tp, hs, c, status);
@@ -963,6 +1178,7 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
   float *delta = rinv + rows, *rho = delta + rows;
   float *cchk = reinterpret_cast<float *>(ws + L.cchk_off);
   float *gchk = reinterpret_cast<float *>(ws + L.gchk_off);
+  float *dk1 = reinterpret_cast<float *>(ws + L.dk1_off);
   CUtensorMap maps[6];
   if (!make_bf16_tile_map(&maps[0], q, BH, T, d, 64) || !make_bf16_tile_map(&maps[1], dout, BH, T, d, 64) ||
       !make_bf16_tile_map(&maps[2], k, BH, T, d, kTile) || !make_bf16_tile_map(&maps[3], v, BH, T, d, kTile) ||
@@ -978,7 +1194,7 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
   const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(dout);
   if (d == 128) bwdtc_rows<128><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
   else bwdtc_rows<64><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
-#define DA_BWD_PASSES_ARGS maps, nlse2, delta, rinv, rho, cchk, gchk, dq, dk, dv, BH, T, Tp, hs, c, status, stream
+#define DA_BWD_PASSES_ARGS maps, nlse2, delta, rinv, rho, cchk, gchk, dk1, dq, dk, dv, BH, T, Tp, hs, c, status, stream
   if (d == 128)
     return earlier ? launch_passes<128, true>(DA_BWD_PASSES_ARGS) : launch_passes<128, false>(DA_BWD_PASSES_ARGS);
   return earlier ? launch_passes<64, true>(DA_BWD_PASSES_ARGS) : launch_passes<64, false>(DA_BWD_PASSES_ARGS);

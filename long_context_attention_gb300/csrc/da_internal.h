@@ -77,13 +77,15 @@ DA_HD BwdWorkspace bwd_workspace_layout(int64_t BH, int64_t T, int d) {
 // ---------------------------------------------------------------------------
 // Tensor-core backward workspace (bf16):
 // [status | -lse2 [BH][Tp] | acc [BH][Tp][d + 4] | 1/R, delta, rho [3][BH][Tp] |
-//  demand checkpoints [BH][Tp/32][Tp] | reverse-sum checkpoints [BH][Tp/32][Tp]]
+//  demand checkpoints [BH][Tp/32][Tp] | reverse-sum checkpoints [BH][Tp/32][Tp] |
+//  dK1 [BH][T][d] fp32]
 // The checkpoints hold, for every key and every 32-query chunk at or after
 // the key's sweep span, committed + eps (forward order) and the sum of dC
-// over the queries after the chunk (reverse order).
+// over the queries after the chunk (reverse order).  dK1 is the part of dK
+// that the reverse pass accumulates (sum_j p dp q_j, before the scale).
 // ---------------------------------------------------------------------------
 struct BwdTcWorkspace {
-  size_t nlse2_off, acc_off, rows_off, cchk_off, gchk_off, total;
+  size_t nlse2_off, acc_off, rows_off, cchk_off, gchk_off, dk1_off, total;
 };
 
 DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T, int d) {
@@ -94,7 +96,8 @@ DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T, int d) {
   w.rows_off = (size_t)round_up((int64_t)w.acc_off + BH * Tp * acc_stride(d) * 4, 256);
   w.cchk_off = (size_t)round_up((int64_t)w.rows_off + 3 * BH * Tp * 4, 256);
   w.gchk_off = (size_t)round_up((int64_t)w.cchk_off + BH * (Tp / 32) * Tp * 4, 256);
-  w.total = (size_t)round_up((int64_t)w.gchk_off + BH * (Tp / 32) * Tp * 4, 256);
+  w.dk1_off = (size_t)round_up((int64_t)w.gchk_off + BH * (Tp / 32) * Tp * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.dk1_off + BH * T * d * 4, 256);
   return w;
 }
 
