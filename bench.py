@@ -471,7 +471,7 @@ def run_train(torch, b, inputs, dev, steps=5, batch=None, T=None, d=None):
             "B": B, "H": H, "T": T, "d": d, "steps": steps, "ms_per_step": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "bwd_ms": bwd_ms,
             "tflops": (fwd_f + bwd_f) / (ms * 1e-3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
-            "backward": "tcgen05: the forward keeps its demand checkpoints; a rho pass, a dK/dV pass, a dQ pass",
+            "backward": "tcgen05: the forward keeps its demand checkpoints; a reverse pass (rho, dV, the u-part of dK), a light pass (the rho-part of dK), a dQ pass",
             "fwd_flop": fwd_f, "bwd_flop": bwd_f}
 
 

@@ -266,7 +266,12 @@ struct KeyCfg {
   static constexpr uint32_t kOffOp = round_up_c(kOffRed + (kRev ? 2 * 4 * 64 * 4 : 0), 1024);
   // R: A^T and u^T (bf16, K-major: 128 keys x 64 queries, 128B-swizzled);
   // L: two buffers of (p rho)^T
-  static constexpr uint32_t kOffBar = kOffOp + 2 * kH128;
+  // R at d = 128 (one CTA per SM) has room for the per-warp transposition
+  // buffers of the partial rho sums, [4][32][36] fp32; at d = 64 they would
+  // not fit beside the second CTA and a register butterfly does the sums.
+  static constexpr bool kXp = kRev && D == 128;
+  static constexpr uint32_t kOffXp = kOffOp + 2 * kH128;
+  static constexpr uint32_t kOffBar = kOffXp + (kXp ? 4 * 32 * 36 * 4 : 0);
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + re-alignment slack
   // TMEM: S' (and dA'), then the accumulators (d columns each):
   //   R: S' 0..63, dA' 64..127, dV, dK1;   L: S' 0..63, dK2
@@ -304,6 +309,28 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&X)[32], int lane)
     }
   }
   return X[0];
+}
+
+// The same sums through shared memory: each lane writes its 32 values as one
+// row of the warp's [32][36] block (the row pitch of 36 words keeps both the
+// 16-byte row stores and the column reads free of bank conflicts), then lane l
+// adds up column l.
+__device__ __forceinline__ float warp_column_sum(const float (&X)[32], float *red, int lane) {
+  float *rowp = red + lane * 36;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<float4 *>(rowp + 4 * j) = make_float4(X[4 * j], X[4 * j + 1], X[4 * j + 2], X[4 * j + 3]);
+  __syncwarp();
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int r = 0; r < 32; r += 4) {
+    s0 += red[r * 36 + lane];
+    s1 += red[(r + 1) * 36 + lane];
+    s2 += red[(r + 2) * 36 + lane];
+    s3 += red[(r + 3) * 36 + lane];
+  }
+  __syncwarp();   // the block is free again
+  return (s0 + s1) + (s2 + s3);
 }
 
 template <int D, bool EARLIER>
@@ -476,6 +503,7 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
     const int swz = row & 7;
     uint8_t *at_row = sAT + (row >> 3) * 1024 + (row & 7) * 128;
     uint8_t *ut_row = sUT + (row >> 3) * 1024 + (row & 7) * 128;
+    float *xp = reinterpret_cast<float *>(smem + C::kOffXp) + warp * 32 * 36;   // d = 128 only
     float grev = 0.f;   // sum of dC over the queries after the current one
     // Checkpoints are read one half tile ahead: they come from DRAM and are
     // needed at the start of each chunk.
@@ -534,7 +562,8 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
           *reinterpret_cast<uint4 *>(at_row + piece * 16) = make_uint4(at[4 * j], at[4 * j + 1], at[4 * j + 2], at[4 * j + 3]);
           *reinterpret_cast<uint4 *>(ut_row + piece * 16) = make_uint4(ut[4 * j], ut[4 * j + 1], ut[4 * j + 2], ut[4 * j + 3]);
         }
-        sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_reduce_scatter32(P, lane);
+        if constexpr (C::kXp) sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_column_sum(P, xp, lane);
+        else sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_reduce_scatter32(P, lane);
       }
       if (!ok) break;
       fence_proxy_async_smem();
