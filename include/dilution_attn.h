@@ -302,8 +302,10 @@ int dilution_attn_debug_decode_stall(const void *q_new, const void *k_new, const
  *
  * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's
  * kernels for a problem of BH = B*H heads and T tokens.  kernel = 0 (row
- * statistics, 128-row query tiles), 1 (demand sweep at d = 64: 128-row query
- * tiles, 384-key spans) or 2 (demand sweep at d = 128: 256-key spans).  For each CTA index c (in launch order), writes 4 int32 to
+ * statistics at d = 64: pairs of 128-row query tiles, heads in groups of
+ * about 96 MB of Q and K), 1 (demand sweep at d = 64: 128-row query tiles,
+ * 384-key spans), 2 (demand sweep at d = 128: 256-key spans) or 3 (row
+ * statistics at d = 128).  For each CTA index c (in launch order), writes 4 int32 to
  * out[4c..4c+3]: head index, first query tile, number of query tiles (row
  * stats: the query tiles it owns; sweep: the query tiles it walks), first key
  * (sweep) or 0.  Returns the number of CTAs; if cap (in

@@ -141,13 +141,38 @@ struct TileWork {
   int bh, q_tile0, n_q_tiles, key0;
 };
 
-// Row statistics: one CTA per pair of query tiles (2 x 128 rows).
+// Row statistics: one CTA per pair of query tiles (2 x 128 rows), each
+// streaming its head's key tiles from the first to its diagonal.  Heads are
+// taken in groups whose Q and K (Tp x d x 2 B each per head) together stay
+// near 96 MB, so that the CTAs in flight share their heads' key tiles in L2
+// instead of re-reading them from DRAM; inside a group the pairs with the
+// most keys launch first, and a smaller remainder group goes first (as in the
+// sweep below, so that its long pairs do not run alone at the end).
+constexpr int64_t kRsGroupBytes = 96ll << 20;
 DA_HD int rowstats_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / (2 * kTile)); }
-DA_HD TileWork rowstats_work(int cta, int BH, int64_t T) {
+DA_HD int rowstats_head_group(int BH, int64_t T, int d) {
+  int64_t hg = kRsGroupBytes / (t_pad(T) * d * 4);
+  if (hg < 1) hg = 1;
+  if (hg > BH) hg = BH;
+  return (int)hg;
+}
+DA_HD TileWork rowstats_work(int cta, int BH, int64_t T, int d) {
   const int npairs = (int)(t_pad(T) / (2 * kTile));
+  const int hg = rowstats_head_group(BH, T, d);
+  const int ngroups = (BH + hg - 1) / hg;
+  const int first = BH - (ngroups - 1) * hg;       // heads in group 0 (1 .. hg)
+  int h0, ng;
+  if (cta < first * npairs) {
+    h0 = 0;
+    ng = first;
+  } else {
+    h0 = first + (cta - first * npairs) / (hg * npairs) * hg;
+    ng = hg;
+  }
+  const int r = cta - h0 * npairs;
   TileWork w;
-  w.bh = cta % BH;
-  const int pair = npairs - 1 - cta / BH;   // the last pair sees the most keys
+  w.bh = h0 + r % ng;
+  const int pair = npairs - 1 - r / ng;   // the last pair sees the most keys
   w.q_tile0 = 2 * pair;
   w.n_q_tiles = 2;
   w.key0 = 0;

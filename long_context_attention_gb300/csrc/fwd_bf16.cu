@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kRsThreads, RsCfg<D>::kCtasPerSm)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const TileWork w = rowstats_work(blockIdx.x, BH, T);
+  const TileWork w = rowstats_work(blockIdx.x, BH, T, D);
   const int n_kt = w.q_tile0 + 2;   // key tiles 0 .. last query tile
   const float c2 = bf16_c2(hs, w.bh, status);
 

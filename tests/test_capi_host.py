@@ -30,13 +30,23 @@ def test_status_strings(lib):
     assert b.dilution_attn_version() >= 100
 
 
-def _sched_rowstats(BH, T):
+def _groups(BH, hg):
+    # group sizes: the remainder (BH mod hg, if any) first, then full groups
+    sizes = ([BH % hg] if BH % hg else []) + [hg] * (BH // hg)
+    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(int)
+    return zip(starts, sizes)
+
+
+def _sched_rowstats(BH, T, d=64):
+    # pairs of 128-row query tiles; heads grouped so their Q and K total ~96 MB
     Tp = -(-T // 256) * 256
     npairs = Tp // 256
+    hg = min(BH, max(1, (96 << 20) // (Tp * d * 4)))
     rows = []
-    for c in range(BH * npairs):
-        pair = npairs - 1 - c // BH
-        rows.append((c % BH, 2 * pair, 2, 0))
+    for h0, n in _groups(BH, hg):
+        for pair in range(npairs - 1, -1, -1):
+            for bh in range(h0, h0 + n):
+                rows.append((bh, 2 * pair, 2, 0))
     return np.array(rows, dtype=np.int32).reshape(-1, 4)
 
 
@@ -47,11 +57,8 @@ def _sched_sweep(BH, T, d=64):
     Tp = -(-T // 256) * 256
     nqt, nspan = Tp // 128, -(-Tp // span_keys)
     hg = min(BH, max(1, (64 << 20) // (Tp * (d + 4) * 4)))
-    # group sizes: the remainder (BH mod hg, if any) first, then full groups
-    sizes = ([BH % hg] if BH % hg else []) + [hg] * (BH // hg)
-    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]]).astype(int)
     rows = []
-    for h0, n in zip(starts, sizes):
+    for h0, n in _groups(BH, hg):
         heads = list(range(h0, h0 + n))
         for span in range(nspan):
             for bh in heads:
@@ -65,6 +72,7 @@ def test_tile_schedules_bit_exact(lib, BH, T):
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 0), _sched_rowstats(BH, T))
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 1), _sched_sweep(BH, T))
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 2), _sched_sweep(BH, T, 128))
+    assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 3), _sched_rowstats(BH, T, 128))
 
 
 @pytest.mark.parametrize("kernel,tiles_per_span", [(1, 3), (2, 2)])
@@ -83,9 +91,10 @@ def test_tile_schedules_cover_triangle_once(kernel, tiles_per_span):
     want = {(bh, kt, qt) for bh in range(BH) for qt in range(Tp // 128) for kt in range(Tp // 128)
             if kt * 128 <= qt * 128 + 127}
     assert set(seen) == want and all(v == 1 for v in seen.values())
-    rs = b.dilution_attn_debug_tile_schedule(BH, T, 0)
-    tiles = sorted((int(r[0]), int(r[1]) + i) for r in rs for i in range(r[2]))
-    assert tiles == sorted((bh, qt) for bh in range(BH) for qt in range(Tp // 128))
+    for k in (0, 3):
+        rs = b.dilution_attn_debug_tile_schedule(BH, T, k)
+        tiles = sorted((int(r[0]), int(r[1]) + i) for r in rs for i in range(r[2]))
+        assert tiles == sorted((bh, qt) for bh in range(BH) for qt in range(Tp // 128))
 
 
 @pytest.mark.parametrize("T,qt,kt", [(256, 0, 0), (256, 1, 0), (200, 1, 1), (130, 1, 1), (1000, 3, 5), (5, 0, 0)])
