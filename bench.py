@@ -121,9 +121,11 @@ def sources_hash(sources=None):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(profile=None, sources=None):
+def profiled_traffic(profile=None, sources=None, workload=None):
     """DRAM bytes per launch (per step for the decode) from a committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+    summary, if it was taken on the current kernel source and on this
+    workload (its `profile_workload` line, e.g. "fwd_bf16_t16384 B=4 H=12
+    T=16384 d=64"), else None."""
     try:
         text = open(profile or SWEEP_PROFILE).read()
     except OSError:
@@ -135,6 +137,8 @@ def profiled_traffic(profile=None, sources=None):
             key, _, val = line.partition(":")
             vals[key.strip().strip("`")] = val.strip().strip("`")
     if vals.get("kernel_source_hash") != sources_hash(sources):
+        return None
+    if workload is not None and vals.get("profile_workload") != workload:
         return None
     try:
         return float(vals["traffic_bytes_per_launch_full_size"])
@@ -416,7 +420,8 @@ def run_decode(torch, b, inputs, dev, warmup, peaks, ctx=None, n_steps=None):
                  "ms_per_step": ms / steps, "tokens_per_s": B * steps / (ms * 1e-3),
                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": gbs / peaks["hbm_gbs"],
-                              "traffic": profiled_traffic(DECODE_PROFILE, DECODE_SOURCES),
+                              "traffic": profiled_traffic(DECODE_PROFILE, DECODE_SOURCES,
+                                                          f"{w.name} B={B} H={H} n_ctx={N} d={d}"),
                               "bytes_per_step": algo_bytes / steps},
                  "gpu_launches": 3 * steps}
 
@@ -560,7 +565,8 @@ def run_ours(args):
             "pct_of_bf16_peak": 100.0 * value / world / peak_t,
             "kernels_ms": kern_ms,
             "roofline": {"bound": "tensor", "kernel": "sweep_kernel", "achieved": sweep_tf, "peak": peak_t,
-                         "unit": "TFLOP/s", "frac": sweep_tf / peak_t, "traffic": profiled_traffic(),
+                         "unit": "TFLOP/s", "frac": sweep_tf / peak_t,
+                         "traffic": profiled_traffic(workload=f"{w.name} B={B} H={H} T={T} d={d}"),
                          "peak_source": f"{peaks_kind} {'sustained' if timed_s > 1.0 else 'burst'} bf16",
                          "rowstats_achieved": rs_tf, "rowstats_frac": rs_tf / peak_t},
             "sfu": sfu_report(B, H, T, kern_ms, torch.cuda.get_device_properties(dev).multi_processor_count,

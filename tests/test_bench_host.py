@@ -50,3 +50,15 @@ def test_traffic_figure_only_for_the_profiled_source(tmp_path):
     assert bench.profiled_traffic(str(prof), [rel]) is None
     assert bench.profiled_traffic(str(tmp_path / "missing.md"), [rel]) is None
 
+
+def test_traffic_figure_only_for_the_profiled_workload(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    rel = os.path.relpath(src, bench.ROOT)
+    prof = tmp_path / "p.md"
+    prof.write_text("kernel_source_hash: `%s`\nprofile_workload: `fwd_x B=4 H=12 T=16384 d=64`\n\n"
+                    "traffic_bytes_per_launch_full_size: `12345`\n" % bench.sources_hash([rel]))
+    assert bench.profiled_traffic(str(prof), [rel], "fwd_x B=4 H=12 T=16384 d=64") == 12345.0
+    assert bench.profiled_traffic(str(prof), [rel], "fwd_x B=2 H=12 T=16384 d=64") is None   # another batch
+    assert bench.profiled_traffic(str(prof), [rel], "fwd_y B=4 H=12 T=16384 d=128") is None
+
