@@ -246,8 +246,9 @@ int dilution_attn_decode_step_ex(const void *q_new, const void *k_new, const voi
  *   - All calls share the array and it keeps the last call's contents (the
  *     status word is cleared at the start of each call): calls that overlap on
  *     the GPU race with each other, so issue them on one stream or order them.
- *   - dilution_attn_get_error cannot reach the array's status word; timeouts
- *     of this entry point are not reported.
+ *   - Errors found on the device (a bounded wait that ran out, an invalid
+ *     per-head scale) land in the array's status word: read and clear it with
+ *     dilution_attn_decode_noalloc_get_error.
  * ---------------------------------------------------------------------- */
 int dilution_attn_decode_step_noalloc(const void *q_new, const void *k_new, const void *v_new,
                                       void *k_cache, void *v_cache, float *demand,
@@ -257,6 +258,13 @@ int dilution_attn_decode_step_noalloc(const void *q_new, const void *k_new, cons
 
 /* Size in bytes of the fixed scratch array of dilution_attn_decode_step_noalloc. */
 size_t dilution_attn_decode_noalloc_scratch_bytes(void);
+
+/* Synchronises `stream` and returns the status word of the fixed array on the
+ * current device (DA_OK, or the first error a kernel of an earlier no-alloc
+ * call recorded, e.g. DA_ERR_TIMEOUT), clearing it; DA_ERR_CUDA if the array
+ * cannot be reached.  Same semantics as dilution_attn_get_error on a
+ * workspace. */
+int dilution_attn_decode_noalloc_get_error(void *stream);
 
 /* ------------------------------------------------------------------------
  * Synchronises `stream`, reads the status word that kernels of the last call

@@ -56,6 +56,7 @@ _SIGNATURES = {
     "dilution_attn_decode_step_noalloc": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                           [_c_float, _c_float, _c_int, _c_void_p]),
     "dilution_attn_decode_noalloc_scratch_bytes": (_c_size_t, []),
+    "dilution_attn_decode_noalloc_get_error": (_c_int, [_c_void_p]),
     "dilution_attn_debug_decode_stall": (_c_int, [_c_void_p] * 6 + [_c_int, _c_int, _c_void_p] + [_c_int] * 3 +
                                          [_c_float, _c_float, _c_int, _c_void_p, _c_size_t, _c_void_p, _c_int, _c_int,
                                           ctypes.c_longlong]),
@@ -376,6 +377,12 @@ def dilution_attn_decode_step_noalloc(q_new, k_new, v_new, k_cache, v_cache, dem
 
 def dilution_attn_decode_noalloc_scratch_bytes() -> int:
     return int(load().dilution_attn_decode_noalloc_scratch_bytes())
+
+
+def dilution_attn_decode_noalloc_get_error(stream=None) -> int:
+    """Status of the no-alloc decode step's fixed array on the current
+    device (synchronises the stream, then reads and clears the word)."""
+    return int(load().dilution_attn_decode_noalloc_get_error(_stream_handle(stream)))
 
 
 def dilution_attn_debug_decode_stall(q_new, k_new, v_new, k_cache, v_cache, demand, n_ctx: int, out=None, *,

@@ -492,3 +492,12 @@ extern "C" int dilution_attn_decode_step_noalloc(const void *q_new, const void *
 }
 
 extern "C" size_t dilution_attn_decode_noalloc_scratch_bytes(void) { return da::kNoAllocScratchBytes; }
+
+// The status word of the fixed array (its first word, as in a workspace):
+// read and cleared like dilution_attn_get_error's.
+extern "C" int dilution_attn_decode_noalloc_get_error(void *stream) {
+  void *scratch = nullptr;
+  const int st = da::noalloc_scratch(&scratch);
+  if (st != DA_OK) return st;
+  return dilution_attn_get_error(scratch, stream);
+}

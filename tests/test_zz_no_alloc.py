@@ -58,6 +58,8 @@ def test_noalloc_matches_workspace_decode_on_consecutive_calls():
         assert np.abs(host64(out) - host64(ref)).max() <= BF16_OUT_ABS
         rd, nd = host64(dem[:, :, :n + 1]), host64(dem2[:, :, :n + 1])
         assert np.all(np.abs(nd - rd) <= 1e-5 * np.maximum(rd, 1.0) + 1e-6)
+        # the fixed array's status word: no error recorded, and reading it clears nothing else
+        assert b.dilution_attn_decode_noalloc_get_error() == b.DA_OK
         assert torch.equal(kc2[:, :, n], kn) and torch.equal(vc2[:, :, n], vn)
 
 
