@@ -68,6 +68,7 @@ __all__ = [
     "dilution_decode_step",
     "dilution_backward_head",
     "dilution_backward",
+    "dilution_backward_rowblocked_head",
 ]
 
 
@@ -329,3 +330,82 @@ def dilution_backward(q, k, v, dout, tau=1.0, eps: float = 1e-6, earlier_only: b
             dq[b, h], dk[b, h], dv[b, h] = dilution_backward_head(q[b, h], k[b, h], v[b, h], dout[b, h],
                                                                   float(taus[b, h]), eps, earlier_only)
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Backward, one head, row-blocked (for T too large for T x T matrices)
+# ---------------------------------------------------------------------------
+def dilution_backward_rowblocked_head(q, k, v, dout, tau: float = 1.0, eps: float = 1e-6, block: int = 1024,
+                                      earlier_only: bool = False):
+    """Same gradients as ``dilution_backward_head``, with O(block * T) memory.
+
+    The chain rule needs, for every (query j, key k), committed_jk (a sum over
+    the queries before j) and sum_{i > j} dC_ik (a sum over the queries
+    after j).  Blocks of queries are taken twice: ascending, as the row-blocked
+    forward, to get lse, R and out of every row and the column demand carried
+    into each block; then descending, carrying sum_i dC_ik of the blocks
+    already visited, to form dp, rho, ds and the three gradients block by
+    block.  Each entry goes through the same formulas as the full version.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(dout, np.float64)
+    T, d = q.shape
+    c = logit_scale(d, tau)
+    starts = list(range(0, T, block))
+    lse = np.empty(T)
+    R = np.empty(T)
+    out = np.empty((T, v.shape[1]))
+    carried_in = []                  # column demand before each block
+    carried = np.zeros(T)
+
+    def block_bids(i0, i1):
+        kk = i1
+        s = c * (q[i0:i1] @ k[:kk].T)
+        mask = np.arange(kk)[None, :] <= np.arange(i0, i1)[:, None]
+        return s, mask, kk
+
+    for i0 in starts:
+        i1 = min(T, i0 + block)
+        s, mask, kk = block_bids(i0, i1)
+        z = np.where(mask, s, -np.inf)
+        m = z.max(axis=1)
+        e = np.where(mask, np.exp(z - m[:, None]), 0.0)
+        l = e.sum(axis=1)
+        p = e / l[:, None]
+        lse[i0:i1] = m + np.log(l)
+        committed = carried[None, :kk] + _exclusive_cumsum_cols(p)
+        share = p / (committed + eps) if earlier_only else p / (committed + p + eps)
+        R[i0:i1] = share.sum(axis=1)
+        out[i0:i1] = (share / R[i0:i1, None]) @ v[:kk]
+        carried_in.append(carried.copy())
+        carried[:kk] += p.sum(axis=0)
+
+    dq = np.empty((T, d))
+    dk = np.zeros((T, d))
+    dv = np.zeros((T, v.shape[1]))
+    delta = np.sum(g * out, axis=1)
+    rev = np.zeros(T)                # sum of dC over the queries of the blocks after this one
+    for bi in range(len(starts) - 1, -1, -1):
+        i0 = starts[bi]
+        i1 = min(T, i0 + block)
+        s, mask, kk = block_bids(i0, i1)
+        p = np.where(mask, np.exp(np.where(mask, s, -np.inf) - lse[i0:i1, None]), 0.0)
+        C = carried_in[bi][None, :kk] + _exclusive_cumsum_cols(p)
+        Dn = C + eps if earlier_only else C + p + eps
+        share = p / Dn
+        A = share / R[i0:i1, None]
+        gb = g[i0:i1]
+        dv[:kk] += A.T @ gb
+        dA = gb @ v[:kk].T
+        dr = np.where(mask, (dA - delta[i0:i1, None]) / R[i0:i1, None], 0.0)
+        dC = -dr * p / Dn**2
+        direct = dr / Dn if earlier_only else dr * (C + eps) / Dn**2
+        dp = direct + _reverse_exclusive_cumsum_cols(dC) + rev[None, :kk]
+        ds = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+        dq[i0:i1] = c * (ds @ k[:kk])
+        dk[:kk] += c * (ds.T @ q[i0:i1])
+        rev[:kk] += dC.sum(axis=0)
+    return dq, dk, dv
+

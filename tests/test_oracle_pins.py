@@ -409,6 +409,22 @@ def test_backward_autograd():
     assert pin_backward_autograd() < 1e-10
 
 
+@pytest.mark.parametrize("T,block,earlier", [(50, 7, False), (64, 16, False), (33, 33, False), (40, 9, True),
+                                             (1, 4, False)])
+def test_backward_rowblocked_equals_full(T, block, earlier):
+    # the row-blocked backward (used at sizes where T x T matrices do not
+    # fit) against the full one, itself pinned by finite differences and
+    # autograd above: blocks that cut the causal triangle anywhere, a single
+    # block, the earlier-demand variant
+    rng = np.random.default_rng(100 + T)
+    q, k, v, g = (rng.normal(size=(T, 8)) * sc for sc in (1.5, 1.0, 1.0, 1.0))
+    eps = 1e-3 if earlier else 1e-6
+    full = od.dilution_backward_head(q, k, v, g, 1.1, eps, earlier_only=earlier)
+    blk = od.dilution_backward_rowblocked_head(q, k, v, g, 1.1, eps, block=block, earlier_only=earlier)
+    for a, b in zip(full, blk):
+        assert np.abs(a - b).max() <= 1e-12 * max(np.abs(a).max(), 1.0)
+
+
 # ---------------------------------------------------------------------------
 # Planted mistakes: each must make at least one pin fail.
 # ---------------------------------------------------------------------------
