@@ -66,6 +66,24 @@ def test_bf16_d128_t4096_sampled():
         check_head([g[bb, hh] for g in got], r, "bf16")
 
 
+def test_bf16_d128_config_t16384_full_heads():
+    """The head-dimension-128 benchmark workload at full size (4 x 12 x 16384
+    x 128), in the launch configuration the benchmark times: two whole heads
+    (the first of the first head group of the row statistics and the sweep,
+    and the last head) against the oracle row by row (out, lse2, row sums)
+    and key by key (demand); the unit-demand invariant on every head."""
+    w = inputs.WORKLOADS["fwd_bf16_t16384_d128"]
+    q, k, v = (x.to(DEV) for x in inputs.make_workload(w, device=DEV))
+    T = w.T
+    out, lse2, rs, dem = run_fwd(q, k, v, 1.0, w.eps)
+    assert torch.isfinite(out.float()).all()
+    err = (dem.double().sum(-1) - T).abs().max().item()
+    assert err <= 1e-5 * T, err
+    ref = oracle_forward(q, k, v, 1.0, w.eps, heads=[(0, 0), (3, 11)])
+    for (bb, hh), r in ref.items():
+        check_head([host64(x[bb, hh]) for x in (out, lse2, rs, dem)], r, "bf16")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n_ctx", [0, 4095, 5000])
 def test_decode_d128(dtype, n_ctx):

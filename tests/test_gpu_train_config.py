@@ -1,5 +1,6 @@
 """GPU parity of the backward at the training configuration, 4 x 12 x 16384 x
-64 bf16 (q, k, v and dout drawn as the benchmark draws them), in the
+64 bf16 (q, k, v and dout drawn as the benchmark draws them), and at the same
+shape with head dimension 128 (the benchmark's d = 128 training line), in the
 benchmark's launch configuration: the forward keeps its demand checkpoints in
 the backward's workspace (DA_FLAG_KEEP_FOR_BACKWARD) and the backward starts
 from them.
@@ -41,9 +42,10 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def test_bwd_training_config_t16384():
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_training_config_t16384(d):
     w = inputs.WORKLOADS["train_bf16_t16384"]
-    B, H, T, d = w.B, w.H, w.T, w.d
+    B, H, T = w.B, w.H, w.T
     q, k, v = inputs.make_qkv(B, H, T, d, q_std=w.q_std, pairs=w.pairs, seed=w.seed, dtype=w.dtype, device=DEV)
     g = inputs.make_like((B, H, T, d), seed=w.seed + 1, dtype=w.dtype, device=DEV)
     keep = b.DA_FLAG_KEEP_FOR_BACKWARD
@@ -69,7 +71,7 @@ def test_bwd_training_config_t16384():
     scale = qdq.abs().sum(-1) + kdk.abs().sum(-1)
     assert ((qdq.sum(-1) - kdk.sum(-1)).abs() <= 2.0 ** -5 * scale).all()
 
-    # two full heads against the oracle (about 10 s of CPU each)
+    # two full heads against the oracle (about 10 s of CPU each at d = 64)
     for bb, hh in [(0, 0), (B - 1, H - 1)]:
         ref = od.dilution_backward_rowblocked_head(host64(q[bb, hh]), host64(k[bb, hh]), host64(v[bb, hh]),
                                                    host64(g[bb, hh]), 1.0, w.eps)
