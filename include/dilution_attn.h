@@ -308,15 +308,18 @@ int dilution_attn_debug_decode_stall(const void *q_new, const void *k_new, const
 /* ------------------------------------------------------------------------
  * Host-only introspection of integer artefacts (no GPU needed).
  *
- * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's
- * kernels for a problem of BH = B*H heads and T tokens.  kernel = 0 (row
+ * dilution_attn_debug_tile_schedule: the work order of the bf16 forward's and
+ * backward's kernels for a problem of BH = B*H heads and T tokens.  kernel = 0 (row
  * statistics at d = 64: pairs of 128-row query tiles, heads in groups of
  * about 96 MB of Q and K), 1 (demand sweep at d = 64: 128-row query tiles,
- * 384-key spans), 2 (demand sweep at d = 128: 256-key spans) or 3 (row
- * statistics at d = 128).  For each CTA index c (in launch order), writes 4 int32 to
- * out[4c..4c+3]: head index, first query tile, number of query tiles (row
- * stats: the query tiles it owns; sweep: the query tiles it walks), first key
- * (sweep) or 0.  Returns the number of CTAs; if cap (in
+ * 384-key spans), 2 (demand sweep at d = 128: 256-key spans), 3 (row
+ * statistics at d = 128), or 4 + 2 * pass + (d == 128) for the tensor-core
+ * backward's passes (pass 0: reverse pass, 1: light dK pass, one CTA per
+ * 128-key tile; 2: dQ pass, one CTA per 128-query tile).  For each CTA index
+ * c (in launch order), writes 4 int32 to out[4c..4c+3]: head index, first
+ * query tile, number of query tiles (row stats: the query tiles it owns;
+ * sweep and key-tile passes: the query tiles it walks, from its diagonal; dQ
+ * pass: 1, its own), first key (sweep and key-tile passes) or 0.  Returns the number of CTAs; if cap (in
  * int32 elements) is too small, writes nothing and returns -(needed).
  *
  * dilution_attn_debug_tile_mask: the causal mask the kernels apply to the

@@ -248,34 +248,6 @@ __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[3
 // so the rest of dK needs rho but not the demand: L (bwdtc_dk2_kernel) forms
 // the bids p again (S' product, one exponential per pair) and accumulates
 // dK2 += (p rho)^T Q, then writes dK = c (dK1 - dK2).
-// Launch order of the three tensor-core passes: tile i = 0, 1, ... (the
-// CTAs with the most work first) for each head in turn, with heads in
-// groups whose two streamed [Tp x d] bf16 operands (R: Q and dout; L: Q and
-// K; the dQ pass: K and V) total about 96 MB, so that the tiles every CTA of a
-// head streams are shared in L2 by the CTAs in flight (DRAM reads at
-// 4x12x16384x64: R 3.25 -> 2.17 GB, L 0.91 -> 0.47 GB, dQ pass 5.57 -> 3.22
-// GB), with a smaller remainder group first so that its longest CTAs do not
-// run alone at the end.  R at d = 64 keeps the plain order: grouped, it
-// measured 0.15 ms slower (7.34 -> 7.49 ms), while the other passes and
-// d = 128 gain (backward 20.01 -> 19.55 ms at d = 128).
-// Returns (head, tile index i).
-__device__ __forceinline__ int2 bwd_order_grouped(int cta, int BH, int Tp, int d, int ntiles) {
-  long long hgl = (96ll << 20) / ((long long)Tp * d * 4);
-  const int hg = (int)(hgl < 1 ? 1 : (hgl > BH ? BH : hgl));
-  const int ngroups = (BH + hg - 1) / hg;
-  const int first = BH - (ngroups - 1) * hg;   // heads in group 0 (1 .. hg)
-  int h0, ng;
-  if (cta < first * ntiles) {
-    h0 = 0;
-    ng = first;
-  } else {
-    h0 = first + (cta - first * ntiles) / (hg * ntiles) * hg;
-    ng = hg;
-  }
-  const int r = cta - h0 * ntiles;
-  return make_int2(h0 + r % ng, r / ng);
-}
-
 constexpr int kModeRev = 0, kModeDk2 = 1;
 
 template <int MODE, int D>
@@ -393,9 +365,12 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // key tile kt = 0 walks the most half tiles
-  const int2 o = D == 128 ? bwd_order_grouped(blockIdx.x, BH, Tp, D, Tp / kTile)
-                          : make_int2(blockIdx.x % BH, blockIdx.x / BH);
+  // bwd_work's order; at d = 64 its plain order written out, which keeps
+  // this kernel's register allocation at 8 bytes of spills (20 through the
+  // general function)
+  const int2 o = D == 64 ? make_int2(blockIdx.x % BH, blockIdx.x / BH)
+                         : make_int2(bwd_work(blockIdx.x, BH, T, D, kBwdRev).bh,
+                                     bwd_work(blockIdx.x, BH, T, D, kBwdRev).q_tile0);
   const int bh = o.x, kt = o.y;
   const int NH = Tp / 64, hq0 = 2 * kt, n = NH - hq0, NC = Tp / 32;
   // as in the forward sweep: a scale of at least 1e-30 keeps -inf logits at -inf
@@ -687,8 +662,8 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeDk2, D>::kCtasPerSm)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int2 o = bwd_order_grouped(blockIdx.x, BH, Tp, D, Tp / kTile);   // key tile 0 walks the most
-  const int bh = o.x, kt = o.y;
+  const TileWork tw = bwd_work(blockIdx.x, BH, T, D, kBwdDk2);
+  const int bh = tw.bh, kt = tw.q_tile0;
   const int NH = Tp / 64, hq0 = 2 * kt, n = NH - hq0;
   const float c2 = fmaxf(head_c2(hs, bh, nullptr), 1e-30f);
 
@@ -935,8 +910,8 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int NQT = Tp / kTile, NC = Tp / 32;
-  const int2 o = bwd_order_grouped(blockIdx.x, BH, Tp, D, NQT);
-  const int bh = o.x, qt = NQT - 1 - o.y;                            // the most key tiles first
+  const TileWork tw = bwd_work(blockIdx.x, BH, T, D, kBwdDq);
+  const int bh = tw.bh, qt = tw.q_tile0;
   const int n = qt + 1;                                              // key tiles 0 .. qt
   const float c2 = fmaxf(head_c2(hs, bh, nullptr), 1e-30f);
 

@@ -302,16 +302,20 @@ int dilution_attn_debug_last_timeout(void *workspace, int32_t *out) {
 }
 
 int dilution_attn_debug_tile_schedule(int BH, int T, int kernel, int32_t *out, size_t cap) {
-  if (BH < 0 || T < 0 || kernel < 0 || kernel > 3) return -1;
+  if (BH < 0 || T < 0 || kernel < 0 || kernel > 9) return -1;
   if (BH == 0 || T == 0) return 0;
   // kernel 0: row statistics at d = 64, 1: sweep at d = 64, 2: sweep at
-  // d = 128, 3: row statistics at d = 128
-  const bool rs = kernel == 0 || kernel == 3;
-  const int d = kernel >= 2 ? 128 : 64;
-  const int n = rs ? rowstats_num_ctas(BH, T) : sweep_num_ctas(BH, T, d);
+  // d = 128, 3: row statistics at d = 128; 4 + 2 pass + (d == 128): the
+  // backward's reverse pass (pass 0), light dK pass (1) and dQ pass (2)
+  const bool rs = kernel == 0 || kernel == 3, bwd = kernel >= 4;
+  const int d = bwd ? ((kernel - 4) % 2 ? 128 : 64) : (kernel == 2 || kernel == 3 ? 128 : 64);
+  const int pass = bwd ? (kernel - 4) / 2 : 0;
+  const int n = bwd ? bwd_num_ctas(BH, T) : rs ? rowstats_num_ctas(BH, T) : sweep_num_ctas(BH, T, d);
   if (out == nullptr || cap < (size_t)n * 4) return -n;
   for (int c = 0; c < n; ++c) {
-    const TileWork w = rs ? rowstats_work(c, BH, T, d) : sweep_work(c, BH, T, d);
+    const TileWork w = bwd  ? bwd_work(c, BH, T, d, pass)
+                       : rs ? rowstats_work(c, BH, T, d)
+                            : sweep_work(c, BH, T, d);
     out[4 * c + 0] = w.bh;
     out[4 * c + 1] = w.q_tile0;
     out[4 * c + 2] = w.n_q_tiles;

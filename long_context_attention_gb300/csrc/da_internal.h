@@ -141,6 +141,27 @@ struct TileWork {
   int bh, q_tile0, n_q_tiles, key0;
 };
 
+// Launch order shared by the kernels below: heads in groups of hg (a smaller
+// remainder group first, so that its longest CTAs do not run alone at the
+// end), and inside a group work item i = 0, 1, ... for each head of the group
+// in turn (item 0 is the longest).  Returns the head in bh and the item in i.
+DA_HD void grouped_order(int cta, int BH, int hg, int items_per_head, int &bh, int &i) {
+  const int ngroups = (BH + hg - 1) / hg;
+  const int first = BH - (ngroups - 1) * hg;       // heads in group 0 (1 .. hg)
+  int h0, ng;
+  if (cta < first * items_per_head) {
+    h0 = 0;
+    ng = first;
+  } else {
+    h0 = first + (cta - first * items_per_head) / (hg * items_per_head) * hg;
+    ng = hg;
+  }
+  const int r = cta - h0 * items_per_head;
+  bh = h0 + r % ng;
+  i = r / ng;
+}
+DA_HD int clamp_group(int64_t hg, int BH) { return (int)(hg < 1 ? 1 : (hg > BH ? BH : hg)); }
+
 // Row statistics: one CTA per pair of query tiles (2 x 128 rows), each
 // streaming its head's key tiles from the first to its diagonal.  Heads are
 // taken in groups whose Q and K (Tp x d x 2 B each per head) together stay
@@ -151,28 +172,15 @@ struct TileWork {
 constexpr int64_t kRsGroupBytes = 96ll << 20;
 DA_HD int rowstats_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / (2 * kTile)); }
 DA_HD int rowstats_head_group(int BH, int64_t T, int d) {
-  int64_t hg = kRsGroupBytes / (t_pad(T) * d * 4);
-  if (hg < 1) hg = 1;
-  if (hg > BH) hg = BH;
-  return (int)hg;
+  return clamp_group(kRsGroupBytes / (t_pad(T) * d * 4), BH);
 }
 DA_HD TileWork rowstats_work(int cta, int BH, int64_t T, int d) {
   const int npairs = (int)(t_pad(T) / (2 * kTile));
-  const int hg = rowstats_head_group(BH, T, d);
-  const int ngroups = (BH + hg - 1) / hg;
-  const int first = BH - (ngroups - 1) * hg;       // heads in group 0 (1 .. hg)
-  int h0, ng;
-  if (cta < first * npairs) {
-    h0 = 0;
-    ng = first;
-  } else {
-    h0 = first + (cta - first * npairs) / (hg * npairs) * hg;
-    ng = hg;
-  }
-  const int r = cta - h0 * npairs;
+  int bh, i;
+  grouped_order(cta, BH, rowstats_head_group(BH, T, d), npairs, bh, i);
   TileWork w;
-  w.bh = h0 + r % ng;
-  const int pair = npairs - 1 - r / ng;   // the last pair sees the most keys
+  w.bh = bh;
+  const int pair = npairs - 1 - i;   // the last pair sees the most keys
   w.q_tile0 = 2 * pair;
   w.n_q_tiles = 2;
   w.key0 = 0;
@@ -196,34 +204,58 @@ DA_HD int sweep_num_spans(int64_t T, int d) {
   return (int)((t_pad(T) + sweep_span_keys(d) - 1) / sweep_span_keys(d));
 }
 DA_HD int sweep_head_group(int BH, int64_t T, int d) {
-  const int64_t per_head = t_pad(T) * acc_stride(d) * 4;
-  int64_t hg = kAccGroupBytes / per_head;
-  if (hg < 1) hg = 1;
-  if (hg > BH) hg = BH;
-  return (int)hg;
+  return clamp_group(kAccGroupBytes / (t_pad(T) * acc_stride(d) * 4), BH);
 }
 DA_HD int sweep_num_ctas(int BH, int64_t T, int d) { return BH * sweep_num_spans(T, d); }
 DA_HD TileWork sweep_work(int cta, int BH, int64_t T, int d) {
   const int nqt = (int)(t_pad(T) / kSweepQTile);
-  const int nspan = sweep_num_spans(T, d);
-  const int hg = sweep_head_group(BH, T, d);
-  const int ngroups = (BH + hg - 1) / hg;
-  const int first = BH - (ngroups - 1) * hg;       // heads in group 0 (1 .. hg)
-  int h0, ng;
-  if (cta < first * nspan) {
-    h0 = 0;
-    ng = first;
-  } else {
-    h0 = first + (cta - first * nspan) / (hg * nspan) * hg;
-    ng = hg;
-  }
-  const int r = cta - h0 * nspan;
+  int bh, span;   // span 0 walks every query tile
+  grouped_order(cta, BH, sweep_head_group(BH, T, d), sweep_num_spans(T, d), bh, span);
   TileWork w;
-  w.bh = h0 + r % ng;
-  const int span = r / ng;                   // span 0 walks every query tile
+  w.bh = bh;
   w.key0 = span * sweep_span_keys(d);
   w.q_tile0 = w.key0 / kSweepQTile;
   w.n_q_tiles = nqt - w.q_tile0;
+  return w;
+}
+
+// Tensor-core backward: the reverse pass (R) and the light dK pass (L) take
+// one CTA per (head, 128-key tile), walking the query half tiles from the
+// last one back to the key tile's diagonal (key tile 0 walks the most); the
+// dQ pass one CTA per (head, 128-query tile), walking key tiles 0 .. its
+// diagonal (the last query tile walks the most).  Heads in groups whose two
+// streamed [Tp x d] bf16 operands (R: Q and dout; L: Q and K; dQ pass: K and
+// V) total about 96 MB, so that the tiles every CTA of a head streams are
+// shared in L2 by the CTAs in flight; R at d = 64 keeps the plain order
+// (every head's key tile 0, then every head's key tile 1, ...), which
+// measured faster there.
+//   R, L:    key0 = first key, q_tile0 = the diagonal query tile,
+//            n_q_tiles = query tiles walked;
+//   dQ pass: q_tile0 = its query tile, n_q_tiles = 1, key0 = 0.
+constexpr int kBwdRev = 0, kBwdDk2 = 1, kBwdDq = 2;
+constexpr int64_t kBwdGroupBytes = 96ll << 20;
+DA_HD int bwd_num_ctas(int BH, int64_t T) { return BH * (int)(t_pad(T) / kTile); }
+DA_HD int bwd_head_group(int BH, int64_t T, int d) { return clamp_group(kBwdGroupBytes / (t_pad(T) * d * 4), BH); }
+DA_HD TileWork bwd_work(int cta, int BH, int64_t T, int d, int pass) {
+  const int nt = (int)(t_pad(T) / kTile);
+  int bh, i;
+  if (pass == kBwdRev && d == 64) {
+    bh = cta % BH;
+    i = cta / BH;
+  } else {
+    grouped_order(cta, BH, bwd_head_group(BH, T, d), nt, bh, i);
+  }
+  TileWork w;
+  w.bh = bh;
+  if (pass == kBwdDq) {
+    w.q_tile0 = nt - 1 - i;
+    w.n_q_tiles = 1;
+    w.key0 = 0;
+  } else {
+    w.key0 = i * kTile;
+    w.q_tile0 = i;
+    w.n_q_tiles = nt - i;
+  }
   return w;
 }
 

@@ -67,12 +67,55 @@ def _sched_sweep(BH, T, d=64):
     return np.array(rows, dtype=np.int32).reshape(-1, 4)
 
 
-@pytest.mark.parametrize("BH,T", [(1, 1), (2, 255), (3, 256), (5, 257), (48, 16384), (12, 131072)])
+def _sched_bwd(BH, T, d, pass_):
+    # one CTA per (head, 128-key tile) for the reverse (0) and light dK (1)
+    # passes, per (head, 128-query tile) for the dQ pass (2); heads grouped
+    # so their two streamed [Tp x d] bf16 operands total ~96 MB, except the
+    # reverse pass at d = 64 (every head's tile 0, then tile 1, ...)
+    Tp = -(-T // 256) * 256
+    nt = Tp // 128
+    hg = min(BH, max(1, (96 << 20) // (Tp * d * 4)))
+    if pass_ == 0 and d == 64:
+        order = [(c % BH, c // BH) for c in range(BH * nt)]
+    else:
+        order = [(bh, i) for h0, n in _groups(BH, hg) for i in range(nt) for bh in range(h0, h0 + n)]
+    rows = [(bh, nt - 1 - i, 1, 0) if pass_ == 2 else (bh, i, nt - i, 128 * i) for bh, i in order]
+    return np.array(rows, dtype=np.int32).reshape(-1, 4)
+
+
+# (5, 131072) and (7, 65536): head groups that do not divide the heads (the
+# remainder group first) in the row statistics and the backward
+@pytest.mark.parametrize("BH,T", [(1, 1), (2, 255), (3, 256), (5, 257), (48, 16384), (12, 131072), (5, 131072),
+                                  (7, 65536)])
 def test_tile_schedules_bit_exact(lib, BH, T):
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 0), _sched_rowstats(BH, T))
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 1), _sched_sweep(BH, T))
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 2), _sched_sweep(BH, T, 128))
     assert np.array_equal(b.dilution_attn_debug_tile_schedule(BH, T, 3), _sched_rowstats(BH, T, 128))
+    for pass_ in range(3):
+        for d in (64, 128):
+            got = b.dilution_attn_debug_tile_schedule(BH, T, 4 + 2 * pass_ + (d == 128))
+            assert np.array_equal(got, _sched_bwd(BH, T, d, pass_)), (pass_, d)
+
+
+@pytest.mark.parametrize("BH,T", [(3, 1000), (5, 131072), (7, 65536)])
+def test_backward_and_rowstats_schedules_cover_once(BH, T):
+    # every (head, key tile) once in the key-tile passes, every (head, query
+    # tile) once in the dQ pass and the row statistics, at both head sizes
+    Tp = -(-T // 256) * 256
+    nt = Tp // 128
+    everything = sorted((bh, t) for bh in range(BH) for t in range(nt))
+    for d in (64, 128):
+        for pass_ in range(3):
+            s = b.dilution_attn_debug_tile_schedule(BH, T, 4 + 2 * pass_ + (d == 128))
+            if pass_ == 2:
+                assert sorted((int(r[0]), int(r[1])) for r in s) == everything
+                assert all(int(r[2]) == 1 for r in s)
+            else:
+                assert sorted((int(r[0]), int(r[3]) // 128) for r in s) == everything
+                assert all(int(r[1]) == int(r[3]) // 128 and int(r[1]) + int(r[2]) == nt for r in s)
+        rs = b.dilution_attn_debug_tile_schedule(BH, T, 0 if d == 64 else 3)
+        assert sorted((int(r[0]), int(r[1]) + i) for r in rs for i in range(r[2])) == everything
 
 
 @pytest.mark.parametrize("kernel,tiles_per_span", [(1, 3), (2, 2)])
