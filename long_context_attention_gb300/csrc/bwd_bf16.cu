@@ -36,7 +36,9 @@
 // S and dA' are formed 64 queries at a time (N = 64) so two CTAs fit an SM
 // at d = 64 (R at d = 128: one, its tiles and N = 128 accumulators take the
 // SM); -lse2 / c2 and -delta ride in a fifth K step of their products (the
-// extension operands of the forward sweep).  Every wait is bounded.
+// extension operands of the forward sweep).  The passes' launch orders are
+// bwd_work's (da_internal.h): heads in groups whose streamed tiles stay in
+// L2.  Every wait is bounded.
 #include "da_internal.h"
 #include "da_ptx.cuh"
 
