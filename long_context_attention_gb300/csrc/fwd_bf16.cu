@@ -104,6 +104,10 @@ struct RowStat {
   // 32 consecutive keys (columns col0 ..) of the row; DIAG masks key > query.
   template <bool DIAG>
   __device__ __forceinline__ void chunk(float (&s)[32], int col0, int row, float c2) {
+    // every key of the chunk after every row of the warp (6 of the 16
+    // warp-chunks of a diagonal tile): nothing to add, exactly as if the
+    // masked chunk were summed
+    if (DIAG && __all_sync(0xffffffffu, col0 > row)) return;
     if (DIAG) {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
