@@ -242,33 +242,49 @@ def blas_threads():
 
 # ------------------------------------------------------------------ CPU oracle sample
 def oracle_sample(q, k, v, rows, tau=1.0, eps=1e-6):
-    """Time the float64 oracle on the first ``rows`` queries of one head."""
+    """Time the float64 oracle on the first ``rows`` queries of one head;
+    returns (algorithmic FLOP, seconds, the oracle's output rows)."""
     import oracle.dilution as od
     t0 = time.perf_counter()
-    od.dilution_forward_rowblocked_head(q, k, v, tau, eps, rows=rows)
+    r = od.dilution_forward_rowblocked_head(q, k, v, tau, eps, rows=rows)
     dt = time.perf_counter() - t0
     d = q.shape[1]
     flops = 3 * d * rows * (rows + 1)    # causal pairs of the first `rows` queries, 3 x 2d each
-    return flops, dt
+    return flops, dt, r["out"]
 
 
-def cpu_baseline(heads, seed=2):
+def cpu_baseline(heads, seed=2, gpu_forward=None):
     """The oracle on `heads` full heads (T = 16384) of the benchmark workload,
-    generated on the host with the same recipe (about 10-30 s of CPU work)."""
+    generated on the host with the same recipe (about 10-30 s of CPU work).
+
+    With ``gpu_forward`` (q, k, v host tensors -> out as float64 NumPy, run by
+    this library's kernels) the same heads also go through the GPU path and
+    the second return value reports the largest |out - oracle| against the
+    bf16 bound of 2e-2; else it is None."""
     import numpy as np
     from long_context_attention_gb300 import inputs
     w = inputs.WORKLOADS["fwd_bf16_t16384"]
     q, k, v = inputs.make_qkv(1, heads, w.T, w.d, q_std=w.q_std, pairs=w.pairs, seed=seed, dtype="bf16")
     tot_f, tot_t = 0, 0.0
+    ref = []
     for h in range(heads):
         qh, kh, vh = (x[0, h].double().numpy() for x in (q, k, v))
-        f, t = oracle_sample(qh, kh, vh, w.T)
+        f, t, o = oracle_sample(qh, kh, vh, w.T)
         tot_f += f
         tot_t += t
-    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+        ref.append(o)
+    base = {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"float64 NumPy oracle (row-blocked), {heads} full heads of 1 x 12 x 16384 x 64 with the "
                       f"workload's recipe ({tot_f / 1e9:.0f} GFLOP algorithmic, {tot_t:.1f} s)",
             "seconds": tot_t, "cpu_count": os.cpu_count(), "np": np.__version__}
+    if gpu_forward is None:
+        return base, None
+    got = gpu_forward(q, k, v)
+    err = max(float(np.abs(got[0, h] - ref[h]).max()) for h in range(heads))
+    parity = {"heads": heads, "rows_per_head": w.T, "shape": f"1 x {heads} x {w.T} x {w.d} bf16, the workload's recipe",
+              "max_abs_err_out": err, "tolerance": 2e-2, "ok": err <= 2e-2,
+              "against": "the float64 oracle's output on the same heads (the cpu_baseline sample)"}
+    return base, parity
 
 
 # ---------------------------------------------------------------------- reference arm
@@ -306,7 +322,7 @@ def run_reference(args):
         oracle_sample(*head(j), rows=min(1024, w.T))
     tot_f, tot_t = 0, 0.0
     for j in range(args.steps):
-        f, t = oracle_sample(*head(j), rows=w.T)
+        f, t, _ = oracle_sample(*head(j), rows=w.T)
         tot_f += f
         tot_t += t
     val = tot_f / tot_t / 1e12
@@ -647,7 +663,12 @@ def run_ours(args):
         line["decode"] = dec
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_heads)
+        def gpu_forward(qh, kh, vh):
+            o = b.dilution_attn_fwd(*(x.to(dev) for x in (qh, kh, vh)), tau=1.0, eps=w.eps)
+            torch.cuda.synchronize()
+            return o.double().cpu().numpy()
+
+        line["cpu_baseline"], line["parity"] = cpu_baseline(args.cpu_heads, gpu_forward=gpu_forward)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

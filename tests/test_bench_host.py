@@ -62,3 +62,26 @@ def test_traffic_figure_only_for_the_profiled_workload(tmp_path):
     assert bench.profiled_traffic(str(prof), [rel], "fwd_x B=2 H=12 T=16384 d=64") is None   # another batch
     assert bench.profiled_traffic(str(prof), [rel], "fwd_y B=4 H=12 T=16384 d=128") is None
 
+
+
+def test_cpu_baseline_reports_parity_of_a_gpu_forward(monkeypatch):
+    # the CPU-baseline leg compares a forward on its own sample with the
+    # oracle's output there (the oracle replaced here by a fast stand-in that
+    # returns zeros): a forward that returns the same passes, one that is off
+    # by 0.05 somewhere fails, none gives no parity entry
+    import numpy as np
+    monkeypatch.setattr(bench, "oracle_sample", lambda q, k, v, rows: (1, 1.0, np.zeros((rows, q.shape[1]))))
+
+    def same(q, k, v):
+        return np.zeros(tuple(q.shape))
+
+    def off(q, k, v):
+        o = same(q, k, v)
+        o[0, 1, 7, 3] += 0.05
+        return o
+
+    base, par = bench.cpu_baseline(2, gpu_forward=same)
+    assert base["kind"] == "oracle" and par["ok"] and par["max_abs_err_out"] == 0.0 and par["heads"] == 2
+    _, par = bench.cpu_baseline(2, gpu_forward=off)
+    assert not par["ok"] and abs(par["max_abs_err_out"] - 0.05) < 1e-12
+    assert bench.cpu_baseline(2)[1] is None
