@@ -45,6 +45,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+
 namespace da {
 
 namespace {
@@ -297,18 +298,28 @@ __device__ __forceinline__ void mma_over_d(uint32_t dt, uint64_t da, uint32_t ha
 // Sum over the warp's 32 keys (lanes) of X[i] for each query i by recursive
 // halving: in each round a lane keeps one half of its values (by one bit of
 // its lane index), sends the other half to the lane that differs in that bit
-// and adds what it receives; lane l ends with the sum for query l.  X is
-// clobbered.
+// and adds what it receives; lane l ends with the sum for query l.  The
+// kept and received values are added two at a time on the packed pipe
+// (backward 13.757 -> 13.742 ms at 4x12x16384x64).  X is clobbered.
 __device__ __forceinline__ float warp_reduce_scatter32(float (&X)[32], int lane) {
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
+  for (int off = 16; off >= 2; off >>= 1) {
     const bool up = (lane & off) != 0;
 #pragma unroll
-    for (int i = 0; i < off; ++i) {
-      const float send = up ? X[i] : X[i + off];
-      const float keep = up ? X[i + off] : X[i];
-      X[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    for (int i = 0; i < off; i += 2) {
+      const float s0 = up ? X[i] : X[i + off], s1 = up ? X[i + 1] : X[i + off + 1];
+      const float2 keep = make_float2(up ? X[i + off] : X[i], up ? X[i + off + 1] : X[i + 1]);
+      const float2 got = make_float2(__shfl_xor_sync(0xffffffffu, s0, off), __shfl_xor_sync(0xffffffffu, s1, off));
+      const float2 sum = fadd2(keep, got);
+      X[i] = sum.x;
+      X[i + 1] = sum.y;
     }
+  }
+  {
+    const bool up = (lane & 1) != 0;
+    const float send = up ? X[0] : X[1];
+    const float keep = up ? X[1] : X[0];
+    X[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
   }
   return X[0];
 }
@@ -911,7 +922,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int NQT = Tp / kTile, NC = Tp / 32;
+  const int NC = Tp / 32;
   const TileWork tw = bwd_work(blockIdx.x, BH, T, D, kBwdDq);
   const int bh = tw.bh, qt = tw.q_tile0;
   const int n = qt + 1;                                              // key tiles 0 .. qt
