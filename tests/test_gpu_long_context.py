@@ -187,3 +187,40 @@ def test_decode_ctx131072_heavy_tailed_demand():
             assert err <= BF16_OUT_ABS, (t, err)
         gd = host64(dem[hd])[:N + steps]
         assert np.all(np.abs(gd - D) <= 1e-5 * np.maximum(D, 1.0) + 1e-6)
+
+
+def test_prefill_t131072_per_head_tau():
+    """1 x 4 x 131072 with a different multiplier per head (the YaRN value for
+    s = 2, 4, 8, 16): at this length the row statistics take heads in groups
+    of 3 and the sweep one head at a time, so each CTA's head comes from the
+    grouped launch order and its multiplier from the per-head array.  Checked
+    against the oracle with each head's own multiplier: out, lse2 and row sums
+    of the first 2048 rows, lse2 of the last 128 rows, the last 128 keys'
+    demand, and the unit-demand invariant."""
+    B, H, T, d = 1, 4, 131072, 64
+    taus = [od.yarn_tau(s) for s in (2.0, 4.0, 8.0, 16.0)]
+    q, k, v = inputs.make_qkv(B, H, T, d, q_std=1.5, pairs=16, seed=701, dtype="bf16", device=DEV)
+    out = torch.empty_like(q)
+    lse2, rs, dem = (torch.empty(B, H, T, device=DEV) for _ in range(3))
+    ws = torch.empty(b.dilution_attn_fwd_workspace_size(B, H, T, d, b.DA_BF16), dtype=torch.uint8, device=DEV)
+    tau_bh = torch.tensor(taus, dtype=torch.float32, device=DEV)
+    b.dilution_attn_fwd_ex(q, k, v, out, lse2, rs, dem, tau_bh=tau_bh, eps=1e-6, workspace=ws)
+    assert b.dilution_attn_get_error(ws) == b.DA_OK
+    torch.cuda.synchronize()
+    err = (dem.double().sum(-1) - T).abs().max().item()
+    assert err <= 1e-4 * T, err            # fp32 demand totals at this length: see test_prefill_config_t131072
+    n = 2048
+    for hh in range(H):
+        tau = float(np.float32(taus[hh]))   # the multiplier as the kernels read it
+        qh, kh, vh = (host64(x[0, hh]) for x in (q, k, v))
+        r = od.dilution_forward_rowblocked_head(qh, kh, vh, tau, 1e-6, rows=n)
+        assert np.abs(host64(out[0, hh][:n]) - r["out"]).max() <= BF16_OUT_ABS
+        assert np.abs(host64(lse2[0, hh][:n]) - r["lse"] * LOG2E).max() <= 2e-3
+        assert np.abs(host64(rs[0, hh][:n]) / r["rowsum"] - 1).max() <= 2e-2
+        c = od.logit_scale(d, tau)
+        tail = np.arange(T - 128, T)
+        lse_t, p_t = _late_rows_exact(qh, kh, tail, c)
+        assert np.abs(host64(lse2[0, hh])[tail] - lse_t * LOG2E).max() <= 2e-3
+        d_tail = p_t[:, T - 128:].sum(0)
+        g_tail = host64(dem[0, hh])[T - 128:]
+        assert np.all(np.abs(g_tail - d_tail) <= DEM_REL * np.maximum(d_tail, 1) + DEM_ABS)
