@@ -51,6 +51,25 @@ namespace da {
 namespace {
 
 constexpr int kBtThreads = 192;                    // 4 demand warps, producer, MMA issuer
+
+// R at d = 64 re-splits its registers (setmaxnreg): warpgroup 0 (the key
+// warps) takes 216 per thread, warpgroup 1 (producer, issuer and two idle
+// warps that complete it) gives up to 40; launched at 128 per thread (two CTAs
+// of 256 threads per SM), the split uses exactly the block's registers.  (At
+// 168 for every warp the key warps spilled; backward 13.754 -> 13.711 ms.)
+template <int D>
+struct RevRegs {
+  static constexpr bool kSplit = D == 64;
+  static constexpr int kThreads = kSplit ? 256 : kBtThreads;
+  static constexpr int kLaunch = kSplit ? 128 : 0;
+  static constexpr int kKey = 216, kCtl = 40;
+  static constexpr int kNeeded = 128 * (kKey + kCtl);
+  static_assert(!kSplit || kNeeded <= kThreads * kLaunch, "register split exceeds the launch registers");
+};
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 // A tile of R rows x d bf16 is stored as d / 64 column halves of R rows x 64
 // (128-byte swizzled rows), R * 128 bytes each.
 constexpr uint32_t kH128 = kTile * 64 * 2;         // one half of a 128-row tile
@@ -347,7 +366,7 @@ __device__ __forceinline__ float warp_column_sum(const float (&X)[32], float *re
 }
 
 template <int D, bool EARLIER>
-__global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
+__global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
     bwdtc_rev_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmGh,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const float *__restrict__ nlse2, const float *__restrict__ delta,
@@ -406,8 +425,8 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  fill_ones_ext(sAExt, threadIdx.x, kBtThreads);
-  zero_smem(smem + C::kOffBExtS, 4 * kExt64, threadIdx.x, kBtThreads);   // both buffers of both rows
+  fill_ones_ext(sAExt, threadIdx.x, RevRegs<D>::kThreads);
+  zero_smem(smem + C::kOffBExtS, 4 * kExt64, threadIdx.x, RevRegs<D>::kThreads);   // both buffers of both rows
   fence_proxy_async_smem();
   if (warp == 5) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -419,103 +438,109 @@ __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeRev, D>::kCtasPerSm)
   const WaitCtx wc{abort_flag, status};
   auto half_of = [&](int u) { return NH - 1 - u; };
 
-  if (warp == 4) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      prefetch_tmap(&tmQh);
-      prefetch_tmap(&tmGh);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kTB);
-      load_tile_halves<D, kH128>(sK, &tmK, kv_full, kt * kTile, bh);
-      load_tile_halves<D, kH128>(sV, &tmV, kv_full, kt * kTile, bh);
-    }
-    int issued = 0;
-    for (int u = 0; u < n; ++u) {
-      const int b = u & 1, h = half_of(u);
-      // the half tile's per-query values are read before waiting for the
-      // buffer, so their global-memory latency overlaps that wait
-      float nl[2], de[2], ri[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const size_t idx = (size_t)bh * Tp + h * 64 + lane + 32 * j;
-        nl[j] = __ldg(nlse2 + idx);
-        de[j] = __ldg(delta + idx);
-        ri[j] = __ldg(rinv + idx);
-      }
-      if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
+  if (warp >= 4) {
+    // warpgroup 1 (producer, issuer, and at d = 64 two idle warps that
+    // complete it): one register re-split for all four warps
+    if constexpr (RevRegs<D>::kSplit) setmaxnreg_dec<RevRegs<D>::kCtl>();
+    if (warp == 4) {
+      // -------------------------------------------------------- producer
       if (lane == 0) {
-        mbar_arrive_expect_tx(&in_full[b], 2 * C::kHB);
-        load_tile_halves<D, kH64>(smem + C::kOffQh + b * C::kHB, &tmQh, &in_full[b], h * 64, bh);
-        load_tile_halves<D, kH64>(smem + C::kOffGh + b * C::kHB, &tmGh, &in_full[b], h * 64, bh);
+        prefetch_tmap(&tmQh);
+        prefetch_tmap(&tmGh);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        mbar_arrive_expect_tx(kv_full, 2 * C::kTB);
+        load_tile_halves<D, kH128>(sK, &tmK, kv_full, kt * kTile, bh);
+        load_tile_halves<D, kH128>(sV, &tmV, kv_full, kt * kTile, bh);
       }
-      ++issued;
+      int issued = 0;
+      for (int u = 0; u < n; ++u) {
+        const int b = u & 1, h = half_of(u);
+        // the half tile's per-query values are read before waiting for the
+        // buffer, so their global-memory latency overlaps that wait
+        float nl[2], de[2], ri[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int qq = lane + 32 * j;
-        put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, nl[j] / c2);
-        put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -de[j]);
-        sRinv[b * 64 + qq] = ri[j];
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&in_full[b]);
-    }
-    if (lane == 0 && *abort_flag) {
-      drain_wait_bt(kv_full, 0);
-      for (int u = (issued > 2 ? issued - 2 : 0); u < issued; ++u) drain_wait_bt(&in_full[u & 1], (u >> 1) & 1);
-    }
-  } else if (warp == 5) {
-    // -------------------------------------------------------- MMA issuer
-    // S'(u), dA'(u) into the slot, then the products of half tile u - 1:
-    // dV += A^T G and dK1 += u^T Q (A^T, u^T: K-major A operands, 16
-    // queries = 32 bytes per K step; G and Q of buffer bp as MN-major B, 16
-    // queries = 2 KB per K step, the two 64-column halves of d = 128 8 KB
-    // apart).
-    if (lane == 0) {
-      constexpr long long kStepKm = 2;                       // K-major: +32 bytes per K step
-      constexpr long long kStepMn = 128;                     // MN-major: +16 rows (2 KB) per K step
-      const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
-      const uint32_t idesc_acc = idesc_bf16(kTile, D, false, true);
-      const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
-      const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
-      bool ok = mbar_wait(kv_full, 0, wc);
-      if (ok) tc_fence_after();
-      for (int u = 0; ok && u <= n; ++u) {
-        if (u < n) {
-          const int b = u & 1;
-          if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(s_free, (u & 1) ^ 1, wc)) break;
-          tc_fence_after();
-          const uint64_t dQh = kdesc(smem + C::kOffQh + b * C::kHB, 0);
-          const uint64_t dGh = kdesc(smem + C::kOffGh + b * C::kHB, 0);
-          const uint64_t dBS = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtS + b * kExt64), 128, 256);
-          const uint64_t dBA = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtA + b * kExt64), 128, 256);
-          mma_over_d<D>(tmem, dK, kH128, dQh, kH64, idesc_s);
-          mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
-          mma_over_d<D>(tmem + 64, dV, kH128, dGh, kH64, idesc_s);
-          mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
-          mma_commit(s_full);
+        for (int j = 0; j < 2; ++j) {
+          const size_t idx = (size_t)bh * Tp + h * 64 + lane + 32 * j;
+          nl[j] = __ldg(nlse2 + idx);
+          de[j] = __ldg(delta + idx);
+          ri[j] = __ldg(rinv + idx);
         }
-        if (u >= 1) {
-          const int up = u - 1, bp = up & 1;
-          if (!mbar_wait(x_full, up & 1, wc)) break;
-          tc_fence_after();
-          const uint64_t dGmn = smem_desc(smem_u32(smem + C::kOffGh + bp * C::kHB), kH64, 1024);
-          const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * C::kHB), kH64, 1024);
-          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc0, kdesc(sAT, 0), dGmn, idesc_acc,
-                                                    up > 0 ? 1u : 0u);
-          MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc1, kdesc(sUT, 0), dQmn, idesc_acc,
-                                                    up > 0 ? 1u : 0u);
-          mma_commit(x_free);
-          mma_commit(&in_empty[bp]);
-          if (u == n) mma_commit(fin);
+        if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&in_full[b], 2 * C::kHB);
+          load_tile_halves<D, kH64>(smem + C::kOffQh + b * C::kHB, &tmQh, &in_full[b], h * 64, bh);
+          load_tile_halves<D, kH64>(smem + C::kOffGh + b * C::kHB, &tmGh, &in_full[b], h * 64, bh);
         }
+        ++issued;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int qq = lane + 32 * j;
+          put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, nl[j] / c2);
+          put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -de[j]);
+          sRinv[b * 64 + qq] = ri[j];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&in_full[b]);
       }
-      mma_commit(drain);
-      drain_wait_bt(drain, 0);
+      if (lane == 0 && *abort_flag) {
+        drain_wait_bt(kv_full, 0);
+        for (int u = (issued > 2 ? issued - 2 : 0); u < issued; ++u) drain_wait_bt(&in_full[u & 1], (u >> 1) & 1);
+      }
+    } else if (warp == 5) {
+      // -------------------------------------------------------- MMA issuer
+      // S'(u), dA'(u) into the slot, then the products of half tile u - 1:
+      // dV += A^T G and dK1 += u^T Q (A^T, u^T: K-major A operands, 16
+      // queries = 32 bytes per K step; G and Q of buffer bp as MN-major B, 16
+      // queries = 2 KB per K step, the two 64-column halves of d = 128 8 KB
+      // apart).
+      if (lane == 0) {
+        constexpr long long kStepKm = 2;                       // K-major: +32 bytes per K step
+        constexpr long long kStepMn = 128;                     // MN-major: +16 rows (2 KB) per K step
+        const uint32_t idesc_s = idesc_bf16(kTile, 64, false, false);
+        const uint32_t idesc_acc = idesc_bf16(kTile, D, false, true);
+        const uint64_t dK = kdesc(sK, 0), dV = kdesc(sV, 0);
+        const uint64_t dAExt = smem_desc_noswizzle(smem_u32(sAExt), 128, 256);
+        bool ok = mbar_wait(kv_full, 0, wc);
+        if (ok) tc_fence_after();
+        for (int u = 0; ok && u <= n; ++u) {
+          if (u < n) {
+            const int b = u & 1;
+            if (!mbar_wait(&in_full[b], (u >> 1) & 1, wc) || !mbar_wait(s_free, (u & 1) ^ 1, wc)) break;
+            tc_fence_after();
+            const uint64_t dQh = kdesc(smem + C::kOffQh + b * C::kHB, 0);
+            const uint64_t dGh = kdesc(smem + C::kOffGh + b * C::kHB, 0);
+            const uint64_t dBS = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtS + b * kExt64), 128, 256);
+            const uint64_t dBA = smem_desc_noswizzle(smem_u32(smem + C::kOffBExtA + b * kExt64), 128, 256);
+            mma_over_d<D>(tmem, dK, kH128, dQh, kH64, idesc_s);
+            mma_bf16_at<0, 0>(tmem, dAExt, dBS, idesc_s, 1u);
+            mma_over_d<D>(tmem + 64, dV, kH128, dGh, kH64, idesc_s);
+            mma_bf16_at<0, 0>(tmem + 64, dAExt, dBA, idesc_s, 1u);
+            mma_commit(s_full);
+          }
+          if (u >= 1) {
+            const int up = u - 1, bp = up & 1;
+            if (!mbar_wait(x_full, up & 1, wc)) break;
+            tc_fence_after();
+            const uint64_t dGmn = smem_desc(smem_u32(smem + C::kOffGh + bp * C::kHB), kH64, 1024);
+            const uint64_t dQmn = smem_desc(smem_u32(smem + C::kOffQh + bp * C::kHB), kH64, 1024);
+            MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc0, kdesc(sAT, 0), dGmn, idesc_acc,
+                                                      up > 0 ? 1u : 0u);
+            MmaRun<0, 4, kStepKm, kStepMn, false>::go(tmem + C::kTmemAcc1, kdesc(sUT, 0), dQmn, idesc_acc,
+                                                      up > 0 ? 1u : 0u);
+            mma_commit(x_free);
+            mma_commit(&in_empty[bp]);
+            if (u == n) mma_commit(fin);
+          }
+        }
+        mma_commit(drain);
+        drain_wait_bt(drain, 0);
+      }
     }
   } else {
     // ------------------------------------------------------ key threads
+    if constexpr (RevRegs<D>::kSplit) setmaxnreg_inc<RevRegs<D>::kKey>();
     const int row = warp * 32 + lane;
     const int key = kt * kTile + row;
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
@@ -1187,6 +1212,15 @@ static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, fl
   // The shared-memory opt-in is a per-device function attribute.
   static PerDeviceOnce once;
   const int prep = once.run([] {
+    if constexpr (RevRegs<D>::kSplit) {
+      // the register split must fit what the block is launched with, or the
+      // key warps' setmaxnreg.inc would never complete: refuse otherwise
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, bwdtc_rev_kernel<D, EARLIER>) != cudaSuccess) return (int)DA_ERR_CUDA;
+      if (fa.numRegs * RevRegs<D>::kThreads < RevRegs<D>::kNeeded || fa.numRegs > RevRegs<D>::kKey ||
+          fa.numRegs < RevRegs<D>::kCtl)
+        return (int)DA_ERR_UNSUPPORTED;
+    }
     return (cudaFuncSetAttribute(bwdtc_rev_kernel<D, EARLIER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  CR::kSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(bwdtc_dk2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1200,7 +1234,7 @@ static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, fl
   const int NT = Tp / kTile;
   const unsigned grid = (unsigned)(NT * BH);
   // maps: 0 Q (64-row boxes), 1 dout (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout (128)
-  bwdtc_rev_kernel<D, EARLIER><<<grid, kBtThreads, CR::kSmemBytes, stream>>>(
+  bwdtc_rev_kernel<D, EARLIER><<<grid, RevRegs<D>::kThreads, CR::kSmemBytes, stream>>>(
       maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, dk1,
       static_cast<__nv_bfloat16 *>(dv), BH, T, Tp, hs, status);
   bwdtc_dk2_kernel<D><<<grid, kBtThreads, CL::kSmemBytes, stream>>>(
