@@ -225,12 +225,12 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
     const float rr = rcp_approx(d.x * d.y);
     const float2 inv = fmul2(make_float2(d.y, d.x), make_float2(rr, rr));   // 1/d0, 1/d1
     const float2 rq = *reinterpret_cast<const float2 *>(rinv_q + col0 + 2 * i);
-    float2 dr = fmul2(make_float2(A[2 * i], A[2 * i + 1]), rq);
+    const float2 w = fmul2(inv, rq);   // 1 / (D R): shared by dr / D and A = r / R
+    float2 dri = fmul2(make_float2(A[2 * i], A[2 * i + 1]), w);
     if (MASK) {
-      if (row_eff > col0 + 2 * i) dr.x = 0.f;
-      if (row_eff > col0 + 2 * i + 1) dr.y = 0.f;
+      if (row_eff > col0 + 2 * i) dri.x = 0.f;
+      if (row_eff > col0 + 2 * i + 1) dri.y = 0.f;
     }
-    const float2 dri = fmul2(dr, inv);
     const float2 ti = fmul2(dri, inv);
     const float2 dir = EARLIER ? dri : fmul2(ti, e);
     const float2 ndc = fmul2(ti, p);
@@ -239,7 +239,7 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
     E[2 * i] = ndc.x;
     E[2 * i + 1] = ndc.y;
     if (AT) {
-      const float2 a = fmul2(fmul2(p, inv), rq);   // A = r / R
+      const float2 a = fmul2(p, w);   // A = r / R
       at[i] = pack_bf16x2(a.x, a.y);
     }
   }
