@@ -400,13 +400,8 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // bwd_work's order; at d = 64 its plain order written out, which keeps
-  // this kernel's register allocation at 8 bytes of spills (20 through the
-  // general function)
-  const int2 o = D == 64 ? make_int2(blockIdx.x % BH, blockIdx.x / BH)
-                         : make_int2(bwd_work(blockIdx.x, BH, T, D, kBwdRev).bh,
-                                     bwd_work(blockIdx.x, BH, T, D, kBwdRev).q_tile0);
-  const int bh = o.x, kt = o.y;
+  const TileWork tw = bwd_work(blockIdx.x, BH, T, D, kBwdRev);
+  const int bh = tw.bh, kt = tw.q_tile0;
   const int NH = Tp / 64, hq0 = 2 * kt, n = NH - hq0, NC = Tp / 32;
   // as in the forward sweep: a scale of at least 1e-30 keeps -inf logits at -inf
   const float c2 = fmaxf(head_c2(hs, bh, nullptr), 1e-30f);
