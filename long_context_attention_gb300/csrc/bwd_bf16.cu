@@ -54,9 +54,10 @@ namespace {
 constexpr int kBtThreads = 192;                    // 4 demand warps, producer, MMA issuer
 
 // R at d = 64 re-splits its registers (setmaxnreg): warpgroup 0 (the key
-// warps) takes 216 per thread, warpgroup 1 (producer, issuer and two idle
-// warps that complete it) gives up to 40; launched at 128 per thread (two CTAs
-// of 256 threads per SM), the split uses exactly the block's registers.  (At
+// warps) takes 224 per thread, warpgroup 1 (producer, issuer and two idle
+// warps that complete it) gives up to 32; launched at 128 per thread (two CTAs
+// of 256 threads per SM), the split uses exactly the block's registers
+// (216 / 40 measured 0.03 ms slower, 232 / 24 spills in warpgroup 1).  (At
 // 168 for every warp the key warps spilled; backward 13.754 -> 13.711 ms, and
 // the room lets the two-chunk loop unroll.)  The same split in the dQ pass
 // measured 0.15 ms slower.
@@ -65,7 +66,7 @@ struct RevRegs {
   static constexpr bool kSplit = D == 64;
   static constexpr int kThreads = kSplit ? 256 : kBtThreads;
   static constexpr int kLaunch = kSplit ? 128 : 0;
-  static constexpr int kKey = 216, kCtl = 40;
+  static constexpr int kKey = 224, kCtl = 32;
   static constexpr int kNeeded = 128 * (kKey + kCtl);
   static_assert(!kSplit || kNeeded <= kThreads * kLaunch, "register split exceeds the launch registers");
 };
@@ -568,8 +569,10 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
       tc_fence_after();
       // partial rho buffer b read
       if (!warp_wait(&r_free[b], ((u >> 1) & 1) ^ 1, wc)) break;
-      // The two chunks unrolled: at d = 64 the key warps' 216 registers leave
-      // the room (backward 13.71 -> 12.84 ms).
+      // The two chunks unrolled: at d = 64 the key warps' registers leave the
+      // room (backward 13.71 -> 12.84 ms).  Loading both chunks from TMEM at
+      // once (one wait, the slot back before any arithmetic) measured slower
+      // (12.75 vs 12.46 ms).
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 1 - cc;   // the chunks backwards
