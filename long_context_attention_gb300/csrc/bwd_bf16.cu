@@ -247,12 +247,21 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
 }
 
 // Reverse walk of one chunk: dp = dir + grev, grev += dC (queries in reverse
-// order; E holds -dC); dp is left in A.
+// order; E holds -dC); dp is left in A.  The running sum is the only serial
+// chain; the additions into A go two at a time on the packed pipe (backward
+// 12.36 -> 12.30 ms with the dQ pass's rho kept negated).
 __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[32], float &grev) {
+  float G[32];
 #pragma unroll
   for (int i = 31; i >= 0; --i) {
-    A[i] += grev;
+    G[i] = grev;
     grev -= E[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 a = fadd2(make_float2(A[i], A[i + 1]), make_float2(G[i], G[i + 1]));
+    A[i] = a.x;
+    A[i + 1] = a.y;
   }
 }
 
@@ -266,7 +275,8 @@ __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[3
 // on tcgen05; one thread per key rebuilds committed inside each 32-query
 // chunk from its demand checkpoint, carries the reverse sum of dC (writing it
 // at every chunk start: the reverse checkpoints), and forms
-//   A = r / R (bf16, for dV),   u = p dp (bf16, for dK1; fp32 for rho);
+//   A = r / R (bf16, for dV),   u = p dp (bf16, for dK1; for rho: bf16 at
+//   d = 64, where the warp sums read the u^T operand back, fp32 at d = 128);
 // the products dV += A^T G and dK1 += u^T Q accumulate in TMEM, and the
 // key tile's partial sums of u (rho_j = sum_k p_jk dp_jk) go to rho.
 // Because ds = p (dp - rho),
@@ -318,33 +328,26 @@ __device__ __forceinline__ void mma_over_d(uint32_t dt, uint64_t da, uint32_t ha
   if constexpr (D == 128) MmaRun<0, 4, 2, 2, false>::go(dt, da + (half_a >> 4), db + (half_b >> 4), idesc, 1u);
 }
 
-// Sum over the warp's 32 keys (lanes) of X[i] for each query i by recursive
-// halving: in each round a lane keeps one half of its values (by one bit of
-// its lane index), sends the other half to the lane that differs in that bit
-// and adds what it receives; lane l ends with the sum for query l.  The
-// kept and received values are added two at a time on the packed pipe
-// (backward 13.757 -> 13.742 ms at 4x12x16384x64).  X is clobbered.
-__device__ __forceinline__ float warp_reduce_scatter32(float (&X)[32], int lane) {
+// The sums over the warp's 32 keys of u for the half tile's 64 queries, read
+// back from the warp's 32 rows of the u^T operand (bf16, 128-byte rows whose
+// 16-byte pieces are swizzled by the row index mod 8): lane l adds up queries
+// 2 l and 2 l + 1, one 4-byte word per row (the 32 lanes read a whole row,
+// free of bank conflicts).  The bf16 values are the ones the dK1 product
+// takes, so sum_k u_jk - rho_j sum_k p_jk stays zero up to the fp32 sums.
+// (The fp32 sums by a register butterfly -- five rounds of shuffles, each
+// lane keeping one half -- took about 110 instructions per 32-query chunk
+// against about 65 here: backward 12.45 -> 12.36 ms at 4x12x16384x64.  The
+// rounding of u to bf16 moves rho by about 2^-9 of its terms' spread, under
+// 0.3 % of max |dQ| in the float64 model of it.)
+__device__ __forceinline__ float2 ut_column_sums(const uint8_t *rows, int lane) {
+  float2 s[4] = {};
 #pragma unroll
-  for (int off = 16; off >= 2; off >>= 1) {
-    const bool up = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < off; i += 2) {
-      const float s0 = up ? X[i] : X[i + off], s1 = up ? X[i + 1] : X[i + off + 1];
-      const float2 keep = make_float2(up ? X[i + off] : X[i], up ? X[i + off + 1] : X[i + 1]);
-      const float2 got = make_float2(__shfl_xor_sync(0xffffffffu, s0, off), __shfl_xor_sync(0xffffffffu, s1, off));
-      const float2 sum = fadd2(keep, got);
-      X[i] = sum.x;
-      X[i + 1] = sum.y;
-    }
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t x = *reinterpret_cast<const uint32_t *>(
+        rows + (i >> 3) * 1024 + (i & 7) * 128 + ((((lane >> 2) ^ (i & 7)) << 4) | ((lane & 3) << 2)));
+    s[i & 3] = fadd2(s[i & 3], make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u)));
   }
-  {
-    const bool up = (lane & 1) != 0;
-    const float send = up ? X[0] : X[1];
-    const float keep = up ? X[1] : X[0];
-    X[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-  }
-  return X[0];
+  return fadd2(fadd2(s[0], s[1]), fadd2(s[2], s[3]));
 }
 
 // The same sums through shared memory: each lane writes its 32 values as one
@@ -594,8 +597,10 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {   // u = p dp
           const float2 x = fmul2(make_float2(P[i], P[i + 1]), make_float2(A[i], A[i + 1]));
-          P[i] = x.x;
-          P[i + 1] = x.y;
+          if constexpr (C::kXp) {
+            P[i] = x.x;
+            P[i + 1] = x.y;
+          }
           ut[i / 2] = pack_bf16x2(x.x, x.y);
         }
         // the previous half tile's products must be done reading A^T, u^T
@@ -611,16 +616,21 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
           *reinterpret_cast<uint4 *>(ut_row + piece * 16) = make_uint4(ut[4 * j], ut[4 * j + 1], ut[4 * j + 2], ut[4 * j + 3]);
         }
         if constexpr (C::kXp) sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_column_sum(P, xp, lane);
-        else sRed[(b * 4 + warp) * 64 + 32 * c + lane] = warp_reduce_scatter32(P, lane);
       }
       if (!ok) break;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(x_full);
-        mbar_arrive(&r_full[b]);
         mbar_arrive(&in_empty[b]);
       }
+      if constexpr (!C::kXp) {
+        // the warp's partial rho from its u^T rows (the products read them
+        // meanwhile)
+        *reinterpret_cast<float2 *>(sRed + (b * 4 + warp) * 64 + 2 * lane) = ut_column_sums(sUT + warp * 4096, lane);
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(&r_full[b]);
       // warps 0 and 1 add the four warps' partial sums of the half tile's
       // 64 queries into rho (one atomic per query and key tile)
       if (warp < 2) {
@@ -1004,7 +1014,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
       put_ext_row(sBExtS, qq, __ldg(nlse2 + idx) / c2);
       put_ext_row(sBExtA, qq, -__ldg(delta + idx));
       sRinv[qq] = __ldg(rinv + idx);
-      sRho[qq] = rho[idx];
+      sRho[qq] = -rho[idx];   // negated: ds = p (dp + (-rho)) on the packed pipe
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -1144,7 +1154,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
           for (int i = 0; i < 16; ++i) {
             const float2 r2 = *reinterpret_cast<const float2 *>(sRho + col0 + 2 * i);
             const float2 x = fmul2(make_float2(P[2 * i], P[2 * i + 1]),
-                                   fadd2(make_float2(A[2 * i], A[2 * i + 1]), make_float2(-r2.x, -r2.y)));
+                                   fadd2(make_float2(A[2 * i], A[2 * i + 1]), r2));
             ds[i] = pack_bf16x2(x.x, x.y);
           }
           // the previous step's dQ product must be done reading the ds buffer
