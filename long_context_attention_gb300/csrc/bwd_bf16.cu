@@ -20,14 +20,17 @@
 //   F   the forward demand sweep again (fwd_bf16.cu) from the given lse2; it
 //       writes committed + eps of every key at every 32-query chunk start
 //       (demand checkpoints) and the forward accumulators (numerator, R);
-//   rows  1/R_j and delta_j = g_j . out_j from those accumulators;
-//   R   key-major, query chunks in reverse order: S = K Q^T and dA' = V G^T -
-//       delta on tcgen05; one thread per key rebuilds committed inside each
-//       chunk from its checkpoint, carries sum_{i > j} dC in a register, and
-//       writes it at every chunk start (reverse checkpoints); it forms
-//       A = r / R and u = p dp, tcgen05 accumulates dV += A^T G and dK1 +=
-//       u^T Q in TMEM, and rho_j (the sum of u over the key tile's lanes) is
-//       added to rho;
+//   rows  from those accumulators, per query row: Gs = G / R (the upstream
+//       gradient over the row sum of the shares, bf16) and delta / R with
+//       delta_j = g_j . out_j;
+//   R   key-major, query chunks in reverse order: S = K Q^T and
+//       dr = V Gs^T - delta / R on tcgen05; one thread per key rebuilds
+//       committed inside each chunk from its checkpoint, carries
+//       sum_{i > j} dC in a register, and writes it at every chunk start
+//       (reverse checkpoints); it forms the shares r and u = p dp, tcgen05
+//       accumulates dV += r^T Gs (= A^T G, A = r / R) and dK1 += u^T Q in
+//       TMEM, and rho_j (the sum of u over the key tile's lanes) is added to
+//       rho;
 //   L   key-major, no demand: the bids p again (S product, one exponential
 //       per pair), dK2 += (p rho)^T Q on tcgen05, dK = c (dK1 - dK2);
 //   Q   query-major: with both checkpoints every chunk is independent; for
@@ -35,8 +38,8 @@
 //       dQ += ds K in TMEM.
 // S and dA' are formed 64 queries at a time (N = 64) so two CTAs fit an SM
 // at d = 64 (R at d = 128: one, its tiles and N = 128 accumulators take the
-// SM); -lse2 / c2 and -delta ride in a fifth K step of their products (the
-// extension operands of the forward sweep).  The passes' launch orders are
+// SM); -lse2 / c2 and -delta / R ride in a fifth K step of their products
+// (the extension operands of the forward sweep).  The passes' launch orders are
 // bwd_work's (da_internal.h): heads in groups whose streamed tiles stay in
 // L2.  Every wait is bounded.
 #include "da_internal.h"
@@ -154,12 +157,13 @@ __global__ void bwdtc_prep(const float *__restrict__ lse2, float *__restrict__ n
   for (int t = 0; t < acc_stride(D) / 4; ++t) ar[t] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// 1/R_j, delta_j = g_j . out_j (out = numerator / R) and rho_j = 0; 16 threads
-// per row, d / 16 columns each.  Rows past T get zeros, so their dr vanish.
+// Per query row j: gs_j = g_j / R_j (bf16), delta_j / R_j with delta_j =
+// g_j . out_j (out = numerator / R), and rho_j = 0; 16 threads per row, d / 16
+// columns each.  Rows past T get zeros, so their dr vanish.
 template <int D>
 __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *__restrict__ g,
-                           float *__restrict__ rinv, float *__restrict__ delta, float *__restrict__ rho, int BH,
-                           int T, int Tp) {
+                           __nv_bfloat16 *__restrict__ gs, float *__restrict__ delta, float *__restrict__ rho,
+                           int BH, int T, int Tp) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = t / 16;
   const int part = (int)(t % 16);
@@ -176,31 +180,35 @@ __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *_
       const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.x));
       const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gg.y));
       dot += (a.x * g01.x + a.y * g01.y) + (a.z * g23.x + a.w * g23.y);
+      reinterpret_cast<uint2 *>(gs + (bh * T + i) * D)[part + 16 * j] =
+          make_uint2(pack_bf16x2(g01.x * inv, g01.y * inv), pack_bf16x2(g23.x * inv, g23.y * inv));
     }
   }
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
   if (live && part == 0) {
-    rinv[row] = inv;
-    delta[row] = dot * inv;
+    delta[row] = dot * inv * inv;
     rho[row] = 0.f;
   }
 }
 
 // ------------------------------------------------------------- chunk engine
 // One key (this thread) against 32 consecutive queries q0 .. q0 + 31 of its
-// column.  In: S' (q.k - lse2 / c2) and dA' (g.v - delta) from TMEM, the
-// chunk's demand checkpoint cpe = committed + eps before q0, 1/R of the
-// queries (shared memory).  Forms, for each query in causal order, p,
+// column.  In: S' (q.k - lse2 / c2) and dr = (g.v - delta) / R from TMEM (the
+// product takes g / R and delta / R), and the chunk's demand checkpoint
+// cpe = committed + eps before q0.  Forms, for each query in causal order, p,
 // e = committed + eps before the query, D, then with ti = dr / D^2
 //   dir = ti e (dr / D for EARLIER),  -dC = ti p,
-// leaving p in P, dir in A and -dC in E (and, with AT, A = r / R packed as
-// bf16 pairs).  Pairs of queries share one reciprocal, 1 / (D0 D1), and go
-// through the packed f32x2 pipe.  MASK zeroes keys after the query
-// (row_eff > column).
+// leaving p in P, dir in A and -dC in E (and, with AT, the share r = p / D
+// packed as bf16 pairs).  Pairs of queries share one reciprocal, 1 / (D0 D1),
+// and go through the packed f32x2 pipe.  MASK zeroes keys after the query
+// (row_eff > column).  (With dout and delta in the products and 1/R read per
+// query pair from shared memory the backward took 12.32 ms at 4x12x16384x64,
+// with dout / R 11.65 ms; a reciprocal per query instead of one per pair
+// 11.75 ms.)
 template <bool MASK, bool EARLIER, bool AT>
 __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], float (&E)[32], uint32_t (&at)[16],
-                                              int row_eff, int col0, float c2, float cpe, const float *rinv_q) {
+                                              int row_eff, int col0, float c2, float cpe) {
   const float2 c2v = make_float2(c2, c2);
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
@@ -225,9 +233,7 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
     const float2 d = EARLIER ? e : fadd2(e, p);
     const float rr = rcp_approx(d.x * d.y);
     const float2 inv = fmul2(make_float2(d.y, d.x), make_float2(rr, rr));   // 1/d0, 1/d1
-    const float2 rq = *reinterpret_cast<const float2 *>(rinv_q + col0 + 2 * i);
-    const float2 w = fmul2(inv, rq);   // 1 / (D R): shared by dr / D and A = r / R
-    float2 dri = fmul2(make_float2(A[2 * i], A[2 * i + 1]), w);
+    float2 dri = fmul2(make_float2(A[2 * i], A[2 * i + 1]), inv);            // dr / D
     if (MASK) {
       if (row_eff > col0 + 2 * i) dri.x = 0.f;
       if (row_eff > col0 + 2 * i + 1) dri.y = 0.f;
@@ -240,7 +246,7 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
     E[2 * i] = ndc.x;
     E[2 * i + 1] = ndc.y;
     if (AT) {
-      const float2 a = fmul2(p, w);   // A = r / R
+      const float2 a = fmul2(p, inv);   // r = p / D
       at[i] = pack_bf16x2(a.x, a.y);
     }
   }
@@ -275,9 +281,9 @@ __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[3
 // on tcgen05; one thread per key rebuilds committed inside each 32-query
 // chunk from its demand checkpoint, carries the reverse sum of dC (writing it
 // at every chunk start: the reverse checkpoints), and forms
-//   A = r / R (bf16, for dV),   u = p dp (bf16, for dK1; for rho: bf16 at
+//   r = p / D (bf16, for dV),   u = p dp (bf16, for dK1; for rho: bf16 at
 //   d = 64, where the warp sums read the u^T operand back, fp32 at d = 128);
-// the products dV += A^T G and dK1 += u^T Q accumulate in TMEM, and the
+// the products dV += r^T Gs and dK1 += u^T Q accumulate in TMEM, and the
 // key tile's partial sums of u (rho_j = sum_k p_jk dp_jk) go to rho.
 // Because ds = p (dp - rho),
 //   dK_k = c sum_j ds_jk q_j = c (sum_j u_jk q_j - sum_j p_jk rho_j q_j),
@@ -297,7 +303,7 @@ struct KeyCfg {
   static constexpr uint32_t kOffAExt = kRev ? kOffGh + 2 * kHB : kOffGh;
   static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;               // [2] -lse2 / c2 rows
   static constexpr uint32_t kOffBExtA = kOffBExtS + 2 * kExt64;           // [2] -delta rows (R)
-  static constexpr uint32_t kOffRows = kOffBExtA + (kRev ? 2 * kExt64 : 0);   // [2][64] fp32: 1/R (R), rho (L)
+  static constexpr uint32_t kOffRows = kOffBExtA + (kRev ? 2 * kExt64 : 0);   // [2][64] fp32: rho (L)
   static constexpr uint32_t kOffRed = kOffRows + 2 * 64 * 4;              // [2][4][64] fp32 partial rho (R)
   static constexpr uint32_t kOffOp = round_up_c(kOffRed + (kRev ? 2 * 4 * 64 * 4 : 0), 1024);
   // R: A^T and u^T (bf16, K-major: 128 keys x 64 queries, 128B-swizzled);
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
     bwdtc_rev_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmGh,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const float *__restrict__ nlse2, const float *__restrict__ delta,
-                     const float *__restrict__ rinv, float *__restrict__ rho, const float *__restrict__ cchk,
+                     float *__restrict__ rho, const float *__restrict__ cchk,
                      float *__restrict__ gchk, float *__restrict__ dk1, __nv_bfloat16 *__restrict__ dv, int BH,
                      int T, int Tp, HeadScale hs, int *status) {
   using C = KeyCfg<kModeRev, D>;
@@ -385,7 +391,6 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
   uint8_t *smem = bt_smem_raw + ((1024u - (smem_u32(bt_smem_raw) & 1023u)) & 1023u);
   uint8_t *sK = smem + C::kOffK, *sV = smem + C::kOffV;
   uint8_t *sAExt = smem + C::kOffAExt;
-  float *sRinv = reinterpret_cast<float *>(smem + C::kOffRows);
   float *sRed = reinterpret_cast<float *>(smem + C::kOffRed);
   uint8_t *sAT = smem + C::kOffOp, *sUT = smem + C::kOffOp + kH128;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
@@ -460,13 +465,12 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
         const int b = u & 1, h = half_of(u);
         // the half tile's per-query values are read before waiting for the
         // buffer, so their global-memory latency overlaps that wait
-        float nl[2], de[2], ri[2];
+        float nl[2], de[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const size_t idx = (size_t)bh * Tp + h * 64 + lane + 32 * j;
           nl[j] = __ldg(nlse2 + idx);
           de[j] = __ldg(delta + idx);
-          ri[j] = __ldg(rinv + idx);
         }
         if (!mbar_wait(&in_empty[b], ((u >> 1) & 1) ^ 1, wc)) break;
         if (lane == 0) {
@@ -480,7 +484,6 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
           const int qq = lane + 32 * j;
           put_ext_row(smem + C::kOffBExtS + b * kExt64, qq, nl[j] / c2);
           put_ext_row(smem + C::kOffBExtA + b * kExt64, qq, -de[j]);
-          sRinv[b * 64 + qq] = ri[j];
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
     } else if (warp == 5) {
       // -------------------------------------------------------- MMA issuer
       // S'(u), dA'(u) into the slot, then the products of half tile u - 1:
-      // dV += A^T G and dK1 += u^T Q (A^T, u^T: K-major A operands, 16
+      // dV += r^T Gs and dK1 += u^T Q (r^T, u^T: K-major A operands, 16
       // queries = 32 bytes per K step; G and Q of buffer bp as MN-major B, 16
       // queries = 2 KB per K step, the two 64-column halves of d = 128 8 KB
       // apart).
@@ -588,9 +591,8 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
         if (cc == 1) release_bt(s_free, lane);
         const size_t ck = ((size_t)bh * NC + (q0h / 32 + c)) * Tp + key;
         const float cpe = cpe_c[c];
-        const float *rq = sRinv + b * 64;
-        if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
-        else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe, rq);
+        if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe);
+        else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe);
         gchk[ck] = grev;   // sum of dC after the chunk
         bwd_chunk_rev(A, E, grev);
         uint32_t ut[16];
@@ -922,8 +924,7 @@ struct QCfg {
   static constexpr uint32_t kOffAExt = kOffDs + 16 * 1024;
   static constexpr uint32_t kOffBExtS = kOffAExt + kExt128;       // 128 query rows
   static constexpr uint32_t kOffBExtA = kOffBExtS + kExt128;
-  static constexpr uint32_t kOffRinv = kOffBExtA + kExt128;       // [128] fp32
-  static constexpr uint32_t kOffRho = kOffRinv + 128 * 4;         // [128] fp32
+  static constexpr uint32_t kOffRho = kOffBExtA + kExt128;        // [128] fp32, negated
   static constexpr uint32_t kOffBar = kOffRho + 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
   static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
@@ -938,8 +939,7 @@ template <int D, bool EARLIER>
 __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
     bwdtc_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                   const float *__restrict__ nlse2, const float *__restrict__ delta, const float *__restrict__ rinv,
-                   const float *__restrict__ rho, const float *__restrict__ cchk, const float *__restrict__ gchk,
+                   const float *__restrict__ nlse2, const float *__restrict__ delta, const float *__restrict__ rho, const float *__restrict__ cchk, const float *__restrict__ gchk,
                    __nv_bfloat16 *__restrict__ dq, int BH, int T, int Tp, HeadScale hs, float c_scalar,
                    int *status) {
   using C = QCfg<D>;
@@ -948,7 +948,6 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
   uint8_t *sQ = smem + C::kOffQ, *sG = smem + C::kOffG, *sK = smem + C::kOffK, *sV = smem + C::kOffV;
   uint8_t *sDs = smem + C::kOffDs, *sAExt = smem + C::kOffAExt;
   uint8_t *sBExtS = smem + C::kOffBExtS, *sBExtA = smem + C::kOffBExtA;
-  float *sRinv = reinterpret_cast<float *>(smem + C::kOffRinv);
   float *sRho = reinterpret_cast<float *>(smem + C::kOffRho);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint64_t *q_full = bars;           // Q, G tiles and the query rows
@@ -1013,7 +1012,6 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
       const size_t idx = (size_t)bh * Tp + qt * kTile + qq;
       put_ext_row(sBExtS, qq, __ldg(nlse2 + idx) / c2);
       put_ext_row(sBExtA, qq, -__ldg(delta + idx));
-      sRinv[qq] = __ldg(rinv + idx);
       sRho[qq] = -rho[idx];   // negated: ds = p (dp + (-rho)) on the packed pipe
     }
     fence_proxy_async_smem();
@@ -1145,8 +1143,8 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
           if (c == 1) release_bt(s_free, lane);
           const int col0 = 64 * hh + 32 * c;   // first query of the chunk inside the tile
           const float cpe = cpe_c[c];
-          if (diag) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row, col0, c2, cpe, sRinv);
-          else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row, col0, c2, cpe, sRinv);
+          if (diag) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row, col0, c2, cpe);
+          else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row, col0, c2, cpe);
           float g0 = g_c[c];
           bwd_chunk_rev(A, E, g0);
           uint32_t ds[16];
@@ -1218,7 +1216,7 @@ int launch_sweep_bf16_chk(const void *q, const void *k, const void *v, const flo
                           cudaStream_t stream);
 
 template <int D, bool EARLIER>
-static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, float *rinv, float *rho, float *cchk,
+static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, float *rho, float *cchk,
                          float *gchk, float *dk1, void *dq, void *dk, void *dv, int BH, int T, int Tp, HeadScale hs,
                          float c, int *status, cudaStream_t stream) {
   using CR = KeyCfg<kModeRev, D>;
@@ -1247,14 +1245,14 @@ static int launch_passes(const CUtensorMap *maps, float *nlse2, float *delta, fl
   if (prep != DA_OK) return prep;
   const int NT = Tp / kTile;
   const unsigned grid = (unsigned)(NT * BH);
-  // maps: 0 Q (64-row boxes), 1 dout (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout (128)
+  // maps: 0 Q (64-row boxes), 1 dout / R (64), 2 K (128), 3 V (128), 4 Q (128), 5 dout / R (128)
   bwdtc_rev_kernel<D, EARLIER><<<grid, RevRegs<D>::kThreads, CR::kSmemBytes, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, dk1,
+      maps[0], maps[1], maps[2], maps[3], nlse2, delta, rho, cchk, gchk, dk1,
       static_cast<__nv_bfloat16 *>(dv), BH, T, Tp, hs, status);
   bwdtc_dk2_kernel<D><<<grid, kBtThreads, CL::kSmemBytes, stream>>>(
       maps[0], maps[2], nlse2, rho, dk1, static_cast<__nv_bfloat16 *>(dk), BH, T, Tp, hs, c, status);
   bwdtc_q_kernel<D, EARLIER><<<grid, kBtThreads, QCfg<D>::kSmemBytes, stream>>>(
-      maps[4], maps[5], maps[2], maps[3], nlse2, delta, rinv, rho, cchk, gchk, static_cast<__nv_bfloat16 *>(dq),
+      maps[4], maps[5], maps[2], maps[3], nlse2, delta, rho, cchk, gchk, static_cast<__nv_bfloat16 *>(dq),
       BH, T, Tp, hs, c, status);
   return cudaGetLastError() == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
@@ -1272,15 +1270,15 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
   int *status = reinterpret_cast<int *>(ws);
   float *nlse2 = reinterpret_cast<float *>(ws + L.nlse2_off);
   float *acc = reinterpret_cast<float *>(ws + L.acc_off);
-  float *rinv = reinterpret_cast<float *>(ws + L.rows_off);
-  float *delta = rinv + rows, *rho = delta + rows;
+  float *delta = reinterpret_cast<float *>(ws + L.rows_off), *rho = delta + rows;
   float *cchk = reinterpret_cast<float *>(ws + L.cchk_off);
   float *gchk = reinterpret_cast<float *>(ws + L.gchk_off);
   float *dk1 = reinterpret_cast<float *>(ws + L.dk1_off);
+  __nv_bfloat16 *gs = reinterpret_cast<__nv_bfloat16 *>(ws + L.gs_off);   // dout / R
   CUtensorMap maps[6];
-  if (!make_bf16_tile_map(&maps[0], q, BH, T, d, 64) || !make_bf16_tile_map(&maps[1], dout, BH, T, d, 64) ||
+  if (!make_bf16_tile_map(&maps[0], q, BH, T, d, 64) || !make_bf16_tile_map(&maps[1], gs, BH, T, d, 64) ||
       !make_bf16_tile_map(&maps[2], k, BH, T, d, kTile) || !make_bf16_tile_map(&maps[3], v, BH, T, d, kTile) ||
-      !make_bf16_tile_map(&maps[4], q, BH, T, d, kTile) || !make_bf16_tile_map(&maps[5], dout, BH, T, d, kTile))
+      !make_bf16_tile_map(&maps[4], q, BH, T, d, kTile) || !make_bf16_tile_map(&maps[5], gs, BH, T, d, kTile))
     return DA_ERR_CUDA;
   const unsigned gp = (unsigned)((rows + 255) / 256), gr = (unsigned)((rows * 16 + 255) / 256);
   if (!have_fwd_state) {
@@ -1290,9 +1288,9 @@ int launch_bwd_bf16_tc(const void *q, const void *k, const void *v, const void *
     if (st != DA_OK) return st;
   }
   const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(dout);
-  if (d == 128) bwdtc_rows<128><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
-  else bwdtc_rows<64><<<gr, 256, 0, stream>>>(acc, g, rinv, delta, rho, BH, T, Tp);
-#define DA_BWD_PASSES_ARGS maps, nlse2, delta, rinv, rho, cchk, gchk, dk1, dq, dk, dv, BH, T, Tp, hs, c, status, stream
+  if (d == 128) bwdtc_rows<128><<<gr, 256, 0, stream>>>(acc, g, gs, delta, rho, BH, T, Tp);
+  else bwdtc_rows<64><<<gr, 256, 0, stream>>>(acc, g, gs, delta, rho, BH, T, Tp);
+#define DA_BWD_PASSES_ARGS maps, nlse2, delta, rho, cchk, gchk, dk1, dq, dk, dv, BH, T, Tp, hs, c, status, stream
   if (d == 128)
     return earlier ? launch_passes<128, true>(DA_BWD_PASSES_ARGS) : launch_passes<128, false>(DA_BWD_PASSES_ARGS);
   return earlier ? launch_passes<64, true>(DA_BWD_PASSES_ARGS) : launch_passes<64, false>(DA_BWD_PASSES_ARGS);

@@ -76,16 +76,19 @@ DA_HD BwdWorkspace bwd_workspace_layout(int64_t BH, int64_t T, int d) {
 
 // ---------------------------------------------------------------------------
 // Tensor-core backward workspace (bf16):
-// [status | -lse2 [BH][Tp] | acc [BH][Tp][d + 4] | 1/R, delta, rho [3][BH][Tp] |
+// [status | -lse2 [BH][Tp] | acc [BH][Tp][d + 4] | delta / R, rho [2][BH][Tp] |
 //  demand checkpoints [BH][Tp/32][Tp] | reverse-sum checkpoints [BH][Tp/32][Tp] |
-//  dK1 [BH][T][d] fp32]
+//  dK1 [BH][T][d] fp32 | dout / R [BH][T][d] bf16]
 // The checkpoints hold, for every key and every 32-query chunk at or after
 // the key's sweep span, committed + eps (forward order) and the sum of dC
 // over the queries after the chunk (reverse order).  dK1 is the part of dK
 // that the reverse pass accumulates (sum_j p dp q_j, before the scale).
+// dout / R (each row of the upstream gradient divided by its row's R) takes
+// the place of dout in the tensor-core products, so they give dr and dV
+// without a 1/R factor per pair.
 // ---------------------------------------------------------------------------
 struct BwdTcWorkspace {
-  size_t nlse2_off, acc_off, rows_off, cchk_off, gchk_off, dk1_off, total;
+  size_t nlse2_off, acc_off, rows_off, cchk_off, gchk_off, dk1_off, gs_off, total;
 };
 
 DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T, int d) {
@@ -94,10 +97,11 @@ DA_HD BwdTcWorkspace bwd_tc_workspace_layout(int64_t BH, int64_t T, int d) {
   w.nlse2_off = kStatusBytes;
   w.acc_off = (size_t)round_up((int64_t)w.nlse2_off + BH * Tp * 4, 256);
   w.rows_off = (size_t)round_up((int64_t)w.acc_off + BH * Tp * acc_stride(d) * 4, 256);
-  w.cchk_off = (size_t)round_up((int64_t)w.rows_off + 3 * BH * Tp * 4, 256);
+  w.cchk_off = (size_t)round_up((int64_t)w.rows_off + 2 * BH * Tp * 4, 256);
   w.gchk_off = (size_t)round_up((int64_t)w.cchk_off + BH * (Tp / 32) * Tp * 4, 256);
   w.dk1_off = (size_t)round_up((int64_t)w.gchk_off + BH * (Tp / 32) * Tp * 4, 256);
-  w.total = (size_t)round_up((int64_t)w.dk1_off + BH * T * d * 4, 256);
+  w.gs_off = (size_t)round_up((int64_t)w.dk1_off + BH * T * d * 4, 256);
+  w.total = (size_t)round_up((int64_t)w.gs_off + BH * T * d * 2, 256);
   return w;
 }
 
