@@ -697,7 +697,9 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
 
 // L: dK2 = sum_j p_jk rho_j q_j, then dK = c (dK1 - dK2).  Half tiles in
 // forward order; one S' slot (the key threads read both chunks at once and
-// hand it back), (p rho)^T buffers double-buffered.
+// hand it back), (p rho)^T buffers double-buffered.  (Carrying |rho| in the
+// exponent, with sign(rho) q as the operand, saves the product by rho per
+// pair but needs a sign-flip pass over Q: backward 11.42 -> 11.49 ms.)
 template <int D>
 __global__ void __launch_bounds__(kBtThreads, KeyCfg<kModeDk2, D>::kCtasPerSm)
     bwdtc_dk2_kernel(const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmK,
