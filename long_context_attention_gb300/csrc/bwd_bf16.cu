@@ -197,14 +197,16 @@ __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *_
 // column.  In: S' (q.k - lse2 / c2) and dr = (g.v - delta) / R from TMEM (the
 // product takes g / R and delta / R), and the chunk's demand checkpoint
 // cpe = committed + eps before q0.  Forms, for each query in causal order, p,
-// e = committed + eps before the query, D, then with ti = dr / D^2
-//   dir = ti e (dr / D for EARLIER),  -dC = ti p,
-// leaving p in P, dir in A and -dC in E (and, with AT, the share r = p / D
-// packed as bf16 pairs; then -dC = dr r / D and dir = dr / D + dC, one
-// product fewer per pair: backward 11.65 -> 11.40 ms.  Folding -rho into
-// dir by a fused multiply-add in the dQ pass spilled there: 11.48 ms).
-// Pairs of queries share one reciprocal, 1 / (D0 D1), and go through the
-// packed f32x2 pipe.  MASK zeroes keys after the query
+// e = committed + eps before the query, D, the share r = p / D and
+//   dr / D,   -dC = (dr / D) r,
+// leaving p in P, dr / D in A and -dC in E (and, with AT, r packed as bf16
+// pairs).  The direct term of dp, dr e / D^2 = dr / D + dC, needs no product
+// of its own: the reverse walk adds the running sum of dC including the
+// query's own (for EARLIER, D = e and the direct term is dr / D itself).
+// (Forming dr e / D^2 per pair: backward 11.40 ms at 4x12x16384x64 against
+// 11.09 ms without; folding -rho into it by a fused multiply-add in the dQ
+// pass spilled there.)  Pairs of queries share one reciprocal, 1 / (D0 D1), and go
+// through the packed f32x2 pipe.  MASK zeroes keys after the query
 // (row_eff > column).  (With dout and delta in the products and 1/R read per
 // query pair from shared memory the backward took 12.32 ms at 4x12x16384x64,
 // with dout / R 11.65 ms; a reciprocal per query instead of one per pair
@@ -213,7 +215,6 @@ template <bool MASK, bool EARLIER, bool AT>
 __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], float (&E)[32], uint32_t (&at)[16],
                                               int row_eff, int col0, float c2, float cpe) {
   const float2 c2v = make_float2(c2, c2);
-  const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     const float2 x = fmul2(make_float2(P[i], P[i + 1]), c2v);
@@ -242,35 +243,34 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
       if (row_eff > col0 + 2 * i) dri.x = 0.f;
       if (row_eff > col0 + 2 * i + 1) dri.y = 0.f;
     }
-    float2 dir, ndc;
-    if (AT) {
-      // with the share r at hand: -dC = dr r / D, dir = dr / D + dC
-      const float2 r = fmul2(p, inv);
-      at[i] = pack_bf16x2(r.x, r.y);
-      ndc = fmul2(dri, r);
-      dir = EARLIER ? dri : ffma2(ndc, m1, dri);
-    } else {
-      const float2 ti = fmul2(dri, inv);
-      dir = EARLIER ? dri : fmul2(ti, e);
-      ndc = fmul2(ti, p);
-    }
-    A[2 * i] = dir.x;
-    A[2 * i + 1] = dir.y;
+    const float2 r = fmul2(p, inv);     // the share p / D
+    const float2 ndc = fmul2(dri, r);   // -dC = dr p / D^2
+    if (AT) at[i] = pack_bf16x2(r.x, r.y);
+    A[2 * i] = dri.x;
+    A[2 * i + 1] = dri.y;
     E[2 * i] = ndc.x;
     E[2 * i + 1] = ndc.y;
   }
 }
 
-// Reverse walk of one chunk: dp = dir + grev, grev += dC (queries in reverse
-// order; E holds -dC); dp is left in A.  The running sum is the only serial
-// chain; the additions into A go two at a time on the packed pipe (backward
-// 12.36 -> 12.30 ms with the dQ pass's rho kept negated).
+// Reverse walk of one chunk (queries in reverse order; E holds -dC, A dr / D):
+// grev += dC, then dp = dr / D + grev (the sum of dC over this query and the
+// later ones); for EARLIER dp = dr / D + grev before this query's dC.  dp is
+// left in A.  The running sum is the only serial chain; the additions into A
+// go two at a time on the packed pipe (backward 12.36 -> 12.30 ms with the
+// dQ pass's rho kept negated).
+template <bool EARLIER>
 __device__ __forceinline__ void bwd_chunk_rev(float (&A)[32], const float (&E)[32], float &grev) {
   float G[32];
 #pragma unroll
   for (int i = 31; i >= 0; --i) {
-    G[i] = grev;
-    grev -= E[i];
+    if (EARLIER) {
+      G[i] = grev;
+      grev -= E[i];
+    } else {
+      grev -= E[i];
+      G[i] = grev;
+    }
   }
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(RevRegs<D>::kThreads, KeyCfg<kModeRev, D>::kCt
         if (need_mask) bwd_chunk_fwd<true, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe);
         else bwd_chunk_fwd<false, EARLIER, true>(P, A, E, at, row_eff, 32 * c, c2, cpe);
         gchk[ck] = grev;   // sum of dC after the chunk
-        bwd_chunk_rev(A, E, grev);
+        bwd_chunk_rev<EARLIER>(A, E, grev);
         uint32_t ut[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {   // u = p dp
@@ -1157,7 +1157,7 @@ __global__ void __launch_bounds__(kBtThreads, QCfg<D>::kCtasPerSm)
           if (diag) bwd_chunk_fwd<true, EARLIER, false>(P, A, E, at, row, col0, c2, cpe);
           else bwd_chunk_fwd<false, EARLIER, false>(P, A, E, at, row, col0, c2, cpe);
           float g0 = g_c[c];
-          bwd_chunk_rev(A, E, g0);
+          bwd_chunk_rev<EARLIER>(A, E, g0);
           uint32_t ds[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {   // ds = p (dp - rho)
