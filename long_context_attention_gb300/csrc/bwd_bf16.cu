@@ -197,12 +197,15 @@ __global__ void bwdtc_rows(const float *__restrict__ acc, const __nv_bfloat16 *_
 // column.  In: S' (q.k - lse2 / c2) and dr = (g.v - delta) / R from TMEM (the
 // product takes g / R and delta / R), and the chunk's demand checkpoint
 // cpe = committed + eps before q0.  Forms, for each query in causal order, p,
-// e = committed + eps before the query, D, the share r = p / D and
+// D = e + p with e = committed + eps before the query (D is the running sum
+// just after the query; for EARLIER D = e, just before it), the share
+// r = p / D and
 //   dr / D,   -dC = (dr / D) r,
 // leaving p in P, dr / D in A and -dC in E (and, with AT, r packed as bf16
 // pairs).  The direct term of dp, dr e / D^2 = dr / D + dC, needs no product
 // of its own: the reverse walk adds the running sum of dC including the
-// query's own (for EARLIER, D = e and the direct term is dr / D itself).
+// query's own (for EARLIER the direct term is dr / D itself).  (Taking D from
+// the running sum instead of adding e + p again: backward 11.09 -> 10.98 ms.)
 // (Forming dr e / D^2 per pair: backward 11.40 ms at 4x12x16384x64 against
 // 11.09 ms without; folding -rho into it by a fused multiply-add in the dQ
 // pass spilled there.)  Pairs of queries share one reciprocal, 1 / (D0 D1), and go
@@ -226,16 +229,22 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
     for (int i = 0; i < 32; ++i)
       if (row_eff > col0 + i) P[i] = 0.f;
   }
+  // D of each query straight from the running sum: committed + eps after the
+  // query (committed + eps + p), or before it for EARLIER
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    E[i] = cpe;   // committed + eps before query i
-    cpe += P[i];
+    if (EARLIER) {
+      E[i] = cpe;
+      cpe += P[i];
+    } else {
+      cpe += P[i];
+      E[i] = cpe;
+    }
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float2 e = make_float2(E[2 * i], E[2 * i + 1]);
     const float2 p = make_float2(P[2 * i], P[2 * i + 1]);
-    const float2 d = EARLIER ? e : fadd2(e, p);
+    const float2 d = make_float2(E[2 * i], E[2 * i + 1]);
     const float rr = rcp_approx(d.x * d.y);
     const float2 inv = fmul2(make_float2(d.y, d.x), make_float2(rr, rr));   // 1/d0, 1/d1
     float2 dri = fmul2(make_float2(A[2 * i], A[2 * i + 1]), inv);            // dr / D
