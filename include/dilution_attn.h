@@ -164,7 +164,9 @@ int dilution_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
  *   lse2 [B,H,T] fp32: the forward's lse2_out for the same q, k, tau.
  *   dtype applies to q, k, v, dout, dq, dk, dv.  DA_BF16 runs on tcgen05
  *   tensor cores (bf16 products, fp32 accumulation and fp32 demand
- *   arithmetic, the demand recomputed from checkpoints every 32 queries);
+ *   arithmetic, the demand recomputed from checkpoints every 32 queries; the
+ *   products' operands are rounded to bf16: the shares, u = p dp, p rho, ds
+ *   and dout divided by each row's sum of shares);
  *   DA_F32 runs on CUDA cores in fp32 (column sums of the demand in fp64).
  * workspace: at least dilution_attn_bwd_workspace_size(); errors as for
  * dilution_attn_fwd.
@@ -180,8 +182,9 @@ int dilution_attn_bwd(const void *q, const void *k, const void *v, const void *d
  * [B*H]) and flags (DA_FLAG_EARLIER_DEMAND_ONLY), which must match the
  * forward that produced lse2.  DA_FLAG_KEEP_FOR_BACKWARD (DA_BF16 only):
  * workspace is the one the forward ran with under the same flag and still
- * holds its state; lse2 is then not read (but must still be a valid pointer).  With the flag, D_jk = committed_jk + eps and
- * the direct term of dp_jk is dr_jk / D_jk.  Errors as for dilution_attn_bwd
+ * holds its state; lse2 is then not read (but must still be a valid pointer).
+ * With DA_FLAG_EARLIER_DEMAND_ONLY, D_jk = committed_jk + eps and the direct
+ * term of dp_jk is dr_jk / D_jk.  Errors as for dilution_attn_bwd
  * plus those of dilution_attn_fwd_ex for tau_bh and flags. */
 int dilution_attn_bwd_ex(const void *q, const void *k, const void *v, const void *dout,
                          const float *lse2, void *dq, void *dk, void *dv,
