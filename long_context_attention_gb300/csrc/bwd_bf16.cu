@@ -231,22 +231,24 @@ __device__ __forceinline__ void bwd_chunk_fwd(float (&P)[32], float (&A)[32], fl
   }
   // D of each query straight from the running sum: committed + eps after the
   // query (committed + eps + p), or before it for EARLIER
+  // (stored pairwise swapped, E[2 i] holding D of query 2 i + 1, so that the
+  // pair (1/D0, 1/D1) = (D1, D0) / (D0 D1) is one packed product)
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     if (EARLIER) {
-      E[i] = cpe;
+      E[i ^ 1] = cpe;
       cpe += P[i];
     } else {
       cpe += P[i];
-      E[i] = cpe;
+      E[i ^ 1] = cpe;
     }
   }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float2 p = make_float2(P[2 * i], P[2 * i + 1]);
-    const float2 d = make_float2(E[2 * i], E[2 * i + 1]);
-    const float rr = rcp_approx(d.x * d.y);
-    const float2 inv = fmul2(make_float2(d.y, d.x), make_float2(rr, rr));   // 1/d0, 1/d1
+    const float2 ds = make_float2(E[2 * i], E[2 * i + 1]);   // (D1, D0)
+    const float rr = rcp_approx(ds.x * ds.y);
+    const float2 inv = fmul2(ds, make_float2(rr, rr));          // 1/D0, 1/D1
     float2 dri = fmul2(make_float2(A[2 * i], A[2 * i + 1]), inv);            // dr / D
     if (MASK) {
       if (row_eff > col0 + 2 * i) dri.x = 0.f;
@@ -358,20 +360,30 @@ __device__ __forceinline__ void mma_over_d(uint32_t dt, uint64_t da, uint32_t ha
 // 2 l and 2 l + 1, one 4-byte word per row (the 32 lanes read a whole row,
 // free of bank conflicts).  The bf16 values are the ones the dK1 product
 // takes, so sum_k u_jk - rho_j sum_k p_jk stays zero up to the fp32 sums.
-// (The fp32 sums by a register butterfly -- five rounds of shuffles, each
-// lane keeping one half -- took about 110 instructions per 32-query chunk
-// against about 65 here: backward 12.45 -> 12.36 ms at 4x12x16384x64.  The
-// rounding of u to bf16 moves rho by about 2^-9 of its terms' spread, under
-// 0.3 % of max |dQ| in the float64 model of it.)
+// Each bf16 half is added into its fp32 sum by a mixed-precision add (the
+// conversion is exact): backward 10.97 -> 10.92 ms at 4x12x16384x64 against
+// unpacking both halves and one packed add, together with the pairwise
+// swapped D in the chunk engine.  (The fp32 sums by a register butterfly --
+// five rounds of shuffles, each lane keeping one half -- took about 110
+// instructions per 32-query chunk against about 65 with the unpacking:
+// backward 12.45 -> 12.36 ms.  The rounding of u to bf16 moves rho by about
+// 2^-9 of its terms' spread, under 0.3 % of max |dQ| in the float64 model
+// of it.)
+__device__ __forceinline__ void add_bf16x2(float &lo_acc, float &hi_acc, uint32_t x) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(lo_acc), "+f"(hi_acc)
+      : "r"(x));
+}
 __device__ __forceinline__ float2 ut_column_sums(const uint8_t *rows, int lane) {
-  float2 s[4] = {};
+  float s0[4] = {}, s1[4] = {};
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const uint32_t x = *reinterpret_cast<const uint32_t *>(
         rows + (i >> 3) * 1024 + (i & 7) * 128 + ((((lane >> 2) ^ (i & 7)) << 4) | ((lane & 3) << 2)));
-    s[i & 3] = fadd2(s[i & 3], make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u)));
+    add_bf16x2(s0[i & 3], s1[i & 3], x);
   }
-  return fadd2(fadd2(s[0], s[1]), fadd2(s[2], s[3]));
+  return make_float2((s0[0] + s0[1]) + (s0[2] + s0[3]), (s1[0] + s1[1]) + (s1[2] + s1[3]));
 }
 
 // The same sums through shared memory: each lane writes its 32 values as one
